@@ -1,0 +1,244 @@
+/*
+ * fsdp_state.h -- C ABI of libfsdpstate, the FSDP / ZeRO-3 sharded-state step
+ * on one GB300 (sm_103a), with N data-parallel ranks simulated as buffers in
+ * one GPU's memory.
+ *
+ * The calls follow the way the FSDP pages state the problem:
+ *   - flatten + pad + shard of a wrap unit (FSDP1 FlatParameter) or per-tensor
+ *     dim-0 sharding (FSDP2 Shard(0)):  fsdp_layout_create / _query / _unit /
+ *     _tensor / _segment;
+ *   - the all-gather that rebuilds the full parameter before forward and again
+ *     before backward:  fsdp_unshard;
+ *   - the gradient reduce-scatter (fp32 reduce dtype, mean over ranks), the
+ *     AdamW step of each rank's 1/N shard and the bf16 recast of the updated
+ *     shard, fused into one pass:  fsdp_reduce_scatter_adamw;
+ *   - initial sharding, summon_full_params(writeback) and the release of the
+ *     full buffer after use:  fsdp_reshard;
+ *   - per-rank model-state bytes of ZeRO stages 0-3:  fsdp_state_bytes.
+ *
+ * Sources (titles and sections of the pages this restates):
+ *   [FSDP-ch18]  "第18章 FSDP：ZeRO 风格的参数分片" (yangyitao.com PyTorch book)
+ *   [ZeRO-state] "NCCL ZeRO/FSDP state sharding" (blog.cptz.space)
+ *   [FSDP2-doc]  "PyTorch FSDP2 后端特性介绍" (MindSpeed-LLM docs)
+ *   [titan]      torchtitan FSDP2 article (gsyq.cn)
+ *
+ * Conventions shared by every call
+ *   - Return value: FSDP_OK (0) or a negative fsdp_status.  All arguments are
+ *     validated before anything is launched; on error nothing is launched and
+ *     no output is touched.
+ *   - Memory: every data buffer is owned by the caller and must stay alive until
+ *     the work queued on the given stream has finished.  Device buffers are
+ *     plain device pointers (cudaMalloc, or any allocator), 16-byte aligned
+ *     (else FSDP_EALIGN).  The library owns only the layout object and the
+ *     small per-device copy of its segment tables.
+ *   - Streams: fsdp_stream_t is a cudaStream_t (NULL = legacy default stream).
+ *     Launch calls are asynchronous and never synchronize; only
+ *     fsdp_check_status and fsdp_layout_prepare block.
+ *   - Shard arrays are [N][stride] row-major: rank r's shard starts at element
+ *     r*stride; stride = fsdp_layout_info.shard_stride (>= S, multiple of 64).
+ *   - The full layout: FLAT -- per unit, the padded flat parameter of N*S_u
+ *     elements (tensors are views into it, padding at the end), units
+ *     concatenated; DIM0 -- the tensors concatenated, each in its own row-major
+ *     shape, no padding.
+ *   - Threads: a layout is immutable after creation; it may be used from any
+ *     thread and stream.  fsdp_layout_destroy must not race with other calls.
+ */
+#ifndef FSDP_STATE_H
+#define FSDP_STATE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FSDP_OK = 0,
+    FSDP_EINVAL = -1,     /* bad argument: NULL, range, unknown enum, bad hyper-parameter  */
+    FSDP_EDTYPE = -2,     /* mixed dtypes inside one FLAT unit, or unsupported dtype       */
+    FSDP_ESHAPE = -3,     /* inconsistent shapes / unit ids                                */
+    FSDP_EALIGN = -4,     /* a buffer is not 16-byte aligned                               */
+    FSDP_EOVERFLOW = -5,  /* an element count does not fit the int64 / device index range  */
+    FSDP_ECUDA = -6,      /* a CUDA call failed (fsdp_last_cuda_error names it)            */
+    FSDP_ETIMEOUT = -7,   /* reserved: a bounded device-side wait gave up                  */
+    FSDP_ENOMEM = -8      /* host or device allocation of the layout tables failed         */
+} fsdp_status;
+
+/* FLAT = FSDP1 FlatParameter ([FSDP-ch18] §18.12; [ZeRO-state] "FlatParameter 与
+ * Padding"): the tensors of a unit are flattened, concatenated and padded to
+ * N*ceil(P_u/N); rank r owns flat elements [r*S_u, (r+1)*S_u), S_u = ceil(P_u/N).
+ * DIM0 = FSDP2 per-parameter Shard(0) ([FSDP2-doc] "DTensor": [4096,4096] on 8
+ * ranks -> [512,4096]; [titan] §2.3): each tensor of d0 rows gets a slot of
+ * c = ceil(d0/N) rows on every rank; rank r owns rows [min(rc,d0), min((r+1)c,d0)),
+ * the rest of its slot is zero padding (a rank may own no row). */
+typedef enum { FSDP_FLAT = 0, FSDP_DIM0 = 1 } fsdp_mode;
+
+typedef enum { FSDP_F32 = 0, FSDP_BF16 = 1 } fsdp_dtype;
+
+typedef struct fsdp_layout fsdp_layout;      /* opaque, host-owned, immutable */
+typedef struct CUstream_st* fsdp_stream_t;    /* same type as cudaStream_t    */
+
+/* AdamW hyper-parameters (decoupled weight decay; Adam with bias correction). */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+} fsdp_adamw_hparams;
+
+typedef struct {
+    int32_t n_tensors, n_units, n_ranks, mode;
+    int64_t numel;          /* P: logical elements, sum of tensor numels              */
+    int64_t shard_numel;    /* S: elements of one rank's shard (sum over units)       */
+    int64_t shard_stride;   /* physical row stride of [N][stride] shard arrays        */
+    int64_t full_numel;     /* elements of the full layout (FLAT: N*S, DIM0: P)       */
+    int64_t pad_numel;      /* N*S - P: padding elements over all ranks               */
+    int64_t n_segments;     /* (tensor or unit, rank) pieces holding logical elements */
+} fsdp_layout_info;
+
+/* Creates a layout of n_tensors tensors.
+ *   ndim[t]      number of dimensions of tensor t (0 = scalar, counted as [1])
+ *   dims         all dimensions, concatenated in tensor order (sum(ndim) entries)
+ *   unit_id[t]   wrap unit (FSDP1) / param group (FSDP2) of tensor t: starts at 0,
+ *                nondecreasing, steps of 0 or 1 (else FSDP_ESHAPE)
+ *   dtype[t]     fsdp_dtype of tensor t's parameter; may be NULL (all the same).
+ *                In FLAT mode all tensors of a unit must share a dtype, as a
+ *                FlatParameter requires one dtype ([FSDP-ch18] §18.12) -> FSDP_EDTYPE.
+ *   n_ranks      N >= 1 simulated data-parallel ranks (<= FSDP_MAX_RANKS)
+ *   mode         FSDP_FLAT or FSDP_DIM0
+ * Pure host computation: needs no GPU.  *out is set only on FSDP_OK. */
+#define FSDP_MAX_RANKS 64
+int fsdp_layout_create(int32_t n_tensors, const int32_t* ndim, const int64_t* dims,
+                       const int32_t* unit_id, const int32_t* dtype, int32_t n_ranks,
+                       int32_t mode, fsdp_layout** out);
+
+/* Frees the layout and its device tables (on every device they were made on).
+ * NULL is accepted.  No call may be using the layout or have queued work that
+ * reads its tables. */
+void fsdp_layout_destroy(fsdp_layout* layout);
+
+int fsdp_layout_query(const fsdp_layout* layout, fsdp_layout_info* out);
+
+/* Unit u: its shard offset and size S_u inside a rank row, its offset and size
+ * in the full layout, and its logical element count P_u. */
+int fsdp_layout_unit(const fsdp_layout* layout, int32_t unit, int64_t* shard_off,
+                     int64_t* shard_numel, int64_t* full_off, int64_t* full_numel,
+                     int64_t* numel);
+
+/* Tensor t: its unit, numel, offset in the full layout; DIM0 only: its shard
+ * offset inside a rank row and its rows per rank slot c (FLAT: both -1, since a
+ * FLAT tensor's shard position depends on the rank -- use fsdp_layout_segment). */
+int fsdp_layout_tensor(const fsdp_layout* layout, int32_t tensor, int32_t* unit,
+                       int64_t* numel, int64_t* full_off, int64_t* shard_off,
+                       int64_t* rows_per_rank);
+
+/* Rank r's view of tensor t ([ZeRO-state] "FlatParameter 与 Padding": a rank's
+ * view of an original parameter may be a 1-D piece, or empty):
+ *   *shard_off  position of the view inside rank r's row (element index)
+ *   *full_off   position of the same elements in the full layout
+ *   *len        number of logical elements (0 when the rank holds none)
+ *   *pad        DIM0: padding elements in rank r's slot of tensor t; FLAT: 0
+ *               (FLAT padding belongs to the unit; see fsdp_layout_unit).
+ * When *len == 0, *shard_off and *full_off are where the view would start. */
+int fsdp_layout_segment(const fsdp_layout* layout, int32_t tensor, int32_t rank,
+                        int64_t* shard_off, int64_t* full_off, int64_t* len, int64_t* pad);
+
+/* Per-rank model-state bytes of ZeRO stage 0..3 ([ZeRO-state] "Canonical ZeRO
+ * 状态公式": stage 0 keeps P, P, 2P per rank; stage 1 shards the optimizer state
+ * (2P/N), stage 2 also the gradient (P/N), stage 3 also the parameter (P/N)).
+ *   param_bytes, grad_bytes   bytes per parameter / gradient element
+ *   optim_bytes               optimizer bytes per element (8: fp32 exp_avg +
+ *                             exp_avg_sq; 12 with an fp32 master copy, [titan] §2.3)
+ *   step_bytes                optimizer metadata per tensor (Adam's step scalar)
+ *   physical                  1: a sharded state counts the rank's padded slot
+ *                             (S elements); 0: only the logical elements it owns
+ * out[0..2] = parameter, gradient, optimizer bytes held by `rank`. */
+int fsdp_state_bytes(const fsdp_layout* layout, int32_t stage, int32_t rank, int32_t physical,
+                     int64_t param_bytes, int64_t grad_bytes, int64_t optim_bytes,
+                     int64_t step_bytes, int64_t out[3]);
+
+/* Allocates and uploads the layout's segment tables on the current CUDA device
+ * and blocks until they are there.  Launch calls do this themselves on their
+ * first use of a layout on a device; call it first to keep that allocation out
+ * of a timed region or of a stream capture.  FSDP_ENOMEM / FSDP_ECUDA on failure. */
+int fsdp_layout_prepare(fsdp_layout* layout);
+
+/* Unshard = all-gather of units [unit_begin, unit_end) ([ZeRO-state] "ZeRO-3 方向：
+ * Parameter Sharding": all_gather_into_tensor(padded_unsharded_flat_param,
+ * sharded_flat_param); [FSDP-ch18] §18.3 and §18.8: FSDP2 copy-in, one all-gather,
+ * copy-out).  Reads the N rank shards, writes the full layout of those units:
+ *   FLAT: every shard element, padding included, to full[u_off + r*S_u + k]
+ *         (the padded flat parameter; its padding comes out as the shards' zeros);
+ *   DIM0: the owned rows of each tensor to their place in the full tensor.
+ *   param_shards  device, [N][stride] of elem_dtype (bf16 param shards, or the
+ *                 fp32 master when the parameter dtype is fp32)
+ *   full          device, full-layout buffer of elem_dtype (full_numel elements;
+ *                 only the units' ranges are written)
+ * The copy is bitwise.  Async on `stream`. */
+int fsdp_unshard(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                 const void* param_shards, void* full, int32_t elem_dtype, fsdp_stream_t stream);
+
+/* The fused reduce-scatter + AdamW + bf16 recast of units [unit_begin, unit_end),
+ * one pass over the rank shards:
+ *   (1) reduce-scatter ([ZeRO-state] "ZeRO-2 方向：Gradient Sharding":
+ *       reduce_scatter_tensor(new_sharded_grad, padded_grad)): for rank r and its
+ *       shard element j, g = (sum over q = 0..N-1, in that order, of
+ *       float(G_q[full index of (r, j)])) / N in fp32 (reduce_dtype = float32,
+ *       [FSDP-ch18] §18.6); padding elements have g = 0;
+ *   (2) AdamW on rank r's fp32 shard of master / exp_avg / exp_avg_sq
+ *       ([ZeRO-state] "Optimizer Step 的所有权": each rank updates only its
+ *       shard), in this order, every operation rounded to fp32:
+ *         p *= 1 - lr*wd;  m = fma(b1, m, (1-b1)*g);  v = fma(b2, v, ((1-b2)*g)*g);
+ *         p = fma(-lr/(1-b1^t), m / (sqrt(v)/sqrt(1-b2^t) + eps), p)
+ *       (the four step constants formed in double, rounded to fp32 once);
+ *   (3) param_shards = bf16(p), round to nearest even ([FSDP-ch18] §18.6:
+ *       bf16 parameters for the all-gather, fp32 master for Adam).
+ *   grad_replicas  host array of N device pointers; replica q is rank q's full
+ *                  gradient in the full layout (full_numel elements of
+ *                  grad_dtype).  FLAT padding positions are never read.
+ *   master, exp_avg, exp_avg_sq   device, [N][stride] fp32, updated in place.
+ *                  Padding elements are not touched: they stay +0 when they
+ *                  start at +0 (fsdp_reshard writes them so), which is exactly
+ *                  what AdamW does to them with g = 0 when 0 <= lr*wd <= 1.
+ *   param_shards   device, [N][stride] bf16, or NULL when the parameter dtype is
+ *                  fp32 (the master is then the parameter).
+ *   grad_shard_out optional device [N][stride] fp32: the reduced gradient shard
+ *                  (FSDP's _saved_grad_shard), padding written as +0; or NULL.
+ *   hp             lr >= 0, 0 <= beta < 1, eps > 0, weight_decay >= 0,
+ *                  lr*weight_decay <= 1, all finite (else FSDP_EINVAL).
+ *   step           1-based step count t shared by all elements.
+ * Async on `stream`. */
+int fsdp_reduce_scatter_adamw(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                              const void* const* grad_replicas, int32_t grad_dtype,
+                              float* master, float* exp_avg, float* exp_avg_sq,
+                              void* param_shards, float* grad_shard_out,
+                              const fsdp_adamw_hparams* hp, int64_t step, fsdp_stream_t stream);
+
+/* Reshard of units [unit_begin, unit_end).
+ *   full == NULL: release only -- the full buffer is the caller's to free or
+ *     reuse ([FSDP-ch18] §18.3: after use the full copy is dropped and the rank is
+ *     back to 1/N); nothing is launched.
+ *   full != NULL: scatter the full layout into the rank shards, the initial
+ *     sharding of a constructed model and the writeback of
+ *     summon_full_params(writeback=True) ([FSDP-ch18] §18.17):
+ *     master (fp32, or NULL) gets the values, param_shards (bf16, or NULL) gets
+ *     their bf16 rounding (nearest even); padding elements get +0, and when the
+ *     range ends at the last unit, so does each row's tail [S, stride).
+ *   full_dtype     FSDP_F32 or FSDP_BF16 (bf16 values widen exactly).
+ * Async on `stream`. */
+int fsdp_reshard(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                 const void* full, int32_t full_dtype, float* master, void* param_shards,
+                 fsdp_stream_t stream);
+
+/* Blocks until `stream` is idle and reports any CUDA error seen there
+ * (FSDP_ECUDA) -- the analogue of a collective's error check. */
+int fsdp_check_status(fsdp_stream_t stream);
+
+/* Static text for a status code; never NULL. */
+const char* fsdp_error_string(int status);
+
+/* Text of the last CUDA error seen by this thread in a library call ("" if none). */
+const char* fsdp_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FSDP_STATE_H */
