@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Benchmark of the sharded-state step on GB300: params/s and achieved HBM GB/s.
+
+One step = one pass of the whole hot path over one synthetic batch of gradients:
+FULL_SHARD = two all-gathers (fsdp_unshard, forward and backward) + the fused
+reduce-scatter + AdamW + bf16 recast (fsdp_reduce_scatter_adamw) over all units.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mlp128m]
+  python bench.py --impl reference      # the CPU oracle on a bounded sample
+
+Prints ONE JSON line (rank 0).  `value` is whole-job params/s with inputs resident
+in HBM; `e2e` is the same metric through the public API with host buffers (the
+gradient replicas copied host->device and the updated parameter shards
+device->host inside every timed step); `roofline` is the dominant kernel's
+algorithmic bytes per launch over its CUDA-event duration against the measured
+HBM copy peak; `cpu_baseline` is the oracle timed on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sharded-step params/sec and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
+PEAK_FALLBACK_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "fsdp_sharded_state_gb300", "csrc", "kernels.cu")
+
+
+# ---------------------------------------------------------------------------
+# helpers that need no GPU (tested on CPU)
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(N, P, S, F, mode, grad_bytes, param_bytes, grad_out=False):
+    """Algorithmic HBM bytes per launch of each kernel, whole layout.
+    rs_adamw: N replicas x P logical gradient elements read; fp32 master, exp_avg,
+    exp_avg_sq read + written for the N*S shard elements (24 B); the bf16 copy
+    written (2 B) when the parameter dtype is bf16; the fp32 reduced gradient
+    (4 B) when requested.  Padding is skipped by the kernel, so the shard terms
+    count logical elements (N*S - pad = P).
+    unshard: the shard elements read and the full-layout elements written
+    (FLAT: N*S each -- the padded flat parameter; DIM0: P each)."""
+    logical_shard = P
+    rs = N * P * grad_bytes + 24 * logical_shard + (2 * logical_shard if param_bytes == 2 else 0)
+    if grad_out:
+        rs += 4 * N * S
+    gathered = N * S if mode == 0 else P
+    unshard = 2 * gathered * param_bytes
+    return {"rs_adamw": rs, "unshard": unshard}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return PEAK_FALLBACK_GBS, "fallback"
+
+
+def kernel_src_hash():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel source changed since."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_src_sha256_16") != kernel_src_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def aggregate_max(value, world, dist=None):
+    """Max of a float over ranks (a no-op for one rank)."""
+    if world <= 1 or dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t = t.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def parse_clocks(csv_text):
+    """Median SM MHz under load, max SM MHz and the throttle reasons seen."""
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in csv_text.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9 or not parts[1].split()[0].isdigit():
+            continue
+        sm.append(float(parts[1].split()[0]))
+        smax.append(float(parts[2].split()[0]))
+        for nm, flag in zip(names, parts[5:9]):
+            if flag.lower().startswith("active"):
+                reasons.add(nm)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    load = [x for x in sm if x > 0.5 * max(sm)] or sm
+    return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.out = ""
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample_setup(w, target_s=1.0):
+    """Host inputs for a bounded sample of workload w: the units [0, u_end) whose
+    oracle step takes about target_s seconds (at least one unit)."""
+    import numpy as np
+
+    import oracle
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = oracle.layout(sh, w.N, w.mode)
+    stride = O["S"]
+    rng = np.random.default_rng(0)
+    u_end = 1
+    numel = int(O["u_numel"][0])
+    # about 2.5e7 elements per second of single-core oracle work at N=4 (measured order)
+    budget = int(2.5e7 * target_s * 4 / max(w.N, 1))
+    while u_end < O["U"] and numel + int(O["u_numel"][u_end]) <= budget:
+        numel += int(O["u_numel"][u_end])
+        u_end += 1
+    lo = int(O["u_full_off"][0])
+    hi = int(O["u_full_off"][u_end - 1] + (w.N * O["u_S"][u_end - 1] if w.mode == 0 else O["u_numel"][u_end - 1]))
+    full = np.zeros(O["F"], np.float32)
+    full[lo:hi] = rng.normal(0, 0.02, hi - lo)
+    gdt = np.uint16 if str(w.grad_dtype).endswith("bfloat16") else np.float32
+    grads = []
+    for _ in range(w.N):
+        g = np.zeros(O["F"], gdt)
+        x = rng.normal(0, w.grad_std, hi - lo).astype(np.float32)
+        g[lo:hi] = oracle.bf16_rne(x) if gdt == np.uint16 else x
+        grads.append(g)
+    bf16 = gdt == np.uint16 or str(w.param_dtype).endswith("bfloat16")
+    master, param = oracle.reshard(sh, w.N, w.mode, full, stride, True, bf16)
+    st = {"sh": sh, "O": O, "stride": stride, "grads": grads, "master": master, "param": param,
+          "m": np.zeros_like(master), "v": np.zeros_like(master), "u_end": u_end, "numel": numel,
+          "out": np.zeros(O["F"], np.uint16 if bf16 else np.float32)}
+    return st
+
+
+def oracle_step(w, st, t, strategy):
+    import oracle
+    src = st["param"] if st["param"] is not None else st["master"]
+    for _ in range(2 if strategy == "full_shard" else 1):
+        oracle.unshard(st["sh"], w.N, w.mode, src, st["stride"], st["O"]["F"], 0, st["u_end"], out=st["out"])
+    oracle.rs_adamw(st["sh"], w.N, w.mode, st["grads"], st["stride"], st["master"], st["m"], st["v"],
+                    param=st["param"], hp=w.hp, step=t, ub=0, ue=st["u_end"])
+
+
+def cpu_baseline(w, strategy, min_seconds=10.0):
+    st = oracle_sample_setup(w, target_s=1.0)
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        steps += 1
+        oracle_step(w, st, steps, strategy)
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return {"value": st["numel"] * steps / el, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": f"units [0,{st['u_end']}) of {w.name} ({st['numel']} params), {steps} oracle steps "
+                      f"({strategy}), single thread, {el:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+def run_ours(args, w, rank, world, dist):
+    import torch
+
+    import fsdp_sharded_state_gb300 as fs
+    from fsdp_sharded_state_gb300 import synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    st = fs.ShardedState(w.shapes, w.unit_ids, w.N, w.mode, param_dtype=w.param_dtype, device=dev)
+    st.layout.prepare()
+    L = st.layout
+    offs = [L.tensor(t)["full_off"] for t in range(len(w.shapes))]
+    full = synth.full_params(w, st.F, offs, device=dev)
+    st.init_from_full(full)
+    del full
+    grads = synth.grad_replicas(w, st.F, 1, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    info = L.info
+    gb = 2 if w.grad_dtype == torch.bfloat16 else 4
+    pb = 2 if w.param_dtype == torch.bfloat16 else 4
+    ab = algorithmic_bytes(w.N, info["numel"], info["shard_numel"], info["full_numel"], w.mode, gb, pb)
+    n_unshard = 2 if args.strategy == "full_shard" else 1
+
+    def step(ev=None):
+        for _ in range(n_unshard):
+            st.unshard()
+        if ev is not None:
+            ev[0].record(stream)
+        st.reduce_scatter_adamw(grads, w.hp)
+        if ev is not None:
+            ev[1].record(stream)
+
+    # clock soak (untimed): bring the clocks to their working point
+    with ClockSampler(dev.index) as clk:
+        t_end = time.time() + args.soak
+        while time.time() < t_end:
+            step()
+            torch.cuda.synchronize(dev)
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+    fs.fsdp_check_status(stream)
+    ms = t0.elapsed_time(t1)
+    rs_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_max = aggregate_max(ms, world, dist)
+
+    # e2e through the public API with host buffers (pinned), copies inside every step
+    host_grads = [g.cpu().pin_memory() for g in grads]
+    out_host = torch.empty(st.param_shards.shape, dtype=st.param_shards.dtype).pin_memory()
+    h2d = sum(g.numel() * g.element_size() for g in host_grads)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for hg, dg in zip(host_grads, grads):
+            dg.copy_(hg, non_blocking=True)
+        for _ in range(n_unshard):
+            st.unshard()
+        st.reduce_scatter_adamw(grads, w.hp)
+        out_host.copy_(st.param_shards, non_blocking=True)
+
+    for _ in range(max(args.warmup, 1)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = aggregate_max(e0.elapsed_time(e1), world, dist)
+
+    clocks = parse_clocks(clk.out)
+    peak, peak_kind = load_peaks()
+    rs_avg = statistics.mean(rs_ms)
+    rs_bytes = ab["rs_adamw"]
+    achieved = rs_bytes / (rs_avg * 1e-3) / 1e9
+    P = info["numel"]
+    launches_per_step = n_unshard + 1
+    res = {
+        "metric": METRIC,
+        "value": world * P * args.steps / (ms_max * 1e-3),
+        "unit": "params/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32" if w.param_dtype == torch.float32 else "bf16+f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shapes": f"{len(w.shapes)} tensors, {P} params", "n_ranks_simulated": w.N,
+                   "layout": "flat" if w.mode == 0 else "dim0", "strategy": args.strategy,
+                   "param_dtype": str(w.param_dtype).replace("torch.", ""),
+                   "grad_dtype": str(w.grad_dtype).replace("torch.", ""),
+                   "master_moments": "float32", "step_bytes": ab["rs_adamw"] + n_unshard * ab["unshard"],
+                   "l2": "inputs larger than L2 (step touches %.2f GB)" % ((ab["rs_adamw"] + n_unshard * ab["unshard"]) / 1e9),
+                   "clock_soak_s": args.soak, "parallelism": f"replicas x{world}"},
+        "step_hbm_gbs": (ab["rs_adamw"] + n_unshard * ab["unshard"]) / (ms_max / args.steps * 1e-3) / 1e9,
+        "roofline": {"kernel": "k_rs_adamw", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_launch": rs_bytes,
+                     "launch_ms": rs_avg, "traffic": profiled_traffic("k_rs_adamw", w.name)},
+        "e2e": {"value": world * P * args.steps / (e2e_ms * 1e-3), "unit": "params/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mlp128m")
+    ap.add_argument("--strategy", choices=["full_shard", "shard_grad_op"], default="full_shard")
+    ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before warm-up")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+
+    from fsdp_sharded_state_gb300 import synth
+    w = synth.WORKLOADS[args.workload]()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        st = oracle_sample_setup(w, target_s=1.0)
+        for k in range(args.warmup):
+            oracle_step(w, st, k + 1, args.strategy)
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            oracle_step(w, st, args.warmup + k + 1, args.strategy)
+        el = time.perf_counter() - t0
+        v = st["numel"] * args.steps / el
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": "params/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "strategy": args.strategy},
+            "cpu_baseline": {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
+                             "sample": f"units [0,{st['u_end']}) of {w.name} ({st['numel']} params) per step, "
+                                       "single thread"},
+            "e2e": {"value": v, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    res = run_ours(args, w, rank, world, dist)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        res["cpu_baseline"] = cpu_baseline(w, args.strategy, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(res))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

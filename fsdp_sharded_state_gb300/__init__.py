@@ -1,0 +1,247 @@
+"""fsdp_sharded_state_gb300 -- the FSDP / ZeRO-3 sharded-state step on one GB300.
+
+Thin ctypes binding of ``libfsdpstate.so`` (C ABI in ``include/fsdp_state.h``).
+The functions here carry the C names and only marshal arguments: torch tensors
+(or raw device pointers) in, status codes checked, ``FsdpError`` out.  Every step
+of the path runs in the library's CUDA kernels; there is no CPU fallback -- if the
+library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libfsdpstate.so")
+
+FSDP_FLAT, FSDP_DIM0 = 0, 1
+FSDP_F32, FSDP_BF16 = 0, 1
+MODES = {"flat": FSDP_FLAT, "dim0": FSDP_DIM0}
+
+FSDP_OK = 0
+STATUS = {0: "FSDP_OK", -1: "FSDP_EINVAL", -2: "FSDP_EDTYPE", -3: "FSDP_ESHAPE", -4: "FSDP_EALIGN",
+          -5: "FSDP_EOVERFLOW", -6: "FSDP_ECUDA", -7: "FSDP_ETIMEOUT", -8: "FSDP_ENOMEM"}
+
+# Every symbol include/fsdp_state.h declares.
+EXPORTS = ("fsdp_layout_create", "fsdp_layout_destroy", "fsdp_layout_query", "fsdp_layout_unit",
+           "fsdp_layout_tensor", "fsdp_layout_segment", "fsdp_state_bytes", "fsdp_layout_prepare",
+           "fsdp_unshard", "fsdp_reduce_scatter_adamw", "fsdp_reshard", "fsdp_check_status",
+           "fsdp_error_string", "fsdp_last_cuda_error")
+
+
+class FsdpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)}"
+        if status == -6 and _lib is not None:
+            msg += f" ({_lib.fsdp_last_cuda_error().decode()})"
+        super().__init__(msg)
+
+
+class LayoutInfo(C.Structure):
+    _fields_ = [("n_tensors", C.c_int32), ("n_units", C.c_int32), ("n_ranks", C.c_int32), ("mode", C.c_int32),
+                ("numel", C.c_int64), ("shard_numel", C.c_int64), ("shard_stride", C.c_int64),
+                ("full_numel", C.c_int64), ("pad_numel", C.c_int64), ("n_segments", C.c_int64)]
+
+
+class AdamWHparams(C.Structure):
+    _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
+                ("weight_decay", C.c_float)]
+
+
+_lib: Optional[C.CDLL] = None
+
+
+def lib() -> C.CDLL:
+    """The loaded libfsdpstate; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libfsdpstate is not built ({LIB_PATH} missing): run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+        L.fsdp_layout_create.argtypes = [i32, vp, vp, vp, vp, i32, i32, C.POINTER(vp)]
+        L.fsdp_layout_destroy.argtypes = [vp]
+        L.fsdp_layout_destroy.restype = None
+        L.fsdp_layout_query.argtypes = [vp, C.POINTER(LayoutInfo)]
+        L.fsdp_layout_unit.argtypes = [vp, i32] + [C.POINTER(i64)] * 5
+        L.fsdp_layout_tensor.argtypes = [vp, i32, C.POINTER(i32)] + [C.POINTER(i64)] * 4
+        L.fsdp_layout_segment.argtypes = [vp, i32, i32] + [C.POINTER(i64)] * 4
+        L.fsdp_state_bytes.argtypes = [vp, i32, i32, i32, i64, i64, i64, i64, C.POINTER(i64)]
+        L.fsdp_layout_prepare.argtypes = [vp]
+        L.fsdp_unshard.argtypes = [vp, i32, i32, vp, vp, i32, vp]
+        L.fsdp_reduce_scatter_adamw.argtypes = [vp, i32, i32, C.POINTER(vp), i32, vp, vp, vp, vp, vp,
+                                                C.POINTER(AdamWHparams), i64, vp]
+        L.fsdp_reshard.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
+        L.fsdp_check_status.argtypes = [vp]
+        L.fsdp_error_string.argtypes = [C.c_int]
+        L.fsdp_error_string.restype = C.c_char_p
+        L.fsdp_last_cuda_error.argtypes = []
+        L.fsdp_last_cuda_error.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != FSDP_OK:
+        raise FsdpError(rc, where)
+
+
+def _ptr(x) -> Optional[int]:
+    """Device address of a tensor (or an int address); None stays NULL."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if not x.is_contiguous():
+        raise ValueError("buffers must be contiguous")
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return FSDP_F32
+    if t.dtype == torch.bfloat16:
+        return FSDP_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+
+
+class Layout:
+    """An fsdp_layout: shapes + unit ids + N + mode -> offsets, padding, segments."""
+
+    def __init__(self, shapes: Sequence[Sequence[int]], unit_ids: Optional[Sequence[int]] = None,
+                 n_ranks: int = 1, mode: int = FSDP_FLAT, dtypes: Optional[Sequence[int]] = None):
+        shapes = [tuple(int(d) for d in s) for s in shapes]
+        T = len(shapes)
+        if unit_ids is None:
+            unit_ids = [0] * T
+        ndim = (C.c_int32 * max(T, 1))(*[len(s) for s in shapes])
+        flat = [d for s in shapes for d in s] or [0]
+        dims = (C.c_int64 * len(flat))(*flat)
+        units = (C.c_int32 * max(T, 1))(*unit_ids)
+        dt = None if dtypes is None else (C.c_int32 * max(T, 1))(*dtypes)
+        h = C.c_void_p()
+        self._h = None
+        _check(lib().fsdp_layout_create(T, ndim, dims, units, dt, n_ranks, mode, C.byref(h)),
+               "fsdp_layout_create")
+        self._h = h
+        self.shapes, self.unit_ids, self.n_ranks, self.mode = shapes, list(unit_ids), n_ranks, mode
+        info = LayoutInfo()
+        _check(lib().fsdp_layout_query(self._h, C.byref(info)), "fsdp_layout_query")
+        self.info = {k: getattr(info, k) for k, _ in LayoutInfo._fields_}
+
+    # -- queries --------------------------------------------------------------
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def N(self) -> int:
+        return self.info["n_ranks"]
+
+    @property
+    def stride(self) -> int:
+        return self.info["shard_stride"]
+
+    @property
+    def n_units(self) -> int:
+        return self.info["n_units"]
+
+    def unit(self, u: int) -> dict:
+        v = [C.c_int64() for _ in range(5)]
+        _check(lib().fsdp_layout_unit(self._h, u, *[C.byref(x) for x in v]), "fsdp_layout_unit")
+        return dict(zip(("shard_off", "shard_numel", "full_off", "full_numel", "numel"), (x.value for x in v)))
+
+    def tensor(self, t: int) -> dict:
+        u = C.c_int32()
+        v = [C.c_int64() for _ in range(4)]
+        _check(lib().fsdp_layout_tensor(self._h, t, C.byref(u), *[C.byref(x) for x in v]), "fsdp_layout_tensor")
+        d = dict(zip(("numel", "full_off", "shard_off", "rows_per_rank"), (x.value for x in v)))
+        d["unit"] = u.value
+        return d
+
+    def segment(self, t: int, r: int) -> dict:
+        v = [C.c_int64() for _ in range(4)]
+        _check(lib().fsdp_layout_segment(self._h, t, r, *[C.byref(x) for x in v]), "fsdp_layout_segment")
+        return dict(zip(("shard_off", "full_off", "len", "pad"), (x.value for x in v)))
+
+    def state_bytes(self, stage: int, rank: int, physical: bool, param_bytes: int, grad_bytes: int,
+                    optim_bytes: int, step_bytes: int = 0):
+        out = (C.c_int64 * 3)()
+        _check(lib().fsdp_state_bytes(self._h, stage, rank, int(physical), param_bytes, grad_bytes, optim_bytes,
+                                      step_bytes, out), "fsdp_state_bytes")
+        return tuple(out)
+
+    def prepare(self) -> None:
+        _check(lib().fsdp_layout_prepare(self._h), "fsdp_layout_prepare")
+
+    def close(self) -> None:
+        if self._h is not None and _lib is not None:
+            _lib.fsdp_layout_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# -- the C names ----------------------------------------------------------------
+def fsdp_layout_create(shapes, unit_ids=None, n_ranks=1, mode=FSDP_FLAT, dtypes=None) -> Layout:
+    return Layout(shapes, unit_ids, n_ranks, mode, dtypes)
+
+
+def fsdp_unshard(layout: Layout, unit_begin: int, unit_end: int, param_shards, full, stream=None,
+                 elem_dtype: Optional[int] = None) -> None:
+    if elem_dtype is None:
+        elem_dtype = _dtype_code(param_shards)
+    _check(lib().fsdp_unshard(layout.handle, unit_begin, unit_end, _ptr(param_shards), _ptr(full), elem_dtype,
+                              _stream(stream)), "fsdp_unshard")
+
+
+def fsdp_reduce_scatter_adamw(layout: Layout, unit_begin: int, unit_end: int, grad_replicas, master, exp_avg,
+                              exp_avg_sq, param_shards=None, grad_shard_out=None,
+                              hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step: int = 1, stream=None,
+                              grad_dtype: Optional[int] = None) -> None:
+    if len(grad_replicas) != layout.N:
+        raise ValueError(f"need {layout.N} gradient replicas, got {len(grad_replicas)}")
+    if grad_dtype is None:
+        grad_dtype = _dtype_code(grad_replicas[0])
+    arr = (C.c_void_p * layout.N)(*[_ptr(g) for g in grad_replicas])
+    h = hp if isinstance(hp, AdamWHparams) else AdamWHparams(*hp)
+    _check(lib().fsdp_reduce_scatter_adamw(layout.handle, unit_begin, unit_end, arr, grad_dtype, _ptr(master),
+                                           _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(param_shards),
+                                           _ptr(grad_shard_out), C.byref(h), step, _stream(stream)),
+           "fsdp_reduce_scatter_adamw")
+
+
+def fsdp_reshard(layout: Layout, unit_begin: int, unit_end: int, full=None, master=None, param_shards=None,
+                 stream=None, full_dtype: Optional[int] = None) -> None:
+    if full is not None and full_dtype is None:
+        full_dtype = _dtype_code(full)
+    _check(lib().fsdp_reshard(layout.handle, unit_begin, unit_end, _ptr(full), full_dtype or 0, _ptr(master),
+                              _ptr(param_shards), _stream(stream)), "fsdp_reshard")
+
+
+def fsdp_check_status(stream=None) -> None:
+    _check(lib().fsdp_check_status(_stream(stream)), "fsdp_check_status")
+
+
+def fsdp_error_string(status: int) -> str:
+    return lib().fsdp_error_string(status).decode()
+
+
+from .state import ShardedState  # noqa: E402  (harness over the calls above)

@@ -1,0 +1,335 @@
+// api.cu -- the extern "C" entry points of libfsdpstate (declared in
+// include/fsdp_state.h): argument validation, per-device segment tables, the
+// AdamW step constants and the kernel launches.  Every check runs before the
+// first launch, so an error return leaves all outputs untouched.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fsdp_state.h"
+#include "kernels.hpp"
+#include "layout.hpp"
+
+using fsdp::Seg;
+using fsdp::SegList;
+
+namespace {
+
+thread_local char g_cuda_err[256] = "";
+
+int cuda_fail(cudaError_t e, const char* where) {
+    std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s (%s)", where, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return FSDP_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device copy of the layout's three segment lists for the current device.
+int device_tables(const fsdp_layout* Lc, const Seg** base) {
+    fsdp_layout* L = const_cast<fsdp_layout*>(Lc);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(L->mu);
+    auto it = L->dev.find(dev);
+    if (it != L->dev.end()) {
+        *base = it->second.base;
+        return FSDP_OK;
+    }
+    const size_t n = L->data.segs.size() + L->gather.segs.size() + L->pad.segs.size();
+    Seg* d = nullptr;
+    e = cudaMalloc(&d, n * sizeof(Seg));
+    if (e != cudaSuccess) {
+        cuda_fail(e, "cudaMalloc(segment tables)");
+        return FSDP_ENOMEM;
+    }
+    std::vector<Seg> h;
+    h.reserve(n);
+    for (const SegList* l : {&L->data, &L->gather, &L->pad}) h.insert(h.end(), l->segs.begin(), l->segs.end());
+    e = cudaMemcpy(d, h.data(), n * sizeof(Seg), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(d);
+        return cuda_fail(e, "cudaMemcpy(segment tables)");
+    }
+    L->dev[dev] = fsdp::DeviceTables{d};
+    *base = d;
+    return FSDP_OK;
+}
+
+// Segment range and tile range of units [ub, ue) in one list.
+struct Range {
+    const Seg* segs;
+    int64_t tile_base, n_tiles;
+};
+Range range_of(const SegList& l, const Seg* dev_base, int32_t ub, int32_t ue) {
+    const int32_t sb = l.unit_begin[ub], se = l.unit_begin[ue];
+    const int64_t t0 = l.segs[sb].tile0, t1 = l.segs[se].tile0;
+    return Range{dev_base + l.dev_off + sb, t0, t1 - t0};
+}
+
+int check_units(const fsdp_layout* L, int32_t ub, int32_t ue) {
+    if (!L) return FSDP_EINVAL;
+    if (ub < 0 || ue > L->U || ub > ue) return FSDP_EINVAL;
+    return FSDP_OK;
+}
+
+int check_ptr(const void* p) {
+    if (!p) return FSDP_EINVAL;
+    if (!aligned16(p)) return FSDP_EALIGN;
+    return FSDP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fsdp_layout_create(int32_t n_tensors, const int32_t* ndim, const int64_t* dims, const int32_t* unit_id,
+                       const int32_t* dtype, int32_t n_ranks, int32_t mode, fsdp_layout** out) {
+    if (!out) return FSDP_EINVAL;
+    if (n_tensors > (1 << 24)) return FSDP_EINVAL;
+    fsdp_layout* L = new (std::nothrow) fsdp_layout();
+    if (!L) return FSDP_ENOMEM;
+    int rc;
+    try {
+        rc = fsdp::build_layout(L, n_tensors, ndim, dims, unit_id, dtype, n_ranks, mode);
+    } catch (const std::bad_alloc&) {
+        rc = FSDP_ENOMEM;
+    }
+    if (rc != FSDP_OK) {
+        delete L;
+        return rc;
+    }
+    *out = L;
+    return FSDP_OK;
+}
+
+void fsdp_layout_destroy(fsdp_layout* L) {
+    if (!L) return;
+    int cur = -1;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    for (auto& kv : L->dev) {
+        if (cudaSetDevice(kv.first) == cudaSuccess) cudaFree(kv.second.base);
+    }
+    if (have_cur && !L->dev.empty()) cudaSetDevice(cur);
+    delete L;
+}
+
+int fsdp_layout_query(const fsdp_layout* L, fsdp_layout_info* o) {
+    if (!L || !o) return FSDP_EINVAL;
+    o->n_tensors = L->T;
+    o->n_units = L->U;
+    o->n_ranks = L->N;
+    o->mode = L->mode;
+    o->numel = L->P;
+    o->shard_numel = L->S;
+    o->shard_stride = L->stride;
+    o->full_numel = L->F;
+    o->pad_numel = int64_t(L->N) * L->S - L->P;
+    o->n_segments = L->n_data_segments;
+    return FSDP_OK;
+}
+
+int fsdp_layout_unit(const fsdp_layout* L, int32_t u, int64_t* shard_off, int64_t* shard_numel,
+                     int64_t* full_off, int64_t* full_numel, int64_t* numel) {
+    if (!L || u < 0 || u >= L->U) return FSDP_EINVAL;
+    if (shard_off) *shard_off = L->u_shard_off[u];
+    if (shard_numel) *shard_numel = L->u_S[u];
+    if (full_off) *full_off = L->u_full_off[u];
+    if (full_numel) *full_numel = L->mode == FSDP_FLAT ? int64_t(L->N) * L->u_S[u] : L->u_numel[u];
+    if (numel) *numel = L->u_numel[u];
+    return FSDP_OK;
+}
+
+int fsdp_layout_tensor(const fsdp_layout* L, int32_t t, int32_t* unit, int64_t* numel, int64_t* full_off,
+                       int64_t* shard_off, int64_t* rows_per_rank) {
+    if (!L || t < 0 || t >= L->T) return FSDP_EINVAL;
+    if (unit) *unit = L->unit[t];
+    if (numel) *numel = L->numel[t];
+    if (full_off) *full_off = L->t_full_off[t];
+    if (shard_off) *shard_off = L->mode == FSDP_DIM0 ? L->t_shard_off[t] : -1;
+    if (rows_per_rank) *rows_per_rank = L->mode == FSDP_DIM0 ? L->rows[t] : -1;
+    return FSDP_OK;
+}
+
+int fsdp_layout_segment(const fsdp_layout* L, int32_t t, int32_t r, int64_t* shard_off, int64_t* full_off,
+                        int64_t* len, int64_t* pad) {
+    if (!L || t < 0 || t >= L->T || r < 0 || r >= L->N) return FSDP_EINVAL;
+    int64_t so, fo, n, pd;
+    if (L->mode == FSDP_FLAT) {
+        const int32_t u = L->unit[t];
+        const int64_t Su = L->u_S[u];
+        const int64_t a = L->t_unit_off[t], b = a + L->numel[t];   // tensor range in the unit's flat
+        const int64_t ra = int64_t(r) * Su, rb = ra + Su;          // rank range
+        int64_t lo = a < ra ? ra : a;
+        if (lo > rb) lo = rb;
+        const int64_t hi = b < rb ? b : rb;
+        n = hi > lo ? hi - lo : 0;
+        so = L->u_shard_off[u] + (lo - ra);
+        fo = L->u_full_off[u] + lo;
+        pd = 0;
+    } else {
+        const int64_t c = L->rows[t];
+        const int64_t rb = std::min<int64_t>(int64_t(r) * c, L->d0[t]);
+        const int64_t re = std::min<int64_t>(int64_t(r + 1) * c, L->d0[t]);
+        n = (re - rb) * L->inner[t];
+        so = L->t_shard_off[t];
+        fo = L->t_full_off[t] + rb * L->inner[t];
+        pd = c * L->inner[t] - n;
+    }
+    if (shard_off) *shard_off = so;
+    if (full_off) *full_off = fo;
+    if (len) *len = n;
+    if (pad) *pad = pd;
+    return FSDP_OK;
+}
+
+int fsdp_state_bytes(const fsdp_layout* L, int32_t stage, int32_t rank, int32_t physical, int64_t pb,
+                     int64_t gb, int64_t ob, int64_t step_bytes, int64_t out[3]) {
+    if (!L || !out || stage < 0 || stage > 3 || rank < 0 || rank >= L->N) return FSDP_EINVAL;
+    if (pb < 0 || gb < 0 || ob < 0 || step_bytes < 0) return FSDP_EINVAL;
+    int64_t own = 0;
+    if (physical) {
+        own = L->S;
+    } else {
+        // Logical elements of this rank: the data segments in its row.
+        const int64_t lo = int64_t(rank) * L->stride, hi = lo + L->stride;
+        for (size_t i = 0; i + 1 < L->data.segs.size(); ++i) {
+            const Seg& s = L->data.segs[i];
+            if (s.shard >= lo && s.shard < hi) own += s.len;
+        }
+    }
+    const int64_t sharded_or_full[2] = {L->P, own};
+    out[0] = sharded_or_full[stage >= 3] * pb;
+    out[1] = sharded_or_full[stage >= 2] * gb;
+    out[2] = sharded_or_full[stage >= 1] * ob + int64_t(L->T) * step_bytes;
+    return FSDP_OK;
+}
+
+int fsdp_layout_prepare(fsdp_layout* L) {
+    if (!L) return FSDP_EINVAL;
+    const Seg* base = nullptr;
+    return device_tables(L, &base);
+}
+
+int fsdp_unshard(const fsdp_layout* L, int32_t ub, int32_t ue, const void* shards, void* full,
+                 int32_t elem_dtype, fsdp_stream_t stream) {
+    int rc = check_units(L, ub, ue);
+    if (rc) return rc;
+    if (elem_dtype != FSDP_F32 && elem_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if ((rc = check_ptr(shards)) || (rc = check_ptr(full))) return rc;
+    const Seg* base = nullptr;
+    if ((rc = device_tables(L, &base))) return rc;
+    const Range R = range_of(L->gather, base, ub, ue);
+    const cudaError_t e = fsdp::launch_unshard(R.segs, R.tile_base, R.n_tiles, elem_dtype == FSDP_BF16, shards,
+                                               full, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "k_unshard launch");
+}
+
+int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, const void* const* grads,
+                              int32_t grad_dtype, float* master, float* exp_avg, float* exp_avg_sq,
+                              void* param_shards, float* grad_shard_out, const fsdp_adamw_hparams* hp,
+                              int64_t step, fsdp_stream_t stream) {
+    int rc = check_units(L, ub, ue);
+    if (rc) return rc;
+    if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if (!grads || !hp || step < 1) return FSDP_EINVAL;
+    for (int32_t q = 0; q < L->N; ++q)
+        if ((rc = check_ptr(grads[q]))) return rc;
+    if ((rc = check_ptr(master)) || (rc = check_ptr(exp_avg)) || (rc = check_ptr(exp_avg_sq))) return rc;
+    if (param_shards && !aligned16(param_shards)) return FSDP_EALIGN;
+    if (grad_shard_out && !aligned16(grad_shard_out)) return FSDP_EALIGN;
+    const float lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
+    if (!std::isfinite(lr) || !std::isfinite(b1) || !std::isfinite(b2) || !std::isfinite(eps) ||
+        !std::isfinite(wd))
+        return FSDP_EINVAL;
+    if (lr < 0.f || b1 < 0.f || b1 >= 1.f || b2 < 0.f || b2 >= 1.f || eps <= 0.f || wd < 0.f ||
+        double(lr) * double(wd) > 1.0)
+        return FSDP_EINVAL;
+
+    // Step constants: formed in double from the fp32 hyper-parameters, rounded once.
+    fsdp::AdamScal sc;
+    const double bc1 = 1.0 - std::pow(double(b1), double(step));
+    const double bc2 = 1.0 - std::pow(double(b2), double(step));
+    sc.decay = float(1.0 - double(lr) * double(wd));
+    sc.om1 = float(1.0 - double(b1));
+    sc.om2 = float(1.0 - double(b2));
+    sc.step_size = float(double(lr) / bc1);
+    sc.bc2s = float(std::sqrt(bc2));
+    sc.beta1 = b1;
+    sc.beta2 = b2;
+    sc.eps = eps;
+    sc.nf = float(L->N);
+
+    fsdp::GradPtrs gp{};
+    for (int32_t q = 0; q < L->N; ++q) gp.p[q] = grads[q];
+
+    const Seg* base = nullptr;
+    if ((rc = device_tables(L, &base))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const Range R = range_of(L->data, base, ub, ue);
+    cudaError_t e = fsdp::launch_rs_adamw(R.segs, R.tile_base, R.n_tiles, grad_dtype == FSDP_BF16, gp, L->N,
+                                          master, exp_avg, exp_avg_sq, static_cast<uint16_t*>(param_shards),
+                                          grad_shard_out, sc, st);
+    if (e != cudaSuccess) return cuda_fail(e, "k_rs_adamw launch");
+    if (grad_shard_out) {
+        const Range P = range_of(L->pad, base, ub, ue);
+        e = fsdp::launch_zero_pad(P.segs, P.tile_base, P.n_tiles, grad_shard_out, nullptr, st);
+        if (e != cudaSuccess) return cuda_fail(e, "k_zero_pad launch");
+    }
+    return FSDP_OK;
+}
+
+int fsdp_reshard(const fsdp_layout* L, int32_t ub, int32_t ue, const void* full, int32_t full_dtype,
+                 float* master, void* param_shards, fsdp_stream_t stream) {
+    int rc = check_units(L, ub, ue);
+    if (rc) return rc;
+    if (!full) return FSDP_OK;   // release only: the full buffer is the caller's
+    if (full_dtype != FSDP_F32 && full_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if ((rc = check_ptr(full))) return rc;
+    if (!master && !param_shards) return FSDP_EINVAL;
+    if ((master && !aligned16(master)) || (param_shards && !aligned16(param_shards))) return FSDP_EALIGN;
+    const Seg* base = nullptr;
+    if ((rc = device_tables(L, &base))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const Range D = range_of(L->data, base, ub, ue);
+    cudaError_t e = fsdp::launch_reshard(D.segs, D.tile_base, D.n_tiles, full_dtype == FSDP_BF16, full, master,
+                                         static_cast<uint16_t*>(param_shards), st);
+    if (e != cudaSuccess) return cuda_fail(e, "k_reshard launch");
+    const Range P = range_of(L->pad, base, ub, ue);
+    e = fsdp::launch_zero_pad(P.segs, P.tile_base, P.n_tiles, master, static_cast<uint16_t*>(param_shards), st);
+    if (e != cudaSuccess) return cuda_fail(e, "k_zero_pad launch");
+    return FSDP_OK;
+}
+
+int fsdp_check_status(fsdp_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetLastError");
+    return FSDP_OK;
+}
+
+const char* fsdp_error_string(int status) {
+    switch (status) {
+        case FSDP_OK: return "FSDP_OK: success";
+        case FSDP_EINVAL: return "FSDP_EINVAL: invalid argument";
+        case FSDP_EDTYPE: return "FSDP_EDTYPE: dtype mismatch or unsupported dtype";
+        case FSDP_ESHAPE: return "FSDP_ESHAPE: inconsistent shapes or unit ids";
+        case FSDP_EALIGN: return "FSDP_EALIGN: buffer not 16-byte aligned";
+        case FSDP_EOVERFLOW: return "FSDP_EOVERFLOW: element count overflows int64";
+        case FSDP_ECUDA: return "FSDP_ECUDA: CUDA error";
+        case FSDP_ETIMEOUT: return "FSDP_ETIMEOUT: bounded device wait gave up";
+        case FSDP_ENOMEM: return "FSDP_ENOMEM: allocation failed";
+        default: return "unknown fsdp_status";
+    }
+}
+
+const char* fsdp_last_cuda_error(void) { return g_cuda_err; }
+
+}  // extern "C"

@@ -1,0 +1,23 @@
+// kernels.hpp -- host-side launchers of the libfsdpstate kernels (kernels.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace fsdp {
+
+cudaError_t launch_rs_adamw(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
+                            const GradPtrs& gp, int N, float* master, float* m, float* v,
+                            uint16_t* param, float* gout, const AdamScal& sc, cudaStream_t st);
+
+cudaError_t launch_unshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16,
+                           const void* src, void* dst, cudaStream_t st);
+
+cudaError_t launch_reshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool full_bf16,
+                           const void* full, float* master, uint16_t* param, cudaStream_t st);
+
+cudaError_t launch_zero_pad(const Seg* segs, int64_t tile_base, int64_t n_tiles, float* a32,
+                            uint16_t* a16, cudaStream_t st);
+
+}  // namespace fsdp

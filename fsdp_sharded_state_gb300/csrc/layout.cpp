@@ -1,0 +1,186 @@
+// layout.cpp -- host-side layout engine of libfsdpstate (no CUDA calls).
+//
+// FLAT ("第18章 FSDP：ZeRO 风格的参数分片" §18.12; "NCCL ZeRO/FSDP state sharding",
+// section "FlatParameter 与 Padding"): the tensors of one unit are flattened and
+// concatenated into P_u elements, padded at the end to N*S_u with
+// S_u = ceil(P_u/N); rank r owns flat elements [r*S_u, (r+1)*S_u).
+// DIM0 ("PyTorch FSDP2 后端特性介绍", section "DTensor"; torchtitan FSDP2 article
+// §2.3): each tensor with d0 rows of `inner` elements gets a slot of c = ceil(d0/N)
+// rows on every rank; rank r owns rows [min(rc,d0), min((r+1)c,d0)).
+#include "layout.hpp"
+
+#include <algorithm>
+
+#include "../../include/fsdp_state.h"
+
+namespace fsdp {
+namespace {
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
+bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow(a, b, out); }
+
+void push(SegList& l, int64_t shard, int64_t full, int64_t len) {
+    if (len <= 0) return;
+    l.segs.push_back(Seg{shard, full, len, 0});
+}
+
+void finish(SegList& l) {
+    int64_t t = 0;
+    for (Seg& s : l.segs) {
+        s.tile0 = t;
+        t += seg_tiles(s.shard, s.len);
+    }
+    l.segs.push_back(Seg{0, -1, 0, t});   // sentinel: tile0 = total tiles
+}
+
+}  // namespace
+
+int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* dims,
+                 const int32_t* unit_id, const int32_t* dtype, int32_t N, int32_t mode) {
+    if (T < 1 || !ndim || !dims || !unit_id) return FSDP_EINVAL;
+    if (N < 1 || N > FSDP_MAX_RANKS) return FSDP_EINVAL;
+    if (mode != FSDP_FLAT && mode != FSDP_DIM0) return FSDP_EINVAL;
+    if (unit_id[0] != 0) return FSDP_ESHAPE;
+    for (int32_t t = 1; t < T; ++t)
+        if (unit_id[t] != unit_id[t - 1] && unit_id[t] != unit_id[t - 1] + 1) return FSDP_ESHAPE;
+    if (dtype)
+        for (int32_t t = 0; t < T; ++t)
+            if (dtype[t] != FSDP_F32 && dtype[t] != FSDP_BF16) return FSDP_EDTYPE;
+
+    L->T = T; L->N = N; L->mode = mode; L->U = unit_id[T - 1] + 1;
+    const int32_t U = L->U;
+    L->numel.assign(T, 0); L->d0.assign(T, 0); L->inner.assign(T, 0); L->rows.assign(T, 0);
+    L->t_full_off.assign(T, 0); L->t_shard_off.assign(T, -1); L->t_unit_off.assign(T, 0);
+    L->unit.assign(unit_id, unit_id + T);
+    L->dtype.assign(T, FSDP_F32);
+    if (dtype) L->dtype.assign(dtype, dtype + T);
+    L->u_numel.assign(U, 0); L->u_S.assign(U, 0); L->u_shard_off.assign(U, 0); L->u_full_off.assign(U, 0);
+
+    // Shapes.
+    int64_t pos = 0;
+    for (int32_t t = 0; t < T; ++t) {
+        if (ndim[t] < 0 || ndim[t] > 16) return FSDP_ESHAPE;
+        int64_t n = 1, in = 1;
+        for (int32_t k = 0; k < ndim[t]; ++k) {
+            const int64_t d = dims[pos + k];
+            if (d < 0) return FSDP_ESHAPE;
+            if (!mul_ok(n, d, &n)) return FSDP_EOVERFLOW;
+            if (k > 0 && !mul_ok(in, d, &in)) return FSDP_EOVERFLOW;
+        }
+        L->numel[t] = n;
+        L->d0[t] = ndim[t] == 0 ? 1 : dims[pos];
+        L->inner[t] = ndim[t] == 0 ? 1 : in;
+        pos += ndim[t];
+    }
+
+    // FlatParameter requires one dtype per unit.
+    if (mode == FSDP_FLAT)
+        for (int32_t t = 1; t < T; ++t)
+            if (L->unit[t] == L->unit[t - 1] && L->dtype[t] != L->dtype[t - 1]) return FSDP_EDTYPE;
+
+    int64_t P = 0;
+    for (int32_t t = 0; t < T; ++t) {
+        const int32_t u = L->unit[t];
+        L->t_unit_off[t] = L->u_numel[u];
+        if (!add_ok(L->u_numel[u], L->numel[t], &L->u_numel[u])) return FSDP_EOVERFLOW;
+        if (!add_ok(P, L->numel[t], &P)) return FSDP_EOVERFLOW;
+    }
+    L->P = P;
+
+    if (mode == FSDP_FLAT) {
+        int64_t so = 0, fo = 0;
+        for (int32_t u = 0; u < U; ++u) {
+            L->u_S[u] = (L->u_numel[u] + N - 1) / N;
+            L->u_shard_off[u] = so;
+            L->u_full_off[u] = fo;
+            int64_t slot;
+            if (!mul_ok(L->u_S[u], N, &slot)) return FSDP_EOVERFLOW;
+            if (!add_ok(so, L->u_S[u], &so) || !add_ok(fo, slot, &fo)) return FSDP_EOVERFLOW;
+        }
+        L->S = so; L->F = fo;
+        for (int32_t t = 0; t < T; ++t)
+            L->t_full_off[t] = L->u_full_off[L->unit[t]] + L->t_unit_off[t];
+    } else {
+        int64_t so = 0, fo = 0;
+        for (int32_t t = 0; t < T; ++t) {
+            L->rows[t] = (L->d0[t] + N - 1) / N;
+            int64_t slot;
+            if (!mul_ok(L->rows[t], L->inner[t], &slot)) return FSDP_EOVERFLOW;
+            L->t_shard_off[t] = so;
+            L->t_full_off[t] = fo;
+            if (!add_ok(so, slot, &so) || !add_ok(fo, L->numel[t], &fo)) return FSDP_EOVERFLOW;
+        }
+        L->S = so; L->F = fo;
+        for (int32_t t = 0; t < T; ++t) {
+            const int32_t u = L->unit[t];
+            if (t == 0 || L->unit[t - 1] != u) {
+                L->u_shard_off[u] = L->t_shard_off[t];
+                L->u_full_off[u] = L->t_full_off[t];
+            }
+            L->u_S[u] += L->rows[t] * L->inner[t];
+        }
+    }
+
+    // Physical row stride: S rounded up to 64 elements, so that every rank row
+    // starts 128-byte aligned for bf16 and 256-byte aligned for fp32.
+    int64_t stride;
+    if (!add_ok(L->S, 63, &stride)) return FSDP_EOVERFLOW;
+    stride = stride / 64 * 64;
+    int64_t total;
+    if (!mul_ok(stride, N, &total)) return FSDP_EOVERFLOW;
+    if (!mul_ok(total, 4, &total)) return FSDP_EOVERFLOW;   // fp32 byte size must fit too
+    if (!mul_ok(L->F, 4, &total)) return FSDP_EOVERFLOW;
+    L->stride = stride;
+
+    // Segment lists, per unit: rank-major, then tensor order.
+    for (SegList* l : {&L->data, &L->gather, &L->pad}) {
+        l->segs.clear();
+        l->unit_begin.assign(U + 1, 0);
+    }
+    int64_t n_data = 0;
+    for (int32_t u = 0; u < U; ++u) {
+        L->data.unit_begin[u] = int32_t(L->data.segs.size());
+        L->gather.unit_begin[u] = int32_t(L->gather.segs.size());
+        L->pad.unit_begin[u] = int32_t(L->pad.segs.size());
+        for (int32_t r = 0; r < N; ++r) {
+            const int64_t row = int64_t(r) * stride;
+            if (mode == FSDP_FLAT) {
+                const int64_t Su = L->u_S[u];
+                const int64_t first = int64_t(r) * Su;                     // flat position
+                const int64_t own = std::max<int64_t>(0, std::min(Su, L->u_numel[u] - first));
+                const int64_t sh = row + L->u_shard_off[u];
+                const int64_t fu = L->u_full_off[u] + first;
+                push(L->data, sh, fu, own);
+                push(L->gather, sh, fu, Su);
+                push(L->pad, sh + own, -1, Su - own);
+                if (own > 0) ++n_data;
+            } else {
+                for (int32_t t = 0; t < T; ++t) {
+                    if (L->unit[t] != u) continue;
+                    const int64_t c = L->rows[t];
+                    const int64_t rb = std::min<int64_t>(int64_t(r) * c, L->d0[t]);
+                    const int64_t re = std::min<int64_t>(int64_t(r + 1) * c, L->d0[t]);
+                    const int64_t own = (re - rb) * L->inner[t];
+                    const int64_t sh = row + L->t_shard_off[t];
+                    const int64_t fu = L->t_full_off[t] + rb * L->inner[t];
+                    push(L->data, sh, fu, own);
+                    push(L->gather, sh, fu, own);
+                    push(L->pad, sh + own, -1, c * L->inner[t] - own);
+                    if (own > 0) ++n_data;
+                }
+            }
+            if (u == U - 1) push(L->pad, row + L->S, -1, stride - L->S);   // row tail
+        }
+    }
+    for (SegList* l : {&L->data, &L->gather, &L->pad}) {
+        l->unit_begin[U] = int32_t(l->segs.size());
+        finish(*l);
+    }
+    L->gather.dev_off = int64_t(L->data.segs.size());
+    L->pad.dev_off = L->gather.dev_off + int64_t(L->gather.segs.size());
+    L->data.dev_off = 0;
+    L->n_data_segments = n_data;
+    return FSDP_OK;
+}
+
+}  // namespace fsdp

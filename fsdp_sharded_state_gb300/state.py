@@ -1,0 +1,84 @@
+"""ShardedState: the buffers of one sharded model state and the step that uses them.
+
+Harness over the C-ABI calls: it allocates the [N][stride] shard arrays and the
+full buffer with torch (device memory is all torch is used for) and issues the
+library calls of one training step in the order the FSDP pages give
+("第18章 FSDP：ZeRO 风格的参数分片" §18.2/§18.3/§18.21; "NCCL ZeRO/FSDP state
+sharding", sections "ZeRO-2 方向" and "ZeRO-3 方向"):
+
+    FULL_SHARD     unshard (forward) -> unshard (backward) -> reduce-scatter+AdamW+cast
+    SHARD_GRAD_OP  unshard (forward)                      -> reduce-scatter+AdamW+cast
+
+The gradients are the caller's: in a model they come out of backward; here they
+are given as N full-layout replicas, one per simulated rank.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import (FSDP_BF16, FSDP_F32, FSDP_FLAT, Layout, fsdp_reduce_scatter_adamw, fsdp_reshard,
+               fsdp_unshard)
+
+STRATEGIES = {"full_shard": 2, "shard_grad_op": 1}   # all-gathers per step
+
+
+class ShardedState:
+    def __init__(self, shapes: Sequence[Sequence[int]], unit_ids: Optional[Sequence[int]], n_ranks: int,
+                 mode: int = FSDP_FLAT, param_dtype: torch.dtype = torch.bfloat16, device="cuda",
+                 with_grad_out: bool = False):
+        if param_dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError("param_dtype must be bfloat16 or float32")
+        code = FSDP_BF16 if param_dtype == torch.bfloat16 else FSDP_F32
+        self.layout = Layout(shapes, unit_ids, n_ranks, mode, [code] * len(shapes))
+        self.N, self.stride = n_ranks, self.layout.stride
+        self.F = self.layout.info["full_numel"]
+        self.P = self.layout.info["numel"]
+        self.param_dtype = param_dtype
+        dev = torch.device(device)
+        z = lambda dt: torch.zeros(self.N, self.stride, dtype=dt, device=dev)
+        self.master, self.exp_avg, self.exp_avg_sq = z(torch.float32), z(torch.float32), z(torch.float32)
+        self.param = z(torch.bfloat16) if param_dtype == torch.bfloat16 else None
+        self.grad_out = z(torch.float32) if with_grad_out else None
+        self.full = torch.zeros(self.F, dtype=param_dtype, device=dev)
+        self.t = 0
+
+    @property
+    def param_shards(self) -> torch.Tensor:
+        """What the all-gather reads: the bf16 copies, or the fp32 master itself."""
+        return self.param if self.param is not None else self.master
+
+    def units(self, ub: int = 0, ue: Optional[int] = None):
+        return ub, self.layout.n_units if ue is None else ue
+
+    def init_from_full(self, full: torch.Tensor, stream=None) -> None:
+        """Initial sharding of a constructed model (fp32 or bf16 full layout); moments to zero."""
+        fsdp_reshard(self.layout, 0, self.layout.n_units, full, self.master, self.param, stream)
+        self.exp_avg.zero_()
+        self.exp_avg_sq.zero_()
+        self.t = 0
+
+    def unshard(self, ub: int = 0, ue: Optional[int] = None, out: Optional[torch.Tensor] = None, stream=None):
+        ub, ue = self.units(ub, ue)
+        fsdp_unshard(self.layout, ub, ue, self.param_shards, self.full if out is None else out, stream)
+        return self.full if out is None else out
+
+    def reduce_scatter_adamw(self, grads, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step: Optional[int] = None,
+                             ub: int = 0, ue: Optional[int] = None, stream=None) -> None:
+        ub, ue = self.units(ub, ue)
+        t = self.t + 1 if step is None else step
+        fsdp_reduce_scatter_adamw(self.layout, ub, ue, grads, self.master, self.exp_avg, self.exp_avg_sq,
+                                  self.param, self.grad_out, hp, t, stream)
+        self.t = t
+
+    def step(self, grads, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), strategy: str = "full_shard", stream=None) -> None:
+        """One sharded step over all units: the all-gathers of the strategy, then
+        the fused reduce-scatter + AdamW + cast."""
+        for _ in range(STRATEGIES[strategy]):
+            self.unshard(stream=stream)
+        self.reduce_scatter_adamw(grads, hp, stream=stream)
+
+    def launches_per_step(self, strategy: str = "full_shard") -> int:
+        """Kernel launches of one step (for a launch count)."""
+        return STRATEGIES[strategy] + 1 + (1 if self.grad_out is not None else 0)

@@ -1,0 +1,208 @@
+"""Helpers of the GPU parity tests: run the CUDA path and the oracle on the same
+seeded inputs and compare.  The oracle gets its inputs from the seeded generators
+(synth) and its layout from its own code, never from the CUDA path.
+
+Tolerances (the stated bar): fp32 state (master, exp_avg, exp_avg_sq, reduced
+gradient) max relative error <= 1e-6 (|x-ref| / max(|ref|, 1e-30)); bf16 params
+<= 1 bf16 ulp; layout, unshard and reshard copies bit-exact.  With the same
+reduction order and IEEE operations the expected difference is 0 ulp, and the
+helpers report the ulp counts they saw.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import fsdp_sharded_state_gb300 as fs
+import oracle
+from fsdp_sharded_state_gb300 import synth
+
+REL_TOL = 1e-6
+BF16_ULP_TOL = 1
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().float().cpu().numpy()
+
+
+def _ordered32(a):
+    i = a.view(np.int32).astype(np.int64)
+    return np.where(i < 0, -(i & 0x7FFFFFFF), i)
+
+
+def _ordered16(a):
+    i = a.astype(np.int64)
+    return np.where(i & 0x8000, -(i & 0x7FFF), i)
+
+
+def ulp_f32(a, b) -> int:
+    if a.size == 0:
+        return 0
+    return int(np.abs(_ordered32(np.ascontiguousarray(a, np.float32)) -
+                      _ordered32(np.ascontiguousarray(b, np.float32))).max())
+
+
+def assert_f32_close(got, ref, what=""):
+    got = np.ascontiguousarray(got, np.float32)
+    ref = np.ascontiguousarray(ref, np.float32)
+    nan_g, nan_r = np.isnan(got), np.isnan(ref)
+    assert np.array_equal(nan_g, nan_r), f"{what}: NaN positions differ"
+    g, r = got[~nan_r], ref[~nan_r]
+    rel = np.abs(g.astype(np.float64) - r) / np.maximum(np.abs(r.astype(np.float64)), 1e-30)
+    assert rel.size == 0 or rel.max() <= REL_TOL, f"{what}: max rel {rel.max():.3g}, max ulp {ulp_f32(g, r)}"
+    return ulp_f32(g, r)
+
+
+def assert_bf16_close(got_u16, ref_u16, what=""):
+    got_u16 = np.ascontiguousarray(got_u16, np.uint16)
+    ref_u16 = np.ascontiguousarray(ref_u16, np.uint16)
+    if got_u16.size == 0:
+        return 0
+    d = np.abs(_ordered16(got_u16) - _ordered16(ref_u16)).max()
+    assert d <= BF16_ULP_TOL, f"{what}: {d} bf16 ulp"
+    return int(d)
+
+
+def grads_np(grads):
+    out = []
+    for g in grads:
+        out.append(u16(g) if g.dtype == torch.bfloat16 else f32(g))
+    return out
+
+
+def make_state(w: synth.Workload, device="cuda", with_grad_out=False):
+    st = fs.ShardedState(w.shapes, w.unit_ids, w.N, w.mode, param_dtype=w.param_dtype, device=device,
+                         with_grad_out=with_grad_out)
+    return st
+
+
+def oracle_offsets(w: synth.Workload):
+    O = oracle.layout(oracle.Shapes(w.shapes, w.unit_ids), w.N, w.mode)
+    return O
+
+
+def run_full_parity(w: synth.Workload, steps=None, strategy="full_shard", with_grad_out=True, check_unshard=True):
+    """Whole-state comparison after every step (small layouts)."""
+    steps = w.steps if steps is None else steps
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = oracle.layout(sh, w.N, w.mode)
+    st = make_state(w, with_grad_out=with_grad_out)
+    assert st.F == O["F"] and st.layout.info["shard_numel"] == O["S"]
+    stride = st.stride
+    full = synth.full_params(w, O["F"], O["t_full_off"], device="cuda")
+    st.init_from_full(full)
+    bf16 = w.param_dtype == torch.bfloat16
+    om, op = oracle.reshard(sh, w.N, w.mode, f32(full), stride, True, bf16)
+    assert np.array_equal(f32(st.master).reshape(-1).view(np.uint32), om.view(np.uint32)), "reshard master"
+    if bf16:
+        assert np.array_equal(u16(st.param).reshape(-1), op), "reshard bf16 param"
+    m = np.zeros_like(om)
+    v = np.zeros_like(om)
+    go = np.zeros_like(om) if with_grad_out else None
+    ulps = []
+    for t in range(1, steps + 1):
+        grads = synth.grad_replicas(w, O["F"], t, device="cuda")
+        st.step(grads, w.hp, strategy=strategy)
+        if check_unshard:
+            # the all-gather of this step saw the parameters before the update
+            ref_full = oracle.unshard(sh, w.N, w.mode, op if bf16 else om, stride, O["F"])
+            got_full = u16(st.full) if bf16 else f32(st.full).view(np.uint32)
+            refv = ref_full if bf16 else ref_full.view(np.uint32)
+            assert np.array_equal(got_full, refv), f"unshard at step {t}"
+        oracle.rs_adamw(sh, w.N, w.mode, grads_np(grads), stride, om, m, v, param=op if bf16 else None,
+                        grad_out=go, hp=w.hp, step=t)
+        torch.cuda.synchronize()
+        u = [assert_f32_close(f32(st.master).reshape(-1), om, f"master step {t}"),
+             assert_f32_close(f32(st.exp_avg).reshape(-1), m, f"exp_avg step {t}"),
+             assert_f32_close(f32(st.exp_avg_sq).reshape(-1), v, f"exp_avg_sq step {t}")]
+        if with_grad_out:
+            u.append(assert_f32_close(f32(st.grad_out).reshape(-1), go, f"grad_out step {t}"))
+        if bf16:
+            u.append(assert_bf16_close(u16(st.param).reshape(-1), op, f"param step {t}"))
+        ulps.append(max(u))
+    return st, ulps
+
+
+def sample_points(w: synth.Workload, O, n_random=200_000, seed=0):
+    """(rank, j) sample of shard positions: the edges of every rank's view of every
+    unit/tensor plus a seeded random set; padding positions kept (checked for +0)."""
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    rng = np.random.default_rng(seed)
+    ranks, js = [], []
+    S = O["S"]
+    edges = set()
+    if w.mode == oracle.FLAT:
+        for u in range(O["U"]):
+            a, n = O["u_shard_off"][u], O["u_S"][u]
+            for j in list(range(a, min(a + 9, a + n))) + list(range(max(a, a + n - 9), a + n)):
+                edges.add(j)
+    else:
+        for t in range(len(w.shapes)):
+            a, n = O["t_shard_off"][t], O["t_slot"][t]
+            for j in list(range(a, min(a + 9, a + n))) + list(range(max(a, a + n - 9), a + n)):
+                edges.add(j)
+    for r in range(w.N):
+        e = np.array(sorted(edges), np.int64)
+        ranks.append(np.full(e.size, r))
+        js.append(e)
+    rr = rng.integers(0, w.N, n_random)
+    jj = rng.integers(0, S, n_random)
+    ranks.append(rr)
+    js.append(jj)
+    r = np.concatenate(ranks)
+    j = np.concatenate(js)
+    fi = np.empty_like(j)
+    for q in range(w.N):
+        sel = r == q
+        fi[sel] = oracle.full_index(sh, w.N, w.mode, q, j[sel])
+    return r.astype(np.int64), j, fi
+
+
+def run_sampled_parity(w: synth.Workload, steps=None, strategy="full_shard", n_random=200_000):
+    """Full-size run on the GPU, oracle on sampled points, tracked across steps."""
+    steps = w.steps if steps is None else steps
+    O = oracle_offsets(w)
+    st = make_state(w, with_grad_out=True)
+    assert st.F == O["F"] and st.layout.info["shard_numel"] == O["S"]
+    full = synth.full_params(w, O["F"], O["t_full_off"], device="cuda")
+    st.init_from_full(full)
+    r, j, fi = sample_points(w, O, n_random)
+    lin = torch.from_numpy(r * st.stride + j).cuda()
+    real = fi >= 0
+    fi_t = torch.from_numpy(np.where(real, fi, 0)).cuda()
+    p = np.where(real, f32(full[fi_t]), 0).astype(np.float32)      # the reshard: master = full value
+    m = np.zeros_like(p)
+    v = np.zeros_like(p)
+    bf16 = w.param_dtype == torch.bfloat16
+    ulps = []
+    for t in range(1, steps + 1):
+        grads = synth.grad_replicas(w, O["F"], t, device="cuda")
+        st.step(grads, w.hp, strategy=strategy)
+        # the all-gather of this step: full[fi] == the pre-update bf16/fp32 parameter at (r, j)
+        got_full = st.full[fi_t]
+        if bf16:
+            ref_par = oracle.bf16_rne(p)
+            assert np.array_equal(u16(got_full)[real], ref_par[real]), f"unshard step {t}"
+        else:
+            assert np.array_equal(f32(got_full)[real].view(np.uint32), p[real].view(np.uint32)), f"unshard step {t}"
+        g_rows = np.zeros((p.size, w.N), np.float32)
+        for q in range(w.N):
+            g_rows[:, q] = np.where(real, f32(grads[q][fi_t]), 0)
+        par, gout = oracle.adamw_points(g_rows, p, m, v, want_param=True, want_grad=True, hp=w.hp, step=t)
+        torch.cuda.synchronize()
+        u = [assert_f32_close(f32(st.master.reshape(-1)[lin]), p, f"master step {t}"),
+             assert_f32_close(f32(st.exp_avg.reshape(-1)[lin]), m, f"exp_avg step {t}"),
+             assert_f32_close(f32(st.exp_avg_sq.reshape(-1)[lin]), v, f"exp_avg_sq step {t}"),
+             assert_f32_close(f32(st.grad_out.reshape(-1)[lin]), gout, f"grad_out step {t}")]
+        if bf16:
+            u.append(assert_bf16_close(u16(st.param.reshape(-1)[lin]), par, f"param step {t}"))
+        ulps.append(max(u))
+        del grads
+    # padding stays +0 (sampled padding positions went through the oracle with g = 0 too)
+    pad = ~real
+    assert not f32(st.master.reshape(-1)[lin])[pad].view(np.uint32).any()
+    return st, ulps

@@ -1,0 +1,216 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every symbol
+include/fsdp_state.h declares, computes layouts bit-exactly equal to the oracle's,
+and rejects bad arguments with the documented status before launching anything.
+
+Every rejected call below carries exactly one invalid argument, so validation
+fails before any CUDA call; no call here can reach a kernel.
+"""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import fsdp_sharded_state_gb300 as fs
+import oracle
+from fsdp_sharded_state_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fsdp_state.h")
+
+
+def declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|void|const char\*)\s+(fsdp_\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared() == sorted(fs.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = fs.lib()
+    for name in declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", fs.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (fsdp_\w+)$", out, re.M))
+    assert set(declared()) <= exported
+
+
+def seg_map(L, r):
+    S = L.info["shard_numel"]
+    m = np.full(S, -1, np.int64)
+    for t in range(L.info["n_tensors"]):
+        s = L.segment(t, r)
+        m[s["shard_off"]:s["shard_off"] + s["len"]] = np.arange(s["full_off"], s["full_off"] + s["len"])
+    return m
+
+
+def small_cases():
+    import random
+    rng = random.Random(3)
+    cases = [([(5, 3), (4,)], [0, 0], 3, 0), ([(5, 3)], [0], 4, 1), ([(1, 7)], [0], 5, 1),
+             ([(0, 4), (3,)], [0, 1], 2, 1), ([(), (2,)], [0, 0], 2, 0), ([(2, 2), (3,), (1,)], [0, 1, 2], 4, 0)]
+    for _ in range(120):
+        T = rng.randint(1, 3)
+        shapes = [tuple(rng.randint(0, 6) for _ in range(rng.randint(0, 3))) for _ in range(T)]
+        units = [0]
+        for _ in range(1, T):
+            units.append(units[-1] + rng.randint(0, 1))
+        cases.append((shapes, units, rng.randint(1, 9), rng.randint(0, 1)))
+    return cases
+
+
+@pytest.mark.parametrize("case", small_cases())
+def test_layout_bit_exact_vs_oracle(oracle_lib, case):
+    shapes, units, N, mode = case
+    L = fs.Layout(shapes, units, N, mode)
+    sh = oracle.Shapes(shapes, units)
+    O = oracle.layout(sh, N, mode)
+    info = L.info
+    assert (info["numel"], info["shard_numel"], info["full_numel"], info["n_units"]) == (O["P"], O["S"], O["F"], O["U"])
+    assert info["pad_numel"] == N * O["S"] - O["P"]
+    assert info["shard_stride"] >= O["S"] and info["shard_stride"] % 64 == 0
+    for u in range(O["U"]):
+        d = L.unit(u)
+        assert (d["shard_off"], d["shard_numel"], d["full_off"], d["numel"]) == \
+            (O["u_shard_off"][u], O["u_S"][u], O["u_full_off"][u], O["u_numel"][u])
+    for t in range(len(shapes)):
+        d = L.tensor(t)
+        assert d["full_off"] == O["t_full_off"][t] and d["unit"] == units[t]
+        if mode == 1:
+            assert d["shard_off"] == O["t_shard_off"][t] and d["rows_per_rank"] == O["t_rows"][t]
+    for r in range(N):
+        exp = oracle.full_index(sh, N, mode, r, np.arange(O["S"]))
+        assert np.array_equal(seg_map(L, r), exp)
+
+
+@pytest.mark.parametrize("make", [synth.tiny_mlp, synth.mlp128m, synth.llama4, synth.dim0_n6,
+                                  lambda: synth.sweep((1 << 29) + 1, 32), lambda: synth.sweep((1 << 20) + 1, 6)])
+def test_workload_layouts_vs_oracle(oracle_lib, make):
+    w = make()
+    L = fs.Layout(w.shapes, w.unit_ids, w.N, w.mode)
+    O = oracle.layout(oracle.Shapes(w.shapes, w.unit_ids), w.N, w.mode)
+    assert (L.info["numel"], L.info["shard_numel"], L.info["full_numel"]) == (O["P"], O["S"], O["F"])
+    for t in range(len(w.shapes)):
+        assert L.tensor(t)["full_off"] == O["t_full_off"][t]
+    # boundaries of every rank's view agree with the oracle's index map
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    for t in range(len(w.shapes)):
+        for r in range(w.N):
+            s = L.segment(t, r)
+            if s["len"] == 0:
+                continue
+            j = np.array([s["shard_off"], s["shard_off"] + s["len"] - 1])
+            assert list(oracle.full_index(sh, w.N, w.mode, r, j)) == [s["full_off"], s["full_off"] + s["len"] - 1]
+
+
+@pytest.mark.parametrize("case", small_cases()[:40])
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+def test_state_bytes_vs_oracle(oracle_lib, case, stage):
+    shapes, units, N, mode = case
+    L = fs.Layout(shapes, units, N, mode)
+    sh = oracle.Shapes(shapes, units)
+    for r in range(N):
+        for phys in (True, False):
+            assert L.state_bytes(stage, r, phys, 2, 4, 12, 4) == oracle.state_bytes(sh, N, mode, stage, r, phys,
+                                                                                      2, 4, 12, 4)
+
+
+# ---------------------------------------------------------------------------
+# validation
+# ---------------------------------------------------------------------------
+def create_status(shapes, units, N, mode, dtypes=None):
+    try:
+        fs.Layout(shapes, units, N, mode, dtypes)
+        return 0
+    except fs.FsdpError as e:
+        return e.status
+
+
+def test_create_rejects_bad_descriptions():
+    assert create_status([(4,)], [0], 0, 0) == -1                    # N < 1
+    assert create_status([(4,)], [0], 65, 0) == -1                   # N > FSDP_MAX_RANKS
+    assert create_status([(4,)], [0], 2, 7) == -1                    # unknown mode
+    assert create_status([(4,), (4,)], [0, 2], 2, 0) == -3           # unit ids skip
+    assert create_status([(4,)], [1], 2, 0) == -3                    # unit ids must start at 0
+    assert create_status([(4, -1)], [0], 2, 0) == -3                 # negative dim
+    assert create_status([(1 << 40, 1 << 40)], [0], 2, 0) == -5      # numel overflows int64
+    assert create_status([(4,), (4,)], [0, 0], 2, 0, [0, 1]) == -2   # FlatParameter needs one dtype
+    assert create_status([(4,), (4,)], [0, 1], 2, 0, [0, 1]) == 0    # ... per unit
+    assert create_status([(4,), (4,)], [0, 0], 2, 1, [0, 1]) == 0    # DIM0 groups may mix
+    assert create_status([(4,)], [0], 2, 0, [5]) == -2               # unknown dtype
+
+
+@pytest.fixture
+def lay():
+    return fs.Layout([(64, 32), (64,)], [0, 1], 4, fs.FSDP_FLAT)
+
+
+A = 1 << 20          # an aligned fake address: every call below fails before using it
+
+
+def test_unshard_validation(lay):
+    lib = fs.lib()
+    assert lib.fsdp_unshard(None, 0, 1, A, A, 0, None) == -1
+    assert lib.fsdp_unshard(lay.handle, 0, 3, A, A, 0, None) == -1      # unit range
+    assert lib.fsdp_unshard(lay.handle, 1, 0, A, A, 0, None) == -1
+    assert lib.fsdp_unshard(lay.handle, 0, 1, A, A, 9, None) == -2      # dtype
+    assert lib.fsdp_unshard(lay.handle, 0, 1, None, A, 0, None) == -1   # NULL
+    assert lib.fsdp_unshard(lay.handle, 0, 1, A + 4, A, 0, None) == -4  # misaligned
+    assert lib.fsdp_unshard(lay.handle, 0, 1, A, A + 8, 0, None) == -4
+
+
+def rs(lay, grads=None, gdt=1, master=A, m=A, v=A, param=None, gout=None, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01),
+       step=1, ub=0, ue=2):
+    lib = fs.lib()
+    arr = (C.c_void_p * 4)(*(grads or [A] * 4))
+    h = fs.AdamWHparams(*hp)
+    return lib.fsdp_reduce_scatter_adamw(lay.handle, ub, ue, arr, gdt, master, m, v, param, gout, C.byref(h),
+                                         step, None)
+
+
+def test_reduce_scatter_adamw_validation(lay):
+    assert rs(lay, ue=3) == -1
+    assert rs(lay, gdt=4) == -2
+    assert rs(lay, step=0) == -1
+    assert rs(lay, grads=[A, A, None, A]) == -1
+    assert rs(lay, grads=[A, A, A + 2, A]) == -4
+    assert rs(lay, master=None) == -1
+    assert rs(lay, v=A + 4) == -4
+    assert rs(lay, param=A + 2) == -4
+    assert rs(lay, gout=A + 4) == -4
+    for bad in [(-1e-3, .9, .999, 1e-8, .01), (1e-3, 1.0, .999, 1e-8, .01), (1e-3, .9, -0.1, 1e-8, .01),
+                (1e-3, .9, .999, 0.0, .01), (1e-3, .9, .999, 1e-8, -1.0), (float("nan"), .9, .999, 1e-8, .01),
+                (1e-3, .9, float("inf"), 1e-8, .01), (2.0, .9, .999, 1e-8, 0.6)]:
+        assert rs(lay, hp=bad) == -1, bad
+
+
+def test_reshard_validation(lay):
+    lib = fs.lib()
+    assert lib.fsdp_reshard(lay.handle, 0, 2, None, 0, A, A, None) == 0      # release only: nothing launched
+    assert lib.fsdp_reshard(lay.handle, 0, 5, None, 0, A, A, None) == -1
+    assert lib.fsdp_reshard(lay.handle, 0, 2, A, 3, A, A, None) == -2
+    assert lib.fsdp_reshard(lay.handle, 0, 2, A + 4, 0, A, A, None) == -4
+    assert lib.fsdp_reshard(lay.handle, 0, 2, A, 0, None, None, None) == -1
+    assert lib.fsdp_reshard(lay.handle, 0, 2, A, 0, A + 4, None, None) == -4
+
+
+def test_queries_validation(lay):
+    lib = fs.lib()
+    x = C.c_int64()
+    assert lib.fsdp_layout_unit(lay.handle, 2, None, None, None, None, None) == -1
+    assert lib.fsdp_layout_tensor(lay.handle, -1, None, None, None, None, None) == -1
+    assert lib.fsdp_layout_segment(lay.handle, 0, 4, C.byref(x), None, None, None) == -1
+    out = (C.c_int64 * 3)()
+    assert lib.fsdp_state_bytes(lay.handle, 4, 0, 1, 4, 4, 8, 0, out) == -1
+    assert lib.fsdp_state_bytes(lay.handle, 3, 4, 1, 4, 4, 8, 0, out) == -1
+    assert lib.fsdp_layout_query(None, None) == -1
+
+
+def test_error_strings():
+    for code, name in fs.STATUS.items():
+        assert fs.fsdp_error_string(code).startswith(name)
+    assert fs.fsdp_error_string(12345) == "unknown fsdp_status"

@@ -1,0 +1,77 @@
+"""Host-side parts of bench.py (CPU): the algorithmic byte model, the clock-log
+parser, and the max-over-ranks timing reduction on two gloo ranks."""
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from fsdp_sharded_state_gb300 import synth  # noqa: E402
+import fsdp_sharded_state_gb300 as fs  # noqa: E402
+
+
+def step_bytes(w, n_unshard=2):
+    L = fs.Layout(w.shapes, w.unit_ids, w.N, w.mode)
+    i = L.info
+    gb = 2 if w.grad_dtype == torch.bfloat16 else 4
+    pb = 2 if w.param_dtype == torch.bfloat16 else 4
+    ab = bench.algorithmic_bytes(w.N, i["numel"], i["shard_numel"], i["full_numel"], w.mode, gb, pb)
+    return ab, ab["rs_adamw"] + n_unshard * ab["unshard"], i["numel"]
+
+
+def test_byte_model_per_element():
+    # fp32 parameters and gradients, N = 4: the fused kernel moves 4N + 24 bytes per
+    # parameter, an all-gather 8; a FULL_SHARD step 56 bytes per parameter.
+    ab, tot, P = step_bytes(synth.mlp128m())
+    assert ab["rs_adamw"] == 40 * P and tot == 56 * P
+    # bf16 parameters and gradients, fp32 state, N = 8: 2N + 26 and 50 per step.
+    ab, tot, P = step_bytes(synth.llama4())
+    assert ab["rs_adamw"] == 42 * P and tot == 50 * P
+    # SHARD_GRAD_OP: one all-gather fewer
+    _, tot1, P = step_bytes(synth.llama4(), n_unshard=1)
+    assert tot1 == 46 * P
+
+
+def test_parse_clocks():
+    csv = "\n".join([
+        "0, 1965 MHz, 2070 MHz, 900.1 W, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1980 MHz, 2070 MHz, 910.0 W, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 345 MHz, 2070 MHz, 100.0 W, 0x0000000000000001, Not Active, Not Active, Not Active, Not Active",
+    ])
+    c = bench.parse_clocks(csv)
+    assert c["sm_max_mhz"] == 2070 and c["sm_mhz"] == pytest.approx(1972.5)
+    assert c["reasons"] == ["sw_power_cap"] and c["samples"] == 3
+    assert bench.parse_clocks("")["samples"] == 0
+
+
+def _agg_worker(rank, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    v = bench.aggregate_max([3.5, 7.25][rank], 2, dist)
+    q.put((rank, v))
+    dist.destroy_process_group()
+
+
+def test_aggregate_max_two_gloo_ranks():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.SimpleQueue()
+    ps = [ctx.Process(target=_agg_worker, args=(r, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get() for _ in range(2))
+    assert got == [(0, 7.25), (1, 7.25)]
+    assert bench.aggregate_max(5.0, 1, None) == 5.0

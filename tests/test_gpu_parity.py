@@ -1,0 +1,67 @@
+"""CUDA path vs oracle on the five workloads (GPU).
+
+Small layouts are compared element by element over the whole state after every
+step; the full-size 4-block Llama (809.5M parameters, N=8) and the FSDP2 dim-0
+group (243M, N=6) are run at full size in the bench's launch configuration and
+compared on sampled positions (every edge of every rank's view, plus 200k random
+positions) that the oracle tracks across the steps.
+"""
+import pytest
+import torch
+
+from fsdp_sharded_state_gb300 import synth
+
+import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_mlp_flat_fp32(oracle_lib):
+    _, ulps = pu.run_full_parity(synth.tiny_mlp(), strategy="full_shard")
+    print("tiny_mlp ulps per step", ulps)
+
+
+def test_tiny_mlp_dim0_bf16(oracle_lib):
+    w = synth.tiny_mlp(mode=synth.DIM0)
+    w.param_dtype = torch.bfloat16
+    w.grad_dtype = torch.bfloat16
+    pu.run_full_parity(w, strategy="shard_grad_op")
+
+
+def test_mlp128m_10_steps(oracle_lib):
+    _, ulps = pu.run_full_parity(synth.mlp128m(), check_unshard=True)
+    assert len(ulps) == 10
+    print("mlp128m ulps per step", ulps)
+
+
+def test_llama_block_reduced_full_compare(oracle_lib):
+    # one Llama-style block with small hidden sizes, every element compared
+    w = synth.llama4(blocks=2, hidden=256, ffn=688, N=8)
+    pu.run_full_parity(w)
+
+
+def test_llama4_full_size_sampled(oracle_lib):
+    _, ulps = pu.run_sampled_parity(synth.llama4())
+    print("llama4 ulps per step", ulps)
+
+
+def test_dim0_reduced_full_compare(oracle_lib):
+    w = synth.dim0_n6(vocab=320, hidden=64, ffn=176, N=6)
+    pu.run_full_parity(w)
+
+
+def test_dim0_n6_full_size_sampled(oracle_lib):
+    _, ulps = pu.run_sampled_parity(synth.dim0_n6())
+    print("dim0_n6 ulps per step", ulps)
+
+
+@pytest.mark.parametrize("N", [2, 4, 8, 16, 32])
+@pytest.mark.parametrize("P", [1 << 20, (1 << 20) + 1])
+def test_sweep_small_full_compare(oracle_lib, P, N):
+    w = synth.sweep(P, N)
+    pu.run_full_parity(w, strategy="full_shard" if P % 2 else "shard_grad_op")
+
+
+@pytest.mark.parametrize("P,N", [((1 << 26) + 1, 8), ((1 << 29) + 1, 32), (1 << 29, 2)])
+def test_sweep_large_sampled(oracle_lib, P, N):
+    pu.run_sampled_parity(synth.sweep(P, N), n_random=100_000)
