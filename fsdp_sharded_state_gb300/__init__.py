@@ -27,7 +27,7 @@ STATUS = {0: "FSDP_OK", -1: "FSDP_EINVAL", -2: "FSDP_EDTYPE", -3: "FSDP_ESHAPE",
 EXPORTS = ("fsdp_layout_create", "fsdp_layout_destroy", "fsdp_layout_query", "fsdp_layout_unit",
            "fsdp_layout_tensor", "fsdp_layout_segment", "fsdp_state_bytes", "fsdp_layout_prepare",
            "fsdp_unshard", "fsdp_reduce_scatter_adamw", "fsdp_reshard", "fsdp_check_status",
-           "fsdp_error_string", "fsdp_last_cuda_error")
+           "fsdp_error_string", "fsdp_last_cuda_error", "fsdp_reduce_scatter_adamw_noalloc")
 
 
 class FsdpError(RuntimeError):
@@ -75,6 +75,7 @@ def lib() -> C.CDLL:
         L.fsdp_reduce_scatter_adamw.argtypes = [vp, i32, i32, C.POINTER(vp), i32, vp, vp, vp, vp, vp,
                                                 C.POINTER(AdamWHparams), i64, vp]
         L.fsdp_reshard.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
+        L.fsdp_reduce_scatter_adamw_noalloc.argtypes = L.fsdp_reduce_scatter_adamw.argtypes
         L.fsdp_check_status.argtypes = [vp]
         L.fsdp_error_string.argtypes = [C.c_int]
         L.fsdp_error_string.restype = C.c_char_p
@@ -226,6 +227,23 @@ def fsdp_reduce_scatter_adamw(layout: Layout, unit_begin: int, unit_end: int, gr
                                            _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(param_shards),
                                            _ptr(grad_shard_out), C.byref(h), step, _stream(stream)),
            "fsdp_reduce_scatter_adamw")
+
+
+def fsdp_reduce_scatter_adamw_noalloc(layout: Layout, unit_begin: int, unit_end: int, grad_replicas, master,
+                                      exp_avg, exp_avg_sq, param_shards=None, grad_shard_out=None,
+                                      hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step: int = 1, stream=None,
+                                      grad_dtype: Optional[int] = None) -> None:
+    """fsdp_reduce_scatter_adamw without any device allocation (fixed in-library scratch)."""
+    if len(grad_replicas) != layout.N:
+        raise ValueError(f"need {layout.N} gradient replicas, got {len(grad_replicas)}")
+    if grad_dtype is None:
+        grad_dtype = _dtype_code(grad_replicas[0])
+    arr = (C.c_void_p * layout.N)(*[_ptr(g) for g in grad_replicas])
+    h = hp if isinstance(hp, AdamWHparams) else AdamWHparams(*hp)
+    _check(lib().fsdp_reduce_scatter_adamw_noalloc(layout.handle, unit_begin, unit_end, arr, grad_dtype,
+                                                   _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+                                                   _ptr(param_shards), _ptr(grad_shard_out), C.byref(h), step,
+                                                   _stream(stream)), "fsdp_reduce_scatter_adamw_noalloc")
 
 
 def fsdp_reshard(layout: Layout, unit_begin: int, unit_end: int, full=None, master=None, param_shards=None,

@@ -1,0 +1,132 @@
+// noalloc.cu -- fsdp_reduce_scatter_adamw_noalloc: the fused reduce-scatter +
+// AdamW + bf16 recast for callers that cannot allocate device memory.
+//
+// The regular entry point keeps each layout's segment table in device memory it
+// allocates with cudaMalloc on first use.  Some callers cannot allow that: code
+// running under a pre-sized memory pool or a custom allocator that owns all device
+// memory, graph-building or real-time paths that must not hit the driver's
+// allocator (cudaMalloc can synchronize the device and may fail under memory
+// pressure mid-step), and embedders that forbid hidden allocations in a library.
+// This variant instead stages the table in one fixed array that lives in the
+// library image: `g_noalloc_segs` below, FSDP_NOALLOC_MAX_SEGMENTS entries of 32
+// bytes (256 KiB), present on every GPU that loads the library until the process
+// exits.  The entry point calls no cudaMalloc, cudaFree or other allocating
+// routine.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fsdp_state.h"
+#include "kernels.hpp"
+#include "layout.hpp"
+
+namespace {
+
+using fsdp::Seg;
+
+// The shared scratch.  Host code must not use this name as an address (on the
+// host it is only a stand-in); it takes the device address from
+// cudaGetSymbolAddress below, once per device.
+static __device__ __align__(256) Seg g_noalloc_segs[FSDP_NOALLOC_MAX_SEGMENTS];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+Seg* g_addr[kMaxDevices] = {};   // device address of g_noalloc_segs, per device
+
+// Set-up, once per device, with that device current: the device address of the
+// scratch array.  (It loads the library's module on that device if needed.)
+int scratch_address(Seg** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FSDP_ECUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FSDP_EINVAL;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_addr[dev]) {
+        Seg* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_segs);
+        if (e != cudaSuccess || !p) return FSDP_ECUDA;
+        g_addr[dev] = p;
+    }
+    *out = g_addr[dev];
+    return FSDP_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int ptr_ok(const void* p) {
+    if (!p) return FSDP_EINVAL;
+    return aligned16(p) ? FSDP_OK : FSDP_EALIGN;
+}
+
+}  // namespace
+
+extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t ub, int32_t ue,
+                                                 const void* const* grads, int32_t grad_dtype, float* master,
+                                                 float* exp_avg, float* exp_avg_sq, void* param_shards,
+                                                 float* grad_shard_out, const fsdp_adamw_hparams* hp,
+                                                 int64_t step, fsdp_stream_t stream) {
+    // ---- the same argument checks as fsdp_reduce_scatter_adamw ----
+    if (!L || ub < 0 || ue > L->U || ub > ue) return FSDP_EINVAL;
+    if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if (!grads || !hp || step < 1) return FSDP_EINVAL;
+    int rc;
+    for (int32_t q = 0; q < L->N; ++q)
+        if ((rc = ptr_ok(grads[q]))) return rc;
+    if ((rc = ptr_ok(master)) || (rc = ptr_ok(exp_avg)) || (rc = ptr_ok(exp_avg_sq))) return rc;
+    if ((param_shards && !aligned16(param_shards)) || (grad_shard_out && !aligned16(grad_shard_out)))
+        return FSDP_EALIGN;
+    const float lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
+    if (!std::isfinite(lr) || !std::isfinite(b1) || !std::isfinite(b2) || !std::isfinite(eps) || !std::isfinite(wd))
+        return FSDP_EINVAL;
+    if (lr < 0.f || b1 < 0.f || b1 >= 1.f || b2 < 0.f || b2 >= 1.f || eps <= 0.f || wd < 0.f ||
+        double(lr) * double(wd) > 1.0)
+        return FSDP_EINVAL;
+
+    // ---- the table entries this call reads: data segments of the unit range plus
+    //      the entry after them (next unit's first segment or the sentinel), then,
+    //      when grad_shard_out is given, the pad segments likewise ----
+    const int32_t sb = L->data.unit_begin[ub], se = L->data.unit_begin[ue];
+    const int32_t pb = L->pad.unit_begin[ub], pe = L->pad.unit_begin[ue];
+    const int64_t n_data = int64_t(se - sb) + 1;
+    const int64_t n_pad = grad_shard_out ? int64_t(pe - pb) + 1 : 0;
+    if (n_data + n_pad > FSDP_NOALLOC_MAX_SEGMENTS) return FSDP_EINVAL;   // beyond the fixed scratch
+
+    Seg* scratch = nullptr;
+    if ((rc = scratch_address(&scratch))) return rc;
+
+    fsdp::AdamScal sc;
+    const double bc1 = 1.0 - std::pow(double(b1), double(step));
+    const double bc2 = 1.0 - std::pow(double(b2), double(step));
+    sc.decay = float(1.0 - double(lr) * double(wd));
+    sc.om1 = float(1.0 - double(b1));
+    sc.om2 = float(1.0 - double(b2));
+    sc.step_size = float(double(lr) / bc1);
+    sc.bc2s = float(std::sqrt(bc2));
+    sc.beta1 = b1;
+    sc.beta2 = b2;
+    sc.eps = eps;
+    sc.nf = float(L->N);
+    fsdp::GradPtrs gp{};
+    for (int32_t q = 0; q < L->N; ++q) gp.p[q] = grads[q];
+
+    // Stream-ordered: the table is written before this call's kernels read it.
+    // Nothing in the scratch needs to start at zero: every entry read is written first.
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(scratch, L->data.segs.data() + sb, size_t(n_data) * sizeof(Seg),
+                                    cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return FSDP_ECUDA;
+    const int64_t t0 = L->data.segs[sb].tile0, t1 = L->data.segs[se].tile0;
+    e = fsdp::launch_rs_adamw(scratch, t0, t1 - t0, grad_dtype == FSDP_BF16, gp, L->N, master, exp_avg, exp_avg_sq,
+                              static_cast<uint16_t*>(param_shards), grad_shard_out, sc, st);
+    if (e != cudaSuccess) return FSDP_ECUDA;
+    if (grad_shard_out) {
+        Seg* pad = scratch + n_data;
+        e = cudaMemcpyAsync(pad, L->pad.segs.data() + pb, size_t(n_pad) * sizeof(Seg), cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return FSDP_ECUDA;
+        const int64_t q0 = L->pad.segs[pb].tile0, q1 = L->pad.segs[pe].tile0;
+        e = fsdp::launch_zero_pad(pad, q0, q1 - q0, grad_shard_out, nullptr, st);
+        if (e != cudaSuccess) return FSDP_ECUDA;
+    }
+    return FSDP_OK;
+}

@@ -237,6 +237,33 @@ const char* fsdp_error_string(int status);
 /* Text of the last CUDA error seen by this thread in a library call ("" if none). */
 const char* fsdp_last_cuda_error(void);
 
+/* fsdp_reduce_scatter_adamw_noalloc -- the pages have no counterpart of this call.
+ * The same computation, arguments, checks and results as fsdp_reduce_scatter_adamw,
+ * for callers that cannot allocate device memory: a pre-sized pool or custom
+ * allocator that owns all device memory, a step that must not enter the driver's
+ * allocator (cudaMalloc may synchronize the device or fail under memory pressure),
+ * or an embedder that forbids hidden allocations in a library.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine: the segment table its kernels
+ * read is staged, on `stream`, in one fixed array inside the library image of
+ * FSDP_NOALLOC_MAX_SEGMENTS 32-byte entries (256 KiB), which every GPU that loads
+ * the library holds until the process exits.
+ *   - The unit range may need at most FSDP_NOALLOC_MAX_SEGMENTS entries: the
+ *     range's (tensor or unit, rank) pieces + 1, plus, when grad_shard_out is given,
+ *     its padding pieces + 1.  A larger range returns FSDP_EINVAL with nothing
+ *     launched; split it into smaller unit ranges.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array and each call rewrites the entries it reads
+ *     before its kernels run, so no state carries over between calls.  Calls whose
+ *     work overlaps on the GPU race on the array: issue them on one stream, or order
+ *     them with events. */
+#define FSDP_NOALLOC_MAX_SEGMENTS 8192
+int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                                      const void* const* grad_replicas, int32_t grad_dtype,
+                                      float* master, float* exp_avg, float* exp_avg_sq,
+                                      void* param_shards, float* grad_shard_out,
+                                      const fsdp_adamw_hparams* hp, int64_t step, fsdp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
