@@ -349,7 +349,7 @@ def main():
     args = ap.parse_args()
 
     from fsdp_sharded_state_gb300 import synth
-    w = synth.WORKLOADS[args.workload]()
+    w = synth.workload(args.workload)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -42,7 +42,9 @@ int device_tables(const fsdp_layout* Lc, const Seg** base) {
         *base = it->second.base;
         return FSDP_OK;
     }
-    const size_t n = L->data.segs.size() + L->gather.segs.size() + L->pad.segs.size();
+    const SegList* lists[] = {&L->data, &L->gather, &L->pad, &L->data_al, &L->data_sh, &L->gather_al, &L->gather_sh};
+    size_t n = 0;
+    for (const SegList* l : lists) n += l->segs.size();
     Seg* d = nullptr;
     e = cudaMalloc(&d, n * sizeof(Seg));
     if (e != cudaSuccess) {
@@ -51,7 +53,7 @@ int device_tables(const fsdp_layout* Lc, const Seg** base) {
     }
     std::vector<Seg> h;
     h.reserve(n);
-    for (const SegList* l : {&L->data, &L->gather, &L->pad}) h.insert(h.end(), l->segs.begin(), l->segs.end());
+    for (const SegList* l : lists) h.insert(h.end(), l->segs.begin(), l->segs.end());   // dev_off order
     e = cudaMemcpy(d, h.data(), n * sizeof(Seg), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         cudaFree(d);
@@ -199,7 +201,7 @@ int fsdp_state_bytes(const fsdp_layout* L, int32_t stage, int32_t rank, int32_t 
     } else {
         // Logical elements of this rank: the data segments in its row.
         const int64_t lo = int64_t(rank) * L->stride, hi = lo + L->stride;
-        for (size_t i = 0; i + 1 < L->data.segs.size(); ++i) {
+        for (size_t i = 0; i + 1 < L->data.segs.size(); ++i) {   // the list's last entry is its sentinel
             const Seg& s = L->data.segs[i];
             if (s.shard >= lo && s.shard < hi) own += s.len;
         }
@@ -225,10 +227,14 @@ int fsdp_unshard(const fsdp_layout* L, int32_t ub, int32_t ue, const void* shard
     if ((rc = check_ptr(shards)) || (rc = check_ptr(full))) return rc;
     const Seg* base = nullptr;
     if ((rc = device_tables(L, &base))) return rc;
-    const Range R = range_of(L->gather, base, ub, ue);
-    const cudaError_t e = fsdp::launch_unshard(R.segs, R.tile_base, R.n_tiles, elem_dtype == FSDP_BF16, shards,
-                                               full, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "k_unshard launch");
+    for (int shifted = 0; shifted < 2; ++shifted) {
+        const Range R = range_of(shifted ? L->gather_sh : L->gather_al, base, ub, ue);
+        const cudaError_t e = fsdp::launch_unshard(R.segs, R.tile_base, R.n_tiles, shifted, elem_dtype == FSDP_BF16,
+                                                   shards, full, int64_t(L->N) * L->stride,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "k_unshard launch");
+    }
+    return FSDP_OK;
 }
 
 int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, const void* const* grads,
@@ -272,11 +278,14 @@ int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, cons
     const Seg* base = nullptr;
     if ((rc = device_tables(L, &base))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const Range R = range_of(L->data, base, ub, ue);
-    cudaError_t e = fsdp::launch_rs_adamw(R.segs, R.tile_base, R.n_tiles, grad_dtype == FSDP_BF16, gp, L->N,
-                                          master, exp_avg, exp_avg_sq, static_cast<uint16_t*>(param_shards),
-                                          grad_shard_out, sc, st);
-    if (e != cudaSuccess) return cuda_fail(e, "k_rs_adamw launch");
+    cudaError_t e;
+    for (int shifted = 0; shifted < 2; ++shifted) {
+        const Range R = range_of(shifted ? L->data_sh : L->data_al, base, ub, ue);
+        e = fsdp::launch_rs_adamw(R.segs, R.tile_base, R.n_tiles, shifted, grad_dtype == FSDP_BF16, gp, L->N, L->F,
+                                  master, exp_avg, exp_avg_sq, static_cast<uint16_t*>(param_shards), grad_shard_out,
+                                  sc, st);
+        if (e != cudaSuccess) return cuda_fail(e, "k_rs_adamw launch");
+    }
     if (grad_shard_out) {
         const Range P = range_of(L->pad, base, ub, ue);
         e = fsdp::launch_zero_pad(P.segs, P.tile_base, P.n_tiles, grad_shard_out, nullptr, st);

@@ -45,15 +45,16 @@ template <typename GT> struct GradIO;
 // bf16 gradients: one 16-byte load per replica covers the 8 elements.
 template <> struct GradIO<uint16_t> {
     static constexpr int kBatch = 8;
-    struct Vec { uint4 w; };
+    static constexpr int kWords = 4;                 // 32-bit words per 8-element vector
+    struct Vec { uint32_t w[4]; };
     static __device__ __forceinline__ Vec load(const void* base, int64_t i) {
-        return Vec{ld_once(static_cast<const uint16_t*>(base) + i)};
+        const uint4 x = ld_once(static_cast<const uint16_t*>(base) + i);
+        return Vec{{x.x, x.y, x.z, x.w}};
     }
-    static __device__ __forceinline__ void add(float (&a)[8], const Vec& x) {
-        a[0] = __fadd_rn(a[0], bf16lo(x.w.x)); a[1] = __fadd_rn(a[1], bf16hi(x.w.x));
-        a[2] = __fadd_rn(a[2], bf16lo(x.w.y)); a[3] = __fadd_rn(a[3], bf16hi(x.w.y));
-        a[4] = __fadd_rn(a[4], bf16lo(x.w.z)); a[5] = __fadd_rn(a[5], bf16hi(x.w.z));
-        a[6] = __fadd_rn(a[6], bf16lo(x.w.w)); a[7] = __fadd_rn(a[7], bf16hi(x.w.w));
+    // element e (0..15) of the window [A, B], as fp32 (bf16 widens exactly)
+    static __device__ __forceinline__ float elem(const Vec& A, const Vec& B, int e) {
+        const uint32_t w = e < 8 ? A.w[e >> 1] : B.w[(e - 8) >> 1];
+        return (e & 1) ? bf16hi(w) : bf16lo(w);
     }
     static __device__ __forceinline__ float load1(const void* base, int64_t i) {
         return bf16f(static_cast<const uint16_t*>(base)[i]);
@@ -63,21 +64,28 @@ template <> struct GradIO<uint16_t> {
 // fp32 gradients: two 16-byte loads per replica.
 template <> struct GradIO<float> {
     static constexpr int kBatch = 4;
-    struct Vec { uint4 a, b; };
+    static constexpr int kWords = 8;
+    struct Vec { uint32_t w[8]; };
     static __device__ __forceinline__ Vec load(const void* base, int64_t i) {
         const float* p = static_cast<const float*>(base) + i;
-        return Vec{ld_once(p), ld_once(p + 4)};
+        const uint4 a = ld_once(p), b = ld_once(p + 4);
+        return Vec{{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w}};
     }
-    static __device__ __forceinline__ void add(float (&a)[8], const Vec& x) {
-        a[0] = __fadd_rn(a[0], __uint_as_float(x.a.x)); a[1] = __fadd_rn(a[1], __uint_as_float(x.a.y));
-        a[2] = __fadd_rn(a[2], __uint_as_float(x.a.z)); a[3] = __fadd_rn(a[3], __uint_as_float(x.a.w));
-        a[4] = __fadd_rn(a[4], __uint_as_float(x.b.x)); a[5] = __fadd_rn(a[5], __uint_as_float(x.b.y));
-        a[6] = __fadd_rn(a[6], __uint_as_float(x.b.z)); a[7] = __fadd_rn(a[7], __uint_as_float(x.b.w));
+    static __device__ __forceinline__ float elem(const Vec& A, const Vec& B, int e) {
+        return __uint_as_float(e < 8 ? A.w[e] : B.w[e - 8]);
     }
     static __device__ __forceinline__ float load1(const void* base, int64_t i) {
         return static_cast<const float*>(base)[i];
     }
 };
+
+template <typename V>
+__device__ __forceinline__ V shfl_down1(const V& v) {
+    V r;
+#pragma unroll
+    for (int k = 0; k < int(sizeof(v.w) / 4); ++k) r.w[k] = __shfl_down_sync(0xffffffffu, v.w[k], 1);
+    return r;
+}
 
 // Sum of the N replicas at 8 consecutive full-layout elements starting at f
 // (16-byte aligned), in rank order.  Loads are issued in batches so that a batch
@@ -95,7 +103,89 @@ __device__ __forceinline__ void reduce8_vec(const GradPtrs& gp, int N, int64_t f
             if (q0 + b < N) buf[b] = IO::load(gp.p[q0 + b], f);
 #pragma unroll
         for (int b = 0; b < IO::kBatch; ++b)
-            if (q0 + b < N) IO::add(acc, buf[b]);
+            if (q0 + b < N) {
+                const typename IO::Vec& x = buf[b];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[k] = __fadd_rn(acc[k], IO::elem(x, x, k));
+            }
+    }
+}
+
+// Elements d..d+7 (d in 1..7, warp-uniform) of the 16-element window [A, B] as fp32.
+__device__ __forceinline__ void window8(const GradIO<uint16_t>::Vec& A, const GradIO<uint16_t>::Vec& B, int d,
+                                        float (&out)[8]) {
+    const uint32_t w[8] = {A.w[0], A.w[1], A.w[2], A.w[3], B.w[0], B.w[1], B.w[2], B.w[3]};
+    uint32_t x[5];
+    switch (d >> 1) {                       // whole 32-bit words first ...
+        case 0: x[0] = w[0]; x[1] = w[1]; x[2] = w[2]; x[3] = w[3]; x[4] = w[4]; break;
+        case 1: x[0] = w[1]; x[1] = w[2]; x[2] = w[3]; x[3] = w[4]; x[4] = w[5]; break;
+        case 2: x[0] = w[2]; x[1] = w[3]; x[2] = w[4]; x[3] = w[5]; x[4] = w[6]; break;
+        default: x[0] = w[3]; x[1] = w[4]; x[2] = w[5]; x[3] = w[6]; x[4] = w[7]; break;
+    }
+    const bool odd = d & 1;                 // ... then one bf16 if d is odd
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t y = odd ? __funnelshift_r(x[k], x[k + 1], 16) : x[k];
+        out[2 * k] = bf16lo(y);
+        out[2 * k + 1] = bf16hi(y);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void window8_f32(const GradIO<float>::Vec& A, const GradIO<float>::Vec& B,
+                                            uint32_t (&x)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = (D + k) < 8 ? A.w[(D + k) & 7] : B.w[(D + k - 8) & 7];
+}
+
+__device__ __forceinline__ void window8(const GradIO<float>::Vec& A, const GradIO<float>::Vec& B, int d,
+                                        float (&out)[8]) {
+    uint32_t x[8];
+    switch (d) {
+        case 1: window8_f32<1>(A, B, x); break;
+        case 2: window8_f32<2>(A, B, x); break;
+        case 3: window8_f32<3>(A, B, x); break;
+        case 4: window8_f32<4>(A, B, x); break;
+        case 5: window8_f32<5>(A, B, x); break;
+        case 6: window8_f32<6>(A, B, x); break;
+        default: window8_f32<7>(A, B, x); break;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) out[k] = __uint_as_float(x[k]);
+}
+
+// The same sum when the 8 full-layout elements start d elements (warp-uniform,
+// 1..7) past a 16-byte boundary fa.  Warp-collective: every lane loads its own
+// aligned vector A at fa, takes its neighbour's (the next aligned vector) with a
+// shuffle and reads elements d..d+7 of the pair; lane 31 loads the next vector
+// itself.  have_a / have_b say whether A / the next vector lie inside the buffer.
+template <typename GT>
+__device__ __forceinline__ void reduce8_shift(int d, const GradPtrs& gp, int N, int64_t fa, bool have_a,
+                                              bool have_b, bool lane31, float (&acc)[8]) {
+    using IO = GradIO<GT>;
+    constexpr int kB = IO::kWords == 4 ? 8 : 4;     // replicas in flight per batch
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+#pragma unroll 1
+    for (int q0 = 0; q0 < N; q0 += kB) {
+        typename IO::Vec A[kB], B[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            if (q0 + b < N) {
+                A[b] = have_a ? IO::load(gp.p[q0 + b], fa) : typename IO::Vec{};
+                B[b] = (lane31 && have_b) ? IO::load(gp.p[q0 + b], fa + kVec) : typename IO::Vec{};
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            if (q0 + b < N) {                                   // uniform: all lanes shuffle
+                const typename IO::Vec nb = shfl_down1(A[b]);
+                float x[8];
+                window8(A[b], lane31 ? B[b] : nb, d, x);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[k] = __fadd_rn(acc[k], x[k]);
+            }
+        }
     }
 }
 
@@ -107,11 +197,15 @@ __device__ __forceinline__ float reduce1(const GradPtrs& gp, int N, int64_t f) {
     return acc;
 }
 
-template <typename GT, bool PARAM, bool GOUT>
+// SHIFT = false: every segment has its full-layout offset congruent to its shard
+// offset mod 8 (plain 16-byte vectors on both sides).  SHIFT = true: none has, and
+// the gradients go through the warp realignment.
+template <typename GT, bool PARAM, bool GOUT, bool SHIFT>
 __global__ void __launch_bounds__(kThreads)
-k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N,
+k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N, int64_t F,
            float* __restrict__ master, float* __restrict__ exp_avg, float* __restrict__ exp_avg_sq,
            uint16_t* __restrict__ param, float* __restrict__ gout, AdamScal sc) {
+    const bool lane31 = (threadIdx.x & 31) == 31;
     int s = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         const int64_t gt = tile_base + t;
@@ -119,21 +213,34 @@ k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, Gra
         const Seg sg = segs[s];
         const int64_t e0 = (sg.shard / kVec + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
         const int64_t lo = sg.shard, hi = sg.shard + sg.len;
-        if (e0 >= hi) continue;
         const int64_t delta = sg.full - sg.shard;            // full index = shard index + delta
+        const int64_t f0 = e0 + delta;
+        const bool interior = e0 >= lo && e0 + kVec <= hi;
+        const int d = int(delta & (kVec - 1));
+        const int64_t fa = f0 - d;
+        const bool have_a = fa >= 0 && fa + kVec <= F;
+        const bool have_b = fa >= 0 && fa + 2 * kVec <= F;
+        const bool fast = SHIFT ? (interior && have_a && have_b) : interior;
+        // Issue the state loads before the gradient loads: both round trips overlap.
+        float4 p0, p1, m0, m1, v0, v1;
+        if (fast) {
+            p0 = ld4(master + e0); p1 = ld4(master + e0 + 4);
+            m0 = ld4(exp_avg + e0); m1 = ld4(exp_avg + e0 + 4);
+            v0 = ld4(exp_avg_sq + e0); v1 = ld4(exp_avg_sq + e0 + 4);
+        }
+        float acc[8];
+        if (!SHIFT) {
+            // gradients 16-byte aligned where the state is: plain vector loads
+            if (e0 >= hi) continue;
+            if (fast) reduce8_vec<GT>(gp, N, f0, acc);
+        } else {
+            // misaligned segment (uniform over the tile): warp-collective realignment
+            reduce8_shift<GT>(d, gp, N, fa, have_a, have_b, lane31, acc);
+            if (e0 >= hi) continue;
+        }
 
-        if (e0 >= lo && e0 + kVec <= hi) {
+        if (fast) {
             // ---- interior vector: 16-byte state traffic ----
-            float4 p0 = ld4(master + e0), p1 = ld4(master + e0 + 4);
-            float4 m0 = ld4(exp_avg + e0), m1 = ld4(exp_avg + e0 + 4);
-            float4 v0 = ld4(exp_avg_sq + e0), v1 = ld4(exp_avg_sq + e0 + 4);
-            float acc[8];
-            if ((delta & (kVec - 1)) == 0) {
-                reduce8_vec<GT>(gp, N, e0 + delta, acc);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) acc[k] = reduce1<GT>(gp, N, e0 + delta + k);
-            }
             float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
             float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
             float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -157,7 +264,7 @@ k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, Gra
                 st4(gout + e0 + 4, make_float4(g[4], g[5], g[6], g[7]));
             }
         } else {
-            // ---- partial vector at a segment edge: element by element ----
+            // ---- partial vector at a segment edge (or next to the buffer end): element by element ----
             const int64_t a = e0 > lo ? e0 : lo;
             const int64_t b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
             for (int64_t e = a; e < b; ++e) {
@@ -175,11 +282,68 @@ k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, Gra
 // ----------------------------------------------------------------------------
 // Unshard: bitwise copy shard -> full.  ET is the element's bit container.
 // ----------------------------------------------------------------------------
+template <typename ET> struct CopyVec {
+    static constexpr int kWords = int(sizeof(ET)) * kVec / 4;   // 32-bit words per 8 elements: 4 or 8
+    uint32_t w[kWords];
+};
+
 template <typename ET>
+__device__ __forceinline__ CopyVec<ET> load_vec(const ET* p) {
+    CopyVec<ET> v;
+#pragma unroll
+    for (int k = 0; k < CopyVec<ET>::kWords / 4; ++k) {
+        const uint4 x = ld_once(p + k * (16 / sizeof(ET)));
+        v.w[4 * k] = x.x; v.w[4 * k + 1] = x.y; v.w[4 * k + 2] = x.z; v.w[4 * k + 3] = x.w;
+    }
+    return v;
+}
+
+template <typename ET>
+__device__ __forceinline__ void store_vec(ET* p, const CopyVec<ET>& v) {
+#pragma unroll
+    for (int k = 0; k < CopyVec<ET>::kWords / 4; ++k)
+        stu4(p + k * (16 / sizeof(ET)), make_uint4(v.w[4 * k], v.w[4 * k + 1], v.w[4 * k + 2], v.w[4 * k + 3]));
+}
+
+// Elements O..O+7 of the window [S, X] as one vector (O compile-time).
+template <typename ET, int O>
+__device__ __forceinline__ CopyVec<ET> window(const CopyVec<ET>& S, const CopyVec<ET>& X) {
+    constexpr int W = CopyVec<ET>::kWords;
+    uint32_t w[2 * W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) { w[k] = S.w[k]; w[W + k] = X.w[k]; }
+    CopyVec<ET> r;
+    if (sizeof(ET) == 4) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) r.w[k] = w[O + k];
+    } else if ((O & 1) == 0) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) r.w[k] = w[(O >> 1) + k];
+    } else {
+#pragma unroll
+        for (int k = 0; k < W; ++k) r.w[k] = __funnelshift_r(w[(O >> 1) + k], w[(O >> 1) + k + 1], 16);
+    }
+    return r;
+}
+
+template <typename ET>
+__device__ __forceinline__ CopyVec<ET> window_any(int o, const CopyVec<ET>& S, const CopyVec<ET>& X) {
+    switch (o) {
+        case 1: return window<ET, 1>(S, X);
+        case 2: return window<ET, 2>(S, X);
+        case 3: return window<ET, 3>(S, X);
+        case 4: return window<ET, 4>(S, X);
+        case 5: return window<ET, 5>(S, X);
+        case 6: return window<ET, 6>(S, X);
+        default: return window<ET, 7>(S, X);
+    }
+}
+
+template <typename ET, bool SHIFT>
 __global__ void __launch_bounds__(kThreads)
-k_unshard(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
-          const ET* __restrict__ src, ET* __restrict__ dst) {
-    constexpr int kU4 = int(sizeof(ET)) * kVec / 16;   // 16-byte words per vector: 1 or 2
+k_unshard(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, const ET* __restrict__ src,
+          ET* __restrict__ dst, int64_t src_limit) {
+    const bool lane31 = (threadIdx.x & 31) == 31;
     int s = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         const int64_t gt = tile_base + t;
@@ -187,18 +351,42 @@ k_unshard(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
         const Seg sg = segs[s];
         const int64_t e0 = (sg.shard / kVec + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
         const int64_t lo = sg.shard, hi = sg.shard + sg.len;
-        if (e0 >= hi) continue;
         const int64_t delta = sg.full - sg.shard;
-        if (e0 >= lo && e0 + kVec <= hi && (delta & (kVec - 1)) == 0) {
-            uint4 w[kU4];
-#pragma unroll
-            for (int k = 0; k < kU4; ++k) w[k] = ld_once(src + e0 + k * (16 / sizeof(ET)));
-#pragma unroll
-            for (int k = 0; k < kU4; ++k) stu4(dst + e0 + delta + k * (16 / sizeof(ET)), w[k]);
-        } else {
-            const int64_t a = e0 > lo ? e0 : lo;
-            const int64_t b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
-            for (int64_t e = a; e < b; ++e) dst[e + delta] = src[e];
+        if (!SHIFT) {
+            if (e0 >= hi) continue;
+            if (e0 >= lo && e0 + kVec <= hi) {
+                store_vec(dst + e0 + delta, load_vec(src + e0));
+            } else {
+                const int64_t a = e0 > lo ? e0 : lo;
+                const int64_t b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
+                for (int64_t e = a; e < b; ++e) dst[e + delta] = src[e];
+            }
+            continue;
+        }
+        // Misaligned segment (uniform over the tile): every lane loads its aligned
+        // source vector S and gets the next one X from its neighbour (lane 31 loads
+        // it); lane t then stores the aligned destination vector [fa+8, fa+16),
+        // made of S[8-d..7] and X[0..7-d].  Destination vectors that are not wholly
+        // inside the segment are written element by element by the source owners.
+        const int d = int(delta & (kVec - 1));
+        CopyVec<ET> S{}, X{};
+        if (e0 + kVec <= src_limit) S = load_vec(src + e0);
+        if (lane31 && e0 + 2 * kVec <= src_limit) X = load_vec(src + e0 + kVec);
+        {
+            const CopyVec<ET> nb = shfl_down1(S);
+            if (!lane31) X = nb;
+        }
+        if (e0 >= hi) continue;
+        const int64_t fa = e0 + delta - d;                    // 8-aligned full index
+        const int64_t rlo = sg.full, rhi = sg.full + sg.len;   // full range of the segment
+        if (fa + kVec >= rlo && fa + 2 * kVec <= rhi) store_vec(dst + fa + kVec, window_any<ET>(kVec - d, S, X));
+        if (fa >= rlo && fa + 2 * kVec <= rhi) continue;       // both my destination vectors are whole
+        const int64_t a = e0 > lo ? e0 : lo;
+        const int64_t b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
+        for (int64_t e = a; e < b; ++e) {
+            const int64_t f = e + delta;
+            const int64_t v0 = f - (f & (kVec - 1));
+            if (!(v0 >= rlo && v0 + kVec <= rhi)) dst[f] = src[e];
         }
     }
 }
@@ -319,47 +507,54 @@ int grid_for(K kernel, int64_t n_tiles) {
 // ----------------------------------------------------------------------------
 // Launchers (host).  They return the cudaError_t of the launch.
 // ----------------------------------------------------------------------------
-template <typename GT>
+template <typename GT, bool SHIFT>
 static cudaError_t launch_rs_t(const Seg* segs, int64_t tile_base, int64_t n_tiles, const GradPtrs& gp,
-                               int N, float* master, float* m, float* v, uint16_t* param, float* gout,
+                               int N, int64_t F, float* master, float* m, float* v, uint16_t* param, float* gout,
                                const AdamScal& sc, cudaStream_t st) {
     if (param && gout) {
-        auto k = k_rs_adamw<GT, true, true>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, master, m, v, param, gout, sc);
+        auto k = k_rs_adamw<GT, true, true, SHIFT>;
+        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc);
     } else if (param) {
-        auto k = k_rs_adamw<GT, true, false>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, master, m, v, param, gout, sc);
+        auto k = k_rs_adamw<GT, true, false, SHIFT>;
+        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc);
     } else if (gout) {
-        auto k = k_rs_adamw<GT, false, true>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, master, m, v, param, gout, sc);
+        auto k = k_rs_adamw<GT, false, true, SHIFT>;
+        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc);
     } else {
-        auto k = k_rs_adamw<GT, false, false>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, master, m, v, param, gout, sc);
+        auto k = k_rs_adamw<GT, false, false, SHIFT>;
+        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc);
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_rs_adamw(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
-                            const GradPtrs& gp, int N, float* master, float* m, float* v,
+cudaError_t launch_rs_adamw(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool shifted, bool grad_bf16,
+                            const GradPtrs& gp, int N, int64_t F, float* master, float* m, float* v,
                             uint16_t* param, float* gout, const AdamScal& sc, cudaStream_t st) {
     if (n_tiles <= 0) return cudaSuccess;
-    return grad_bf16 ? launch_rs_t<uint16_t>(segs, tile_base, n_tiles, gp, N, master, m, v, param, gout, sc, st)
-                     : launch_rs_t<float>(segs, tile_base, n_tiles, gp, N, master, m, v, param, gout, sc, st);
+    if (grad_bf16)
+        return shifted ? launch_rs_t<uint16_t, true>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc, st)
+                       : launch_rs_t<uint16_t, false>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc, st);
+    return shifted ? launch_rs_t<float, true>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc, st)
+                   : launch_rs_t<float, false>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc, st);
 }
 
-cudaError_t launch_unshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16,
-                           const void* src, void* dst, cudaStream_t st) {
-    if (n_tiles <= 0) return cudaSuccess;
-    if (bf16) {
-        auto k = k_unshard<uint16_t>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles,
-                                                      static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst));
-    } else {
-        auto k = k_unshard<uint32_t>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles,
-                                                      static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst));
-    }
+template <typename ET, bool SHIFT>
+static cudaError_t launch_unshard_t(const Seg* segs, int64_t tile_base, int64_t n_tiles, const void* src, void* dst,
+                                    int64_t src_limit, cudaStream_t st) {
+    auto k = k_unshard<ET, SHIFT>;
+    k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, static_cast<const ET*>(src),
+                                                  static_cast<ET*>(dst), src_limit);
     return cudaGetLastError();
+}
+
+cudaError_t launch_unshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool shifted, bool bf16,
+                           const void* src, void* dst, int64_t src_limit, cudaStream_t st) {
+    if (n_tiles <= 0) return cudaSuccess;
+    if (bf16)
+        return shifted ? launch_unshard_t<uint16_t, true>(segs, tile_base, n_tiles, src, dst, src_limit, st)
+                       : launch_unshard_t<uint16_t, false>(segs, tile_base, n_tiles, src, dst, src_limit, st);
+    return shifted ? launch_unshard_t<uint32_t, true>(segs, tile_base, n_tiles, src, dst, src_limit, st)
+                   : launch_unshard_t<uint32_t, false>(segs, tile_base, n_tiles, src, dst, src_limit, st);
 }
 
 template <bool FB>

@@ -7,12 +7,13 @@
 
 namespace fsdp {
 
-cudaError_t launch_rs_adamw(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
-                            const GradPtrs& gp, int N, float* master, float* m, float* v,
+// shifted: the segment range is the "shifted" alignment class (see layout.hpp).
+cudaError_t launch_rs_adamw(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool shifted, bool grad_bf16,
+                            const GradPtrs& gp, int N, int64_t F, float* master, float* m, float* v,
                             uint16_t* param, float* gout, const AdamScal& sc, cudaStream_t st);
 
-cudaError_t launch_unshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16,
-                           const void* src, void* dst, cudaStream_t st);
+cudaError_t launch_unshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool shifted, bool bf16,
+                           const void* src, void* dst, int64_t src_limit, cudaStream_t st);
 
 cudaError_t launch_reshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool full_bf16,
                            const void* full, float* master, uint16_t* param, cudaStream_t st);

@@ -24,6 +24,12 @@ void push(SegList& l, int64_t shard, int64_t full, int64_t len) {
     l.segs.push_back(Seg{shard, full, len, 0});
 }
 
+// Also files the piece under its alignment class.
+void push2(SegList& all, SegList& al, SegList& sh, int64_t shard, int64_t full, int64_t len) {
+    push(all, shard, full, len);
+    push(((full - shard) & (kVec - 1)) == 0 ? al : sh, shard, full, len);
+}
+
 void finish(SegList& l) {
     int64_t t = 0;
     for (Seg& s : l.segs) {
@@ -133,15 +139,14 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
     L->stride = stride;
 
     // Segment lists, per unit: rank-major, then tensor order.
-    for (SegList* l : {&L->data, &L->gather, &L->pad}) {
+    SegList* lists[] = {&L->data, &L->gather, &L->pad, &L->data_al, &L->data_sh, &L->gather_al, &L->gather_sh};
+    for (SegList* l : lists) {
         l->segs.clear();
         l->unit_begin.assign(U + 1, 0);
     }
     int64_t n_data = 0;
     for (int32_t u = 0; u < U; ++u) {
-        L->data.unit_begin[u] = int32_t(L->data.segs.size());
-        L->gather.unit_begin[u] = int32_t(L->gather.segs.size());
-        L->pad.unit_begin[u] = int32_t(L->pad.segs.size());
+        for (SegList* l : lists) l->unit_begin[u] = int32_t(l->segs.size());
         for (int32_t r = 0; r < N; ++r) {
             const int64_t row = int64_t(r) * stride;
             if (mode == FSDP_FLAT) {
@@ -150,8 +155,8 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
                 const int64_t own = std::max<int64_t>(0, std::min(Su, L->u_numel[u] - first));
                 const int64_t sh = row + L->u_shard_off[u];
                 const int64_t fu = L->u_full_off[u] + first;
-                push(L->data, sh, fu, own);
-                push(L->gather, sh, fu, Su);
+                push2(L->data, L->data_al, L->data_sh, sh, fu, own);
+                push2(L->gather, L->gather_al, L->gather_sh, sh, fu, Su);
                 push(L->pad, sh + own, -1, Su - own);
                 if (own > 0) ++n_data;
             } else {
@@ -163,8 +168,8 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
                     const int64_t own = (re - rb) * L->inner[t];
                     const int64_t sh = row + L->t_shard_off[t];
                     const int64_t fu = L->t_full_off[t] + rb * L->inner[t];
-                    push(L->data, sh, fu, own);
-                    push(L->gather, sh, fu, own);
+                    push2(L->data, L->data_al, L->data_sh, sh, fu, own);
+                    push2(L->gather, L->gather_al, L->gather_sh, sh, fu, own);
                     push(L->pad, sh + own, -1, c * L->inner[t] - own);
                     if (own > 0) ++n_data;
                 }
@@ -172,13 +177,13 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
             if (u == U - 1) push(L->pad, row + L->S, -1, stride - L->S);   // row tail
         }
     }
-    for (SegList* l : {&L->data, &L->gather, &L->pad}) {
+    int64_t off = 0;
+    for (SegList* l : lists) {
         l->unit_begin[U] = int32_t(l->segs.size());
         finish(*l);
+        l->dev_off = off;                       // position in the device table
+        off += int64_t(l->segs.size());
     }
-    L->gather.dev_off = int64_t(L->data.segs.size());
-    L->pad.dev_off = L->gather.dev_off + int64_t(L->gather.segs.size());
-    L->data.dev_off = 0;
     L->n_data_segments = n_data;
     return FSDP_OK;
 }

@@ -9,6 +9,10 @@
 //   pad     (rank, piece) -> padding elements of the shard rows (and, attached to
 //           the last unit, each row's physical tail [S, stride)): reshard zero-fill,
 //           grad_shard_out zero-fill
+// The data and gather lists are also kept split by alignment class: pieces whose
+// full-layout offset is congruent to their shard offset mod 8 ("aligned": 16-byte
+// vectors line up on both sides) and the rest ("shifted"), so that each class runs
+// in a kernel compiled for it.
 #pragma once
 
 #include <cstdint>
@@ -39,6 +43,7 @@ struct fsdp_layout {
     std::vector<int32_t> unit, dtype;
     std::vector<int64_t> u_numel, u_S, u_shard_off, u_full_off;
     fsdp::SegList data, gather, pad;
+    fsdp::SegList data_al, data_sh, gather_al, gather_sh;   // split by alignment class
     int64_t n_data_segments = 0;
 
     std::mutex mu;                                  // guards dev

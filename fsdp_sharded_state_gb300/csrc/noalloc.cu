@@ -83,14 +83,16 @@ extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t u
         double(lr) * double(wd) > 1.0)
         return FSDP_EINVAL;
 
-    // ---- the table entries this call reads: data segments of the unit range plus
-    //      the entry after them (next unit's first segment or the sentinel), then,
-    //      when grad_shard_out is given, the pad segments likewise ----
-    const int32_t sb = L->data.unit_begin[ub], se = L->data.unit_begin[ue];
+    // ---- the table entries this call reads: for each alignment class, the data
+    //      segments of the unit range plus the entry after them (next unit's first
+    //      segment or the sentinel); then, when grad_shard_out is given, the pad
+    //      segments likewise ----
+    const fsdp::SegList* cls[2] = {&L->data_al, &L->data_sh};
+    int64_t n_cls[2];
+    for (int c = 0; c < 2; ++c) n_cls[c] = int64_t(cls[c]->unit_begin[ue] - cls[c]->unit_begin[ub]) + 1;
     const int32_t pb = L->pad.unit_begin[ub], pe = L->pad.unit_begin[ue];
-    const int64_t n_data = int64_t(se - sb) + 1;
     const int64_t n_pad = grad_shard_out ? int64_t(pe - pb) + 1 : 0;
-    if (n_data + n_pad > FSDP_NOALLOC_MAX_SEGMENTS) return FSDP_EINVAL;   // beyond the fixed scratch
+    if (n_cls[0] + n_cls[1] + n_pad > FSDP_NOALLOC_MAX_SEGMENTS) return FSDP_EINVAL;   // beyond the fixed scratch
 
     Seg* scratch = nullptr;
     if ((rc = scratch_address(&scratch))) return rc;
@@ -113,15 +115,21 @@ extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t u
     // Stream-ordered: the table is written before this call's kernels read it.
     // Nothing in the scratch needs to start at zero: every entry read is written first.
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(scratch, L->data.segs.data() + sb, size_t(n_data) * sizeof(Seg),
-                                    cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return FSDP_ECUDA;
-    const int64_t t0 = L->data.segs[sb].tile0, t1 = L->data.segs[se].tile0;
-    e = fsdp::launch_rs_adamw(scratch, t0, t1 - t0, grad_dtype == FSDP_BF16, gp, L->N, master, exp_avg, exp_avg_sq,
-                              static_cast<uint16_t*>(param_shards), grad_shard_out, sc, st);
-    if (e != cudaSuccess) return FSDP_ECUDA;
+    cudaError_t e;
+    Seg* next = scratch;
+    for (int c = 0; c < 2; ++c) {
+        const int32_t sb = cls[c]->unit_begin[ub], se = cls[c]->unit_begin[ue];
+        e = cudaMemcpyAsync(next, cls[c]->segs.data() + sb, size_t(n_cls[c]) * sizeof(Seg), cudaMemcpyHostToDevice,
+                            st);
+        if (e != cudaSuccess) return FSDP_ECUDA;
+        const int64_t t0 = cls[c]->segs[sb].tile0, t1 = cls[c]->segs[se].tile0;
+        e = fsdp::launch_rs_adamw(next, t0, t1 - t0, c == 1, grad_dtype == FSDP_BF16, gp, L->N, L->F, master, exp_avg,
+                                  exp_avg_sq, static_cast<uint16_t*>(param_shards), grad_shard_out, sc, st);
+        if (e != cudaSuccess) return FSDP_ECUDA;
+        next += n_cls[c];
+    }
     if (grad_shard_out) {
-        Seg* pad = scratch + n_data;
+        Seg* pad = next;
         e = cudaMemcpyAsync(pad, L->pad.segs.data() + pb, size_t(n_pad) * sizeof(Seg), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) return FSDP_ECUDA;
         const int64_t q0 = L->pad.segs[pb].tile0, q1 = L->pad.segs[pe].tile0;

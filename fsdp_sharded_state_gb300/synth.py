@@ -100,6 +100,16 @@ def sweep(P: int, N: int) -> Workload:
 WORKLOADS = {"tiny_mlp": tiny_mlp, "mlp128m": mlp128m, "llama4": llama4, "dim0_n6": dim0_n6}
 
 
+def workload(name: str) -> Workload:
+    """A workload by name; sweep points are named sweep_P<numel>_N<ranks>."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]()
+    if name.startswith("sweep_P"):
+        p, n = name[len("sweep_P"):].split("_N")
+        return sweep(int(p), int(n))
+    raise KeyError(f"unknown workload {name!r}: {sorted(WORKLOADS)} or sweep_P<numel>_N<ranks>")
+
+
 def _gen(seed: int, device) -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed(seed)

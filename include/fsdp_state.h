@@ -248,7 +248,7 @@ const char* fsdp_last_cuda_error(void);
  * FSDP_NOALLOC_MAX_SEGMENTS 32-byte entries (256 KiB), which every GPU that loads
  * the library holds until the process exits.
  *   - The unit range may need at most FSDP_NOALLOC_MAX_SEGMENTS entries: the
- *     range's (tensor or unit, rank) pieces + 1, plus, when grad_shard_out is given,
+ *     range's (tensor or unit, rank) pieces + 2, plus, when grad_shard_out is given,
  *     its padding pieces + 1.  A larger range returns FSDP_EINVAL with nothing
  *     launched; split it into smaller unit ranges.
  *   - The first call on a device looks up the array's device address
