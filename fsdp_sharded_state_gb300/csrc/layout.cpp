@@ -127,11 +127,47 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
         }
     }
 
-    // Physical row stride: S rounded up to 64 elements, so that every rank row
-    // starts 128-byte aligned for bf16 and 256-byte aligned for fp32.
+    // Physical row stride.  Rank r's piece of unit/tensor x sits at shard index
+    // r*stride + off_x and at full index full_x + r*len_x; 16-byte vectors line up on
+    // both sides when the two are congruent mod 8.  That depends on stride mod 8
+    // only, so pick the residue that keeps the most logical elements congruent and
+    // prefer 0 (then stride = S rounded up to 64: rows 128/256-byte aligned).  A
+    // single FLAT unit with S odd, say, gets stride = S and every rank lines up.
+    int64_t aligned_elems[kVec] = {0};
+    for (int32_t u = 0; u < U; ++u) {
+        for (int32_t r = 0; r < N; ++r) {
+            if (mode == FSDP_FLAT) {
+                const int64_t own = std::max<int64_t>(0, std::min(L->u_S[u], L->u_numel[u] - int64_t(r) * L->u_S[u]));
+                for (int sig = 0; sig < kVec; ++sig) {
+                    const int64_t dlt = L->u_full_off[u] + int64_t(r) * L->u_S[u] - int64_t(r) * sig - L->u_shard_off[u];
+                    if ((dlt & (kVec - 1)) == 0) aligned_elems[sig] += own;
+                }
+            } else {
+                for (int32_t t = 0; t < T; ++t) {
+                    if (L->unit[t] != u) continue;
+                    const int64_t c = L->rows[t];
+                    const int64_t rb = std::min<int64_t>(int64_t(r) * c, L->d0[t]);
+                    const int64_t re = std::min<int64_t>(int64_t(r + 1) * c, L->d0[t]);
+                    const int64_t own = (re - rb) * L->inner[t];
+                    for (int sig = 0; sig < kVec; ++sig) {
+                        const int64_t dlt = L->t_full_off[t] + rb * L->inner[t] - int64_t(r) * sig - L->t_shard_off[t];
+                        if ((dlt & (kVec - 1)) == 0) aligned_elems[sig] += own;
+                    }
+                }
+            }
+        }
+    }
+    int best = 0;
+    for (int sig = 1; sig < kVec; ++sig)
+        if (aligned_elems[sig] > aligned_elems[best]) best = sig;
     int64_t stride;
-    if (!add_ok(L->S, 63, &stride)) return FSDP_EOVERFLOW;
-    stride = stride / 64 * 64;
+    if (best == 0) {
+        if (!add_ok(L->S, 63, &stride)) return FSDP_EOVERFLOW;
+        stride = stride / 64 * 64;
+    } else {
+        const int64_t rem = ((best - L->S) % kVec + kVec) % kVec;     // stride = S + rem = best (mod 8)
+        if (!add_ok(L->S, rem, &stride)) return FSDP_EOVERFLOW;
+    }
     int64_t total;
     if (!mul_ok(stride, N, &total)) return FSDP_EOVERFLOW;
     if (!mul_ok(total, 4, &total)) return FSDP_EOVERFLOW;   // fp32 byte size must fit too

@@ -35,7 +35,10 @@
  *     Launch calls are asynchronous and never synchronize; only
  *     fsdp_check_status and fsdp_layout_prepare block.
  *   - Shard arrays are [N][stride] row-major: rank r's shard starts at element
- *     r*stride; stride = fsdp_layout_info.shard_stride (>= S, multiple of 64).
+ *     r*stride; stride = fsdp_layout_info.shard_stride >= S.  The layout picks
+ *     stride mod 8 so that as many rank views as possible sit at a shard index
+ *     congruent to their full-layout index mod 8 (16-byte vectors line up on both
+ *     sides); when that costs nothing, stride is a multiple of 64.
  *   - The full layout: FLAT -- per unit, the padded flat parameter of N*S_u
  *     elements (tensors are views into it, padding at the end), units
  *     concatenated; DIM0 -- the tensors concatenated, each in its own row-major
@@ -87,7 +90,7 @@ typedef struct {
     int32_t n_tensors, n_units, n_ranks, mode;
     int64_t numel;          /* P: logical elements, sum of tensor numels              */
     int64_t shard_numel;    /* S: elements of one rank's shard (sum over units)       */
-    int64_t shard_stride;   /* physical row stride of [N][stride] shard arrays        */
+    int64_t shard_stride;   /* physical row stride of [N][stride] shard arrays (>= S)  */
     int64_t full_numel;     /* elements of the full layout (FLAT: N*S, DIM0: P)       */
     int64_t pad_numel;      /* N*S - P: padding elements over all ranks               */
     int64_t n_segments;     /* (tensor or unit, rank) pieces holding logical elements */
