@@ -28,10 +28,15 @@ struct Seg {
     int64_t tile0;   // index of the segment's first tile in its list
 };
 
-// Tiles a segment occupies (vectors are aligned on the shard side).
+// First vector of a segment's first tile: tiles sit on absolute multiples of
+// kTileElems shard elements, so every warp's accesses are whole cache lines
+// whatever the row stride.
+__host__ __device__ inline int64_t seg_vec0(int64_t shard) { return (shard / kTileElems) * kThreads; }
+
+// Tiles a segment occupies.
 __host__ __device__ inline int64_t seg_tiles(int64_t shard, int64_t len) {
     if (len <= 0) return 0;
-    const int64_t v0 = shard / kVec;
+    const int64_t v0 = seg_vec0(shard);
     const int64_t v1 = (shard + len + kVec - 1) / kVec;
     return (v1 - v0 + kThreads - 1) / kThreads;
 }

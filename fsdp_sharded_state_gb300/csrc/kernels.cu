@@ -197,11 +197,97 @@ __device__ __forceinline__ float reduce1(const GradPtrs& gp, int N, int64_t f) {
     return acc;
 }
 
+// fp32 gradients on aligned segments, "split" thread mapping: within its warp's 256
+// elements, lane l owns the two 4-element chunks [4l, 4l+4) and [128+4l, 128+4l+4),
+// so every 16-byte load or store instruction of the warp covers 512 contiguous
+// bytes (whole sectors).  Same arithmetic, same order as the other paths.
+__device__ __forceinline__ void rs_tile_f32_split(const Seg& sg, int64_t gt, const GradPtrs& gp, int N,
+                                                  float* __restrict__ master, float* __restrict__ exp_avg,
+                                                  float* __restrict__ exp_avg_sq, uint16_t* __restrict__ param,
+                                                  float* __restrict__ gout, const AdamScal& sc) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t x0 = (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads) * kVec + warp * 256 + lane * 4;
+    const int64_t lo = sg.shard, hi = sg.shard + sg.len;
+    const int64_t delta = sg.full - sg.shard;
+    if (x0 >= hi) return;
+    const int64_t x1 = x0 + 128;
+    const bool fast = x0 >= lo && x1 + 4 <= hi;
+    if (fast) {
+        const float4 pa = ld4(master + x0), pb = ld4(master + x1);
+        const float4 ma = ld4(exp_avg + x0), mb = ld4(exp_avg + x1);
+        const float4 va = ld4(exp_avg_sq + x0), vb = ld4(exp_avg_sq + x1);
+        float acc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+#pragma unroll 1
+        for (int q0 = 0; q0 < N; q0 += 2) {                 // 2 replicas x 2 chunks in flight
+            uint4 ga[2], gb[2];
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+                if (q0 + b < N) {
+                    const float* g = static_cast<const float*>(gp.p[q0 + b]);
+                    ga[b] = ld_once(g + x0 + delta);
+                    gb[b] = ld_once(g + x1 + delta);
+                }
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+                if (q0 + b < N) {
+                    acc[0] = __fadd_rn(acc[0], __uint_as_float(ga[b].x)); acc[1] = __fadd_rn(acc[1], __uint_as_float(ga[b].y));
+                    acc[2] = __fadd_rn(acc[2], __uint_as_float(ga[b].z)); acc[3] = __fadd_rn(acc[3], __uint_as_float(ga[b].w));
+                    acc[4] = __fadd_rn(acc[4], __uint_as_float(gb[b].x)); acc[5] = __fadd_rn(acc[5], __uint_as_float(gb[b].y));
+                    acc[6] = __fadd_rn(acc[6], __uint_as_float(gb[b].z)); acc[7] = __fadd_rn(acc[7], __uint_as_float(gb[b].w));
+                }
+        }
+        // compute and store one 4-element chunk at a time (fewer live registers)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int64_t xc = c ? x1 : x0;
+            const float4 pc = c ? pb : pa, mc = c ? mb : ma, vc = c ? vb : va;
+            float p[4] = {pc.x, pc.y, pc.z, pc.w};
+            float m[4] = {mc.x, mc.y, mc.z, mc.w};
+            float v[4] = {vc.x, vc.y, vc.z, vc.w};
+            float g[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                g[k] = __fdiv_rn(acc[4 * c + k], sc.nf);
+                adamw1(sc, g[k], p[k], m[k], v[k]);
+            }
+            st4(master + xc, make_float4(p[0], p[1], p[2], p[3]));
+            st4(exp_avg + xc, make_float4(m[0], m[1], m[2], m[3]));
+            st4(exp_avg_sq + xc, make_float4(v[0], v[1], v[2], v[3]));
+            if (param)
+                *reinterpret_cast<uint2*>(param + xc) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
+            if (gout) st4(gout + xc, make_float4(g[0], g[1], g[2], g[3]));
+        }
+        return;
+    }
+    // a chunk at a segment edge: element by element
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+        const int64_t xc = c ? x1 : x0;
+        const int64_t a = xc > lo ? xc : lo;
+        const int64_t b = (xc + 4) < hi ? (xc + 4) : hi;
+        for (int64_t e = a; e < b; ++e) {
+            float acc = 0.0f;
+            for (int q = 0; q < N; ++q) acc = __fadd_rn(acc, static_cast<const float*>(gp.p[q])[e + delta]);
+            const float gg = __fdiv_rn(acc, sc.nf);
+            float pp = master[e], mm = exp_avg[e], vv = exp_avg_sq[e];
+            adamw1(sc, gg, pp, mm, vv);
+            master[e] = pp; exp_avg[e] = mm; exp_avg_sq[e] = vv;
+            if (param) param[e] = to_bf16(pp);
+            if (gout) gout[e] = gg;
+        }
+    }
+}
+
 // SHIFT = false: every segment has its full-layout offset congruent to its shard
 // offset mod 8 (plain 16-byte vectors on both sides).  SHIFT = true: none has, and
 // the gradients go through the warp realignment.
+// Occupancy: the aligned instances keep 3 CTAs (24 warps) per SM -- at 2 the
+// DRAM queue drains between tiles and a launch loses 5-20 % of bandwidth -- so
+// they are held to 85 registers; the shifted ones need more and keep 2.
 template <typename GT, bool PARAM, bool GOUT, bool SHIFT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, SHIFT ? 2 : 3)
 k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N, int64_t F,
            float* __restrict__ master, float* __restrict__ exp_avg, float* __restrict__ exp_avg_sq,
            uint16_t* __restrict__ param, float* __restrict__ gout, AdamScal sc) {
@@ -211,7 +297,11 @@ k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, Gra
         const int64_t gt = tile_base + t;
         s = advance_seg(segs, s, gt);
         const Seg sg = segs[s];
-        const int64_t e0 = (sg.shard / kVec + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
+        if (!SHIFT && sizeof(GT) == 4) {
+            rs_tile_f32_split(sg, gt, gp, N, master, exp_avg, exp_avg_sq, param, gout, sc);
+            continue;
+        }
+        const int64_t e0 = (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
         const int64_t lo = sg.shard, hi = sg.shard + sg.len;
         const int64_t delta = sg.full - sg.shard;            // full index = shard index + delta
         const int64_t f0 = e0 + delta;
@@ -349,9 +439,28 @@ k_unshard(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, cons
         const int64_t gt = tile_base + t;
         s = advance_seg(segs, s, gt);
         const Seg sg = segs[s];
-        const int64_t e0 = (sg.shard / kVec + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
+        const int64_t e0 = (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
         const int64_t lo = sg.shard, hi = sg.shard + sg.len;
         const int64_t delta = sg.full - sg.shard;
+        if (!SHIFT && sizeof(ET) == 4) {
+            // 32-bit elements: split mapping (see rs_tile_f32_split), whole sectors per instruction
+            const int64_t x0 = e0 - int64_t(threadIdx.x) * kVec + (threadIdx.x >> 5) * 256 + (threadIdx.x & 31) * 4;
+            if (x0 >= hi) continue;
+            const int64_t x1 = x0 + 128;
+            if (x0 >= lo && x1 + 4 <= hi) {
+                const uint4 a = ld_once(src + x0), b = ld_once(src + x1);
+                stu4(dst + x0 + delta, a);
+                stu4(dst + x1 + delta, b);
+            } else {
+                for (int c = 0; c < 2; ++c) {
+                    const int64_t xc = c ? x1 : x0;
+                    const int64_t a = xc > lo ? xc : lo;
+                    const int64_t b = (xc + 4) < hi ? (xc + 4) : hi;
+                    for (int64_t e = a; e < b; ++e) dst[e + delta] = src[e];
+                }
+            }
+            continue;
+        }
         if (!SHIFT) {
             if (e0 >= hi) continue;
             if (e0 >= lo && e0 + kVec <= hi) {
@@ -409,7 +518,7 @@ k_reshard(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
         const int64_t gt = tile_base + t;
         s = advance_seg(segs, s, gt);
         const Seg sg = segs[s];
-        const int64_t e0 = (sg.shard / kVec + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
+        const int64_t e0 = (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
         const int64_t lo = sg.shard, hi = sg.shard + sg.len;
         if (e0 >= hi) continue;
         const int64_t delta = sg.full - sg.shard;
@@ -454,7 +563,7 @@ k_zero_pad(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
         const int64_t gt = tile_base + t;
         s = advance_seg(segs, s, gt);
         const Seg sg = segs[s];
-        const int64_t e0 = (sg.shard / kVec + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
+        const int64_t e0 = (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
         const int64_t lo = sg.shard, hi = sg.shard + sg.len;
         if (e0 >= hi) continue;
         if (e0 >= lo && e0 + kVec <= hi) {
