@@ -185,3 +185,62 @@ def state_bytes(sh, N, mode, stage, rank, physical, pb, gb, ob, step_bytes=0):
     if rc != 0:
         raise ValueError("oracle_state_bytes failed")
     return tuple(int(x) for x in out)
+
+
+def rs_clip_adamw(sh, N, mode, grads, stride, master, m, v, max_norm, param=None, grad_out=None,
+                  hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step=1, ub=0, ue=None):
+    """Reduce-scatter, sharded clip_grad_norm_, AdamW; in place.  Returns the norm."""
+    if ue is None:
+        ue = int(sh.unit[-1]) + 1
+    keep, arr, dt = _grad_ptrs(grads)
+    lr, b1, b2, eps, wd = hp
+    norm = C.c_double()
+    rc = lib().oracle_rs_clip_adamw(*sh.args(), C.c_int32(N), C.c_int32(mode), C.c_int32(ub), C.c_int32(ue),
+                                    arr, C.c_int32(dt), C.c_int64(stride), _p(master), _p(m), _p(v), _p(param),
+                                    _p(grad_out), C.c_float(max_norm), C.c_float(lr), C.c_float(b1), C.c_float(b2),
+                                    C.c_float(eps), C.c_float(wd), C.c_int64(step), C.byref(norm))
+    if rc != 0:
+        raise ValueError("oracle_rs_clip_adamw failed")
+    return norm.value
+
+
+def accumulate(acc, micro, first):
+    """acc = micro (first) or acc + micro, fp32, in place."""
+    micro = np.ascontiguousarray(micro)
+    dt = BF16 if micro.dtype == np.uint16 else F32
+    rc = lib().oracle_accumulate(C.c_int64(acc.size), _p(acc), _p(micro), C.c_int32(dt), C.c_int32(int(first)))
+    if rc != 0:
+        raise ValueError("oracle_accumulate failed")
+
+
+def hsdp_adamw(sh, N, mode, R, grads, stride, master, m, v, param=None, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step=1):
+    """grads: R*N replicas (group-major).  master/m/v/param: R copies of [N][stride]."""
+    keep, arr, dt = _grad_ptrs(grads)
+    lr, b1, b2, eps, wd = hp
+    rc = lib().oracle_hsdp_adamw(*sh.args(), C.c_int32(N), C.c_int32(mode), C.c_int32(R), arr, C.c_int32(dt),
+                                 C.c_int64(stride), _p(master), _p(m), _p(v), _p(param), C.c_float(lr),
+                                 C.c_float(b1), C.c_float(b2), C.c_float(eps), C.c_float(wd), C.c_int64(step))
+    if rc != 0:
+        raise ValueError("oracle_hsdp_adamw failed")
+
+
+def zero1_owners(sh, N):
+    owner = np.zeros(sh.T, np.int32)
+    rc = lib().oracle_zero1_owners(C.c_int32(sh.T), _p(sh.ndim), _p(sh.dims), C.c_int32(N), _p(owner))
+    if rc != 0:
+        raise ValueError("oracle_zero1_owners failed")
+    return owner
+
+
+def zero1_adamw(sh, N, grads, stride, master, m, v, params, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step=1):
+    """params: N full replicas (fp32, or uint16 bf16 when master is given); in place."""
+    keep, arr, dt = _grad_ptrs(grads)
+    params = [np.ascontiguousarray(p) for p in params]
+    parr = (C.c_void_p * N)(*[p.ctypes.data for p in params])
+    lr, b1, b2, eps, wd = hp
+    rc = lib().oracle_zero1_adamw(C.c_int32(sh.T), _p(sh.ndim), _p(sh.dims), C.c_int32(N), arr, C.c_int32(dt),
+                                  C.c_int64(stride), _p(master), _p(m), _p(v), parr, C.c_float(lr), C.c_float(b1),
+                                  C.c_float(b2), C.c_float(eps), C.c_float(wd), C.c_int64(step))
+    if rc != 0:
+        raise ValueError("oracle_zero1_adamw failed")
+    return params

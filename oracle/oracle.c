@@ -458,3 +458,186 @@ int oracle_state_bytes(int32_t T, const int32_t* ndim, const int64_t* dims, cons
     ol_free(&L);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Rows beyond the core step                                                  */
+/* ------------------------------------------------------------------------- */
+
+/* Sharded clip_grad_norm_ between the reduce-scatter and AdamW
+ * ([FSDP-ch18] §18.18: each rank's local sum of squares, an all-reduce of the
+ * sums, the square root, every rank scales its own gradient slice).  Reading of
+ * the constants the page leaves to torch's clip_grad_norm_: L2 norm,
+ * coef = min(1, max_norm / (norm + 1e-6)).  The sum of squares is accumulated in
+ * double over every rank's logical shard elements; coef is rounded to fp32 once
+ * and each reduced gradient is scaled by it (one fp32 multiply) before AdamW.
+ * grad_out (optional) receives the clipped gradient; *total_norm the norm. */
+int oracle_rs_clip_adamw(int32_t T, const int32_t* ndim, const int64_t* dims, const int32_t* unit_id,
+                         int32_t N, int32_t mode, int32_t ub, int32_t ue,
+                         const void* const* grads, int32_t grad_dtype, int64_t stride,
+                         float* master, float* m, float* v, uint16_t* param, float* grad_out, float max_norm,
+                         float lr, float beta1, float beta2, float eps, float wd, int64_t step,
+                         double* total_norm) {
+    olayout L;
+    if (ol_build(&L, T, ndim, dims, unit_id, N, mode)) return -1;
+    if (ub < 0 || ue > L.U || ub > ue || stride < L.S || step < 1) { ol_free(&L); return -1; }
+    float* g = calloc((size_t)N * (size_t)stride + 1, sizeof(float));
+    if (!g) { ol_free(&L); return -1; }
+    /* (1) reduce-scatter, (2) the sum of squares over all ranks */
+    double ss = 0.0;
+    for (int32_t u = ub; u < ue; ++u)
+        for (int32_t r = 0; r < N; ++r)
+            for (int64_t k = 0; k < L.u_S[u]; ++k) {
+                int64_t j = L.u_shard_off[u] + k;
+                int64_t fi = ol_full_index(&L, r, j, NULL);
+                float x = fi >= 0 ? reduce_mean(grads, grad_dtype, N, fi) : 0.0f;
+                g[(int64_t)r * stride + j] = x;
+                ss += (double)x * (double)x;
+            }
+    /* (3) the norm and the clip coefficient */
+    double norm = sqrt(ss);
+    double c = (double)max_norm / (norm + 1e-6);
+    if (c > 1.0) c = 1.0;
+    float coef = (float)c;
+    if (total_norm) *total_norm = norm;
+    /* (4) each rank's slice scaled, then AdamW */
+    oscal s = scalars(lr, beta1, beta2, eps, wd, step);
+    for (int32_t u = ub; u < ue; ++u)
+        for (int32_t r = 0; r < N; ++r)
+            for (int64_t k = 0; k < L.u_S[u]; ++k) {
+                int64_t e = (int64_t)r * stride + L.u_shard_off[u] + k;
+                float gc = g[e] * coef;
+                adamw_elem(&s, gc, &master[e], &m[e], &v[e]);
+                if (param) param[e] = oracle_bf16_rne(master[e]);
+                if (grad_out) grad_out[e] = gc;
+            }
+    free(g);
+    ol_free(&L);
+    return 0;
+}
+
+/* Gradient accumulation without synchronisation ([FSDP-ch18] §18.26: no_sync /
+ * set_requires_gradient_sync(False) -- the unsharded gradient accumulates
+ * locally, the reduce-scatter runs once on the last micro-batch).  One replica:
+ * acc = micro on the first micro-batch (first != 0), else acc = acc + micro, in
+ * fp32, over n full-layout elements. */
+int oracle_accumulate(int64_t n, float* acc, const void* micro, int32_t micro_dtype, int32_t first) {
+    for (int64_t i = 0; i < n; ++i) {
+        float x = load_grad(micro, micro_dtype, i);
+        acc[i] = first ? x : acc[i] + x;
+    }
+    return 0;
+}
+
+/* HSDP ([FSDP-ch18] §18.9: shard within the group, replicate across groups; the
+ * reduce-scatter runs in the shard dimension, then one all-reduce across the
+ * replica groups).  R groups of N ranks; grads[rho*N + q] is rank q of group
+ * rho.  Per shard element: g_rho = (sum_q G[rho][q]) / N (rank order), then
+ * g = (sum_rho g_rho) / R (group order); every group's state copy gets the same
+ * AdamW update.  master/m/v/param: R copies of [N][stride], copy rho at
+ * rho*N*stride.  (The torchtitan article §3.4 orders the two collectives the
+ * other way round; this follows the book chapter.) */
+int oracle_hsdp_adamw(int32_t T, const int32_t* ndim, const int64_t* dims, const int32_t* unit_id,
+                      int32_t N, int32_t mode, int32_t R, const void* const* grads, int32_t grad_dtype,
+                      int64_t stride, float* master, float* m, float* v, uint16_t* param,
+                      float lr, float beta1, float beta2, float eps, float wd, int64_t step) {
+    olayout L;
+    if (R < 1 || ol_build(&L, T, ndim, dims, unit_id, N, mode)) return -1;
+    if (stride < L.S || step < 1) { ol_free(&L); return -1; }
+    oscal s = scalars(lr, beta1, beta2, eps, wd, step);
+    const int64_t copy = (int64_t)N * stride;
+    for (int32_t r = 0; r < N; ++r)
+        for (int64_t j = 0; j < L.S; ++j) {
+            int64_t fi = ol_full_index(&L, r, j, NULL);
+            float g = 0.0f;
+            if (fi >= 0) {
+                float outer = 0.0f;
+                for (int32_t rho = 0; rho < R; ++rho)
+                    outer = outer + reduce_mean(grads + (int64_t)rho * N, grad_dtype, N, fi);
+                g = outer / (float)R;
+            }
+            for (int32_t rho = 0; rho < R; ++rho) {
+                int64_t e = rho * copy + (int64_t)r * stride + j;
+                adamw_elem(&s, g, &master[e], &m[e], &v[e]);
+                if (param) param[e] = oracle_bf16_rne(master[e]);
+            }
+        }
+    ol_free(&L);
+    return 0;
+}
+
+/* ZeRO-1 owner partition ([ZeRO-state] "ZeRO-1：Optimizer State Sharding": each
+ * rank updates about 1/N of the parameters -- whole parameters -- and
+ * broadcasts them; "常见错误" warns against balancing owners by parameter count
+ * instead of bytes).  Reading, after torch's ZeroRedundancyOptimizer: tensors
+ * sorted by size, largest first (stable), each given to the rank with the
+ * fewest elements so far (lowest rank on ties).  owner[t] receives the rank. */
+int oracle_zero1_owners(int32_t T, const int32_t* ndim, const int64_t* dims, int32_t N, int32_t* owner) {
+    if (T < 1 || N < 1) return -1;
+    int64_t* numel = calloc((size_t)T, 8);
+    int32_t* order = calloc((size_t)T, 4);
+    int64_t* load = calloc((size_t)N, 8);
+    int64_t pos = 0;
+    for (int32_t t = 0; t < T; ++t) {
+        int64_t n = 1;
+        for (int32_t k = 0; k < ndim[t]; ++k) n *= dims[pos + k];
+        pos += ndim[t];
+        numel[t] = n;
+        order[t] = t;
+    }
+    /* stable insertion sort by size, largest first */
+    for (int32_t i = 1; i < T; ++i) {
+        int32_t x = order[i], j = i - 1;
+        while (j >= 0 && numel[order[j]] < numel[x]) { order[j + 1] = order[j]; --j; }
+        order[j + 1] = x;
+    }
+    for (int32_t i = 0; i < T; ++i) {
+        int32_t best = 0;
+        for (int32_t r = 1; r < N; ++r) if (load[r] < load[best]) best = r;
+        owner[order[i]] = best;
+        load[best] += numel[order[i]];
+    }
+    free(numel); free(order); free(load);
+    return 0;
+}
+
+/* ZeRO-1 step ([ZeRO-state] "ZeRO-1：Optimizer State Sharding": the gradient is
+ * all-reduced (averaged), the owner updates its parameters with its optimizer
+ * state, then broadcasts the updated parameters to every rank).  params[q] is
+ * rank q's full replica of all parameters (P elements, tensors concatenated;
+ * fp32, or bf16 when master != NULL).  Owner state for tensor t lives in the
+ * owner's row at the tensor's place among the owner's tensors (tensor order):
+ * master/m/v are [N][stride].  For fp32 parameters (master == NULL) the owner's
+ * own replica is the parameter AdamW updates. */
+int oracle_zero1_adamw(int32_t T, const int32_t* ndim, const int64_t* dims, int32_t N,
+                       const void* const* grads, int32_t grad_dtype, int64_t stride,
+                       float* master, float* m, float* v, void* const* params,
+                       float lr, float beta1, float beta2, float eps, float wd, int64_t step) {
+    if (T < 1 || N < 1 || step < 1) return -1;
+    int32_t* owner = calloc((size_t)T, 4);
+    int64_t* off_in_row = calloc((size_t)N, 8);
+    oracle_zero1_owners(T, ndim, dims, N, owner);
+    oscal s = scalars(lr, beta1, beta2, eps, wd, step);
+    int64_t pos = 0, full = 0;
+    for (int32_t t = 0; t < T; ++t) {
+        int64_t n = 1;
+        for (int32_t k = 0; k < ndim[t]; ++k) n *= dims[pos + k];
+        pos += ndim[t];
+        int32_t o = owner[t];
+        int64_t row = (int64_t)o * stride + off_in_row[o];
+        if (off_in_row[o] + n > stride) { free(owner); free(off_in_row); return -1; }
+        for (int64_t k = 0; k < n; ++k) {
+            float g = reduce_mean(grads, grad_dtype, N, full + k);
+            float p = master ? master[row + k] : ((float*)params[o])[full + k];
+            adamw_elem(&s, g, &p, &m[row + k], &v[row + k]);
+            if (master) master[row + k] = p;
+            for (int32_t q = 0; q < N; ++q) {          /* the broadcast */
+                if (master) ((uint16_t*)params[q])[full + k] = oracle_bf16_rne(p);
+                else ((float*)params[q])[full + k] = p;
+            }
+        }
+        off_in_row[o] += n;
+        full += n;
+    }
+    free(owner); free(off_in_row);
+    return 0;
+}

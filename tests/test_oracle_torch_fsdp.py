@@ -84,7 +84,7 @@ def test_torch_fsdp_matches_oracle(oracle_lib, tmp_path, mode, n, shapes):
     v = np.zeros_like(master)
     gout = np.zeros_like(master)
     for t in range(steps):
-        grads = [pack_full(L, outs[r]["grads"][t]) for r in range(n)]
+        grads = [pack_full(L, outs[r]["grads"][t][0]) for r in range(n)]
         oracle.rs_adamw(sh, n, omode, grads, stride, master, m, v, grad_out=gout, hp=HP, step=t + 1)
         # reduce-scatter result of every rank: torch may sum in another order and FSDP1
         # divides before and after the reduction (by 2 and 1.5 at world size 3), so
