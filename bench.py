@@ -31,7 +31,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sharded-step params/sec and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
 PEAK_FALLBACK_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "fsdp_sharded_state_gb300", "csrc", "kernels.cu")
+KERNEL_SRC = [os.path.join(ROOT, "fsdp_sharded_state_gb300", "csrc", f)
+              for f in ("kernels.cu", "device_ops.cuh", "common.cuh")]
 
 
 # ---------------------------------------------------------------------------
@@ -65,8 +66,12 @@ def load_peaks():
 
 
 def kernel_src_hash():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the sources the core kernels compile from."""
+    h = hashlib.sha256()
+    for p in KERNEL_SRC:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel, workload):

@@ -15,9 +15,9 @@ from typing import Optional, Sequence
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libfsdpstate.so")
 
-FSDP_FLAT, FSDP_DIM0 = 0, 1
+FSDP_FLAT, FSDP_DIM0, FSDP_ZERO1 = 0, 1, 2
 FSDP_F32, FSDP_BF16 = 0, 1
-MODES = {"flat": FSDP_FLAT, "dim0": FSDP_DIM0}
+MODES = {"flat": FSDP_FLAT, "dim0": FSDP_DIM0, "zero1": FSDP_ZERO1}
 
 FSDP_OK = 0
 STATUS = {0: "FSDP_OK", -1: "FSDP_EINVAL", -2: "FSDP_EDTYPE", -3: "FSDP_ESHAPE", -4: "FSDP_EALIGN",
@@ -27,7 +27,9 @@ STATUS = {0: "FSDP_OK", -1: "FSDP_EINVAL", -2: "FSDP_EDTYPE", -3: "FSDP_ESHAPE",
 EXPORTS = ("fsdp_layout_create", "fsdp_layout_destroy", "fsdp_layout_query", "fsdp_layout_unit",
            "fsdp_layout_tensor", "fsdp_layout_segment", "fsdp_state_bytes", "fsdp_layout_prepare",
            "fsdp_unshard", "fsdp_reduce_scatter_adamw", "fsdp_reshard", "fsdp_check_status",
-           "fsdp_error_string", "fsdp_last_cuda_error", "fsdp_reduce_scatter_adamw_noalloc")
+           "fsdp_error_string", "fsdp_last_cuda_error", "fsdp_reduce_scatter_adamw_noalloc",
+           "fsdp_layout_owner", "fsdp_clip_workspace_bytes", "fsdp_reduce_scatter_clip_adamw",
+           "fsdp_accumulate_grads", "fsdp_hsdp_reduce_scatter_adamw", "fsdp_zero1_adamw_broadcast")
 
 
 class FsdpError(RuntimeError):
@@ -76,6 +78,16 @@ def lib() -> C.CDLL:
                                                 C.POINTER(AdamWHparams), i64, vp]
         L.fsdp_reshard.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]
         L.fsdp_reduce_scatter_adamw_noalloc.argtypes = L.fsdp_reduce_scatter_adamw.argtypes
+        L.fsdp_layout_owner.argtypes = [vp, i32, C.POINTER(i32)]
+        L.fsdp_clip_workspace_bytes.argtypes = []
+        L.fsdp_clip_workspace_bytes.restype = C.c_size_t
+        L.fsdp_reduce_scatter_clip_adamw.argtypes = [vp, i32, i32, C.POINTER(vp), i32, vp, vp, vp, vp, vp, C.c_float,
+                                                     vp, vp, C.POINTER(AdamWHparams), i64, vp]
+        L.fsdp_accumulate_grads.argtypes = [vp, i32, i32, C.POINTER(vp), C.POINTER(vp), i32, i32, vp]
+        L.fsdp_hsdp_reduce_scatter_adamw.argtypes = [vp, i32, i32, i32, C.POINTER(vp), i32, vp, vp, vp, vp,
+                                                     C.POINTER(AdamWHparams), i64, vp]
+        L.fsdp_zero1_adamw_broadcast.argtypes = [vp, i32, i32, C.POINTER(vp), i32, vp, vp, vp, C.POINTER(vp), i32,
+                                                 C.POINTER(AdamWHparams), i64, vp]
         L.fsdp_check_status.argtypes = [vp]
         L.fsdp_error_string.argtypes = [C.c_int]
         L.fsdp_error_string.restype = C.c_char_p
@@ -178,6 +190,11 @@ class Layout:
         _check(lib().fsdp_layout_segment(self._h, t, r, *[C.byref(x) for x in v]), "fsdp_layout_segment")
         return dict(zip(("shard_off", "full_off", "len", "pad"), (x.value for x in v)))
 
+    def owner(self, t: int) -> int:
+        r = C.c_int32()
+        _check(lib().fsdp_layout_owner(self._h, t, C.byref(r)), "fsdp_layout_owner")
+        return r.value
+
     def state_bytes(self, stage: int, rank: int, physical: bool, param_bytes: int, grad_bytes: int,
                     optim_bytes: int, step_bytes: int = 0):
         out = (C.c_int64 * 3)()
@@ -244,6 +261,73 @@ def fsdp_reduce_scatter_adamw_noalloc(layout: Layout, unit_begin: int, unit_end:
                                                    _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
                                                    _ptr(param_shards), _ptr(grad_shard_out), C.byref(h), step,
                                                    _stream(stream)), "fsdp_reduce_scatter_adamw_noalloc")
+
+
+def _ptr_array(xs):
+    return (C.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+
+
+def _hp(hp):
+    return hp if isinstance(hp, AdamWHparams) else AdamWHparams(*hp)
+
+
+def fsdp_clip_workspace_bytes() -> int:
+    return int(lib().fsdp_clip_workspace_bytes())
+
+
+def fsdp_reduce_scatter_clip_adamw(layout: Layout, unit_begin: int, unit_end: int, grad_replicas, master, exp_avg,
+                                   exp_avg_sq, param_shards, grad_shard, max_norm: float, workspace,
+                                   norm_out=None, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step: int = 1,
+                                   stream=None, grad_dtype: Optional[int] = None) -> None:
+    if len(grad_replicas) != layout.N:
+        raise ValueError(f"need {layout.N} gradient replicas, got {len(grad_replicas)}")
+    if grad_dtype is None:
+        grad_dtype = _dtype_code(grad_replicas[0])
+    _check(lib().fsdp_reduce_scatter_clip_adamw(layout.handle, unit_begin, unit_end, _ptr_array(grad_replicas),
+                                                grad_dtype, _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+                                                _ptr(param_shards), _ptr(grad_shard), float(max_norm),
+                                                _ptr(workspace), _ptr(norm_out), C.byref(_hp(hp)), step,
+                                                _stream(stream)), "fsdp_reduce_scatter_clip_adamw")
+
+
+def fsdp_accumulate_grads(layout: Layout, unit_begin: int, unit_end: int, acc, micro, first: bool,
+                          stream=None, micro_dtype: Optional[int] = None) -> None:
+    if len(acc) != layout.N or len(micro) != layout.N:
+        raise ValueError(f"need {layout.N} accumulators and micro-gradients")
+    if micro_dtype is None:
+        micro_dtype = _dtype_code(micro[0])
+    _check(lib().fsdp_accumulate_grads(layout.handle, unit_begin, unit_end, _ptr_array(acc), _ptr_array(micro),
+                                       micro_dtype, int(bool(first)), _stream(stream)), "fsdp_accumulate_grads")
+
+
+def fsdp_hsdp_reduce_scatter_adamw(layout: Layout, unit_begin: int, unit_end: int, n_groups: int, grad_replicas,
+                                   master, exp_avg, exp_avg_sq, param_shards=None,
+                                   hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step: int = 1, stream=None,
+                                   grad_dtype: Optional[int] = None) -> None:
+    if len(grad_replicas) != layout.N * n_groups:
+        raise ValueError(f"need {layout.N * n_groups} gradient replicas, got {len(grad_replicas)}")
+    if grad_dtype is None:
+        grad_dtype = _dtype_code(grad_replicas[0])
+    _check(lib().fsdp_hsdp_reduce_scatter_adamw(layout.handle, unit_begin, unit_end, n_groups,
+                                                _ptr_array(grad_replicas), grad_dtype, _ptr(master), _ptr(exp_avg),
+                                                _ptr(exp_avg_sq), _ptr(param_shards), C.byref(_hp(hp)), step,
+                                                _stream(stream)), "fsdp_hsdp_reduce_scatter_adamw")
+
+
+def fsdp_zero1_adamw_broadcast(layout: Layout, unit_begin: int, unit_end: int, grad_replicas, master, exp_avg,
+                               exp_avg_sq, param_replicas, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step: int = 1,
+                               stream=None, grad_dtype: Optional[int] = None,
+                               param_dtype: Optional[int] = None) -> None:
+    if len(grad_replicas) != layout.N or len(param_replicas) != layout.N:
+        raise ValueError(f"need {layout.N} gradient and parameter replicas")
+    if grad_dtype is None:
+        grad_dtype = _dtype_code(grad_replicas[0])
+    if param_dtype is None:
+        param_dtype = _dtype_code(param_replicas[0])
+    _check(lib().fsdp_zero1_adamw_broadcast(layout.handle, unit_begin, unit_end, _ptr_array(grad_replicas),
+                                            grad_dtype, _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+                                            _ptr_array(param_replicas), param_dtype, C.byref(_hp(hp)), step,
+                                            _stream(stream)), "fsdp_zero1_adamw_broadcast")
 
 
 def fsdp_reshard(layout: Layout, unit_begin: int, unit_end: int, full=None, master=None, param_shards=None,

@@ -12,13 +12,15 @@
 #include <cuda_runtime.h>
 
 #include "../../include/fsdp_state.h"
+#include "internal.hpp"
 #include "kernels.hpp"
 #include "layout.hpp"
 
 using fsdp::Seg;
 using fsdp::SegList;
 
-namespace {
+namespace fsdp {
+namespace detail {
 
 thread_local char g_cuda_err[256] = "";
 
@@ -42,7 +44,8 @@ int device_tables(const fsdp_layout* Lc, const Seg** base) {
         *base = it->second.base;
         return FSDP_OK;
     }
-    const SegList* lists[] = {&L->data, &L->gather, &L->pad, &L->data_al, &L->data_sh, &L->gather_al, &L->gather_sh};
+    const SegList* lists[] = {&L->data, &L->gather, &L->pad, &L->data_al, &L->data_sh, &L->gather_al, &L->gather_sh,
+                              &L->fullr};
     size_t n = 0;
     for (const SegList* l : lists) n += l->segs.size();
     Seg* d = nullptr;
@@ -64,11 +67,6 @@ int device_tables(const fsdp_layout* Lc, const Seg** base) {
     return FSDP_OK;
 }
 
-// Segment range and tile range of units [ub, ue) in one list.
-struct Range {
-    const Seg* segs;
-    int64_t tile_base, n_tiles;
-};
 Range range_of(const SegList& l, const Seg* dev_base, int32_t ub, int32_t ue) {
     const int32_t sb = l.unit_begin[ub], se = l.unit_begin[ue];
     const int64_t t0 = l.segs[sb].tile0, t1 = l.segs[se].tile0;
@@ -87,7 +85,40 @@ int check_ptr(const void* p) {
     return FSDP_OK;
 }
 
-}  // namespace
+int check_hparams(const fsdp_adamw_hparams* hp) {
+    if (!hp) return FSDP_EINVAL;
+    const float lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
+    if (!std::isfinite(lr) || !std::isfinite(b1) || !std::isfinite(b2) || !std::isfinite(eps) ||
+        !std::isfinite(wd))
+        return FSDP_EINVAL;
+    if (lr < 0.f || b1 < 0.f || b1 >= 1.f || b2 < 0.f || b2 >= 1.f || eps <= 0.f || wd < 0.f ||
+        double(lr) * double(wd) > 1.0)
+        return FSDP_EINVAL;
+    return FSDP_OK;
+}
+
+AdamScal adam_scalars(const fsdp_adamw_hparams* hp, int64_t step, int32_t n_avg) {
+    // formed in double from the fp32 hyper-parameters, rounded once
+    AdamScal sc;
+    const double b1 = hp->beta1, b2 = hp->beta2, lr = hp->lr, wd = hp->weight_decay;
+    const double bc1 = 1.0 - std::pow(b1, double(step));
+    const double bc2 = 1.0 - std::pow(b2, double(step));
+    sc.decay = float(1.0 - lr * wd);
+    sc.om1 = float(1.0 - b1);
+    sc.om2 = float(1.0 - b2);
+    sc.step_size = float(lr / bc1);
+    sc.bc2s = float(std::sqrt(bc2));
+    sc.beta1 = hp->beta1;
+    sc.beta2 = hp->beta2;
+    sc.eps = hp->eps;
+    sc.nf = float(n_avg);
+    return sc;
+}
+
+}  // namespace detail
+}  // namespace fsdp
+
+using namespace fsdp::detail;
 
 extern "C" {
 
@@ -154,7 +185,7 @@ int fsdp_layout_tensor(const fsdp_layout* L, int32_t t, int32_t* unit, int64_t* 
     if (unit) *unit = L->unit[t];
     if (numel) *numel = L->numel[t];
     if (full_off) *full_off = L->t_full_off[t];
-    if (shard_off) *shard_off = L->mode == FSDP_DIM0 ? L->t_shard_off[t] : -1;
+    if (shard_off) *shard_off = L->mode != FSDP_FLAT ? L->t_shard_off[t] : -1;
     if (rows_per_rank) *rows_per_rank = L->mode == FSDP_DIM0 ? L->rows[t] : -1;
     return FSDP_OK;
 }
@@ -163,7 +194,12 @@ int fsdp_layout_segment(const fsdp_layout* L, int32_t t, int32_t r, int64_t* sha
                         int64_t* len, int64_t* pad) {
     if (!L || t < 0 || t >= L->T || r < 0 || r >= L->N) return FSDP_EINVAL;
     int64_t so, fo, n, pd;
-    if (L->mode == FSDP_FLAT) {
+    if (L->mode == FSDP_ZERO1) {
+        so = L->t_shard_off[t];
+        fo = L->t_full_off[t];
+        n = L->owner[t] == r ? L->numel[t] : 0;
+        pd = 0;
+    } else if (L->mode == FSDP_FLAT) {
         const int32_t u = L->unit[t];
         const int64_t Su = L->u_S[u];
         const int64_t a = L->t_unit_off[t], b = a + L->numel[t];   // tensor range in the unit's flat
@@ -188,6 +224,13 @@ int fsdp_layout_segment(const fsdp_layout* L, int32_t t, int32_t r, int64_t* sha
     if (full_off) *full_off = fo;
     if (len) *len = n;
     if (pad) *pad = pd;
+    return FSDP_OK;
+}
+
+int fsdp_layout_owner(const fsdp_layout* L, int32_t t, int32_t* rank) {
+    if (!L || t < 0 || t >= L->T || !rank) return FSDP_EINVAL;
+    if (L->mode != FSDP_ZERO1) return FSDP_EINVAL;
+    *rank = L->owner[t];
     return FSDP_OK;
 }
 
@@ -224,6 +267,7 @@ int fsdp_unshard(const fsdp_layout* L, int32_t ub, int32_t ue, const void* shard
     int rc = check_units(L, ub, ue);
     if (rc) return rc;
     if (elem_dtype != FSDP_F32 && elem_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;          // parameters are replicated: nothing to gather
     if ((rc = check_ptr(shards)) || (rc = check_ptr(full))) return rc;
     const Seg* base = nullptr;
     if ((rc = device_tables(L, &base))) return rc;
@@ -250,27 +294,9 @@ int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, cons
     if ((rc = check_ptr(master)) || (rc = check_ptr(exp_avg)) || (rc = check_ptr(exp_avg_sq))) return rc;
     if (param_shards && !aligned16(param_shards)) return FSDP_EALIGN;
     if (grad_shard_out && !aligned16(grad_shard_out)) return FSDP_EALIGN;
-    const float lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
-    if (!std::isfinite(lr) || !std::isfinite(b1) || !std::isfinite(b2) || !std::isfinite(eps) ||
-        !std::isfinite(wd))
-        return FSDP_EINVAL;
-    if (lr < 0.f || b1 < 0.f || b1 >= 1.f || b2 < 0.f || b2 >= 1.f || eps <= 0.f || wd < 0.f ||
-        double(lr) * double(wd) > 1.0)
-        return FSDP_EINVAL;
-
-    // Step constants: formed in double from the fp32 hyper-parameters, rounded once.
-    fsdp::AdamScal sc;
-    const double bc1 = 1.0 - std::pow(double(b1), double(step));
-    const double bc2 = 1.0 - std::pow(double(b2), double(step));
-    sc.decay = float(1.0 - double(lr) * double(wd));
-    sc.om1 = float(1.0 - double(b1));
-    sc.om2 = float(1.0 - double(b2));
-    sc.step_size = float(double(lr) / bc1);
-    sc.bc2s = float(std::sqrt(bc2));
-    sc.beta1 = b1;
-    sc.beta2 = b2;
-    sc.eps = eps;
-    sc.nf = float(L->N);
+    if ((rc = check_hparams(hp))) return rc;
+    if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;
+    const fsdp::AdamScal sc = adam_scalars(hp, step, L->N);
 
     fsdp::GradPtrs gp{};
     for (int32_t q = 0; q < L->N; ++q) gp.p[q] = grads[q];

@@ -1,0 +1,31 @@
+// internal.hpp -- helpers shared by the libfsdpstate entry points (api.cu, rows.cu).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fsdp_state.h"
+#include "common.cuh"
+#include "layout.hpp"
+
+namespace fsdp {
+namespace detail {
+
+// Segment range and tile range of units [ub, ue) in one list.
+struct Range {
+    const Seg* segs;
+    int64_t tile_base, n_tiles;
+};
+
+int cuda_fail(cudaError_t e, const char* where);        // records the error text, returns FSDP_ECUDA
+bool aligned16(const void* p);
+int device_tables(const fsdp_layout* L, const Seg** base);   // per-device copy of the segment lists
+Range range_of(const SegList& l, const Seg* dev_base, int32_t ub, int32_t ue);
+int check_units(const fsdp_layout* L, int32_t ub, int32_t ue);
+int check_ptr(const void* p);                            // non-NULL and 16-byte aligned
+int check_hparams(const fsdp_adamw_hparams* hp);
+AdamScal adam_scalars(const fsdp_adamw_hparams* hp, int64_t step, int32_t n_avg);
+
+}  // namespace detail
+}  // namespace fsdp

@@ -45,7 +45,7 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
                  const int32_t* unit_id, const int32_t* dtype, int32_t N, int32_t mode) {
     if (T < 1 || !ndim || !dims || !unit_id) return FSDP_EINVAL;
     if (N < 1 || N > FSDP_MAX_RANKS) return FSDP_EINVAL;
-    if (mode != FSDP_FLAT && mode != FSDP_DIM0) return FSDP_EINVAL;
+    if (mode != FSDP_FLAT && mode != FSDP_DIM0 && mode != FSDP_ZERO1) return FSDP_EINVAL;
     if (unit_id[0] != 0) return FSDP_ESHAPE;
     for (int32_t t = 1; t < T; ++t)
         if (unit_id[t] != unit_id[t - 1] && unit_id[t] != unit_id[t - 1] + 1) return FSDP_ESHAPE;
@@ -106,6 +106,42 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
         L->S = so; L->F = fo;
         for (int32_t t = 0; t < T; ++t)
             L->t_full_off[t] = L->u_full_off[L->unit[t]] + L->t_unit_off[t];
+    } else if (mode == FSDP_ZERO1) {
+        // Whole tensors on owner ranks: largest first (stable), each to the rank
+        // holding the fewest elements so far, lowest rank on ties.  In its owner's
+        // row a tensor sits at an offset congruent to its full offset mod 8.
+        std::vector<int32_t> order(T);
+        for (int32_t t = 0; t < T; ++t) order[t] = t;
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int32_t a, int32_t b) { return L->numel[a] > L->numel[b]; });
+        std::vector<int64_t> load(N, 0);
+        L->owner.assign(T, 0);
+        for (int32_t t : order) {
+            int32_t best = 0;
+            for (int32_t r = 1; r < N; ++r)
+                if (load[r] < load[best]) best = r;
+            L->owner[t] = best;
+            load[best] += L->numel[t];
+        }
+        int64_t fo = 0;
+        std::vector<int64_t> fill(N, 0);
+        for (int32_t t = 0; t < T; ++t) {
+            L->t_full_off[t] = fo;
+            const int32_t o = L->owner[t];
+            const int64_t at = fill[o] + ((fo - fill[o]) & (kVec - 1));   // == fo (mod 8)
+            L->t_shard_off[t] = at;
+            fill[o] = at + L->numel[t];
+            if (!add_ok(fo, L->numel[t], &fo)) return FSDP_EOVERFLOW;
+        }
+        int64_t S = 0;
+        for (int32_t r = 0; r < N; ++r) S = std::max(S, fill[r]);
+        L->S = S; L->F = fo;
+        for (int32_t t = 0; t < T; ++t) {
+            const int32_t u = L->unit[t];
+            if (t == 0 || L->unit[t - 1] != u) L->u_full_off[u] = L->t_full_off[t];
+            L->u_shard_off[u] = 0;
+            L->u_S[u] = S;                       // every unit spans the owner rows
+        }
     } else {
         int64_t so = 0, fo = 0;
         for (int32_t t = 0; t < T; ++t) {
@@ -136,7 +172,9 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
     int64_t aligned_elems[kVec] = {0};
     for (int32_t u = 0; u < U; ++u) {
         for (int32_t r = 0; r < N; ++r) {
-            if (mode == FSDP_FLAT) {
+            if (mode == FSDP_ZERO1) {
+                break;
+            } else if (mode == FSDP_FLAT) {
                 const int64_t own = std::max<int64_t>(0, std::min(L->u_S[u], L->u_numel[u] - int64_t(r) * L->u_S[u]));
                 for (int sig = 0; sig < kVec; ++sig) {
                     const int64_t dlt = L->u_full_off[u] + int64_t(r) * L->u_S[u] - int64_t(r) * sig - L->u_shard_off[u];
@@ -158,7 +196,7 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
         }
     }
     int best = 0;
-    for (int sig = 1; sig < kVec; ++sig)
+    for (int sig = 1; sig < kVec && mode != FSDP_ZERO1; ++sig)
         if (aligned_elems[sig] > aligned_elems[best]) best = sig;
     int64_t stride;
     if (best == 0) {
@@ -175,7 +213,8 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
     L->stride = stride;
 
     // Segment lists, per unit: rank-major, then tensor order.
-    SegList* lists[] = {&L->data, &L->gather, &L->pad, &L->data_al, &L->data_sh, &L->gather_al, &L->gather_sh};
+    SegList* lists[] = {&L->data, &L->gather, &L->pad, &L->data_al, &L->data_sh, &L->gather_al, &L->gather_sh,
+                        &L->fullr};
     for (SegList* l : lists) {
         l->segs.clear();
         l->unit_begin.assign(U + 1, 0);
@@ -183,6 +222,34 @@ int build_layout(fsdp_layout* L, int32_t T, const int32_t* ndim, const int64_t* 
     int64_t n_data = 0;
     for (int32_t u = 0; u < U; ++u) {
         for (SegList* l : lists) l->unit_begin[u] = int32_t(l->segs.size());
+        // logical full-layout ranges of the unit
+        if (mode == FSDP_FLAT) {
+            push(L->fullr, L->u_full_off[u], L->u_full_off[u], L->u_numel[u]);
+        } else {
+            for (int32_t t = 0; t < T; ++t)
+                if (L->unit[t] == u) push(L->fullr, L->t_full_off[t], L->t_full_off[t], L->numel[t]);
+        }
+        if (mode == FSDP_ZERO1) {
+            for (int32_t t = 0; t < T; ++t) {
+                if (L->unit[t] != u) continue;
+                const int64_t sh = int64_t(L->owner[t]) * stride + L->t_shard_off[t];
+                push2(L->data, L->data_al, L->data_sh, sh, L->t_full_off[t], L->numel[t]);
+                if (L->numel[t] > 0) ++n_data;
+            }
+            if (u == U - 1) {                       // each row's unused tail: zero at reshard
+                std::vector<std::pair<int64_t, int64_t>> used;
+                for (int32_t r = 0; r < N; ++r) {
+                    int64_t at = 0;
+                    for (int32_t t = 0; t < T; ++t) {
+                        if (L->owner[t] != r) continue;
+                        push(L->pad, int64_t(r) * stride + at, -1, L->t_shard_off[t] - at);   // alignment gap
+                        at = L->t_shard_off[t] + L->numel[t];
+                    }
+                    push(L->pad, int64_t(r) * stride + at, -1, stride - at);
+                }
+            }
+            continue;
+        }
         for (int32_t r = 0; r < N; ++r) {
             const int64_t row = int64_t(r) * stride;
             if (mode == FSDP_FLAT) {

@@ -6,6 +6,8 @@
 //   data    (rank, piece) -> logical elements:        reduce-scatter+AdamW, reshard
 //   gather  (rank, piece) -> elements the all-gather copies:  unshard
 //           (FLAT: the whole S_u slot, padding included; DIM0: the owned rows)
+//   fullr   the logical ranges of the full layout, tiled on the full side:
+//           per-replica work on the gradients (accumulation)
 //   pad     (rank, piece) -> padding elements of the shard rows (and, attached to
 //           the last unit, each row's physical tail [S, stride)): reshard zero-fill,
 //           grad_shard_out zero-fill
@@ -44,6 +46,8 @@ struct fsdp_layout {
     std::vector<int64_t> u_numel, u_S, u_shard_off, u_full_off;
     fsdp::SegList data, gather, pad;
     fsdp::SegList data_al, data_sh, gather_al, gather_sh;   // split by alignment class
+    fsdp::SegList fullr;        // logical full-layout ranges (shard field = full index)
+    std::vector<int32_t> owner;  // ZeRO-1: owner rank of each tensor
     int64_t n_data_segments = 0;
 
     std::mutex mu;                                  // guards dev

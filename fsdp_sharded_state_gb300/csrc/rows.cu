@@ -1,0 +1,591 @@
+// rows.cu -- the rows beyond the core step: sharded clip_grad_norm_ before AdamW,
+// gradient accumulation without sync, HSDP (shard groups x replica groups) and the
+// ZeRO-1 owner step with its broadcast.  Same tile machinery, segment lists and
+// AdamW element as the core kernels (common.cuh, device_ops.cuh).
+#include <cmath>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "device_ops.cuh"
+#include "internal.hpp"
+#include "kernels.hpp"
+
+using fsdp::Seg;
+using namespace fsdp::detail;
+
+namespace fsdp {
+namespace {
+
+constexpr int kMaxPartials = 4096;                  // per launch of the norm pass
+constexpr size_t kClipHeader = 64;                  // double norm, float coef
+constexpr size_t kClipWorkspace = kClipHeader + 2 * kMaxPartials * sizeof(double);
+
+std::mutex g_grid_mu;
+std::map<std::pair<const void*, int>, int> g_grid_cache;
+
+template <typename K>
+int grid_of(K kernel, int64_t n_tiles, int cap = 1 << 30) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+    int blocks = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_grid_mu);
+        auto it = g_grid_cache.find(key);
+        if (it != g_grid_cache.end()) blocks = it->second;
+    }
+    if (blocks == 0) {
+        int sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+        blocks = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+        std::lock_guard<std::mutex> lk(g_grid_mu);
+        g_grid_cache[key] = blocks;
+    }
+    int64_t g = n_tiles < blocks ? n_tiles : blocks;
+    return int(g < cap ? g : cap);
+}
+
+__device__ __forceinline__ int64_t tile_e0(const Seg& sg, int64_t gt) {
+    return (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
+}
+
+// Sum of a double over the CTA in a fixed order (warp trees, then warp 0 in order).
+__device__ __forceinline__ double block_sum(double x) {
+    __shared__ double warp_part[kThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+    if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = x;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kThreads / 32; ++w) t += warp_part[w];
+    return t;                                   // valid in thread 0
+}
+
+// ---------------------------------------------------------------------------
+// Sharded clip_grad_norm_: (1) reduce-scatter into the fp32 gradient shard and
+// per-CTA sums of squares; (2) the norm and the clip coefficient; (3) AdamW on
+// the scaled shard.
+// ---------------------------------------------------------------------------
+template <typename GT, bool SHIFT>
+__global__ void __launch_bounds__(kThreads, 2)
+k_rs_norm(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N, int64_t F,
+          float* __restrict__ gout, float nf, double* __restrict__ part) {
+    const bool lane31 = (threadIdx.x & 31) == 31;
+    double ss = 0.0;
+    int s = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int64_t gt = tile_base + t;
+        s = advance_seg(segs, s, gt);
+        const Seg sg = segs[s];
+        const int64_t e0 = tile_e0(sg, gt);
+        const int64_t lo = sg.shard, hi = sg.shard + sg.len, delta = sg.full - sg.shard;
+        const int64_t f0 = e0 + delta;
+        const bool interior = e0 >= lo && e0 + kVec <= hi;
+        const int d = int(delta & (kVec - 1));
+        const int64_t fa = f0 - d;
+        const bool have_a = fa >= 0 && fa + kVec <= F;
+        const bool have_b = fa >= 0 && fa + 2 * kVec <= F;
+        const bool fast = SHIFT ? (interior && have_a && have_b) : interior;
+        float acc[8];
+        if (!SHIFT) {
+            if (e0 >= hi) continue;
+            if (fast) reduce8_vec<GT>(gp, N, f0, acc);
+        } else {
+            reduce8_shift<GT>(d, gp, N, fa, have_a, have_b, lane31, acc);
+            if (e0 >= hi) continue;
+        }
+        if (fast) {
+            float g[8], sq = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                g[k] = __fdiv_rn(acc[k], nf);
+                sq = __fmaf_rn(g[k], g[k], sq);
+            }
+            st4(gout + e0, make_float4(g[0], g[1], g[2], g[3]));
+            st4(gout + e0 + 4, make_float4(g[4], g[5], g[6], g[7]));
+            ss += double(sq);
+        } else {
+            const int64_t a = e0 > lo ? e0 : lo, b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
+            for (int64_t e = a; e < b; ++e) {
+                const float g = __fdiv_rn(reduce1<GT>(gp, N, e + delta), nf);
+                gout[e] = g;
+                ss += double(g) * double(g);
+            }
+        }
+    }
+    const double tot = block_sum(ss);
+    if (threadIdx.x == 0) part[blockIdx.x] = tot;
+}
+
+__global__ void k_norm_finalize(const double* __restrict__ part, int n_part, float max_norm,
+                                double* __restrict__ ws_norm, float* __restrict__ ws_coef,
+                                float* __restrict__ norm_out) {
+    double x = 0.0;
+    for (int i = threadIdx.x; i < n_part; i += blockDim.x) x += part[i];
+    const double tot = block_sum(x);
+    if (threadIdx.x == 0) {
+        const double norm = sqrt(tot);
+        double c = double(max_norm) / (norm + 1e-6);
+        if (c > 1.0) c = 1.0;
+        *ws_norm = norm;
+        *ws_coef = float(c);
+        if (norm_out) {
+            norm_out[0] = float(norm);
+            norm_out[1] = float(c);
+        }
+    }
+}
+
+template <bool PARAM>
+__global__ void __launch_bounds__(kThreads, 3)
+k_adamw_scaled(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, float* __restrict__ gshard,
+               const float* __restrict__ coef_p, float* __restrict__ master, float* __restrict__ exp_avg,
+               float* __restrict__ exp_avg_sq, uint16_t* __restrict__ param, AdamScal sc) {
+    const float coef = *coef_p;
+    int s = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int64_t gt = tile_base + t;
+        s = advance_seg(segs, s, gt);
+        const Seg sg = segs[s];
+        const int64_t e0 = tile_e0(sg, gt);
+        const int64_t lo = sg.shard, hi = sg.shard + sg.len;
+        if (e0 >= hi) continue;
+        if (e0 >= lo && e0 + kVec <= hi) {
+            const float4 g0 = ld4(gshard + e0), g1 = ld4(gshard + e0 + 4);
+            const float4 p0 = ld4(master + e0), p1 = ld4(master + e0 + 4);
+            const float4 m0 = ld4(exp_avg + e0), m1 = ld4(exp_avg + e0 + 4);
+            const float4 v0 = ld4(exp_avg_sq + e0), v1 = ld4(exp_avg_sq + e0 + 4);
+            float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                g[k] = __fmul_rn(g[k], coef);
+                adamw1(sc, g[k], p[k], m[k], v[k]);
+            }
+            st4(gshard + e0, make_float4(g[0], g[1], g[2], g[3]));
+            st4(gshard + e0 + 4, make_float4(g[4], g[5], g[6], g[7]));
+            st4(master + e0, make_float4(p[0], p[1], p[2], p[3]));
+            st4(master + e0 + 4, make_float4(p[4], p[5], p[6], p[7]));
+            st4(exp_avg + e0, make_float4(m[0], m[1], m[2], m[3]));
+            st4(exp_avg + e0 + 4, make_float4(m[4], m[5], m[6], m[7]));
+            st4(exp_avg_sq + e0, make_float4(v[0], v[1], v[2], v[3]));
+            st4(exp_avg_sq + e0 + 4, make_float4(v[4], v[5], v[6], v[7]));
+            if (PARAM)
+                stu4(param + e0, make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                                            pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7])));
+        } else {
+            const int64_t a = e0 > lo ? e0 : lo, b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
+            for (int64_t e = a; e < b; ++e) {
+                const float g = __fmul_rn(gshard[e], coef);
+                float p = master[e], m = exp_avg[e], v = exp_avg_sq[e];
+                adamw1(sc, g, p, m, v);
+                gshard[e] = g; master[e] = p; exp_avg[e] = m; exp_avg_sq[e] = v;
+                if (PARAM) param[e] = to_bf16(p);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Gradient accumulation: acc[q] = micro[q] (first) or acc[q] + micro[q], fp32,
+// over the logical full-layout ranges (tiles on the full side).
+// ---------------------------------------------------------------------------
+struct AccPtrs {
+    float* acc[kMaxRanks];
+    const void* micro[kMaxRanks];
+};
+
+template <typename MT>
+__global__ void __launch_bounds__(kThreads)
+k_accumulate(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, AccPtrs ap, int N, int first) {
+    int s = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int64_t gt = tile_base + t;
+        s = advance_seg(segs, s, gt);
+        const Seg sg = segs[s];
+        const int64_t e0 = tile_e0(sg, gt);
+        const int64_t lo = sg.shard, hi = sg.shard + sg.len;
+        if (e0 >= hi) continue;
+        if (e0 >= lo && e0 + kVec <= hi) {
+#pragma unroll 1
+            for (int q = 0; q < N; ++q) {
+                float x[8];
+                const typename GradIO<MT>::Vec mv = GradIO<MT>::load(ap.micro[q], e0);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x[k] = GradIO<MT>::elem(mv, mv, k);
+                float* a = ap.acc[q] + e0;
+                if (!first) {
+                    const float4 a0 = ld4(a), a1 = ld4(a + 4);
+                    x[0] = __fadd_rn(a0.x, x[0]); x[1] = __fadd_rn(a0.y, x[1]);
+                    x[2] = __fadd_rn(a0.z, x[2]); x[3] = __fadd_rn(a0.w, x[3]);
+                    x[4] = __fadd_rn(a1.x, x[4]); x[5] = __fadd_rn(a1.y, x[5]);
+                    x[6] = __fadd_rn(a1.z, x[6]); x[7] = __fadd_rn(a1.w, x[7]);
+                }
+                st4(a, make_float4(x[0], x[1], x[2], x[3]));
+                st4(a + 4, make_float4(x[4], x[5], x[6], x[7]));
+            }
+        } else {
+            const int64_t a = e0 > lo ? e0 : lo, b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
+            for (int q = 0; q < N; ++q)
+                for (int64_t e = a; e < b; ++e) {
+                    const float x = GradIO<MT>::load1(ap.micro[q], e);
+                    ap.acc[q][e] = first ? x : __fadd_rn(ap.acc[q][e], x);
+                }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// HSDP: g = (sum over groups rho of (sum over q of G[rho*N + q]) / N) / R, then
+// the same AdamW on each group's copy of the state (copy rho at rho*copy).
+// Aligned segments take 16-byte vectors; shifted ones go element by element.
+// ---------------------------------------------------------------------------
+template <typename GT, bool PARAM>
+__global__ void __launch_bounds__(kThreads, 2)
+k_hsdp_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N, int R,
+             int64_t copy, float* __restrict__ master, float* __restrict__ exp_avg,
+             float* __restrict__ exp_avg_sq, uint16_t* __restrict__ param, AdamScal sc, float rf) {
+    int s = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int64_t gt = tile_base + t;
+        s = advance_seg(segs, s, gt);
+        const Seg sg = segs[s];
+        const int64_t e0 = tile_e0(sg, gt);
+        const int64_t lo = sg.shard, hi = sg.shard + sg.len, delta = sg.full - sg.shard;
+        if (e0 >= hi) continue;
+        // 16-byte vectors need the gradients aligned where the state is, and every
+        // state copy's base (rho * copy) on an 8-element boundary
+        const bool vec = e0 >= lo && e0 + kVec <= hi && ((delta * int64_t(sizeof(GT))) & 15) == 0 &&
+                         (copy & (kVec - 1)) == 0;
+        if (vec) {
+            float g[8], outer[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) outer[k] = 0.0f;
+#pragma unroll 1
+            for (int rho = 0; rho < R; ++rho) {
+                float acc[8];
+                reduce8_vec<GT>(gp, N, e0 + delta, acc, rho * N);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) outer[k] = __fadd_rn(outer[k], __fdiv_rn(acc[k], sc.nf));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) g[k] = __fdiv_rn(outer[k], rf);
+#pragma unroll 1
+            for (int rho = 0; rho < R; ++rho) {
+                const int64_t e = rho * copy + e0;
+                const float4 p0 = ld4(master + e), p1 = ld4(master + e + 4);
+                const float4 m0 = ld4(exp_avg + e), m1 = ld4(exp_avg + e + 4);
+                const float4 v0 = ld4(exp_avg_sq + e), v1 = ld4(exp_avg_sq + e + 4);
+                float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+                float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) adamw1(sc, g[k], p[k], m[k], v[k]);
+                st4(master + e, make_float4(p[0], p[1], p[2], p[3]));
+                st4(master + e + 4, make_float4(p[4], p[5], p[6], p[7]));
+                st4(exp_avg + e, make_float4(m[0], m[1], m[2], m[3]));
+                st4(exp_avg + e + 4, make_float4(m[4], m[5], m[6], m[7]));
+                st4(exp_avg_sq + e, make_float4(v[0], v[1], v[2], v[3]));
+                st4(exp_avg_sq + e + 4, make_float4(v[4], v[5], v[6], v[7]));
+                if (PARAM)
+                    stu4(param + e, make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                                               pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7])));
+            }
+        } else {
+            const int64_t a = e0 > lo ? e0 : lo, b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
+            for (int64_t e = a; e < b; ++e) {
+                float outer = 0.0f;
+                for (int rho = 0; rho < R; ++rho) {
+                    float acc = 0.0f;
+                    for (int q = 0; q < N; ++q) acc = __fadd_rn(acc, GradIO<GT>::load1(gp.p[rho * N + q], e + delta));
+                    outer = __fadd_rn(outer, __fdiv_rn(acc, sc.nf));
+                }
+                const float g = __fdiv_rn(outer, rf);
+                for (int rho = 0; rho < R; ++rho) {
+                    const int64_t x = rho * copy + e;
+                    float p = master[x], m = exp_avg[x], v = exp_avg_sq[x];
+                    adamw1(sc, g, p, m, v);
+                    master[x] = p; exp_avg[x] = m; exp_avg_sq[x] = v;
+                    if (PARAM) param[x] = to_bf16(p);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// ZeRO-1: g = mean over the N replicas; the owner's AdamW (master in its row,
+// or, for fp32 parameters, the owner's own replica); the broadcast writes the
+// updated parameter into all N replicas.  Owner rows keep every tensor congruent
+// to its full offset mod 8, so all segments take 16-byte vectors.
+// ---------------------------------------------------------------------------
+struct ParamPtrs {
+    void* p[kMaxRanks];
+};
+
+template <typename GT, bool MASTER>
+__global__ void __launch_bounds__(kThreads, 2)
+k_zero1_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N,
+              int64_t stride, float* __restrict__ master, float* __restrict__ exp_avg,
+              float* __restrict__ exp_avg_sq, ParamPtrs pp, AdamScal sc) {
+    int s = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int64_t gt = tile_base + t;
+        s = advance_seg(segs, s, gt);
+        const Seg sg = segs[s];
+        const int64_t e0 = tile_e0(sg, gt);
+        const int64_t lo = sg.shard, hi = sg.shard + sg.len, delta = sg.full - sg.shard;
+        if (e0 >= hi) continue;
+        const int owner = int(sg.shard / stride);
+        if (e0 >= lo && e0 + kVec <= hi && (delta & (kVec - 1)) == 0) {
+            const int64_t f0 = e0 + delta;
+            float p[8];
+            if (MASTER) {
+                const float4 p0 = ld4(master + e0), p1 = ld4(master + e0 + 4);
+                p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w; p[4] = p1.x; p[5] = p1.y; p[6] = p1.z; p[7] = p1.w;
+            } else {
+                const float* w = static_cast<const float*>(pp.p[owner]) + f0;
+                const float4 p0 = ld4(w), p1 = ld4(w + 4);
+                p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w; p[4] = p1.x; p[5] = p1.y; p[6] = p1.z; p[7] = p1.w;
+            }
+            const float4 m0 = ld4(exp_avg + e0), m1 = ld4(exp_avg + e0 + 4);
+            const float4 v0 = ld4(exp_avg_sq + e0), v1 = ld4(exp_avg_sq + e0 + 4);
+            float acc[8];
+            reduce8_vec<GT>(gp, N, f0, acc);
+            float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) adamw1(sc, __fdiv_rn(acc[k], sc.nf), p[k], m[k], v[k]);
+            if (MASTER) {
+                st4(master + e0, make_float4(p[0], p[1], p[2], p[3]));
+                st4(master + e0 + 4, make_float4(p[4], p[5], p[6], p[7]));
+            }
+            st4(exp_avg + e0, make_float4(m[0], m[1], m[2], m[3]));
+            st4(exp_avg + e0 + 4, make_float4(m[4], m[5], m[6], m[7]));
+            st4(exp_avg_sq + e0, make_float4(v[0], v[1], v[2], v[3]));
+            st4(exp_avg_sq + e0 + 4, make_float4(v[4], v[5], v[6], v[7]));
+            if (MASTER) {                         // bf16 replicas
+                const uint4 w = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                                           pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+#pragma unroll 1
+                for (int q = 0; q < N; ++q) stu4(static_cast<uint16_t*>(pp.p[q]) + f0, w);
+            } else {                              // fp32 replicas
+#pragma unroll 1
+                for (int q = 0; q < N; ++q) {
+                    float* w = static_cast<float*>(pp.p[q]) + f0;
+                    st4(w, make_float4(p[0], p[1], p[2], p[3]));
+                    st4(w + 4, make_float4(p[4], p[5], p[6], p[7]));
+                }
+            }
+        } else {
+            const int64_t a = e0 > lo ? e0 : lo, b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
+            for (int64_t e = a; e < b; ++e) {
+                const int64_t f = e + delta;
+                float p = MASTER ? master[e] : static_cast<const float*>(pp.p[owner])[f];
+                float m = exp_avg[e], v = exp_avg_sq[e];
+                adamw1(sc, __fdiv_rn(reduce1<GT>(gp, N, f), sc.nf), p, m, v);
+                if (MASTER) master[e] = p;
+                exp_avg[e] = m; exp_avg_sq[e] = v;
+                for (int q = 0; q < N; ++q) {
+                    if (MASTER) static_cast<uint16_t*>(pp.p[q])[f] = to_bf16(p);
+                    else static_cast<float*>(pp.p[q])[f] = p;
+                }
+            }
+        }
+    }
+}
+
+int ptrs_ok(const void* const* v, int n) {
+    if (!v) return FSDP_EINVAL;
+    for (int i = 0; i < n; ++i) {
+        const int rc = check_ptr(v[i]);
+        if (rc) return rc;
+    }
+    return FSDP_OK;
+}
+
+}  // namespace
+}  // namespace fsdp
+
+using namespace fsdp;
+
+extern "C" {
+
+size_t fsdp_clip_workspace_bytes(void) { return kClipWorkspace; }
+
+int fsdp_reduce_scatter_clip_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, const void* const* grads,
+                                   int32_t grad_dtype, float* master, float* exp_avg, float* exp_avg_sq,
+                                   void* param_shards, float* grad_shard, float max_norm, void* workspace,
+                                   float* norm_out, const fsdp_adamw_hparams* hp, int64_t step,
+                                   fsdp_stream_t stream) {
+    int rc = check_units(L, ub, ue);
+    if (rc) return rc;
+    if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;
+    if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if (step < 1 || !(max_norm > 0.f) || !std::isfinite(max_norm)) return FSDP_EINVAL;
+    if ((rc = ptrs_ok(grads, L->N)) || (rc = check_ptr(master)) || (rc = check_ptr(exp_avg)) ||
+        (rc = check_ptr(exp_avg_sq)) || (rc = check_ptr(grad_shard)) || (rc = check_ptr(workspace)))
+        return rc;
+    if (param_shards && !aligned16(param_shards)) return FSDP_EALIGN;
+    if (norm_out && (reinterpret_cast<uintptr_t>(norm_out) & 7u)) return FSDP_EALIGN;
+    if ((rc = check_hparams(hp))) return rc;
+    const AdamScal sc = adam_scalars(hp, step, L->N);
+    GradPtrs gp{};
+    for (int32_t q = 0; q < L->N; ++q) gp.p[q] = grads[q];
+    const Seg* base = nullptr;
+    if ((rc = device_tables(L, &base))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    double* ws_norm = reinterpret_cast<double*>(ws);
+    float* ws_coef = reinterpret_cast<float*>(ws + 8);
+    double* part = reinterpret_cast<double*>(ws + kClipHeader);
+
+    // (1) reduce-scatter + sums of squares, one partial per CTA, per alignment class
+    int n_part = 0;
+    for (int shifted = 0; shifted < 2; ++shifted) {
+        const Range R = range_of(shifted ? L->data_sh : L->data_al, base, ub, ue);
+        if (R.n_tiles <= 0) continue;
+        const bool bf = grad_dtype == FSDP_BF16;
+        auto launch = [&](auto kernel) {
+            const int grid = grid_of(kernel, R.n_tiles, kMaxPartials);
+            kernel<<<grid, kThreads, 0, st>>>(R.segs, R.tile_base, R.n_tiles, gp, L->N, L->F, grad_shard,
+                                              float(L->N), part + n_part);
+            n_part += grid;
+        };
+        if (bf) shifted ? launch(k_rs_norm<uint16_t, true>) : launch(k_rs_norm<uint16_t, false>);
+        else shifted ? launch(k_rs_norm<float, true>) : launch(k_rs_norm<float, false>);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "k_rs_norm launch");
+    }
+    // padding of the gradient shard: +0
+    const Range P = range_of(L->pad, base, ub, ue);
+    cudaError_t e = fsdp::launch_zero_pad(P.segs, P.tile_base, P.n_tiles, grad_shard, nullptr, st);
+    if (e != cudaSuccess) return cuda_fail(e, "k_zero_pad launch");
+    // (2) norm and coefficient
+    k_norm_finalize<<<1, kThreads, 0, st>>>(part, n_part, max_norm, ws_norm, ws_coef, norm_out);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "k_norm_finalize launch");
+    // (3) AdamW on the scaled shard
+    const Range D = range_of(L->data, base, ub, ue);
+    if (D.n_tiles > 0) {
+        if (param_shards) {
+            auto k = k_adamw_scaled<true>;
+            k<<<grid_of(k, D.n_tiles), kThreads, 0, st>>>(D.segs, D.tile_base, D.n_tiles, grad_shard, ws_coef,
+                                                          master, exp_avg, exp_avg_sq,
+                                                          static_cast<uint16_t*>(param_shards), sc);
+        } else {
+            auto k = k_adamw_scaled<false>;
+            k<<<grid_of(k, D.n_tiles), kThreads, 0, st>>>(D.segs, D.tile_base, D.n_tiles, grad_shard, ws_coef,
+                                                          master, exp_avg, exp_avg_sq, nullptr, sc);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "k_adamw_scaled launch");
+    }
+    return FSDP_OK;
+}
+
+int fsdp_accumulate_grads(const fsdp_layout* L, int32_t ub, int32_t ue, float* const* acc,
+                          const void* const* micro, int32_t micro_dtype, int32_t first, fsdp_stream_t stream) {
+    int rc = check_units(L, ub, ue);
+    if (rc) return rc;
+    if (micro_dtype != FSDP_F32 && micro_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if (!acc || !micro) return FSDP_EINVAL;
+    if ((rc = ptrs_ok(reinterpret_cast<const void* const*>(acc), L->N)) || (rc = ptrs_ok(micro, L->N))) return rc;
+    AccPtrs ap{};
+    for (int32_t q = 0; q < L->N; ++q) {
+        ap.acc[q] = acc[q];
+        ap.micro[q] = micro[q];
+    }
+    const Seg* base = nullptr;
+    if ((rc = device_tables(L, &base))) return rc;
+    const Range R = range_of(L->fullr, base, ub, ue);
+    if (R.n_tiles <= 0) return FSDP_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (micro_dtype == FSDP_BF16) {
+        auto k = k_accumulate<uint16_t>;
+        k<<<grid_of(k, R.n_tiles), kThreads, 0, st>>>(R.segs, R.tile_base, R.n_tiles, ap, L->N, first ? 1 : 0);
+    } else {
+        auto k = k_accumulate<float>;
+        k<<<grid_of(k, R.n_tiles), kThreads, 0, st>>>(R.segs, R.tile_base, R.n_tiles, ap, L->N, first ? 1 : 0);
+    }
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "k_accumulate launch");
+}
+
+int fsdp_hsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, int32_t n_groups,
+                                   const void* const* grads, int32_t grad_dtype, float* master, float* exp_avg,
+                                   float* exp_avg_sq, void* param_shards, const fsdp_adamw_hparams* hp,
+                                   int64_t step, fsdp_stream_t stream) {
+    int rc = check_units(L, ub, ue);
+    if (rc) return rc;
+    if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;
+    if (n_groups < 1 || int64_t(n_groups) * L->N > kMaxRanks || step < 1) return FSDP_EINVAL;
+    if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if ((rc = ptrs_ok(grads, n_groups * L->N)) || (rc = check_ptr(master)) || (rc = check_ptr(exp_avg)) ||
+        (rc = check_ptr(exp_avg_sq)))
+        return rc;
+    if (param_shards && !aligned16(param_shards)) return FSDP_EALIGN;
+    if ((rc = check_hparams(hp))) return rc;
+    const AdamScal sc = adam_scalars(hp, step, L->N);
+    GradPtrs gp{};
+    for (int32_t q = 0; q < n_groups * L->N; ++q) gp.p[q] = grads[q];
+    const Seg* base = nullptr;
+    if ((rc = device_tables(L, &base))) return rc;
+    const Range D = range_of(L->data, base, ub, ue);
+    if (D.n_tiles <= 0) return FSDP_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t copy = int64_t(L->N) * L->stride;
+    auto launch = [&](auto k) {
+        k<<<grid_of(k, D.n_tiles), kThreads, 0, st>>>(D.segs, D.tile_base, D.n_tiles, gp, L->N, n_groups, copy,
+                                                      master, exp_avg, exp_avg_sq,
+                                                      static_cast<uint16_t*>(param_shards), sc, float(n_groups));
+    };
+    const bool bf = grad_dtype == FSDP_BF16;
+    if (param_shards) bf ? launch(k_hsdp_adamw<uint16_t, true>) : launch(k_hsdp_adamw<float, true>);
+    else bf ? launch(k_hsdp_adamw<uint16_t, false>) : launch(k_hsdp_adamw<float, false>);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "k_hsdp_adamw launch");
+}
+
+int fsdp_zero1_adamw_broadcast(const fsdp_layout* L, int32_t ub, int32_t ue, const void* const* grads,
+                               int32_t grad_dtype, float* master, float* exp_avg, float* exp_avg_sq,
+                               void* const* param_replicas, int32_t param_dtype, const fsdp_adamw_hparams* hp,
+                               int64_t step, fsdp_stream_t stream) {
+    int rc = check_units(L, ub, ue);
+    if (rc) return rc;
+    if (L->mode != FSDP_ZERO1 || step < 1) return FSDP_EINVAL;
+    if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if (param_dtype != FSDP_F32 && param_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if ((param_dtype == FSDP_BF16) != (master != nullptr)) return FSDP_EINVAL;   // bf16 replicas need a master
+    if ((rc = ptrs_ok(grads, L->N)) || (rc = ptrs_ok(const_cast<const void* const*>(param_replicas), L->N)) ||
+        (rc = check_ptr(exp_avg)) || (rc = check_ptr(exp_avg_sq)))
+        return rc;
+    if (master && !aligned16(master)) return FSDP_EALIGN;
+    if ((rc = check_hparams(hp))) return rc;
+    const AdamScal sc = adam_scalars(hp, step, L->N);
+    GradPtrs gp{};
+    ParamPtrs pp{};
+    for (int32_t q = 0; q < L->N; ++q) {
+        gp.p[q] = grads[q];
+        pp.p[q] = param_replicas[q];
+    }
+    const Seg* base = nullptr;
+    if ((rc = device_tables(L, &base))) return rc;
+    const Range D = range_of(L->data, base, ub, ue);
+    if (D.n_tiles <= 0) return FSDP_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    auto launch = [&](auto k) {
+        k<<<grid_of(k, D.n_tiles), kThreads, 0, st>>>(D.segs, D.tile_base, D.n_tiles, gp, L->N, L->stride, master,
+                                                      exp_avg, exp_avg_sq, pp, sc);
+    };
+    const bool bf = grad_dtype == FSDP_BF16;
+    if (master) bf ? launch(k_zero1_adamw<uint16_t, true>) : launch(k_zero1_adamw<float, true>);
+    else bf ? launch(k_zero1_adamw<uint16_t, false>) : launch(k_zero1_adamw<float, false>);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "k_zero1_adamw launch");
+}
+
+}  // extern "C"

@@ -49,6 +49,7 @@
 #ifndef FSDP_STATE_H
 #define FSDP_STATE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -73,8 +74,15 @@ typedef enum {
  * DIM0 = FSDP2 per-parameter Shard(0) ([FSDP2-doc] "DTensor": [4096,4096] on 8
  * ranks -> [512,4096]; [titan] §2.3): each tensor of d0 rows gets a slot of
  * c = ceil(d0/N) rows on every rank; rank r owns rows [min(rc,d0), min((r+1)c,d0)),
- * the rest of its slot is zero padding (a rank may own no row). */
-typedef enum { FSDP_FLAT = 0, FSDP_DIM0 = 1 } fsdp_mode;
+ * the rest of its slot is zero padding (a rank may own no row).
+ * ZERO1 = ZeRO-1 owner partition ([ZeRO-state] "ZeRO-1：Optimizer State
+ * Sharding"): parameters stay whole and replicated; each tensor's optimizer state
+ * lives on one owner rank.  Owners: tensors by size, largest first, each to the
+ * rank with the fewest elements so far (lowest rank on ties) -- balanced by size,
+ * not by count.  The owner's row holds its tensors in tensor order, each at an
+ * offset congruent to its full-layout offset mod 8.  The full layout is the
+ * tensors concatenated (P elements); fsdp_unshard does not apply. */
+typedef enum { FSDP_FLAT = 0, FSDP_DIM0 = 1, FSDP_ZERO1 = 2 } fsdp_mode;
 
 typedef enum { FSDP_F32 = 0, FSDP_BF16 = 1 } fsdp_dtype;
 
@@ -239,6 +247,79 @@ const char* fsdp_error_string(int status);
 
 /* Text of the last CUDA error seen by this thread in a library call ("" if none). */
 const char* fsdp_last_cuda_error(void);
+
+/* ZeRO-1 layouts: the owner rank of tensor t (FSDP_EINVAL for other modes). */
+int fsdp_layout_owner(const fsdp_layout* layout, int32_t tensor, int32_t* rank);
+
+/* Sharded clip_grad_norm_ between the reduce-scatter and AdamW ([FSDP-ch18]
+ * §18.18: every rank computes the sum of squares of its gradient shard, one
+ * all-reduce adds them, the square root is the global norm, every rank scales its
+ * own shard).  The clip coefficient follows torch's clip_grad_norm_ (L2 norm):
+ * coef = min(1, max_norm / (norm + 1e-6)), formed in double and rounded to fp32
+ * once; each reduced gradient is multiplied by it (one fp32 rounding) and then
+ * goes through the AdamW and bf16 steps of fsdp_reduce_scatter_adamw.
+ * Three kernels on `stream`: the reduce-scatter writes the fp32 gradient shard and
+ * per-CTA partial sums of squares (fixed order, so the norm is reproducible on a
+ * given GPU), one CTA adds the partials in double, the update pass scales the
+ * shard and runs AdamW.
+ *   grad_shard  required device [N][stride] fp32: receives the CLIPPED reduced
+ *               gradient (padding +0); it is also the working buffer.
+ *   max_norm    > 0 and finite.
+ *   workspace   device scratch of fsdp_clip_workspace_bytes() bytes, 16-byte
+ *               aligned, owned by the caller; no initial contents needed.
+ *   norm_out    optional device float[2] (8-byte aligned): total norm, coef.
+ * Other arguments and errors as fsdp_reduce_scatter_adamw. */
+size_t fsdp_clip_workspace_bytes(void);
+int fsdp_reduce_scatter_clip_adamw(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                                   const void* const* grad_replicas, int32_t grad_dtype,
+                                   float* master, float* exp_avg, float* exp_avg_sq,
+                                   void* param_shards, float* grad_shard, float max_norm,
+                                   void* workspace, float* norm_out,
+                                   const fsdp_adamw_hparams* hp, int64_t step, fsdp_stream_t stream);
+
+/* Gradient accumulation without synchronisation ([FSDP-ch18] §18.26: no_sync /
+ * set_requires_gradient_sync(False) -- the unsharded gradients accumulate
+ * locally and the reduce-scatter runs once, on the last micro-batch).  For every
+ * rank q and every logical element of units [unit_begin, unit_end) in the full
+ * layout: acc[q] = micro[q] (first != 0) or acc[q] + micro[q], in fp32.  Feed the
+ * accumulators to fsdp_reduce_scatter_adamw (grad_dtype FSDP_F32) afterwards.
+ *   acc    host array of N device pointers, fp32 full-layout buffers (FLAT
+ *          padding positions are not touched)
+ *   micro  host array of N device pointers, micro_dtype full-layout gradients */
+int fsdp_accumulate_grads(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                          float* const* acc, const void* const* micro, int32_t micro_dtype,
+                          int32_t first, fsdp_stream_t stream);
+
+/* HSDP step ([FSDP-ch18] §18.9: shard inside a group, replicate across groups;
+ * reduce-scatter in the shard dimension, then one all-reduce across the replica
+ * groups; torchtitan article §3).  R = n_groups groups of N ranks (R*N <=
+ * FSDP_MAX_RANKS); grad_replicas[rho*N + q] is rank q of group rho.  For every
+ * shard element: g_rho = (sum over q, in order, of G[rho][q]) / N, then
+ * g = (sum over rho, in order, of g_rho) / R -- the book's order (the torchtitan
+ * article puts the all-reduce first) -- and every group's copy of the state gets
+ * the same AdamW update.
+ *   master, exp_avg, exp_avg_sq, param_shards: R copies of [N][stride], copy rho
+ *   at element rho*N*stride (param_shards bf16 or NULL). */
+int fsdp_hsdp_reduce_scatter_adamw(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                                   int32_t n_groups, const void* const* grad_replicas, int32_t grad_dtype,
+                                   float* master, float* exp_avg, float* exp_avg_sq, void* param_shards,
+                                   const fsdp_adamw_hparams* hp, int64_t step, fsdp_stream_t stream);
+
+/* ZeRO-1 step on an FSDP_ZERO1 layout ([ZeRO-state] "ZeRO-1：Optimizer State
+ * Sharding": gradients all-reduced, every rank updates only the parameters it
+ * owns, then broadcasts them).  For every element: g = (sum over q of G_q) / N;
+ * the owner's AdamW; the updated parameter is written into all N replicas.
+ *   grad_replicas  N device pointers, full layout (P elements), grad_dtype
+ *   master         [N][stride] fp32 owner rows, required with bf16 replicas;
+ *                  NULL with fp32 replicas (the owner's replica is the parameter)
+ *   exp_avg, exp_avg_sq  [N][stride] fp32 owner rows
+ *   param_replicas host array of N device pointers, full layout, param_dtype
+ * fsdp_reshard fills master from full parameters; fsdp_unshard does not apply. */
+int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                               const void* const* grad_replicas, int32_t grad_dtype,
+                               float* master, float* exp_avg, float* exp_avg_sq,
+                               void* const* param_replicas, int32_t param_dtype,
+                               const fsdp_adamw_hparams* hp, int64_t step, fsdp_stream_t stream);
 
 /* fsdp_reduce_scatter_adamw_noalloc -- the pages have no counterpart of this call.
  * The same computation, arguments, checks and results as fsdp_reduce_scatter_adamw,

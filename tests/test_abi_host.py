@@ -23,7 +23,7 @@ HEADER = os.path.join(ROOT, "include", "fsdp_state.h")
 
 def declared():
     src = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|void|const char\*)\s+(fsdp_\w+)\s*\(", src, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|void|size_t|const char\*)\s+(fsdp_\w+)\s*\(", src, re.M)))
 
 
 def test_header_declares_the_binding_names():
@@ -227,3 +227,61 @@ def test_single_unit_flat_views_line_up(P, N):
         s = L.segment(0, r)
         if s["len"]:
             assert (s["full_off"] - (r * L.stride + s["shard_off"])) % 8 == 0, (P, N, r)
+
+
+def test_rows_validation(lay):
+    lib = fs.lib()
+    h = fs.AdamWHparams(*synth.HP)
+    g4 = (C.c_void_p * 4)(*([A] * 4))
+    # clip: bad max_norm, missing workspace / grad shard, misaligned norm_out, ZeRO-1 layout
+    clip = lambda **k: lib.fsdp_reduce_scatter_clip_adamw(
+        k.get("L", lay.handle), 0, 2, g4, 1, A, A, A, None, k.get("gs", A), k.get("mx", 1.0), k.get("ws", A),
+        k.get("no", None), C.byref(h), 1, None)
+    assert clip(mx=0.0) == -1 and clip(mx=float("nan")) == -1 and clip(mx=-1.0) == -1
+    assert clip(gs=None) == -1 and clip(ws=None) == -1 and clip(ws=A + 4) == -4 and clip(no=A + 4) == -4
+    assert fs.fsdp_clip_workspace_bytes() >= 64 + 8 * 2 * 4096
+    # accumulation: bad dtype, NULL / misaligned pointers
+    acc = (C.c_void_p * 4)(*([A] * 4))
+    assert lib.fsdp_accumulate_grads(lay.handle, 0, 2, acc, g4, 7, 1, None) == -2
+    assert lib.fsdp_accumulate_grads(lay.handle, 0, 2, (C.c_void_p * 4)(A, A, None, A), g4, 1, 1, None) == -1
+    assert lib.fsdp_accumulate_grads(lay.handle, 0, 2, acc, (C.c_void_p * 4)(A, A, A, A + 2), 1, 1, None) == -4
+    assert lib.fsdp_accumulate_grads(lay.handle, 0, 3, acc, g4, 1, 1, None) == -1
+    # HSDP: group count
+    g8 = (C.c_void_p * 8)(*([A] * 8))
+    assert lib.fsdp_hsdp_reduce_scatter_adamw(lay.handle, 0, 2, 0, g8, 1, A, A, A, None, C.byref(h), 1, None) == -1
+    assert lib.fsdp_hsdp_reduce_scatter_adamw(lay.handle, 0, 2, 17, g8, 1, A, A, A, None, C.byref(h), 1,
+                                              None) == -1   # 17 * 4 > 64 ranks
+    # ZeRO-1 only on ZeRO-1 layouts; bf16 replicas need a master; fp32 replicas take none
+    zl = fs.Layout([(7, 5), (3,), (9, 2)], None, 4, fs.FSDP_ZERO1)
+    p4 = (C.c_void_p * 4)(*([A] * 4))
+    z = lambda L, master, pdt: lib.fsdp_zero1_adamw_broadcast(L, 0, 1, g4, 1, master, A, A, p4, pdt, C.byref(h), 1,
+                                                              None)
+    assert z(lay.handle, None, 0) == -1
+    assert z(zl.handle, None, 1) == -1 and z(zl.handle, A, 0) == -1
+    # the other calls refuse ZeRO-1 layouts
+    assert lib.fsdp_unshard(zl.handle, 0, 1, A, A, 0, None) == -1
+    assert lib.fsdp_reduce_scatter_adamw(zl.handle, 0, 1, g4, 1, A, A, A, None, None, C.byref(h), 1, None) == -1
+    owner = C.c_int32()
+    assert lib.fsdp_layout_owner(lay.handle, 0, C.byref(owner)) == -1
+
+
+def test_zero1_layout_vs_oracle_owners(oracle_lib):
+    shapes = [(7, 5), (3,), (9, 2), (4, 4), (11,), (6, 6), (257, 33)]
+    for N in (1, 2, 3, 4, 7):
+        L = fs.Layout(shapes, None, N, fs.FSDP_ZERO1)
+        owners = oracle.zero1_owners(oracle.Shapes(shapes), N)
+        assert [L.owner(t) for t in range(len(shapes))] == list(owners)
+        for t in range(len(shapes)):
+            d = L.tensor(t)
+            o = owners[t]
+            assert (d["full_off"] - (o * L.stride + d["shard_off"])) % 8 == 0
+            for r in range(N):
+                s = L.segment(t, r)
+                assert s["len"] == (int(np.prod(shapes[t])) if r == o else 0)
+        # owner rows hold their tensors without overlap, inside the stride
+        for r in range(N):
+            spans = sorted((L.tensor(t)["shard_off"], L.tensor(t)["shard_off"] + int(np.prod(shapes[t])))
+                           for t in range(len(shapes)) if owners[t] == r)
+            for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+                assert a1 <= b0
+            assert not spans or spans[-1][1] <= L.stride

@@ -1,0 +1,218 @@
+"""The rows beyond the core step on the GPU, against the oracle (GPU):
+sharded clip_grad_norm_, gradient accumulation without sync, HSDP, ZeRO-1."""
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_state_gb300 as fs
+import oracle
+from fsdp_sharded_state_gb300 import synth
+
+import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+HP = synth.HP
+
+
+def W(shapes, units, N, mode, dtype=torch.bfloat16, name="rows"):
+    return synth.Workload(name, 11, list(shapes), list(units), N, mode, dtype, dtype, 3, 1e-3)
+
+
+def logical(O, shapes):
+    mask = np.zeros(O["F"], bool)
+    for t, s in enumerate(shapes):
+        mask[O["t_full_off"][t]:O["t_full_off"][t] + int(np.prod(s) if s else 1)] = True
+    return mask
+
+
+# ---------------------------------------------------------------------------
+CLIP_CASES = [
+    (W([(37, 5), (3,), (11, 13)], [0, 1, 1], 6, synth.FLAT), 1e-4),       # clipping active
+    (W([(37, 5), (3,), (11, 13)], [0, 1, 1], 6, synth.FLAT), 1e3),        # not active
+    (W([(130, 64), (7,), (9, 3)], [0, 0, 0], 4, synth.DIM0), 5e-3),
+    (W([(1 << 24,)], [0], 8, synth.FLAT), 1e-2),                           # 16M params
+    (W([(64, 32), (64,)], [0, 0], 4, synth.FLAT, torch.float32), 2e-3),    # fp32
+]
+
+
+@pytest.mark.parametrize("w,max_norm", CLIP_CASES)
+def test_clip_vs_oracle(oracle_lib, w, max_norm):
+    st = pu.make_state(w, with_grad_out=True)
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = pu.oracle_offsets(w)
+    full = synth.full_params(w, st.F, O["t_full_off"])
+    st.init_from_full(full)
+    bf16 = w.param_dtype == torch.bfloat16
+    om, op = oracle.reshard(sh, w.N, w.mode, pu.f32(full), st.stride, True, bf16)
+    m, v, go = np.zeros_like(om), np.zeros_like(om), np.zeros_like(om)
+    ws = torch.empty(fs.fsdp_clip_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    norm_out = torch.zeros(2, dtype=torch.float32, device="cuda")
+    for t in range(1, 4):
+        grads = synth.grad_replicas(w, st.F, t)
+        fs.fsdp_reduce_scatter_clip_adamw(st.layout, 0, st.layout.n_units, grads, st.master, st.exp_avg,
+                                          st.exp_avg_sq, st.param, st.grad_out, max_norm, ws, norm_out, w.hp, t)
+        ref_norm = oracle.rs_clip_adamw(sh, w.N, w.mode, pu.grads_np(grads), st.stride, om, m, v, max_norm,
+                                        param=op if bf16 else None, grad_out=go, hp=w.hp, step=t)
+        torch.cuda.synchronize()
+        got_norm, got_coef = norm_out.tolist()
+        assert got_norm == pytest.approx(ref_norm, rel=1e-6)
+        assert got_coef == pytest.approx(min(1.0, max_norm / (ref_norm + 1e-6)), rel=1e-6)
+        pu.assert_f32_close(pu.f32(st.grad_out).reshape(-1), go, f"clipped grad step {t}")
+        pu.assert_f32_close(pu.f32(st.master).reshape(-1), om, f"master step {t}")
+        pu.assert_f32_close(pu.f32(st.exp_avg).reshape(-1), m, f"exp_avg step {t}")
+        pu.assert_f32_close(pu.f32(st.exp_avg_sq).reshape(-1), v, f"exp_avg_sq step {t}")
+        if bf16:
+            pu.assert_bf16_close(pu.u16(st.param).reshape(-1), op, f"param step {t}")
+
+
+def test_clip_inactive_equals_plain_step(oracle_lib):
+    # coefficient 1: bit for bit the unclipped fused step
+    w = W([(300, 7), (5,)], [0, 0], 4, synth.FLAT)
+    a, b = pu.make_state(w, with_grad_out=True), pu.make_state(w, with_grad_out=True)
+    O = pu.oracle_offsets(w)
+    full = synth.full_params(w, a.F, O["t_full_off"])
+    a.init_from_full(full)
+    b.init_from_full(full)
+    ws = torch.empty(fs.fsdp_clip_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    grads = synth.grad_replicas(w, a.F, 1)
+    fs.fsdp_reduce_scatter_clip_adamw(a.layout, 0, 1, grads, a.master, a.exp_avg, a.exp_avg_sq, a.param, a.grad_out,
+                                      1e6, ws, None, w.hp, 1)
+    b.reduce_scatter_adamw(grads, w.hp, step=1)
+    torch.cuda.synchronize()
+    for x, y in ((a.master, b.master), (a.exp_avg, b.exp_avg), (a.param, b.param), (a.grad_out, b.grad_out)):
+        assert torch.equal(x, y)
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("w", [W([(37, 5), (3,), (11, 13)], [0, 1, 1], 6, synth.FLAT),
+                               W([(130, 64), (7,), (9, 3)], [0, 0, 1], 4, synth.DIM0),
+                               W([(1 << 22,)], [0], 4, synth.FLAT)])
+@pytest.mark.parametrize("micro_dtype", [torch.bfloat16, torch.float32])
+def test_accumulate_then_step_vs_oracle(oracle_lib, w, micro_dtype):
+    M = 3
+    st = pu.make_state(w)
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = pu.oracle_offsets(w)
+    mask = logical(O, w.shapes)
+    full = synth.full_params(w, st.F, O["t_full_off"])
+    st.init_from_full(full)
+    om, op = oracle.reshard(sh, w.N, w.mode, pu.f32(full), st.stride, True, True)
+    m, v = np.zeros_like(om), np.zeros_like(om)
+    acc = [torch.zeros(st.F, dtype=torch.float32, device="cuda") for _ in range(w.N)]
+    ref_acc = [np.zeros(st.F, np.float32) for _ in range(w.N)]
+    for mi in range(M):
+        micro = [g.to(micro_dtype) for g in synth.grad_replicas(w, st.F, 10 + mi)]
+        fs.fsdp_accumulate_grads(st.layout, 0, st.layout.n_units, acc, micro, first=(mi == 0))
+        for q in range(w.N):
+            mq = pu.u16(micro[q]) if micro_dtype == torch.bfloat16 else pu.f32(micro[q])
+            oracle.accumulate(ref_acc[q], mq, first=(mi == 0))
+    torch.cuda.synchronize()
+    for q in range(w.N):
+        assert np.array_equal(pu.f32(acc[q])[mask].view(np.uint32), ref_acc[q][mask].view(np.uint32))
+    st.reduce_scatter_adamw(acc, w.hp, step=1)
+    oracle.rs_adamw(sh, w.N, w.mode, ref_acc, st.stride, om, m, v, param=op, hp=w.hp, step=1)
+    torch.cuda.synchronize()
+    pu.assert_f32_close(pu.f32(st.master).reshape(-1), om, "master")
+    pu.assert_bf16_close(pu.u16(st.param).reshape(-1), op, "param")
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("w,R", [(W([(37, 5), (3,), (11, 13)], [0, 1, 1], 3, synth.FLAT), 2),
+                                 (W([(130, 64), (7,), (9, 3)], [0, 0, 0], 4, synth.DIM0), 2),
+                                 (W([(1 << 22,)], [0], 4, synth.FLAT), 4),
+                                 (W([(64, 32), (64,)], [0, 0], 2, synth.FLAT, torch.float32), 3)])
+def test_hsdp_vs_oracle(oracle_lib, w, R):
+    L = fs.Layout(w.shapes, w.unit_ids, w.N, w.mode)
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = pu.oracle_offsets(w)
+    N, stride, F = w.N, L.stride, L.info["full_numel"]
+    full = synth.full_params(w, F, O["t_full_off"])
+    bf16 = w.param_dtype == torch.bfloat16
+    master = torch.zeros(R, N, stride, dtype=torch.float32, device="cuda")
+    param = torch.zeros(R, N, stride, dtype=torch.bfloat16, device="cuda") if bf16 else None
+    fs.fsdp_reshard(L, 0, L.n_units, full, master[0], param[0] if bf16 else None)
+    for rho in range(1, R):                  # every group starts from the same shards
+        master[rho].copy_(master[0])
+        if bf16:
+            param[rho].copy_(param[0])
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    om1, op1 = oracle.reshard(sh, N, w.mode, pu.f32(full), stride, True, bf16)
+    om = np.concatenate([om1] * R)
+    op = np.concatenate([op1] * R) if bf16 else None
+    rm, rv = np.zeros_like(om), np.zeros_like(om)
+    for t in range(1, 4):
+        grads = [synth.grad_replica(w, F, t, rho * N + q) for rho in range(R) for q in range(N)]
+        fs.fsdp_hsdp_reduce_scatter_adamw(L, 0, L.n_units, R, grads, master, m, v, param, w.hp, t)
+        oracle.hsdp_adamw(sh, N, w.mode, R, pu.grads_np(grads), stride, om, rm, rv, param=op, hp=w.hp, step=t)
+        torch.cuda.synchronize()
+        pu.assert_f32_close(pu.f32(master).reshape(-1), om, f"master step {t}")
+        pu.assert_f32_close(pu.f32(m).reshape(-1), rm, f"exp_avg step {t}")
+        pu.assert_f32_close(pu.f32(v).reshape(-1), rv, f"exp_avg_sq step {t}")
+        if bf16:
+            pu.assert_bf16_close(pu.u16(param).reshape(-1), op, f"param step {t}")
+
+
+# ---------------------------------------------------------------------------
+ZSHAPES = [(7, 5), (3,), (9, 2), (4, 4), (11,), (6, 6), (257, 33)]
+
+
+def oracle_zero1_rows(sh, N, owners):
+    """The oracle's packing: each owner's tensors back to back, in tensor order."""
+    sizes = [int(np.prod(s) if s else 1) for s in sh.shapes]
+    off, fill = [], [0] * N
+    for t, o in enumerate(owners):
+        off.append(fill[o])
+        fill[o] += sizes[t]
+    return off, max(fill)
+
+
+@pytest.mark.parametrize("shapes,N", [(ZSHAPES, 3), (ZSHAPES, 4), ([(1 << 20,), (1000, 17), (333,)], 2)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_zero1_vs_oracle(oracle_lib, shapes, N, bf16):
+    L = fs.Layout(shapes, None, N, fs.FSDP_ZERO1)
+    sh = oracle.Shapes(shapes)
+    owners = oracle.zero1_owners(sh, N)
+    assert [L.owner(t) for t in range(len(shapes))] == list(owners)
+    for t in range(len(shapes)):
+        d = L.tensor(t)
+        assert (d["full_off"] - (owners[t] * L.stride + d["shard_off"])) % 8 == 0     # congruent placement
+    P = L.info["numel"]
+    w = W(shapes, [0] * len(shapes), N, synth.DIM0, torch.bfloat16 if bf16 else torch.float32)
+    offs = [L.tensor(t)["full_off"] for t in range(len(shapes))]
+    full = synth.full_params(w, P, offs)
+    stride = L.stride
+    pdt = torch.bfloat16 if bf16 else torch.float32
+    params = [full.to(pdt).clone() for _ in range(N)]
+    master = torch.zeros(N, stride, dtype=torch.float32, device="cuda") if bf16 else None
+    if bf16:
+        fs.fsdp_reshard(L, 0, L.n_units, full, master, None)
+    m = torch.zeros(N, stride, dtype=torch.float32, device="cuda")
+    v = torch.zeros_like(m)
+    ooff, ostride = oracle_zero1_rows(sh, N, owners)
+    rm = np.zeros(N * ostride, np.float32)
+    rv = np.zeros_like(rm)
+    rmaster = None
+    if bf16:
+        rmaster = np.zeros(N * ostride, np.float32)
+        f = pu.f32(full)
+        for t, o in enumerate(owners):
+            n = int(np.prod(shapes[t]))
+            rmaster[o * ostride + ooff[t]:o * ostride + ooff[t] + n] = f[offs[t]:offs[t] + n]
+    rparams = [pu.u16(p) if bf16 else pu.f32(p) for p in params]
+    for t in range(1, 4):
+        grads = synth.grad_replicas(w, P, t)
+        fs.fsdp_zero1_adamw_broadcast(L, 0, L.n_units, grads, master, m, v, params, w.hp, t)
+        rparams = oracle.zero1_adamw(sh, N, pu.grads_np(grads), ostride, rmaster, rm, rv, rparams, hp=w.hp, step=t)
+        torch.cuda.synchronize()
+        for q in range(N):
+            if bf16:
+                pu.assert_bf16_close(pu.u16(params[q]), rparams[q], f"replica {q} step {t}")
+            else:
+                pu.assert_f32_close(pu.f32(params[q]), rparams[q], f"replica {q} step {t}")
+        gm, gv = pu.f32(m).reshape(-1), pu.f32(v).reshape(-1)
+        for k, o in enumerate(owners):
+            n = int(np.prod(shapes[k]))
+            a = o * stride + L.tensor(k)["shard_off"]
+            b = o * ostride + ooff[k]
+            pu.assert_f32_close(gm[a:a + n], rm[b:b + n], f"exp_avg t{k}")
+            pu.assert_f32_close(gv[a:a + n], rv[b:b + n], f"exp_avg_sq t{k}")
