@@ -340,6 +340,102 @@ def run_ours(args, w, rank, world, dist):
     return res
 
 
+def row_bytes(row, w, P, N, R=2):
+    """Algorithmic HBM bytes of one call of a row (whole layout, logical elements).
+    clip:  N replicas read; fp32 gradient shard written, re-read and rewritten
+           (clipped); master/m/v read + written; bf16 params written.
+    accum: per replica the micro-gradient read and the fp32 accumulator read + written.
+    hsdp:  R*N replicas read; R copies of master/m/v read + written (+ bf16 params).
+    zero1: N replicas read; the owner's m/v (and master, or its own fp32 replica)
+           read + written; the updated parameter written into all N replicas."""
+    import torch
+    gb = 2 if w.grad_dtype == torch.bfloat16 else 4
+    bf = w.param_dtype == torch.bfloat16
+    if row == "clip":
+        return N * P * gb + 4 * P + 8 * P + 24 * P + (2 * P if bf else 0)
+    if row == "accum":
+        return N * P * (gb + 8)
+    if row == "hsdp":
+        return R * N * P * gb + R * P * (24 + (2 if bf else 0))
+    if row == "zero1":
+        return N * P * gb + P * (16 + (8 if bf else 4)) + N * P * (2 if bf else 4)
+    raise KeyError(row)
+
+
+def run_row(args, w):
+    """Times one call of a row beyond the core step (clip / accum / hsdp / zero1)."""
+    import torch
+
+    import fsdp_sharded_state_gb300 as fs
+    from fsdp_sharded_state_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, R = w.N, args.groups
+    mode = fs.FSDP_ZERO1 if args.row == "zero1" else w.mode
+    L = fs.Layout(w.shapes, w.unit_ids, N, mode)
+    L.prepare()
+    P, F, stride = L.info["numel"], L.info["full_numel"], L.stride
+    offs = [L.tensor(t)["full_off"] for t in range(len(w.shapes))]
+    full = synth.full_params(w, F, offs, device=dev)
+    bf = w.param_dtype == torch.bfloat16
+    z = lambda *shape, dt=torch.float32: torch.zeros(*shape, dtype=dt, device=dev)
+    if args.row in ("clip", "accum"):
+        st = fs.ShardedState(w.shapes, w.unit_ids, N, w.mode, param_dtype=w.param_dtype, device=dev,
+                             with_grad_out=True)
+        st.init_from_full(full)
+        grads = synth.grad_replicas(w, F, 1, device=dev)
+        if args.row == "clip":
+            ws = z(fs.fsdp_clip_workspace_bytes(), dt=torch.uint8)
+            call = lambda t: fs.fsdp_reduce_scatter_clip_adamw(st.layout, 0, st.layout.n_units, grads,
+                                                               st.master, st.exp_avg, st.exp_avg_sq, st.param,
+                                                               st.grad_out, 1e-2, ws, None, w.hp, t)
+        else:
+            acc = [z(F) for _ in range(N)]
+            call = lambda t: fs.fsdp_accumulate_grads(st.layout, 0, st.layout.n_units, acc, grads, first=False)
+    elif args.row == "hsdp":
+        master = z(R, N, stride)
+        param = z(R, N, stride, dt=torch.bfloat16) if bf else None
+        fs.fsdp_reshard(L, 0, L.n_units, full, master[0], param[0] if bf else None)
+        for rho in range(1, R):
+            master[rho].copy_(master[0])
+            if bf:
+                param[rho].copy_(param[0])
+        m, v = torch.zeros_like(master), torch.zeros_like(master)
+        grads = [synth.grad_replica(w, F, 1, k, device=dev) for k in range(R * N)]
+        call = lambda t: fs.fsdp_hsdp_reduce_scatter_adamw(L, 0, L.n_units, R, grads, master, m, v, param, w.hp, t)
+    else:   # zero1
+        master = z(N, stride) if bf else None
+        if bf:
+            fs.fsdp_reshard(L, 0, L.n_units, full, master, None)
+        m, v = z(N, stride), z(N, stride)
+        params = [full.to(w.param_dtype).clone() for _ in range(N)]
+        grads = synth.grad_replicas(w, F, 1, device=dev)
+        call = lambda t: fs.fsdp_zero1_adamw_broadcast(L, 0, L.n_units, grads, master, m, v, params, w.hp, t)
+    del full
+    for k in range(args.warmup):
+        call(k + 1)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k, (a, b) in enumerate(evs):
+        a.record()
+        call(args.warmup + k + 1)
+        b.record()
+    torch.cuda.synchronize()
+    fs.fsdp_check_status()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    med = statistics.median(ms)
+    nbytes = row_bytes(args.row, w, P, N, R)
+    peak, peak_kind = load_peaks()
+    achieved = nbytes / (med * 1e-3) / 1e9
+    return {"row": args.row, "metric": METRIC, "value": P / (med * 1e-3), "unit": "params/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_call": med, "higher_is_better": True,
+            "data": "synthetic", "config": {"workload": w.name, "n_ranks_simulated": N,
+                                            "groups": R if args.row == "hsdp" else None},
+            "roofline": {"call": args.row, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_call": nbytes}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -351,6 +447,9 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before warm-up")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--row", choices=["step", "clip", "accum", "hsdp", "zero1"], default="step",
+                    help="time a row beyond the core step instead (one JSON line, no cpu baseline)")
+    ap.add_argument("--groups", type=int, default=2, help="HSDP replica groups for --row hsdp")
     args = ap.parse_args()
 
     from fsdp_sharded_state_gb300 import synth
@@ -383,6 +482,10 @@ def main():
                                        "single thread"},
             "e2e": {"value": v, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
+        return
+
+    if args.row != "step":
+        print(json.dumps(run_row(args, w)))
         return
 
     if world > 1:
