@@ -144,48 +144,46 @@ __global__ void __launch_bounds__(kThreads, 3)
 k_adamw_scaled(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, float* __restrict__ gshard,
                const float* __restrict__ coef_p, float* __restrict__ master, float* __restrict__ exp_avg,
                float* __restrict__ exp_avg_sq, uint16_t* __restrict__ param, AdamScal sc) {
+    // split lane mapping: lane l owns [4l, 4l+4) and [128+4l, 128+4l+4) of its warp's
+    // 256 elements, so each 16-byte instruction covers 512 contiguous bytes
     const float coef = *coef_p;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int s = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         const int64_t gt = tile_base + t;
         s = advance_seg(segs, s, gt);
         const Seg sg = segs[s];
-        const int64_t e0 = tile_e0(sg, gt);
+        const int64_t x0 = (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads) * kVec + warp * 256 + lane * 4;
         const int64_t lo = sg.shard, hi = sg.shard + sg.len;
-        if (e0 >= hi) continue;
-        if (e0 >= lo && e0 + kVec <= hi) {
-            const float4 g0 = ld4(gshard + e0), g1 = ld4(gshard + e0 + 4);
-            const float4 p0 = ld4(master + e0), p1 = ld4(master + e0 + 4);
-            const float4 m0 = ld4(exp_avg + e0), m1 = ld4(exp_avg + e0 + 4);
-            const float4 v0 = ld4(exp_avg_sq + e0), v1 = ld4(exp_avg_sq + e0 + 4);
-            float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-            float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        if (x0 >= hi) continue;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                g[k] = __fmul_rn(g[k], coef);
-                adamw1(sc, g[k], p[k], m[k], v[k]);
-            }
-            st4(gshard + e0, make_float4(g[0], g[1], g[2], g[3]));
-            st4(gshard + e0 + 4, make_float4(g[4], g[5], g[6], g[7]));
-            st4(master + e0, make_float4(p[0], p[1], p[2], p[3]));
-            st4(master + e0 + 4, make_float4(p[4], p[5], p[6], p[7]));
-            st4(exp_avg + e0, make_float4(m[0], m[1], m[2], m[3]));
-            st4(exp_avg + e0 + 4, make_float4(m[4], m[5], m[6], m[7]));
-            st4(exp_avg_sq + e0, make_float4(v[0], v[1], v[2], v[3]));
-            st4(exp_avg_sq + e0 + 4, make_float4(v[4], v[5], v[6], v[7]));
-            if (PARAM)
-                stu4(param + e0, make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                                            pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7])));
-        } else {
-            const int64_t a = e0 > lo ? e0 : lo, b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
-            for (int64_t e = a; e < b; ++e) {
-                const float g = __fmul_rn(gshard[e], coef);
-                float p = master[e], m = exp_avg[e], v = exp_avg_sq[e];
-                adamw1(sc, g, p, m, v);
-                gshard[e] = g; master[e] = p; exp_avg[e] = m; exp_avg_sq[e] = v;
-                if (PARAM) param[e] = to_bf16(p);
+        for (int c = 0; c < 2; ++c) {
+            const int64_t xc = x0 + 128 * c;
+            if (xc >= lo && xc + 4 <= hi) {
+                const float4 gq = ld4(gshard + xc), pq = ld4(master + xc);
+                const float4 mq = ld4(exp_avg + xc), vq = ld4(exp_avg_sq + xc);
+                float g[4] = {gq.x, gq.y, gq.z, gq.w}, p[4] = {pq.x, pq.y, pq.z, pq.w};
+                float m[4] = {mq.x, mq.y, mq.z, mq.w}, v[4] = {vq.x, vq.y, vq.z, vq.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    g[k] = __fmul_rn(g[k], coef);
+                    adamw1(sc, g[k], p[k], m[k], v[k]);
+                }
+                st4(gshard + xc, make_float4(g[0], g[1], g[2], g[3]));
+                st4(master + xc, make_float4(p[0], p[1], p[2], p[3]));
+                st4(exp_avg + xc, make_float4(m[0], m[1], m[2], m[3]));
+                st4(exp_avg_sq + xc, make_float4(v[0], v[1], v[2], v[3]));
+                if (PARAM)
+                    *reinterpret_cast<uint2*>(param + xc) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
+            } else {
+                const int64_t a = xc > lo ? xc : lo, b = (xc + 4) < hi ? (xc + 4) : hi;
+                for (int64_t e = a; e < b; ++e) {
+                    const float g = __fmul_rn(gshard[e], coef);
+                    float p = master[e], m = exp_avg[e], v = exp_avg_sq[e];
+                    adamw1(sc, g, p, m, v);
+                    gshard[e] = g; master[e] = p; exp_avg[e] = m; exp_avg_sq[e] = v;
+                    if (PARAM) param[e] = to_bf16(p);
+                }
             }
         }
     }
