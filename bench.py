@@ -307,7 +307,7 @@ def run_ours(args, w, rank, world, dist):
     rs_bytes = ab["rs_adamw"]
     achieved = rs_bytes / (rs_avg * 1e-3) / 1e9
     P = info["numel"]
-    launches_per_step = n_unshard + 1
+    launches_per_step = st.launches_per_step(args.strategy)
     res = {
         "metric": METRIC,
         "value": world * P * args.steps / (ms_max * 1e-3),

@@ -79,6 +79,31 @@ class ShardedState:
             self.unshard(stream=stream)
         self.reduce_scatter_adamw(grads, hp, stream=stream)
 
+    def launch_counts(self) -> dict:
+        """Kernels one call launches: one per alignment class present (shard and
+        full-layout offsets congruent mod 8 or not) -- the layout files every rank's
+        piece under one of the two -- plus the zero-fill of the gradient shard's
+        padding when a gradient shard is written."""
+        L, N, stride = self.layout, self.N, self.stride
+        data, gather = set(), set()
+        for t in range(len(L.shapes)):
+            for r in range(N):
+                sg = L.segment(t, r)
+                if sg["len"]:
+                    data.add((sg["full_off"] - (r * stride + sg["shard_off"])) % 8 == 0)
+        if L.mode == 0:                      # FLAT: the all-gather copies whole S_u slots
+            for u in range(L.n_units):
+                d = L.unit(u)
+                if d["shard_numel"]:
+                    for r in range(N):
+                        gather.add((d["full_off"] + r * d["shard_numel"] - (r * stride + d["shard_off"])) % 8 == 0)
+        else:
+            gather = set(data)
+        pad = 1 if (self.grad_out is not None and self.layout.info["pad_numel"] + N * (stride - self.layout.info[
+            "shard_numel"]) > 0) else 0
+        return {"unshard": len(gather), "reduce_scatter_adamw": len(data) + pad}
+
     def launches_per_step(self, strategy: str = "full_shard") -> int:
         """Kernel launches of one step (for a launch count)."""
-        return STRATEGIES[strategy] + 1 + (1 if self.grad_out is not None else 0)
+        c = self.launch_counts()
+        return STRATEGIES[strategy] * c["unshard"] + c["reduce_scatter_adamw"]
