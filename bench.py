@@ -31,8 +31,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sharded-step params/sec and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
 PEAK_FALLBACK_GBS = 6800.0
-KERNEL_SRC = [os.path.join(ROOT, "fsdp_sharded_state_gb300", "csrc", f)
-              for f in ("kernels.cu", "device_ops.cuh", "common.cuh")]
+KERNEL_SRC = {k: [os.path.join(ROOT, "fsdp_sharded_state_gb300", "csrc", f) for f in (src, "device_ops.cuh", "common.cuh")]
+              for k, src in (("k_rs_adamw", "kernels.cu"), ("k_rs_adamw_staged", "staged.cu"))}
 
 
 # ---------------------------------------------------------------------------
@@ -65,10 +65,10 @@ def load_peaks():
     return PEAK_FALLBACK_GBS, "fallback"
 
 
-def kernel_src_hash():
-    """Hash of the sources the core kernels compile from."""
+def kernel_src_hash(kernel="k_rs_adamw"):
+    """Hash of the sources a core kernel compiles from."""
     h = hashlib.sha256()
-    for p in KERNEL_SRC:
+    for p in KERNEL_SRC[kernel]:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -82,7 +82,7 @@ def profiled_traffic(kernel, workload):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("kernel_src_sha256_16") != kernel_src_hash():
+    if d.get("kernel_src_sha256_16") != kernel_src_hash(kernel):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -223,6 +223,7 @@ def run_ours(args, w, rank, world, dist):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
+    fs.fsdp_set_rs_kernel(args.rs_kernel)
     st = fs.ShardedState(w.shapes, w.unit_ids, w.N, w.mode, param_dtype=w.param_dtype, device=dev)
     st.layout.prepare()
     L = st.layout
@@ -307,7 +308,8 @@ def run_ours(args, w, rank, world, dist):
     rs_bytes = ab["rs_adamw"]
     achieved = rs_bytes / (rs_avg * 1e-3) / 1e9
     P = info["numel"]
-    launches_per_step = st.launches_per_step(args.strategy)
+    launches_per_step = st.launches_per_step(args.strategy, w.grad_dtype)
+    kname = "k_rs_adamw_staged" if fs.fsdp_rs_kernel_for(L, w.grad_dtype) == "staged" else "k_rs_adamw"
     res = {
         "metric": METRIC,
         "value": world * P * args.steps / (ms_max * 1e-3),
@@ -329,9 +331,9 @@ def run_ours(args, w, rank, world, dist):
                    "l2": "inputs larger than L2 (step touches %.2f GB)" % ((ab["rs_adamw"] + n_unshard * ab["unshard"]) / 1e9),
                    "clock_soak_s": args.soak, "parallelism": f"replicas x{world}"},
         "step_hbm_gbs": (ab["rs_adamw"] + n_unshard * ab["unshard"]) / (ms_max / args.steps * 1e-3) / 1e9,
-        "roofline": {"kernel": "k_rs_adamw", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_launch": rs_bytes,
-                     "launch_ms": rs_avg, "traffic": profiled_traffic("k_rs_adamw", w.name)},
+                     "launch_ms": rs_avg, "traffic": profiled_traffic(kname, w.name)},
         "e2e": {"value": world * P * args.steps / (e2e_ms * 1e-3), "unit": "params/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": launches_per_step * args.steps,
@@ -450,6 +452,8 @@ def main():
     ap.add_argument("--row", choices=["step", "clip", "accum", "hsdp", "zero1"], default="step",
                     help="time a row beyond the core step instead (one JSON line, no cpu baseline)")
     ap.add_argument("--groups", type=int, default=2, help="HSDP replica groups for --row hsdp")
+    ap.add_argument("--rs-kernel", choices=["auto", "direct", "staged"], default="auto",
+                    help="kernel of the fused reduce-scatter + AdamW step")
     args = ap.parse_args()
 
     from fsdp_sharded_state_gb300 import synth

@@ -19,6 +19,9 @@ FSDP_FLAT, FSDP_DIM0, FSDP_ZERO1 = 0, 1, 2
 FSDP_F32, FSDP_BF16 = 0, 1
 MODES = {"flat": FSDP_FLAT, "dim0": FSDP_DIM0, "zero1": FSDP_ZERO1}
 
+FSDP_RS_AUTO, FSDP_RS_DIRECT, FSDP_RS_STAGED = 0, 1, 2
+RS_KERNELS = {"auto": FSDP_RS_AUTO, "direct": FSDP_RS_DIRECT, "staged": FSDP_RS_STAGED}
+
 FSDP_OK = 0
 STATUS = {0: "FSDP_OK", -1: "FSDP_EINVAL", -2: "FSDP_EDTYPE", -3: "FSDP_ESHAPE", -4: "FSDP_EALIGN",
           -5: "FSDP_EOVERFLOW", -6: "FSDP_ECUDA", -7: "FSDP_ETIMEOUT", -8: "FSDP_ENOMEM"}
@@ -29,7 +32,8 @@ EXPORTS = ("fsdp_layout_create", "fsdp_layout_destroy", "fsdp_layout_query", "fs
            "fsdp_unshard", "fsdp_reduce_scatter_adamw", "fsdp_reshard", "fsdp_check_status",
            "fsdp_error_string", "fsdp_last_cuda_error", "fsdp_reduce_scatter_adamw_noalloc",
            "fsdp_layout_owner", "fsdp_clip_workspace_bytes", "fsdp_reduce_scatter_clip_adamw",
-           "fsdp_accumulate_grads", "fsdp_hsdp_reduce_scatter_adamw", "fsdp_zero1_adamw_broadcast")
+           "fsdp_accumulate_grads", "fsdp_hsdp_reduce_scatter_adamw", "fsdp_zero1_adamw_broadcast",
+           "fsdp_set_rs_kernel", "fsdp_rs_kernel_for", "fsdp_wait_selftest")
 
 
 class FsdpError(RuntimeError):
@@ -89,6 +93,9 @@ def lib() -> C.CDLL:
         L.fsdp_zero1_adamw_broadcast.argtypes = [vp, i32, i32, C.POINTER(vp), i32, vp, vp, vp, C.POINTER(vp), i32,
                                                  C.POINTER(AdamWHparams), i64, vp]
         L.fsdp_check_status.argtypes = [vp]
+        L.fsdp_set_rs_kernel.argtypes = [i32]
+        L.fsdp_rs_kernel_for.argtypes = [vp, i32]
+        L.fsdp_wait_selftest.argtypes = [i64, vp]
         L.fsdp_error_string.argtypes = [C.c_int]
         L.fsdp_error_string.restype = C.c_char_p
         L.fsdp_last_cuda_error.argtypes = []
@@ -340,6 +347,31 @@ def fsdp_reshard(layout: Layout, unit_begin: int, unit_end: int, full=None, mast
 
 def fsdp_check_status(stream=None) -> None:
     _check(lib().fsdp_check_status(_stream(stream)), "fsdp_check_status")
+
+
+def fsdp_set_rs_kernel(kind) -> int:
+    """Selects the kernel of fsdp_reduce_scatter_adamw ("auto", "direct", "staged"
+    or the FSDP_RS_* code); returns the previous code."""
+    code = RS_KERNELS[kind] if isinstance(kind, str) else int(kind)
+    prev = lib().fsdp_set_rs_kernel(code)
+    if prev < 0:
+        raise FsdpError(prev, "fsdp_set_rs_kernel")
+    return prev
+
+
+def fsdp_rs_kernel_for(layout: Layout, grad_dtype) -> str:
+    """"direct" or "staged": the kernel fsdp_reduce_scatter_adamw runs for this
+    layout and gradient dtype (a torch dtype or FSDP_F32/FSDP_BF16) right now."""
+    import torch
+    code = grad_dtype if isinstance(grad_dtype, int) else {torch.float32: FSDP_F32, torch.bfloat16: FSDP_BF16}[grad_dtype]
+    rc = lib().fsdp_rs_kernel_for(layout.handle, code)
+    if rc < 0:
+        raise FsdpError(rc, "fsdp_rs_kernel_for")
+    return {FSDP_RS_DIRECT: "direct", FSDP_RS_STAGED: "staged"}[rc]
+
+
+def fsdp_wait_selftest(timeout_ns: int, stream=None) -> None:
+    _check(lib().fsdp_wait_selftest(int(timeout_ns), _stream(stream)), "fsdp_wait_selftest")
 
 
 def fsdp_error_string(status: int) -> str:

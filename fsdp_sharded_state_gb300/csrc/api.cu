@@ -3,6 +3,7 @@
 // AdamW step constants and the kernel launches.  Every check runs before the
 // first launch, so an error return leaves all outputs untouched.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -15,6 +16,7 @@
 #include "internal.hpp"
 #include "kernels.hpp"
 #include "layout.hpp"
+#include "staged.hpp"
 
 using fsdp::Seg;
 using fsdp::SegList;
@@ -23,6 +25,11 @@ namespace fsdp {
 namespace detail {
 
 thread_local char g_cuda_err[256] = "";
+
+// Kernel choice of fsdp_reduce_scatter_adamw (fsdp_rs_kernel).
+std::atomic<int> g_rs_kernel{FSDP_RS_AUTO};
+// Time limit of each mbarrier wait in the staged kernel.
+constexpr uint64_t kWaitNs = 1000000000ull;
 
 int cuda_fail(cudaError_t e, const char* where) {
     std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s (%s)", where, cudaGetErrorName(e),
@@ -305,12 +312,22 @@ int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, cons
     if ((rc = device_tables(L, &base))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    for (int shifted = 0; shifted < 2; ++shifted) {
-        const Range R = range_of(shifted ? L->data_sh : L->data_al, base, ub, ue);
-        e = fsdp::launch_rs_adamw(R.segs, R.tile_base, R.n_tiles, shifted, grad_dtype == FSDP_BF16, gp, L->N, L->F,
-                                  master, exp_avg, exp_avg_sq, static_cast<uint16_t*>(param_shards), grad_shard_out,
-                                  sc, st);
-        if (e != cudaSuccess) return cuda_fail(e, "k_rs_adamw launch");
+    const bool bf16 = grad_dtype == FSDP_BF16;
+    const int kind = g_rs_kernel.load();
+    const bool staged = kind == FSDP_RS_STAGED || (kind == FSDP_RS_AUTO && fsdp::staged_fits(L->N, bf16));
+    if (staged) {
+        if (!fsdp::staged_fits(L->N, bf16)) return FSDP_EINVAL;
+        const Range R = range_of(L->data, base, ub, ue);
+        e = fsdp::launch_rs_adamw_staged(R.segs, R.tile_base, R.n_tiles, bf16, gp, L->N, master, exp_avg, exp_avg_sq,
+                                         static_cast<uint16_t*>(param_shards), grad_shard_out, sc, kWaitNs, st);
+        if (e != cudaSuccess) return cuda_fail(e, "k_rs_adamw_staged launch");
+    } else {
+        for (int shifted = 0; shifted < 2; ++shifted) {
+            const Range R = range_of(shifted ? L->data_sh : L->data_al, base, ub, ue);
+            e = fsdp::launch_rs_adamw(R.segs, R.tile_base, R.n_tiles, shifted, bf16, gp, L->N, L->F, master, exp_avg,
+                                      exp_avg_sq, static_cast<uint16_t*>(param_shards), grad_shard_out, sc, st);
+            if (e != cudaSuccess) return cuda_fail(e, "k_rs_adamw launch");
+        }
     }
     if (grad_shard_out) {
         const Range P = range_of(L->pad, base, ub, ue);
@@ -347,6 +364,33 @@ int fsdp_check_status(fsdp_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetLastError");
+    unsigned int gave_up = 0;
+    e = fsdp::take_wait_error(&gave_up);
+    if (e != cudaSuccess) return cuda_fail(e, "wait status read");
+    return gave_up ? FSDP_ETIMEOUT : FSDP_OK;
+}
+
+int fsdp_set_rs_kernel(int32_t kind) {
+    if (kind != FSDP_RS_AUTO && kind != FSDP_RS_DIRECT && kind != FSDP_RS_STAGED) return FSDP_EINVAL;
+    return g_rs_kernel.exchange(kind);
+}
+
+int fsdp_rs_kernel_for(const fsdp_layout* L, int32_t grad_dtype) {
+    if (!L) return FSDP_EINVAL;
+    if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const int kind = g_rs_kernel.load();
+    if (kind == FSDP_RS_DIRECT) return FSDP_RS_DIRECT;
+    if (kind == FSDP_RS_STAGED) return FSDP_RS_STAGED;
+    return fsdp::staged_fits(L->N, grad_dtype == FSDP_BF16) ? FSDP_RS_STAGED : FSDP_RS_DIRECT;
+}
+
+int fsdp_wait_selftest(int64_t timeout_ns, fsdp_stream_t stream) {
+    if (timeout_ns <= 0 || timeout_ns > 10000000000LL) return FSDP_EINVAL;
+    const cudaError_t e = fsdp::launch_wait_selftest(uint64_t(timeout_ns), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "k_wait_selftest launch");
     return FSDP_OK;
 }
 

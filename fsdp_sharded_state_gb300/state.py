@@ -19,7 +19,7 @@ from typing import Optional, Sequence
 import torch
 
 from . import (FSDP_BF16, FSDP_F32, FSDP_FLAT, Layout, fsdp_reduce_scatter_adamw, fsdp_reshard,
-               fsdp_unshard)
+               fsdp_rs_kernel_for, fsdp_unshard)
 
 STRATEGIES = {"full_shard": 2, "shard_grad_op": 1}   # all-gathers per step
 
@@ -79,11 +79,12 @@ class ShardedState:
             self.unshard(stream=stream)
         self.reduce_scatter_adamw(grads, hp, stream=stream)
 
-    def launch_counts(self) -> dict:
-        """Kernels one call launches: one per alignment class present (shard and
-        full-layout offsets congruent mod 8 or not) -- the layout files every rank's
-        piece under one of the two -- plus the zero-fill of the gradient shard's
-        padding when a gradient shard is written."""
+    def launch_counts(self, grad_dtype: torch.dtype = torch.bfloat16) -> dict:
+        """Kernels one call launches.  The all-gather and the direct reduce-scatter
+        kernels: one per alignment class present (shard and full-layout offsets
+        congruent mod 8 or not) -- the layout files every rank's piece under one of
+        the two; the staged reduce-scatter kernel: one for both.  Plus the zero-fill
+        of the gradient shard's padding when a gradient shard is written."""
         L, N, stride = self.layout, self.N, self.stride
         data, gather = set(), set()
         for t in range(len(L.shapes)):
@@ -101,9 +102,11 @@ class ShardedState:
             gather = set(data)
         pad = 1 if (self.grad_out is not None and self.layout.info["pad_numel"] + N * (stride - self.layout.info[
             "shard_numel"]) > 0) else 0
-        return {"unshard": len(gather), "reduce_scatter_adamw": len(data) + pad}
+        staged = fsdp_rs_kernel_for(self.layout, grad_dtype) == "staged"
+        rs = (1 if data else 0) if staged else len(data)
+        return {"unshard": len(gather), "reduce_scatter_adamw": rs + pad}
 
-    def launches_per_step(self, strategy: str = "full_shard") -> int:
+    def launches_per_step(self, strategy: str = "full_shard", grad_dtype: torch.dtype = torch.bfloat16) -> int:
         """Kernel launches of one step (for a launch count)."""
-        c = self.launch_counts()
+        c = self.launch_counts(grad_dtype)
         return STRATEGIES[strategy] * c["unshard"] + c["reduce_scatter_adamw"]

@@ -64,7 +64,7 @@ typedef enum {
     FSDP_EALIGN = -4,     /* a buffer is not 16-byte aligned                               */
     FSDP_EOVERFLOW = -5,  /* an element count does not fit the int64 / device index range  */
     FSDP_ECUDA = -6,      /* a CUDA call failed (fsdp_last_cuda_error names it)            */
-    FSDP_ETIMEOUT = -7,   /* reserved: a bounded device-side wait gave up                  */
+    FSDP_ETIMEOUT = -7,   /* a bounded device-side wait gave up (fsdp_check_status)        */
     FSDP_ENOMEM = -8      /* host or device allocation of the layout tables failed         */
 } fsdp_status;
 
@@ -239,7 +239,9 @@ int fsdp_reshard(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end
                  fsdp_stream_t stream);
 
 /* Blocks until `stream` is idle and reports any CUDA error seen there
- * (FSDP_ECUDA) -- the analogue of a collective's error check. */
+ * (FSDP_ECUDA) -- the analogue of a collective's error check -- or, failing that,
+ * a bounded device-side wait that gave up on the current device since the last
+ * check (FSDP_ETIMEOUT; the record is cleared). */
 int fsdp_check_status(fsdp_stream_t stream);
 
 /* Static text for a status code; never NULL. */
@@ -320,6 +322,38 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
                                float* master, float* exp_avg, float* exp_avg_sq,
                                void* const* param_replicas, int32_t param_dtype,
                                const fsdp_adamw_hparams* hp, int64_t step, fsdp_stream_t stream);
+
+/* Kernel choice of fsdp_reduce_scatter_adamw (process-wide; the pages have no
+ * counterpart, the result is the same either way, bit for bit):
+ *   FSDP_RS_AUTO    the staged kernel when at least two of its pipeline stages fit
+ *                   in one CTA's shared memory (a stage holds 2048 elements of the
+ *                   three fp32 state arrays and of all N gradient replicas: up to
+ *                   N = 16 with bf16 gradients, N = 8 with fp32), else the direct
+ *                   kernels.  The default.
+ *   FSDP_RS_DIRECT  the direct kernels: 16-byte loads straight into registers, one
+ *                   launch per alignment class.
+ *   FSDP_RS_STAGED  the staged kernel: the bulk-copy engine (cp.async.bulk) moves
+ *                   each tile's state and gradient slices into shared memory, an
+ *                   mbarrier per stage counts the bytes, one launch for both
+ *                   alignment classes.  A call it does not fit returns FSDP_EINVAL.
+ * Returns the previous choice, or FSDP_EINVAL for an unknown one.  Not ordered
+ * with calls in flight on other threads. */
+typedef enum { FSDP_RS_AUTO = 0, FSDP_RS_DIRECT = 1, FSDP_RS_STAGED = 2 } fsdp_rs_kernel;
+int fsdp_set_rs_kernel(int32_t kind);
+
+/* The kernel fsdp_reduce_scatter_adamw would run for this layout and gradient
+ * dtype on the current device under the current choice: FSDP_RS_DIRECT or
+ * FSDP_RS_STAGED (FSDP_EINVAL / FSDP_EDTYPE for a bad argument, FSDP_ECUDA if the
+ * device cannot be queried).  Launches per call: staged 1, direct 1 per alignment
+ * class present (fsdp_layout_segment tells the class of each piece). */
+int fsdp_rs_kernel_for(const fsdp_layout* layout, int32_t grad_dtype);
+
+/* Diagnostic of the bounded device waits: launches one kernel whose mbarrier
+ * expects 16 bytes that nothing delivers.  Its wait gives up after timeout_ns
+ * nanoseconds (0 < timeout_ns <= 10^10) and records the failure; the next
+ * fsdp_check_status returns FSDP_ETIMEOUT and clears it.  The staged kernel
+ * records a wait that gives up the same way (limit: 1 s per wait). */
+int fsdp_wait_selftest(int64_t timeout_ns, fsdp_stream_t stream);
 
 /* fsdp_reduce_scatter_adamw_noalloc -- the pages have no counterpart of this call.
  * The same computation, arguments, checks and results as fsdp_reduce_scatter_adamw,
