@@ -278,13 +278,15 @@ int fsdp_unshard(const fsdp_layout* L, int32_t ub, int32_t ue, const void* shard
     if ((rc = check_ptr(shards)) || (rc = check_ptr(full))) return rc;
     const Seg* base = nullptr;
     if ((rc = device_tables(L, &base))) return rc;
-    for (int shifted = 0; shifted < 2; ++shifted) {
-        const Range R = range_of(shifted ? L->gather_sh : L->gather_al, base, ub, ue);
-        const cudaError_t e = fsdp::launch_unshard(R.segs, R.tile_base, R.n_tiles, shifted, elem_dtype == FSDP_BF16,
-                                                   shards, full, int64_t(L->N) * L->stride,
-                                                   reinterpret_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return cuda_fail(e, "k_unshard launch");
-    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool bf16 = elem_dtype == FSDP_BF16;
+    // aligned class: bulk copies through shared memory; shifted class: warp realignment
+    const Range A = range_of(L->gather_al, base, ub, ue);
+    cudaError_t e = fsdp::launch_unshard_bulk(A.segs, A.tile_base, A.n_tiles, bf16, shards, full, kWaitNs, st);
+    if (e != cudaSuccess) return cuda_fail(e, "k_unshard_bulk launch");
+    const Range R = range_of(L->gather_sh, base, ub, ue);
+    e = fsdp::launch_unshard_shifted(R.segs, R.tile_base, R.n_tiles, bf16, shards, full, int64_t(L->N) * L->stride, st);
+    if (e != cudaSuccess) return cuda_fail(e, "k_unshard_shift launch");
     return FSDP_OK;
 }
 

@@ -3,7 +3,9 @@
 //   k_rs_adamw   fused reduce-scatter (fp32 mean over N gradient replicas, fixed
 //                rank order) + AdamW on the fp32 master/exp_avg/exp_avg_sq shard +
 //                bf16 recast of the updated shard: one HBM pass per shard element.
-//   k_unshard    all-gather of the rank shards into the full layout (bitwise copy).
+//   k_unshard_shift  all-gather (bitwise copy shard -> full) of the pieces whose
+//                full-layout offset is not congruent to their shard offset mod 8
+//                (the aligned ones go through bulk copies: k_unshard_bulk).
 //   k_reshard    full layout -> rank shards (fp32 master and/or bf16 param), and
 //   k_zero_pad   the zero-fill of shard padding.
 //
@@ -257,10 +259,13 @@ __device__ __forceinline__ CopyVec<ET> window_any(int o, const CopyVec<ET>& S, c
     }
 }
 
-template <typename ET, bool SHIFT>
+// All-gather of the shifted class (pieces whose full-layout offset is not congruent
+// to their shard offset mod 8); the aligned class goes through bulk copies
+// (k_unshard_bulk).
+template <typename ET>
 __global__ void __launch_bounds__(kThreads)
-k_unshard(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, const ET* __restrict__ src,
-          ET* __restrict__ dst, int64_t src_limit) {
+k_unshard_shift(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, const ET* __restrict__ src,
+                ET* __restrict__ dst, int64_t src_limit) {
     const bool lane31 = (threadIdx.x & 31) == 31;
     int s = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
@@ -270,36 +275,6 @@ k_unshard(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, cons
         const int64_t e0 = (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads + threadIdx.x) * kVec;
         const int64_t lo = sg.shard, hi = sg.shard + sg.len;
         const int64_t delta = sg.full - sg.shard;
-        if (!SHIFT && sizeof(ET) == 4) {
-            // 32-bit elements: split mapping (see rs_tile_f32_split), whole sectors per instruction
-            const int64_t x0 = e0 - int64_t(threadIdx.x) * kVec + (threadIdx.x >> 5) * 256 + (threadIdx.x & 31) * 4;
-            if (x0 >= hi) continue;
-            const int64_t x1 = x0 + 128;
-            if (x0 >= lo && x1 + 4 <= hi) {
-                const uint4 a = ld_once(src + x0), b = ld_once(src + x1);
-                stu4(dst + x0 + delta, a);
-                stu4(dst + x1 + delta, b);
-            } else {
-                for (int c = 0; c < 2; ++c) {
-                    const int64_t xc = c ? x1 : x0;
-                    const int64_t a = xc > lo ? xc : lo;
-                    const int64_t b = (xc + 4) < hi ? (xc + 4) : hi;
-                    for (int64_t e = a; e < b; ++e) dst[e + delta] = src[e];
-                }
-            }
-            continue;
-        }
-        if (!SHIFT) {
-            if (e0 >= hi) continue;
-            if (e0 >= lo && e0 + kVec <= hi) {
-                store_vec(dst + e0 + delta, load_vec(src + e0));
-            } else {
-                const int64_t a = e0 > lo ? e0 : lo;
-                const int64_t b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
-                for (int64_t e = a; e < b; ++e) dst[e + delta] = src[e];
-            }
-            continue;
-        }
         // Misaligned segment (uniform over the tile): every lane loads its aligned
         // source vector S and gets the next one X from its neighbour (lane 31 loads
         // it); lane t then stores the aligned destination vector [fa+8, fa+16),
@@ -475,23 +450,20 @@ cudaError_t launch_rs_adamw(const Seg* segs, int64_t tile_base, int64_t n_tiles,
                    : launch_rs_t<float, false>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc, st);
 }
 
-template <typename ET, bool SHIFT>
+template <typename ET>
 static cudaError_t launch_unshard_t(const Seg* segs, int64_t tile_base, int64_t n_tiles, const void* src, void* dst,
                                     int64_t src_limit, cudaStream_t st) {
-    auto k = k_unshard<ET, SHIFT>;
+    auto k = k_unshard_shift<ET>;
     k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, static_cast<const ET*>(src),
                                                   static_cast<ET*>(dst), src_limit);
     return cudaGetLastError();
 }
 
-cudaError_t launch_unshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool shifted, bool bf16,
-                           const void* src, void* dst, int64_t src_limit, cudaStream_t st) {
+cudaError_t launch_unshard_shifted(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16, const void* src,
+                                   void* dst, int64_t src_limit, cudaStream_t st) {
     if (n_tiles <= 0) return cudaSuccess;
-    if (bf16)
-        return shifted ? launch_unshard_t<uint16_t, true>(segs, tile_base, n_tiles, src, dst, src_limit, st)
-                       : launch_unshard_t<uint16_t, false>(segs, tile_base, n_tiles, src, dst, src_limit, st);
-    return shifted ? launch_unshard_t<uint32_t, true>(segs, tile_base, n_tiles, src, dst, src_limit, st)
-                   : launch_unshard_t<uint32_t, false>(segs, tile_base, n_tiles, src, dst, src_limit, st);
+    return bf16 ? launch_unshard_t<uint16_t>(segs, tile_base, n_tiles, src, dst, src_limit, st)
+                : launch_unshard_t<uint32_t>(segs, tile_base, n_tiles, src, dst, src_limit, st);
 }
 
 template <bool FB>

@@ -19,6 +19,10 @@ cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n
                                    const GradPtrs& gp, int N, float* master, float* m, float* v, uint16_t* param,
                                    float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st);
 
+// All-gather (shard -> full, bitwise) of a segment range of the aligned class.
+cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16, const void* src,
+                                void* dst, uint64_t wait_ns, cudaStream_t st);
+
 // One kernel whose only wait cannot complete: exercises the bounded-wait exit.
 cudaError_t launch_wait_selftest(uint64_t wait_ns, cudaStream_t st);
 
