@@ -373,6 +373,7 @@ def run_row(args, w):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    fs.fsdp_set_rs_kernel(args.rs_kernel)
     N, R = w.N, args.groups
     mode = fs.FSDP_ZERO1 if args.row == "zero1" else w.mode
     L = fs.Layout(w.shapes, w.unit_ids, N, mode)

@@ -26,10 +26,15 @@ namespace detail {
 
 thread_local char g_cuda_err[256] = "";
 
-// Kernel choice of fsdp_reduce_scatter_adamw (fsdp_rs_kernel).
+// Kernel choice of the reduce-scatter calls (fsdp_rs_kernel).
 std::atomic<int> g_rs_kernel{FSDP_RS_AUTO};
-// Time limit of each mbarrier wait in the staged kernel.
-constexpr uint64_t kWaitNs = 1000000000ull;
+
+int choose_staged(bool fits, bool preferred, bool* staged) {
+    const int kind = g_rs_kernel.load();
+    if (kind == FSDP_RS_STAGED && !fits) return FSDP_EINVAL;
+    *staged = kind == FSDP_RS_STAGED || (kind == FSDP_RS_AUTO && fits && preferred);
+    return FSDP_OK;
+}
 
 int cuda_fail(cudaError_t e, const char* where) {
     std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s (%s)", where, cudaGetErrorName(e),
@@ -315,10 +320,9 @@ int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, cons
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     const bool bf16 = grad_dtype == FSDP_BF16;
-    const int kind = g_rs_kernel.load();
-    const bool staged = kind == FSDP_RS_STAGED || (kind == FSDP_RS_AUTO && fsdp::staged_fits(L->N, bf16));
+    bool staged = false;
+    if ((rc = choose_staged(fsdp::staged_fits(L->N, bf16), true, &staged))) return rc;
     if (staged) {
-        if (!fsdp::staged_fits(L->N, bf16)) return FSDP_EINVAL;
         const Range R = range_of(L->data, base, ub, ue);
         e = fsdp::launch_rs_adamw_staged(R.segs, R.tile_base, R.n_tiles, bf16, gp, L->N, master, exp_avg, exp_avg_sq,
                                          static_cast<uint16_t*>(param_shards), grad_shard_out, sc, kWaitNs, st);

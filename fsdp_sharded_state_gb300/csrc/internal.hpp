@@ -27,5 +27,14 @@ int check_ptr(const void* p);                            // non-NULL and 16-byte
 int check_hparams(const fsdp_adamw_hparams* hp);
 AdamScal adam_scalars(const fsdp_adamw_hparams* hp, int64_t step, int32_t n_avg);
 
+// Time limit of each mbarrier wait in the staged kernels.
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+// Whether a call runs its staged kernel, under the process-wide choice
+// (fsdp_set_rs_kernel), whether the staged kernel fits this call and whether the
+// automatic choice prefers it (measured faster): FSDP_OK and *staged set, or
+// FSDP_EINVAL when the staged kernel is forced but does not fit.
+int choose_staged(bool fits, bool preferred, bool* staged);
+
 }  // namespace detail
 }  // namespace fsdp

@@ -10,6 +10,7 @@
 #include "device_ops.cuh"
 #include "internal.hpp"
 #include "kernels.hpp"
+#include "staged.hpp"
 
 using fsdp::Seg;
 using namespace fsdp::detail;
@@ -443,12 +444,26 @@ int fsdp_reduce_scatter_clip_adamw(const fsdp_layout* L, int32_t ub, int32_t ue,
     float* ws_coef = reinterpret_cast<float*>(ws + 8);
     double* part = reinterpret_cast<double*>(ws + kClipHeader);
 
-    // (1) reduce-scatter + sums of squares, one partial per CTA, per alignment class
+    // (1) reduce-scatter + sums of squares: staged (one partial per consumer warp, one
+    // launch) or direct (one partial per CTA, one launch per alignment class)
+    const bool bf = grad_dtype == FSDP_BF16;
+    const Range D1 = range_of(L->data, base, ub, ue);
+    bool staged = false;
+    // the automatic choice keeps the direct kernel here: on GB300 the staged pass was
+    // no faster on the 128 MiB fp32 layout and 5 % slower on the 4-block Llama
+    if ((rc = choose_staged(fsdp::norm_staged_fits(L->N, bf) &&
+                                fsdp::norm_staged_partials(D1.n_tiles) <= kMaxPartials,
+                            false, &staged)))
+        return rc;
     int n_part = 0;
-    for (int shifted = 0; shifted < 2; ++shifted) {
+    if (staged && D1.n_tiles > 0) {
+        const cudaError_t e = fsdp::launch_rs_norm_staged(D1.segs, D1.tile_base, D1.n_tiles, bf, gp, L->N, grad_shard,
+                                                          part, &n_part, kWaitNs, st);
+        if (e != cudaSuccess) return cuda_fail(e, "k_rs_norm_staged launch");
+    }
+    for (int shifted = 0; shifted < 2 && !staged; ++shifted) {
         const Range R = range_of(shifted ? L->data_sh : L->data_al, base, ub, ue);
         if (R.n_tiles <= 0) continue;
-        const bool bf = grad_dtype == FSDP_BF16;
         auto launch = [&](auto kernel) {
             const int grid = grid_of(kernel, R.n_tiles, kMaxPartials);
             kernel<<<grid, kThreads, 0, st>>>(R.segs, R.tile_base, R.n_tiles, gp, L->N, L->F, grad_shard,
@@ -500,8 +515,15 @@ int fsdp_accumulate_grads(const fsdp_layout* L, int32_t ub, int32_t ue, float* c
     const Seg* base = nullptr;
     if ((rc = device_tables(L, &base))) return rc;
     const Range R = range_of(L->fullr, base, ub, ue);
+    bool staged = false;
+    if ((rc = choose_staged(true, true, &staged))) return rc;
     if (R.n_tiles <= 0) return FSDP_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (staged) {
+        const cudaError_t e = fsdp::launch_accumulate_staged(R.segs, R.tile_base, R.n_tiles, L->N, acc, micro,
+                                                             micro_dtype == FSDP_BF16, first != 0, kWaitNs, st);
+        return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "k_accumulate_staged launch");
+    }
     if (micro_dtype == FSDP_BF16) {
         auto k = k_accumulate<uint16_t>;
         k<<<grid_of(k, R.n_tiles), kThreads, 0, st>>>(R.segs, R.tile_base, R.n_tiles, ap, L->N, first ? 1 : 0);
@@ -533,15 +555,24 @@ int fsdp_hsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue,
     const Seg* base = nullptr;
     if ((rc = device_tables(L, &base))) return rc;
     const Range D = range_of(L->data, base, ub, ue);
+    const int64_t copy = int64_t(L->N) * L->stride;
+    const bool bf = grad_dtype == FSDP_BF16;
+    bool staged = false;
+    if ((rc = choose_staged(fsdp::hsdp_staged_fits(L->N, n_groups, bf, copy), true, &staged))) return rc;
     if (D.n_tiles <= 0) return FSDP_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t copy = int64_t(L->N) * L->stride;
+    if (staged) {
+        const cudaError_t e = fsdp::launch_hsdp_adamw_staged(D.segs, D.tile_base, D.n_tiles, bf, gp, L->N, n_groups,
+                                                             copy, master, exp_avg, exp_avg_sq,
+                                                             static_cast<uint16_t*>(param_shards), sc,
+                                                             float(n_groups), kWaitNs, st);
+        return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "k_hsdp_adamw_staged launch");
+    }
     auto launch = [&](auto k) {
         k<<<grid_of(k, D.n_tiles), kThreads, 0, st>>>(D.segs, D.tile_base, D.n_tiles, gp, L->N, n_groups, copy,
                                                       master, exp_avg, exp_avg_sq,
                                                       static_cast<uint16_t*>(param_shards), sc, float(n_groups));
     };
-    const bool bf = grad_dtype == FSDP_BF16;
     if (param_shards) bf ? launch(k_hsdp_adamw<uint16_t, true>) : launch(k_hsdp_adamw<float, true>);
     else bf ? launch(k_hsdp_adamw<uint16_t, false>) : launch(k_hsdp_adamw<float, false>);
     const cudaError_t e = cudaGetLastError();

@@ -1,37 +1,45 @@
 // staged.cu -- kernels whose inputs the bulk-copy (TMA) engine stages in shared
-// memory (sm_103a): the fused reduce-scatter + AdamW + bf16 recast, and the
-// all-gather of the aligned class (k_unshard_bulk, further down).
+// memory (sm_103a).
 //
-// Same contract and arithmetic as k_rs_adamw in kernels.cu ("NCCL ZeRO/FSDP state
-// sharding", "ZeRO-2 方向"/"ZeRO-3 方向": each rank keeps only the 1/N slice of
-// the reduce-scattered gradient and updates its own optimizer state with it; "第18章
-// FSDP" §18.16: fp32 reduce, AdamW on the fp32 master, cast to param_dtype).  What
-// differs is how the bytes move:
+// One pipeline, four uses.  A persistent CTA per SM walks its work items (a tile of
+// 2048 elements of one segment, or of one segment and one replica); per item, a
+// producer warp issues one cp.async.bulk global -> shared per input array into a
+// free stage and writes the item's geometry into the stage header, and a "full"
+// mbarrier per stage counts the bytes in (complete_tx).  16 consumer warps wait on
+// it, read their 4 elements of every staged array into registers, release the
+// stage on an "empty" mbarrier (one arrive per warp) and only then compute and
+// store, so the next copies go out while they do.  No CTA-wide barrier in the loop;
+// the bytes in flight per SM do not depend on registers.  The uses:
 //
-//  * One CTA per SM, persistent over its tiles (a tile is 2048 shard elements of
-//    one segment, the tiling of the segment tables), with 2 to 4 pipeline stages
-//    in shared memory, as many as keep about 96 KB in flight; a stage holds the
-//    tile's fp32 master/exp_avg/exp_avg_sq slices and its N gradient slices.
-//  * Warp-specialised: one producer warp issues, per tile, one cp.async.bulk per
-//    array (N + 3 copies) into a free stage and writes the tile's geometry into the
-//    stage header; a "full" mbarrier per stage counts the bytes in (complete_tx).
-//    16 consumer warps wait on it, read the stage into registers and release it on
-//    an "empty" mbarrier before they compute, so the next copies go out while they
-//    do.  No CTA-wide barrier in the loop; the bytes in flight per SM do not depend
-//    on registers.
-//  * A gradient piece whose full-layout offset is not congruent to its shard offset
-//    mod 8 is copied as the 16-byte-aligned window around it and read from shared
-//    memory at the offset: no warp shuffle, one kernel for both alignment classes.
-//  * Each consumer thread owns 4 consecutive elements of the tile: 16-byte
-//    shared-memory reads of the state, 16-byte (fp32) and 8-byte (bf16) global
-//    stores that cover whole sectors per warp.  The at most 3 elements at each end
-//    of a segment that the 16-byte copies leave out go element by element from
-//    global memory.
+//   k_rs_adamw_staged    the fused reduce-scatter (fp32 mean over the N replicas,
+//                        fixed rank order) + AdamW + bf16 recast ("NCCL ZeRO/FSDP
+//                        state sharding", "ZeRO-2 方向"/"ZeRO-3 方向"; "第18章 FSDP"
+//                        §18.6): stage = 3 fp32 state slices + N gradient slices.
+//   k_hsdp_adamw_staged  the same step for R replica groups of N shard ranks ("第18章
+//                        FSDP" §18.9): mean within each group, mean over the groups,
+//                        AdamW on each group's copy of the state.
+//   k_rs_norm_staged     pass 1 of the sharded clip_grad_norm_ ("第18章 FSDP" §18.18):
+//                        the reduce-scatter into the fp32 gradient shard plus the sum
+//                        of squares, one partial per consumer warp.
+//   k_accumulate_staged  fp32 accumulation of one micro-batch into each replica's
+//                        gradient buffer ("第18章 FSDP" §18.26, no_sync).
+//
+// Arithmetic and its order are those of the direct kernels (kernels.cu, rows.cu),
+// bit for bit.  A gradient piece whose full-layout offset is not congruent to its
+// shard offset mod 8 is copied as the 16-byte-aligned window around it and read
+// from shared memory at its offset: no warp shuffle, one launch for both alignment
+// classes.  Each consumer thread owns 4 consecutive elements of an item: 16-byte
+// shared-memory reads, 16-byte (fp32) and 8-byte (bf16) global stores that cover
+// whole sectors per warp.  The at most 7 elements at each end of a segment that
+// the 16-byte copies leave out go element by element from global memory.
+//
+// The all-gather of the aligned class (k_unshard_bulk, further down) moves whole
+// tiles global -> shared -> global with bulk copies and no thread touching them.
 //
 // Every wait on an mbarrier is bounded in time; a warp that gives up records
-// FSDP_ETIMEOUT in a device word that fsdp_check_status reads and returns (the
+// FSDP_ETIMEOUT in a device word that fsdp_check_status reads and returns (a
 // producer first waits, bounded, for the copies it has in flight), after which the
-// CTA's other waits run out in turn.  Nothing else in the kernel waits.
+// CTA's other waits run out in turn.  Nothing else in these kernels waits.
 #include <map>
 #include <mutex>
 #include <type_traits>
@@ -48,11 +56,11 @@ __device__ unsigned int g_wait_error = 0;
 
 namespace {
 
-constexpr int kStThreads = 512;                 // consumer threads: 4 elements each per tile
+constexpr int kStThreads = 512;                 // consumer threads: 4 elements each per item
 constexpr int kConsumerWarps = kStThreads / 32;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 constexpr int kInFlightBytes = 96 * 1024;       // stage bytes in flight per SM to aim for
-constexpr int kFrontBytes = 512;                // mbarriers + per-stage tile geometry
+constexpr int kFrontBytes = 1024;               // mbarriers + per-stage item geometry
 constexpr int kStateBytes = int(kTileElems) * 4;
 
 // ---- PTX wrappers: mbarrier, bulk copy, timer ------------------------------------
@@ -89,15 +97,20 @@ __device__ __forceinline__ uint64_t global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Waits for phase `parity` of the barrier to complete, for at most limit_ns
-// nanoseconds (and at most 2^24 polls); false if it gave up.
+// Waits for phase `parity` of the barrier to complete, for at most about limit_ns
+// nanoseconds (and at most 2^24 polls); false if it gave up.  The clock is read
+// once every 64 polls, starting at the 64th: a read of %globaltimer is slow, and
+// most waits end within the first polls.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
+    uint64_t t0 = 0;
 #pragma unroll 1
     for (uint32_t i = 0; i < (1u << 24); ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > limit_ns) return false;
+        if ((i & 63) == 63) {
+            const uint64_t now = global_ns();
+            if (i == 63) t0 = now;
+            else if (now - t0 > limit_ns) return false;
+        }
     }
     return false;
 }
@@ -115,9 +128,11 @@ __device__ __forceinline__ int64_t ceil_to(int64_t x, int64_t a) { return (x + a
 // Geometry of one tile: its shard range [s0, s1) (inside the 2048-element block
 // at t0), the full-layout shift delta, and the 16-byte-aligned sub-ranges the
 // bulk copies bring in: state [as, bs) (shard side), gradients [ag, bg) (full
-// side), staged at shared offset (x - t0) and (f - gbase) respectively.
+// side), staged at shared offset (x - t0) and (f - gbase) respectively.  q is the
+// first replica of a per-replica item.
 struct TileGeom {
     int64_t t0, s0, s1, delta, as, bs, ag, bg, gbase;
+    int32_t q;
 };
 
 template <typename GT>
@@ -134,11 +149,12 @@ __device__ __forceinline__ TileGeom tile_geom(const Seg& sg, int64_t gt) {
     g.ag = ceil_to(g.s0 + g.delta, E);
     g.bg = floor_to(g.s1 + g.delta, E);
     g.gbase = floor_to(g.t0 + g.delta, E);
+    g.q = 0;
     return g;
 }
 
 // Four gradient elements at shared element offset o (GT elements) of one staged
-// slice, as fp32; r = o mod (elements per read) is uniform over the tile.
+// slice, as fp32; r = o mod 4 is uniform over the item.
 __device__ __forceinline__ float4 smem_grad4(const unsigned char* base, int o, const float*) {
     const float* p = reinterpret_cast<const float*>(base);
     const int r = o & 3;
@@ -164,24 +180,38 @@ __device__ __forceinline__ float4 smem_grad4(const unsigned char* base, int o, c
     }
     return make_float4(bf16lo(w0), bf16hi(w0), bf16lo(w1), bf16hi(w1));
 }
+template <typename GT>
+__device__ __forceinline__ float4 grad4(const unsigned char* base, int o) {
+    return smem_grad4(base, o, static_cast<const GT*>(nullptr));
+}
 
-struct StageLayout {
-    int n_stages;      // 2..4
-    int grank_bytes;   // bytes of one staged gradient slice: 2048 elements + 16
-    int stage_bytes;   // 3 * 8192 + N * grank_bytes
-};
+__device__ __forceinline__ float4 lds4(const unsigned char* p) { return *reinterpret_cast<const float4*>(p); }
 
-template <typename GT, bool PARAM, bool GOUT>
-__global__ void __launch_bounds__(kStThreads + 32, 1)
-k_rs_adamw_staged(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N,
-                  float* master, float* exp_avg, float* exp_avg_sq, uint16_t* __restrict__ param,
-                  float* __restrict__ gout, AdamScal sc, StageLayout sl, uint64_t wait_ns) {
+// Bytes of one staged gradient slice: a tile plus the 16 bytes a shifted window adds.
+template <typename GT>
+__host__ __device__ constexpr int grank_bytes() { return int(kTileElems * sizeof(GT)) + 16; }
+
+// ----------------------------------------------------------------------------
+// The pipeline.  Pol supplies, for item i of the launch:
+//   geom(i, cursor)            its geometry (producer side, once per item), resolved
+//                              before the producer waits for a free stage when
+//                              Pol::kGeomFirst, else after (measured on GB300: the
+//                              fused step gains 1-3 % from the first order, HSDP and
+//                              accumulation lose 3-4 % with it)
+//   bytes(g)                   the bytes its copies bring in
+//   issue(g, stage, bar, lane) its copies (all producer lanes call it)
+//   consume(g, stage, tid, release)  the consumers' work; release() (all lanes of
+//                              each consumer warp call it once) frees the stage;
+//                              returns the thread's contribution to a sum
+//   finish(tid, sum)           after the consumer's last item, with the thread's sum
+// ----------------------------------------------------------------------------
+template <class Pol>
+__device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
     extern __shared__ __align__(128) unsigned char smem[];
+    static_assert(16 * kMaxStages + kMaxStages * sizeof(TileGeom) <= kFrontBytes, "front region");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int S = sl.n_stages;
     const int64_t G = gridDim.x;
-    const int64_t n_mine = blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + G - 1) / G : 0;
-    // front region: full[S] and empty[S] mbarriers, then one TileGeom per stage
+    const int64_t n_mine = blockIdx.x < n_items ? (n_items - blockIdx.x + G - 1) / G : 0;
     const uint32_t full0 = smem_addr(smem), empty0 = full0 + 8 * kMaxStages;
     TileGeom* geo = reinterpret_cast<TileGeom*>(smem + 16 * kMaxStages);
     unsigned char* stage0 = smem + kFrontBytes;
@@ -196,50 +226,40 @@ k_rs_adamw_staged(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_til
     __syncthreads();
 
     if (warp == kConsumerWarps) {
-        // ---- producer warp: bring tile j of this CTA into stage j mod S ----
-        int ps = 0;                                  // segment cursor
+        // ---- producer warp: item j of this CTA into stage j mod S ----
+        int cursor = 0;
         int64_t j = 0;
         for (; j < n_mine; ++j) {
             const int st = int(j % S);
             const int64_t use = j / S;
-            if (use > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * st, uint32_t((use - 1) & 1), wait_ns))) {
+            // the item's geometry (segment-table reads) before or after the wait for a
+            // free stage: Pol::kGeomFirst, chosen per use by measurement
+            TileGeom g;
+            if (Pol::kGeomFirst) g = pol.geom(blockIdx.x + j * G, cursor);
+            if (use > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * st, uint32_t((use - 1) & 1), wait_ns))) {
                 if (lane == 0) atomicOr(&g_wait_error, 1u);
                 break;
             }
-            const int64_t gt = tile_base + blockIdx.x + j * G;
-            ps = advance_seg(segs, ps, gt);
-            const TileGeom g = tile_geom<GT>(segs[ps], gt);
+            if (!Pol::kGeomFirst) g = pol.geom(blockIdx.x + j * G, cursor);
             const uint32_t bar = full0 + 8 * st;
-            const uint32_t sbase = smem_addr(stage0 + int64_t(st) * sl.stage_bytes);
-            const uint32_t sbytes = g.bs > g.as ? uint32_t(g.bs - g.as) * 4u : 0u;
-            const uint32_t gbytes = g.bg > g.ag ? uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
             if (lane == 0) {
-                geo[st] = g;                                          // released by the arrive
-                mbar_arrive_tx(bar, 3u * sbytes + uint32_t(N) * gbytes);
+                geo[st] = g;                                  // released by the arrive
+                mbar_arrive_tx(bar, pol.bytes(g));
             }
             __syncwarp();
-            for (int k = lane; k < N + 3; k += 32) {
-                if (k < 3) {
-                    const float* arr = k == 0 ? master : (k == 1 ? exp_avg : exp_avg_sq);
-                    if (sbytes) bulk_g2s(sbase + k * kStateBytes + uint32_t(g.as - g.t0) * 4u, arr + g.as, sbytes, bar);
-                } else if (gbytes) {
-                    const int q = k - 3;
-                    bulk_g2s(sbase + 3 * kStateBytes + q * sl.grank_bytes +
-                                 uint32_t(g.ag - g.gbase) * uint32_t(sizeof(GT)),
-                             static_cast<const GT*>(gp.p[q]) + g.ag, gbytes, bar);
-                }
-            }
+            pol.issue(g, smem_addr(stage0 + int64_t(st) * stage_bytes), bar, lane);
         }
         if (j < n_mine) {
-            // gave up: let the copies already issued land before the CTA's shared memory goes away
+            // gave up: let the copies already issued land before the shared memory goes away
             for (int64_t k = j - S > 0 ? j - S : 0; k < j; ++k)
                 mbar_wait_bounded(full0 + 8 * int(k % S), uint32_t((k / S) & 1), wait_ns);
         }
         return;
     }
 
-    // ---- consumer warps: 4 elements per thread per tile ----
-    const int c = tid * 4;
+    // ---- consumer warps ----
+    double sum = 0.0;
     for (int64_t j = 0; j < n_mine; ++j) {
         const int st = int(j % S);
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * st, uint32_t((j / S) & 1), wait_ns))) {
@@ -247,30 +267,74 @@ k_rs_adamw_staged(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_til
             return;
         }
         const TileGeom g = geo[st];
-        const unsigned char* sb = stage0 + int64_t(st) * sl.stage_bytes;
-        const int64_t x = g.t0 + c;
-        const int64_t f = x + g.delta;
+        const uint32_t empty = empty0 + 8 * st;
+        sum += pol.consume(g, stage0 + int64_t(st) * stage_bytes, tid, [&] {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty);
+        });
+    }
+    pol.finish(tid, sum);
+}
+
+// ---- fused reduce-scatter + AdamW + cast ------------------------------------------
+template <typename GT, bool PARAM, bool GOUT>
+struct RsAdamw {
+    static constexpr bool kGeomFirst = true;
+    const Seg* segs;
+    int64_t tile_base;
+    GradPtrs gp;
+    int N;
+    float *master, *exp_avg, *exp_avg_sq;
+    uint16_t* param;
+    float* gout;
+    AdamScal sc;
+
+    __device__ TileGeom geom(int64_t i, int& cur) const {
+        const int64_t gt = tile_base + i;
+        cur = advance_seg(segs, cur, gt);
+        return tile_geom<GT>(segs[cur], gt);
+    }
+    __device__ uint32_t bytes(const TileGeom& g) const {
+        const uint32_t sb = g.bs > g.as ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t gb = g.bg > g.ag ? uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
+        return 3u * sb + uint32_t(N) * gb;
+    }
+    __device__ void issue(const TileGeom& g, uint32_t sbase, uint32_t bar, int lane) const {
+        const uint32_t sb = g.bs > g.as ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t gb = g.bg > g.ag ? uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
+        for (int k = lane; k < N + 3; k += 32) {
+            if (k < 3) {
+                const float* arr = k == 0 ? master : (k == 1 ? exp_avg : exp_avg_sq);
+                if (sb) bulk_g2s(sbase + k * kStateBytes + uint32_t(g.as - g.t0) * 4u, arr + g.as, sb, bar);
+            } else if (gb) {
+                const int q = k - 3;
+                bulk_g2s(sbase + 3 * kStateBytes + q * grank_bytes<GT>() + uint32_t(g.ag - g.gbase) * uint32_t(sizeof(GT)),
+                         static_cast<const GT*>(gp.p[q]) + g.ag, gb, bar);
+            }
+        }
+    }
+    template <class Release>
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Release release) const {
+        const int c = tid * 4;
+        const int64_t x = g.t0 + c, f = x + g.delta;
         const bool live = x + 4 > g.s0 && x < g.s1;
         const bool fast = x >= g.s0 && x + 4 <= g.s1 && f >= g.ag && f + 4 <= g.bg;
         float4 pv, mv, vv;
         float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
         if (fast) {
-            // everything this thread needs from the stage, into registers
-            pv = *reinterpret_cast<const float4*>(sb + 0 * kStateBytes + c * 4);
-            mv = *reinterpret_cast<const float4*>(sb + 1 * kStateBytes + c * 4);
-            vv = *reinterpret_cast<const float4*>(sb + 2 * kStateBytes + c * 4);
+            pv = lds4(sb + 0 * kStateBytes + c * 4);
+            mv = lds4(sb + 1 * kStateBytes + c * 4);
+            vv = lds4(sb + 2 * kStateBytes + c * 4);
             const int o = int(f - g.gbase);
             const unsigned char* gs = sb + 3 * kStateBytes;
 #pragma unroll 4
             for (int q = 0; q < N; ++q) {            // fixed rank order
-                const float4 x4 = smem_grad4(gs + q * sl.grank_bytes, o, static_cast<const GT*>(nullptr));
+                const float4 x4 = grad4<GT>(gs + q * grank_bytes<GT>(), o);
                 a0 = __fadd_rn(a0, x4.x); a1 = __fadd_rn(a1, x4.y);
                 a2 = __fadd_rn(a2, x4.z); a3 = __fadd_rn(a3, x4.w);
             }
         }
-        // the stage is free for the producer once the whole warp has read it
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * st);
+        release();
         if (fast) {
             float p[4] = {pv.x, pv.y, pv.z, pv.w};
             float m[4] = {mv.x, mv.y, mv.z, mv.w};
@@ -297,7 +361,306 @@ k_rs_adamw_staged(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_til
                 if (GOUT) gout[e] = gg;
             }
         }
+        return 0.0;
     }
+    __device__ void finish(int, double) const {}
+};
+
+// ---- HSDP: R replica groups x N shard ranks -----------------------------------------
+// g = (sum over groups rho of (sum over q of G[rho*N + q]) / N) / R, then AdamW on
+// each group's copy of the state (copy rho at element offset rho * copy).
+template <typename GT, bool PARAM>
+struct HsdpAdamw {
+    static constexpr bool kGeomFirst = false;
+    static constexpr int kMaxR = 3;
+    const Seg* segs;
+    int64_t tile_base;
+    GradPtrs gp;
+    int N, R;
+    int64_t copy;
+    float *master, *exp_avg, *exp_avg_sq;
+    uint16_t* param;
+    AdamScal sc;
+    float rf;
+
+    __device__ TileGeom geom(int64_t i, int& cur) const {
+        const int64_t gt = tile_base + i;
+        cur = advance_seg(segs, cur, gt);
+        return tile_geom<GT>(segs[cur], gt);
+    }
+    __device__ uint32_t bytes(const TileGeom& g) const {
+        const uint32_t sb = g.bs > g.as ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t gb = g.bg > g.ag ? uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
+        return 3u * uint32_t(R) * sb + uint32_t(R * N) * gb;
+    }
+    __device__ void issue(const TileGeom& g, uint32_t sbase, uint32_t bar, int lane) const {
+        const uint32_t sb = g.bs > g.as ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t gb = g.bg > g.ag ? uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
+        const int ns = 3 * R;
+        for (int k = lane; k < ns + R * N; k += 32) {
+            if (k < ns) {
+                const int arr_i = k % 3, rho = k / 3;
+                const float* arr = arr_i == 0 ? master : (arr_i == 1 ? exp_avg : exp_avg_sq);
+                if (sb) bulk_g2s(sbase + k * kStateBytes + uint32_t(g.as - g.t0) * 4u, arr + rho * copy + g.as, sb, bar);
+            } else if (gb) {
+                const int q = k - ns;
+                bulk_g2s(sbase + ns * kStateBytes + q * grank_bytes<GT>() + uint32_t(g.ag - g.gbase) * uint32_t(sizeof(GT)),
+                         static_cast<const GT*>(gp.p[q]) + g.ag, gb, bar);
+            }
+        }
+    }
+    template <class Release>
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Release release) const {
+        const int c = tid * 4;
+        const int64_t x = g.t0 + c, f = x + g.delta;
+        const bool live = x + 4 > g.s0 && x < g.s1;
+        const bool fast = x >= g.s0 && x + 4 <= g.s1 && f >= g.ag && f + 4 <= g.bg;
+        float4 st[3 * kMaxR];
+        float o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f;
+        if (fast) {
+#pragma unroll
+            for (int k = 0; k < 3 * kMaxR; ++k)
+                if (k < 3 * R) st[k] = lds4(sb + k * kStateBytes + c * 4);
+            const int o = int(f - g.gbase);
+            const unsigned char* gs = sb + 3 * R * kStateBytes;
+            for (int rho = 0; rho < R; ++rho) {
+                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll 4
+                for (int q = 0; q < N; ++q) {
+                    const float4 x4 = grad4<GT>(gs + (rho * N + q) * grank_bytes<GT>(), o);
+                    a0 = __fadd_rn(a0, x4.x); a1 = __fadd_rn(a1, x4.y);
+                    a2 = __fadd_rn(a2, x4.z); a3 = __fadd_rn(a3, x4.w);
+                }
+                o0 = __fadd_rn(o0, __fdiv_rn(a0, sc.nf)); o1 = __fadd_rn(o1, __fdiv_rn(a1, sc.nf));
+                o2 = __fadd_rn(o2, __fdiv_rn(a2, sc.nf)); o3 = __fadd_rn(o3, __fdiv_rn(a3, sc.nf));
+            }
+        }
+        release();
+        if (fast) {
+            const float gg[4] = {__fdiv_rn(o0, rf), __fdiv_rn(o1, rf), __fdiv_rn(o2, rf), __fdiv_rn(o3, rf)};
+#pragma unroll
+            for (int rho = 0; rho < kMaxR; ++rho) {
+                if (rho >= R) break;
+                float p[4] = {st[3 * rho].x, st[3 * rho].y, st[3 * rho].z, st[3 * rho].w};
+                float m[4] = {st[3 * rho + 1].x, st[3 * rho + 1].y, st[3 * rho + 1].z, st[3 * rho + 1].w};
+                float v[4] = {st[3 * rho + 2].x, st[3 * rho + 2].y, st[3 * rho + 2].z, st[3 * rho + 2].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) adamw1(sc, gg[k], p[k], m[k], v[k]);
+                const int64_t e = rho * copy + x;
+                st4(master + e, make_float4(p[0], p[1], p[2], p[3]));
+                st4(exp_avg + e, make_float4(m[0], m[1], m[2], m[3]));
+                st4(exp_avg_sq + e, make_float4(v[0], v[1], v[2], v[3]));
+                if (PARAM)
+                    *reinterpret_cast<uint2*>(param + e) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
+            }
+        } else if (live) {
+            const int64_t a = x > g.s0 ? x : g.s0;
+            const int64_t b = (x + 4) < g.s1 ? (x + 4) : g.s1;
+            for (int64_t e = a; e < b; ++e) {
+                float outer = 0.0f;
+                for (int rho = 0; rho < R; ++rho) {
+                    float acc = 0.0f;
+                    for (int q = 0; q < N; ++q)
+                        acc = __fadd_rn(acc, GradIO<GT>::load1(gp.p[rho * N + q], e + g.delta));
+                    outer = __fadd_rn(outer, __fdiv_rn(acc, sc.nf));
+                }
+                const float gg = __fdiv_rn(outer, rf);
+                for (int rho = 0; rho < R; ++rho) {
+                    const int64_t y = rho * copy + e;
+                    float pp = master[y], mm = exp_avg[y], vv = exp_avg_sq[y];
+                    adamw1(sc, gg, pp, mm, vv);
+                    master[y] = pp; exp_avg[y] = mm; exp_avg_sq[y] = vv;
+                    if (PARAM) param[y] = to_bf16(pp);
+                }
+            }
+        }
+        return 0.0;
+    }
+    __device__ void finish(int, double) const {}
+};
+
+// ---- clip pass 1: reduce-scatter into the fp32 shard + sums of squares ---------------
+// Each 4-element chunk's squares are summed in fp32 (fma), the chunks in double; one
+// partial per consumer warp (warp tree, lane order), written to part[CTA * 16 + warp].
+template <typename GT>
+struct RsNorm {
+    static constexpr bool kGeomFirst = false;
+    const Seg* segs;
+    int64_t tile_base;
+    GradPtrs gp;
+    int N;
+    float* gout;
+    float nf;
+    double* part;
+
+    __device__ TileGeom geom(int64_t i, int& cur) const {
+        const int64_t gt = tile_base + i;
+        cur = advance_seg(segs, cur, gt);
+        return tile_geom<GT>(segs[cur], gt);
+    }
+    __device__ uint32_t bytes(const TileGeom& g) const {
+        return g.bg > g.ag ? uint32_t(N) * uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
+    }
+    __device__ void issue(const TileGeom& g, uint32_t sbase, uint32_t bar, int lane) const {
+        if (g.bg <= g.ag) return;
+        const uint32_t gb = uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT));
+        for (int q = lane; q < N; q += 32)
+            bulk_g2s(sbase + q * grank_bytes<GT>() + uint32_t(g.ag - g.gbase) * uint32_t(sizeof(GT)),
+                     static_cast<const GT*>(gp.p[q]) + g.ag, gb, bar);
+    }
+    template <class Release>
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Release release) const {
+        const int c = tid * 4;
+        const int64_t x = g.t0 + c, f = x + g.delta;
+        const bool live = x + 4 > g.s0 && x < g.s1;
+        const bool fast = x >= g.s0 && x + 4 <= g.s1 && f >= g.ag && f + 4 <= g.bg;
+        double ss = 0.0;
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+        if (fast) {
+            const int o = int(f - g.gbase);
+#pragma unroll 4
+            for (int q = 0; q < N; ++q) {
+                const float4 x4 = grad4<GT>(sb + q * grank_bytes<GT>(), o);
+                a0 = __fadd_rn(a0, x4.x); a1 = __fadd_rn(a1, x4.y);
+                a2 = __fadd_rn(a2, x4.z); a3 = __fadd_rn(a3, x4.w);
+            }
+        }
+        release();
+        if (fast) {
+            const float g0 = __fdiv_rn(a0, nf), g1 = __fdiv_rn(a1, nf), g2 = __fdiv_rn(a2, nf), g3 = __fdiv_rn(a3, nf);
+            st4(gout + x, make_float4(g0, g1, g2, g3));
+            float sq = __fmul_rn(g0, g0);
+            sq = __fmaf_rn(g1, g1, sq);
+            sq = __fmaf_rn(g2, g2, sq);
+            sq = __fmaf_rn(g3, g3, sq);
+            ss += double(sq);
+        } else if (live) {
+            const int64_t a = x > g.s0 ? x : g.s0;
+            const int64_t b = (x + 4) < g.s1 ? (x + 4) : g.s1;
+            for (int64_t e = a; e < b; ++e) {
+                const float gg = __fdiv_rn(reduce1<GT>(gp, N, e + g.delta), nf);
+                gout[e] = gg;
+                ss += double(gg) * double(gg);
+            }
+        }
+        return ss;
+    }
+    __device__ void finish(int tid, double x) const {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+        if ((tid & 31) == 0) part[int64_t(blockIdx.x) * kConsumerWarps + (tid >> 5)] = x;
+    }
+};
+
+// ---- accumulation of one micro-batch into each replica's fp32 buffer ----------------
+// Items are (tile of the full layout, group of Q consecutive replicas): the stage
+// holds the group's micro-batch slices, then (unless FIRST) its accumulator slices,
+// so that one item moves about as many bytes as a tile of the fused step.  For
+// each replica q of the group, acc[q] = micro[q] (FIRST) or acc[q] + micro[q], one
+// fp32 addition per element.
+template <typename MT, bool FIRST>
+struct Accumulate {
+    static constexpr bool kGeomFirst = false;
+    static constexpr int kMaxQ = 8;
+    const Seg* segs;                   // logical full-layout ranges (shard field = full index)
+    int64_t tile_base;
+    int N, Q, NG;                      // replicas, replicas per item, groups (ceil(N / Q))
+    float* acc[kMaxRanks];
+    const void* micro[kMaxRanks];
+
+    static constexpr int kMicroBytes = int(kTileElems * sizeof(MT));
+    __device__ int nq(const TileGeom& g) const { return (N - g.q) < Q ? (N - g.q) : Q; }
+    __device__ TileGeom geom(int64_t i, int& cur) const {
+        const int64_t gt = tile_base + i / NG;
+        cur = advance_seg(segs, cur, gt);
+        TileGeom g = tile_geom<MT>(segs[cur], gt);     // delta = 0: micro and acc share the index
+        g.as = g.ag; g.bs = g.bg;                        // one aligned interior for both arrays
+        g.q = int32_t(i % NG) * Q;
+        return g;
+    }
+    __device__ uint32_t bytes(const TileGeom& g) const {
+        if (g.bg <= g.ag) return 0u;
+        const uint32_t n = uint32_t(g.bg - g.ag);
+        return uint32_t(nq(g)) * (n * uint32_t(sizeof(MT)) + (FIRST ? 0u : n * 4u));
+    }
+    __device__ void issue(const TileGeom& g, uint32_t sbase, uint32_t bar, int lane) const {
+        if (g.bg <= g.ag) return;
+        const uint32_t n = uint32_t(g.bg - g.ag);
+        const int k = nq(g);
+        for (int c = lane; c < (FIRST ? k : 2 * k); c += 32) {
+            if (c < k)
+                bulk_g2s(sbase + c * kMicroBytes + uint32_t(g.ag - g.t0) * uint32_t(sizeof(MT)),
+                         static_cast<const MT*>(micro[g.q + c]) + g.ag, n * uint32_t(sizeof(MT)), bar);
+            else
+                bulk_g2s(sbase + Q * kMicroBytes + (c - k) * kStateBytes + uint32_t(g.ag - g.t0) * 4u,
+                         acc[g.q + c - k] + g.ag, n * 4u, bar);
+        }
+    }
+    template <class Release>
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Release release) const {
+        const int c = tid * 4;
+        const int64_t x = g.t0 + c;
+        const bool live = x + 4 > g.s0 && x < g.s1;
+        const bool fast = x >= g.ag && x + 4 <= g.bg;
+        const int k = nq(g);
+        float4 out[kMaxQ];
+        if (fast) {
+#pragma unroll
+            for (int r = 0; r < kMaxQ; ++r) {
+                if (r >= k) break;
+                float4 mv = grad4<MT>(sb + r * kMicroBytes, c);
+                if (!FIRST) {
+                    const float4 av = lds4(sb + Q * kMicroBytes + r * kStateBytes + c * 4);
+                    mv.x = __fadd_rn(av.x, mv.x); mv.y = __fadd_rn(av.y, mv.y);
+                    mv.z = __fadd_rn(av.z, mv.z); mv.w = __fadd_rn(av.w, mv.w);
+                }
+                out[r] = mv;
+            }
+        }
+        release();
+        if (fast) {
+#pragma unroll
+            for (int r = 0; r < kMaxQ; ++r) {
+                if (r >= k) break;
+                st4(acc[g.q + r] + x, out[r]);
+            }
+        } else if (live) {
+            const int64_t lo = x > g.s0 ? x : g.s0;
+            const int64_t hi = (x + 4) < g.s1 ? (x + 4) : g.s1;
+            for (int r = 0; r < k; ++r)
+                for (int64_t e = lo; e < hi; ++e) {
+                    const float v = GradIO<MT>::load1(micro[g.q + r], e);
+                    acc[g.q + r][e] = FIRST ? v : __fadd_rn(acc[g.q + r][e], v);
+                }
+        }
+        return 0.0;
+    }
+    __device__ void finish(int, double) const {}
+};
+
+// ---- the kernels ------------------------------------------------------------------
+template <typename GT, bool PARAM, bool GOUT>
+__global__ void __launch_bounds__(kStThreads + 32, 1)
+k_rs_adamw_staged(RsAdamw<GT, PARAM, GOUT> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+}
+
+template <typename GT, bool PARAM>
+__global__ void __launch_bounds__(kStThreads + 32, 1)
+k_hsdp_adamw_staged(HsdpAdamw<GT, PARAM> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+}
+
+template <typename GT>
+__global__ void __launch_bounds__(kStThreads + 32, 1)
+k_rs_norm_staged(RsNorm<GT> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+}
+
+template <typename MT, bool FIRST>
+__global__ void __launch_bounds__(kStThreads + 32, 1)
+k_accumulate_staged(Accumulate<MT, FIRST> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
 }
 
 // ----------------------------------------------------------------------------
@@ -412,36 +775,41 @@ __global__ void k_wait_selftest(uint64_t wait_ns) {
 }
 
 // ---- host side ------------------------------------------------------------------
-std::mutex g_st_mu;
-std::map<std::pair<const void*, int>, std::pair<int, int>> g_st_cache;   // (kernel, dev) -> (SMs, smem set)
-
 int optin_smem(int dev) {
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     return v;
 }
 
-StageLayout stage_layout(int N, bool grad_bf16, int dev) {
-    StageLayout sl{};
-    const int gs = grad_bf16 ? 2 : 4;
-    sl.grank_bytes = int(kTileElems) * gs + 16;
-    sl.stage_bytes = 3 * kStateBytes + N * sl.grank_bytes;
+// Stages for a stage of `stage_bytes`: as many as keep about 96 KB in flight (the
+// stages beyond the one being consumed), between 2 and kMaxStages, within the
+// opt-in shared memory; 0 if two do not fit.  Measured on GB300 (fused step): about
+// 50-100 KB in flight per SM streams best; 3-4 stages of 57 KB lost up to 10 % of
+// the bandwidth, fewer than 40 KB in flight lost 8 %.
+int stage_count(int stage_bytes, int dev) {
     const int avail = optin_smem(dev) - kFrontBytes;
-    const int fit = avail > 0 ? avail / sl.stage_bytes : 0;
-    // Stages beyond the one being consumed are in flight.  Measured on GB300: about
-    // 50-100 KB in flight per SM streams best; more (3-4 stages of 57 KB) lost up to
-    // 10 % of the bandwidth, fewer than 40 KB lost 8 %.
-    int want = kInFlightBytes / sl.stage_bytes + 1;
+    const int fit = avail > 0 ? avail / stage_bytes : 0;
+    int want = kInFlightBytes / stage_bytes + 1;
     want = want < 2 ? 2 : (want > kMaxStages ? kMaxStages : want);
-    sl.n_stages = fit < want ? fit : want;
-    return sl;
+    const int s = fit < want ? fit : want;
+    return s >= 2 ? s : 0;
 }
 
-template <typename K>
-cudaError_t launch_staged_k(K kernel, const Seg* segs, int64_t tile_base, int64_t n_tiles, const GradPtrs& gp,
-                            int N, float* master, float* m, float* v, uint16_t* param, float* gout,
-                            const AdamScal& sc, const StageLayout& sl, uint64_t wait_ns, int dev, cudaStream_t st) {
-    const int smem = kFrontBytes + sl.n_stages * sl.stage_bytes;
+std::mutex g_st_mu;
+std::map<std::pair<const void*, int>, std::pair<int, int>> g_st_cache;   // (kernel, dev) -> (SMs, smem set)
+
+// One CTA of 544 threads per SM (at most one per item).
+template <typename K, typename Pol>
+cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage_bytes, uint64_t wait_ns,
+                            cudaStream_t st, int* grid_out = nullptr) {
+    if (grid_out) *grid_out = 0;
+    if (n_items <= 0) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int S = stage_count(stage_bytes, dev);
+    if (S < 2) return cudaErrorInvalidValue;
+    const int smem = kFrontBytes + S * stage_bytes;
     const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
     int sms = 0, set = 0;
     {
@@ -450,56 +818,130 @@ cudaError_t launch_staged_k(K kernel, const Seg* segs, int64_t tile_base, int64_
         if (it != g_st_cache.end()) { sms = it->second.first; set = it->second.second; }
     }
     if (set < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
         std::lock_guard<std::mutex> lk(g_st_mu);
         g_st_cache[key] = std::make_pair(sms, smem);
     }
-    const int64_t blocks = n_tiles < sms ? n_tiles : (sms > 0 ? sms : 1);
-    kernel<<<int(blocks), kStThreads + 32, smem, st>>>(segs, tile_base, n_tiles, gp, N, master, m, v, param, gout, sc, sl,
-                                                  wait_ns);
+    const int64_t blocks = n_items < sms ? n_items : (sms > 0 ? sms : 1);
+    kernel<<<int(blocks), kStThreads + 32, smem, st>>>(pol, n_items, S, stage_bytes, wait_ns);
+    if (grid_out) *grid_out = int(blocks);
     return cudaGetLastError();
 }
 
-template <typename GT>
-cudaError_t launch_staged_t(const Seg* segs, int64_t tile_base, int64_t n_tiles, const GradPtrs& gp, int N,
-                            float* master, float* m, float* v, uint16_t* param, float* gout, const AdamScal& sc,
-                            const StageLayout& sl, uint64_t wait_ns, int dev, cudaStream_t st) {
-    if (param && gout)
-        return launch_staged_k(k_rs_adamw_staged<GT, true, true>, segs, tile_base, n_tiles, gp, N, master, m, v, param,
-                               gout, sc, sl, wait_ns, dev, st);
-    if (param)
-        return launch_staged_k(k_rs_adamw_staged<GT, true, false>, segs, tile_base, n_tiles, gp, N, master, m, v,
-                               param, gout, sc, sl, wait_ns, dev, st);
-    if (gout)
-        return launch_staged_k(k_rs_adamw_staged<GT, false, true>, segs, tile_base, n_tiles, gp, N, master, m, v,
-                               param, gout, sc, sl, wait_ns, dev, st);
-    return launch_staged_k(k_rs_adamw_staged<GT, false, false>, segs, tile_base, n_tiles, gp, N, master, m, v, param,
-                           gout, sc, sl, wait_ns, dev, st);
+int rs_stage_bytes(int N, bool bf16) { return 3 * kStateBytes + N * (bf16 ? grank_bytes<uint16_t>() : grank_bytes<float>()); }
+int hsdp_stage_bytes(int N, int R, bool bf16) {
+    return 3 * R * kStateBytes + R * N * (bf16 ? grank_bytes<uint16_t>() : grank_bytes<float>());
+}
+int norm_stage_bytes(int N, bool bf16) { return N * (bf16 ? grank_bytes<uint16_t>() : grank_bytes<float>()); }
+int acc_stage_bytes(int Q, bool bf16, bool first) { return Q * (int(kTileElems) * (bf16 ? 2 : 4) + (first ? 0 : kStateBytes)); }
+
+bool fits(int stage_bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    return stage_count(stage_bytes, dev) >= 2;
 }
 
 }  // namespace
 
-bool staged_fits(int N, bool grad_bf16) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    return stage_layout(N, grad_bf16, dev).n_stages >= 2;
+bool staged_fits(int N, bool grad_bf16) { return fits(rs_stage_bytes(N, grad_bf16)); }
+
+bool hsdp_staged_fits(int N, int R, bool grad_bf16, int64_t copy) {
+    return R <= HsdpAdamw<float, false>::kMaxR && (copy & 3) == 0 && fits(hsdp_stage_bytes(N, R, grad_bf16));
+}
+
+bool norm_staged_fits(int N, bool grad_bf16) { return fits(norm_stage_bytes(N, grad_bf16)); }
+
+int norm_staged_partials(int64_t n_tiles) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = n_tiles < sms ? n_tiles : sms;
+    return int(blocks) * kConsumerWarps;
 }
 
 cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
                                    const GradPtrs& gp, int N, float* master, float* m, float* v, uint16_t* param,
                                    float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st) {
-    if (n_tiles <= 0) return cudaSuccess;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const StageLayout sl = stage_layout(N, grad_bf16, dev);
-    if (sl.n_stages < 2) return cudaErrorInvalidValue;
-    return grad_bf16 ? launch_staged_t<uint16_t>(segs, tile_base, n_tiles, gp, N, master, m, v, param, gout, sc, sl,
-                                                 wait_ns, dev, st)
-                     : launch_staged_t<float>(segs, tile_base, n_tiles, gp, N, master, m, v, param, gout, sc, sl,
-                                              wait_ns, dev, st);
+    const int sb = rs_stage_bytes(N, grad_bf16);
+    auto go = [&](auto tag_gt, auto tag_p, auto tag_g) {
+        using GT = decltype(tag_gt);
+        constexpr bool P = decltype(tag_p)::value, O = decltype(tag_g)::value;
+        RsAdamw<GT, P, O> pol{segs, tile_base, gp, N, master, m, v, param, gout, sc};
+        return launch_pipeline(k_rs_adamw_staged<GT, P, O>, pol, n_tiles, sb, wait_ns, st);
+    };
+    using T = std::true_type;
+    using F = std::false_type;
+    if (grad_bf16) {
+        if (param) return gout ? go(uint16_t{}, T{}, T{}) : go(uint16_t{}, T{}, F{});
+        return gout ? go(uint16_t{}, F{}, T{}) : go(uint16_t{}, F{}, F{});
+    }
+    if (param) return gout ? go(float{}, T{}, T{}) : go(float{}, T{}, F{});
+    return gout ? go(float{}, F{}, T{}) : go(float{}, F{}, F{});
+}
+
+cudaError_t launch_hsdp_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
+                                     const GradPtrs& gp, int N, int R, int64_t copy, float* master, float* m,
+                                     float* v, uint16_t* param, const AdamScal& sc, float rf, uint64_t wait_ns,
+                                     cudaStream_t st) {
+    const int sb = hsdp_stage_bytes(N, R, grad_bf16);
+    auto go = [&](auto tag_gt, auto tag_p) {
+        using GT = decltype(tag_gt);
+        constexpr bool P = decltype(tag_p)::value;
+        HsdpAdamw<GT, P> pol{segs, tile_base, gp, N, R, copy, master, m, v, param, sc, rf};
+        return launch_pipeline(k_hsdp_adamw_staged<GT, P>, pol, n_tiles, sb, wait_ns, st);
+    };
+    if (grad_bf16) return param ? go(uint16_t{}, std::true_type{}) : go(uint16_t{}, std::false_type{});
+    return param ? go(float{}, std::true_type{}) : go(float{}, std::false_type{});
+}
+
+cudaError_t launch_rs_norm_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
+                                  const GradPtrs& gp, int N, float* gout, double* part, int* n_part, uint64_t wait_ns,
+                                  cudaStream_t st) {
+    const int sb = norm_stage_bytes(N, grad_bf16);
+    int grid = 0;
+    cudaError_t e;
+    if (grad_bf16) {
+        RsNorm<uint16_t> pol{segs, tile_base, gp, N, gout, float(N), part};
+        e = launch_pipeline(k_rs_norm_staged<uint16_t>, pol, n_tiles, sb, wait_ns, st, &grid);
+    } else {
+        RsNorm<float> pol{segs, tile_base, gp, N, gout, float(N), part};
+        e = launch_pipeline(k_rs_norm_staged<float>, pol, n_tiles, sb, wait_ns, st, &grid);
+    }
+    *n_part = grid * kConsumerWarps;
+    return e;
+}
+
+cudaError_t launch_accumulate_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, int N, float* const* acc,
+                                     const void* const* micro, bool micro_bf16, bool first, uint64_t wait_ns,
+                                     cudaStream_t st) {
+    // replicas per item: as many as keep a stage near the in-flight target (at most 8)
+    const int per = acc_stage_bytes(1, micro_bf16, first);
+    int Q = kInFlightBytes / per;
+    Q = Q < 1 ? 1 : (Q > Accumulate<float, false>::kMaxQ ? Accumulate<float, false>::kMaxQ : Q);
+    if (Q > N) Q = N;
+    const int NG = (N + Q - 1) / Q;
+    const int sb = acc_stage_bytes(Q, micro_bf16, first);
+    const int64_t n_items = n_tiles * NG;
+    auto go = [&](auto tag_mt, auto tag_first) {
+        using MT = decltype(tag_mt);
+        constexpr bool FIRST = decltype(tag_first)::value;
+        Accumulate<MT, FIRST> pol{};
+        pol.segs = segs;
+        pol.tile_base = tile_base;
+        pol.N = N;
+        pol.Q = Q;
+        pol.NG = NG;
+        for (int q = 0; q < N; ++q) {
+            pol.acc[q] = acc[q];
+            pol.micro[q] = micro[q];
+        }
+        return launch_pipeline(k_accumulate_staged<MT, FIRST>, pol, n_items, sb, wait_ns, st);
+    };
+    if (micro_bf16) return first ? go(uint16_t{}, std::true_type{}) : go(uint16_t{}, std::false_type{});
+    return first ? go(float{}, std::true_type{}) : go(float{}, std::false_type{});
 }
 
 cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16, const void* src,

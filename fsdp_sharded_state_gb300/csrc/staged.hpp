@@ -9,15 +9,42 @@
 
 namespace fsdp {
 
-// Whether at least two pipeline stages (3 fp32 state slices + N gradient slices
-// of one 2048-element tile each) fit in one CTA's shared memory on this device.
+// Whether at least two pipeline stages fit in one CTA's shared memory on this
+// device.  Fused step: a stage holds 2048 elements of the 3 fp32 state arrays and of
+// the N gradient replicas.  HSDP: of 3R state arrays and R*N replicas (and every
+// state copy must start on a 16-byte boundary: copy % 4 == 0, R <= 3).  Clip pass 1:
+// of the N replicas.
 bool staged_fits(int N, bool grad_bf16);
+bool hsdp_staged_fits(int N, int R, bool grad_bf16, int64_t copy);
+bool norm_staged_fits(int N, bool grad_bf16);
 
-// Fused reduce-scatter + AdamW + cast over one segment range of either alignment
-// class; wait_ns bounds every mbarrier wait.
+// Partials k_rs_norm_staged writes for a launch over n_tiles tiles (one per
+// consumer warp of each CTA).
+int norm_staged_partials(int64_t n_tiles);
+
+// Each launcher covers one segment range of either alignment class; wait_ns
+// bounds every mbarrier wait.
 cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
                                    const GradPtrs& gp, int N, float* master, float* m, float* v, uint16_t* param,
                                    float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st);
+
+// HSDP: replicas gp.p[rho*N + q]; state copy rho at element offset rho * copy; rf = R.
+cudaError_t launch_hsdp_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
+                                     const GradPtrs& gp, int N, int R, int64_t copy, float* master, float* m,
+                                     float* v, uint16_t* param, const AdamScal& sc, float rf, uint64_t wait_ns,
+                                     cudaStream_t st);
+
+// Clip pass 1: the fp32 mean into gout and the sums of squares into part[0 .. *n_part).
+cudaError_t launch_rs_norm_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
+                                  const GradPtrs& gp, int N, float* gout, double* part, int* n_part, uint64_t wait_ns,
+                                  cudaStream_t st);
+
+// Accumulation over the logical full-layout ranges (segs: the "fullr" list): for
+// each replica q, acc[q] = micro[q] (first) or acc[q] + micro[q].  acc and micro are
+// host arrays of N device pointers.
+cudaError_t launch_accumulate_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, int N, float* const* acc,
+                                     const void* const* micro, bool micro_bf16, bool first, uint64_t wait_ns,
+                                     cudaStream_t st);
 
 // All-gather (shard -> full, bitwise) of a segment range of the aligned class.
 cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16, const void* src,

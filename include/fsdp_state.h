@@ -323,19 +323,30 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
                                void* const* param_replicas, int32_t param_dtype,
                                const fsdp_adamw_hparams* hp, int64_t step, fsdp_stream_t stream);
 
-/* Kernel choice of fsdp_reduce_scatter_adamw (process-wide; the pages have no
- * counterpart, the result is the same either way, bit for bit):
- *   FSDP_RS_AUTO    the staged kernel when at least two of its pipeline stages fit
- *                   in one CTA's shared memory (a stage holds 2048 elements of the
- *                   three fp32 state arrays and of all N gradient replicas: up to
- *                   N = 16 with bf16 gradients, N = 8 with fp32), else the direct
- *                   kernels.  The default.
+/* Kernel choice of the calls that reduce over gradient replicas (process-wide;
+ * the pages have no counterpart, the result is the same either way, bit for bit,
+ * except the clip norm's last bits, see below): fsdp_reduce_scatter_adamw,
+ * pass 1 of fsdp_reduce_scatter_clip_adamw, fsdp_hsdp_reduce_scatter_adamw and
+ * fsdp_accumulate_grads.
+ *   FSDP_RS_AUTO    the staged kernel where at least two of its pipeline stages fit
+ *                   in one CTA's shared memory, else the direct kernels; the clip
+ *                   pass keeps the direct kernel (measured as fast or faster).  A stage
+ *                   holds 2048 elements of each array the call reads: for
+ *                   fsdp_reduce_scatter_adamw the three fp32 state arrays and the N
+ *                   gradient replicas (fits up to N = 16 with bf16 gradients, N = 8
+ *                   with fp32); for HSDP 3R state arrays and R*N replicas (R <= 3,
+ *                   and N*stride a multiple of 4); for the clip pass the N replicas;
+ *                   for accumulation one micro-batch replica and its accumulator
+ *                   (always fits).  The default.
  *   FSDP_RS_DIRECT  the direct kernels: 16-byte loads straight into registers, one
  *                   launch per alignment class.
- *   FSDP_RS_STAGED  the staged kernel: the bulk-copy engine (cp.async.bulk) moves
- *                   each tile's state and gradient slices into shared memory, an
- *                   mbarrier per stage counts the bytes, one launch for both
- *                   alignment classes.  A call it does not fit returns FSDP_EINVAL.
+ *   FSDP_RS_STAGED  the staged kernels: the bulk-copy engine (cp.async.bulk) moves
+ *                   each tile of every input array into shared memory, an mbarrier
+ *                   per stage counts the bytes, one launch for both alignment
+ *                   classes.  A call whose staged kernel does not fit returns
+ *                   FSDP_EINVAL.
+ * The clip norm is a double sum whose grouping differs between the two (one
+ * partial per CTA or per warp); both are deterministic run to run.
  * Returns the previous choice, or FSDP_EINVAL for an unknown one.  Not ordered
  * with calls in flight on other threads. */
 typedef enum { FSDP_RS_AUTO = 0, FSDP_RS_DIRECT = 1, FSDP_RS_STAGED = 2 } fsdp_rs_kernel;

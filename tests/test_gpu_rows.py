@@ -1,5 +1,9 @@
 """The rows beyond the core step on the GPU, against the oracle (GPU):
-sharded clip_grad_norm_, gradient accumulation without sync, HSDP, ZeRO-1."""
+sharded clip_grad_norm_, gradient accumulation without sync, HSDP, ZeRO-1.
+
+Every test runs three times: with the default kernel choice (the bulk-copy
+staged kernels where they fit and are preferred), with the direct kernels forced
+and with the staged kernels forced (an HSDP case they do not hold is skipped)."""
 import numpy as np
 import pytest
 import torch
@@ -12,6 +16,13 @@ import parity_util as pu
 
 pytestmark = pytest.mark.gpu
 HP = synth.HP
+
+
+@pytest.fixture(autouse=True, params=["auto", "direct", "staged"])
+def rs_kind(request):
+    prev = fs.fsdp_set_rs_kernel(request.param)
+    yield request.param
+    fs.fsdp_set_rs_kernel(prev)
 
 
 def W(shapes, units, N, mode, dtype=torch.bfloat16, name="rows"):
@@ -120,8 +131,11 @@ def test_accumulate_then_step_vs_oracle(oracle_lib, w, micro_dtype):
 @pytest.mark.parametrize("w,R", [(W([(37, 5), (3,), (11, 13)], [0, 1, 1], 3, synth.FLAT), 2),
                                  (W([(130, 64), (7,), (9, 3)], [0, 0, 0], 4, synth.DIM0), 2),
                                  (W([(1 << 22,)], [0], 4, synth.FLAT), 4),
-                                 (W([(64, 32), (64,)], [0, 0], 2, synth.FLAT, torch.float32), 3)])
-def test_hsdp_vs_oracle(oracle_lib, w, R):
+                                 (W([(64, 32), (64,)], [0, 0], 2, synth.FLAT, torch.float32), 3),
+                                 (W([((1 << 20) + 1,)], [0], 8, synth.FLAT), 2),
+                                 (W([(333, 17), (5,), (64, 64)], [0, 0, 1], 2, synth.FLAT), 3),
+                                 (W([(300, 40), (9,)], [0, 0], 4, synth.FLAT, torch.float32), 2)])
+def test_hsdp_vs_oracle(oracle_lib, rs_kind, w, R):
     L = fs.Layout(w.shapes, w.unit_ids, w.N, w.mode)
     sh = oracle.Shapes(w.shapes, w.unit_ids)
     O = pu.oracle_offsets(w)
@@ -142,7 +156,12 @@ def test_hsdp_vs_oracle(oracle_lib, w, R):
     rm, rv = np.zeros_like(om), np.zeros_like(om)
     for t in range(1, 4):
         grads = [synth.grad_replica(w, F, t, rho * N + q) for rho in range(R) for q in range(N)]
-        fs.fsdp_hsdp_reduce_scatter_adamw(L, 0, L.n_units, R, grads, master, m, v, param, w.hp, t)
+        try:
+            fs.fsdp_hsdp_reduce_scatter_adamw(L, 0, L.n_units, R, grads, master, m, v, param, w.hp, t)
+        except fs.FsdpError as e:
+            if rs_kind == "staged" and e.status == -1:
+                pytest.skip("the staged HSDP kernel does not hold this case")
+            raise
         oracle.hsdp_adamw(sh, N, w.mode, R, pu.grads_np(grads), stride, om, rm, rv, param=op, hp=w.hp, step=t)
         torch.cuda.synchronize()
         pu.assert_f32_close(pu.f32(master).reshape(-1), om, f"master step {t}")

@@ -32,7 +32,7 @@ def staged_fits(N: int, grad_bytes: int) -> bool:
     # a stage: 2048 elements of master/exp_avg/exp_avg_sq (fp32) + of N gradient replicas (+16 B each)
     optin = torch.cuda.get_device_properties(0).shared_memory_per_block_optin
     stage = 3 * 8192 + N * (2048 * grad_bytes + 16)
-    return (optin - 128) // stage >= 2
+    return (optin - 1024) // stage >= 2
 
 
 def W(shapes, units, N, mode, dtype, steps=2):
@@ -117,6 +117,16 @@ def test_staged_refuses_what_does_not_fit(rs_kernel):
         assert e.value.status == -1
     with pytest.raises(fs.FsdpError):
         fs.fsdp_set_rs_kernel(7)
+    # HSDP with 4 replica groups: more state copies than the staged kernel holds
+    w = W([(4096,)], [0], 4, synth.FLAT, torch.bfloat16)
+    L = fs.Layout(w.shapes, w.unit_ids, w.N, w.mode)
+    R, stride = 4, L.stride
+    master = torch.zeros(R, w.N, stride, dtype=torch.float32, device="cuda")
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    grads = [torch.zeros(L.info["full_numel"], dtype=torch.bfloat16, device="cuda") for _ in range(R * w.N)]
+    with pytest.raises(fs.FsdpError) as e:
+        fs.fsdp_hsdp_reduce_scatter_adamw(L, 0, 1, R, grads, master, m, v, None, w.hp, 1)
+    assert e.value.status == -1
 
 
 def test_bounded_wait_gives_up_and_context_survives(oracle_lib, rs_kernel):
