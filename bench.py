@@ -276,32 +276,29 @@ def run_ours(args, w, rank, world, dist):
     rs_ms = [a.elapsed_time(b) for a, b in evs]
     ms_max = aggregate_max(ms, world, dist)
 
-    # e2e through the public API with host buffers (pinned), copies inside every step
+    # e2e through the public API with host buffers (pinned): every step copies its N
+    # gradient replicas host -> device and its updated parameter shards back
+    # (HostFeed overlaps those copies with the neighbouring steps' compute)
     host_grads = [g.cpu().pin_memory() for g in grads]
     out_host = torch.empty(st.param_shards.shape, dtype=st.param_shards.dtype).pin_memory()
     h2d = sum(g.numel() * g.element_size() for g in host_grads)
     d2h = out_host.numel() * out_host.element_size()
-
-    def e2e_step():
-        for hg, dg in zip(host_grads, grads):
-            dg.copy_(hg, non_blocking=True)
-        for _ in range(n_unshard):
-            st.unshard()
-        st.reduce_scatter_adamw(grads, w.hp)
-        out_host.copy_(st.param_shards, non_blocking=True)
-
+    feed = fs.HostFeed(st, w.grad_dtype, stream=stream)
     for _ in range(max(args.warmup, 1)):
-        e2e_step()
+        feed.step(host_grads, out_host, w.hp, args.strategy)
+    feed.finish()
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    feed.begin()
     for _ in range(args.steps):
-        e2e_step()
+        feed.step(host_grads, out_host, w.hp, args.strategy)
+    feed.finish()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = aggregate_max(e0.elapsed_time(e1), world, dist)
-
+    del feed
     clocks = parse_clocks(clk.out)
     peak, peak_kind = load_peaks()
     rs_avg = statistics.mean(rs_ms)

@@ -379,3 +379,4 @@ def fsdp_error_string(status: int) -> str:
 
 
 from .state import ShardedState  # noqa: E402  (harness over the calls above)
+from .hostfeed import HostFeed  # noqa: E402  (host-fed steps over ShardedState)
