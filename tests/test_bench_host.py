@@ -75,3 +75,11 @@ def test_aggregate_max_two_gloo_ranks():
     got = sorted(q.get() for _ in range(2))
     assert got == [(0, 7.25), (1, 7.25)]
     assert bench.aggregate_max(5.0, 1, None) == 5.0
+
+
+def test_launch_stats():
+    import bench
+    s = bench.launch_stats([1.0, 1.0, 1.0, 1.0])
+    assert s["median_ms"] == 1.0 and s["p95_ms"] == 1.0 and s["cv"] == 0.0 and not s["cv_flag"]
+    s = bench.launch_stats([1.0, 2.0, 3.0, 4.0, 100.0])
+    assert s["median_ms"] == 3.0 and s["p95_ms"] == 100.0 and s["cv_flag"] and s["n"] == 5
