@@ -192,26 +192,33 @@ template <typename GT>
 __host__ __device__ constexpr int grank_bytes() { return int(kTileElems * sizeof(GT)) + 16; }
 
 // ----------------------------------------------------------------------------
-// The pipeline.  Pol supplies, for item i of the launch:
-//   geom(i, cursor)            its geometry (producer side, once per item), resolved
+// The pipeline.  A launch covers n_units units (tiles); CTA b takes units b, b + G,
+// b + 2G, ... and, when Pol::groups() = NG > 1, every unit as NG consecutive items
+// (group 0 .. NG-1), so that a unit's groups meet the same consumer threads in order
+// and a per-thread Pol::Carry can hold partial results from one group to the next.
+// Pol supplies, for unit u and group k:
+//   geom(u, k, cursor)         the item's geometry (producer side, once per item), resolved
 //                              before the producer waits for a free stage when
 //                              Pol::kGeomFirst, else after (measured on GB300: the
 //                              fused step gains 1-3 % from the first order, HSDP and
 //                              accumulation lose 3-4 % with it)
 //   bytes(g)                   the bytes its copies bring in
 //   issue(g, stage, bar, lane) its copies (all producer lanes call it)
-//   consume(g, stage, tid, release)  the consumers' work; release() (all lanes of
-//                              each consumer warp call it once) frees the stage;
+//   consume(g, stage, tid, carry, release)  the consumers' work; release() (all lanes
+//                              of each consumer warp call it once) frees the stage;
 //                              returns the thread's contribution to a sum
 //   finish(tid, sum)           after the consumer's last item, with the thread's sum
 // ----------------------------------------------------------------------------
+struct NoCarry {};
+
 template <class Pol>
-__device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
+__device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, int S, int stage_bytes, uint64_t wait_ns) {
     extern __shared__ __align__(128) unsigned char smem[];
     static_assert(16 * kMaxStages + kMaxStages * sizeof(TileGeom) <= kFrontBytes, "front region");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t G = gridDim.x;
-    const int64_t n_mine = blockIdx.x < n_items ? (n_items - blockIdx.x + G - 1) / G : 0;
+    const int NG = pol.groups();
+    const int64_t n_mine = blockIdx.x < n_units ? (n_units - blockIdx.x + G - 1) / G * NG : 0;
     const uint32_t full0 = smem_addr(smem), empty0 = full0 + 8 * kMaxStages;
     TileGeom* geo = reinterpret_cast<TileGeom*>(smem + 16 * kMaxStages);
     unsigned char* stage0 = smem + kFrontBytes;
@@ -235,13 +242,13 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_items, in
             // the item's geometry (segment-table reads) before or after the wait for a
             // free stage: Pol::kGeomFirst, chosen per use by measurement
             TileGeom g;
-            if (Pol::kGeomFirst) g = pol.geom(blockIdx.x + j * G, cursor);
+            if (Pol::kGeomFirst) g = pol.geom(blockIdx.x + (j / NG) * G, int(j % NG), cursor);
             if (use > 0 &&
                 !__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * st, uint32_t((use - 1) & 1), wait_ns))) {
                 if (lane == 0) atomicOr(&g_wait_error, 1u);
                 break;
             }
-            if (!Pol::kGeomFirst) g = pol.geom(blockIdx.x + j * G, cursor);
+            if (!Pol::kGeomFirst) g = pol.geom(blockIdx.x + (j / NG) * G, int(j % NG), cursor);
             const uint32_t bar = full0 + 8 * st;
             if (lane == 0) {
                 geo[st] = g;                                  // released by the arrive
@@ -260,6 +267,7 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_items, in
 
     // ---- consumer warps ----
     double sum = 0.0;
+    typename Pol::Carry carry{};
     for (int64_t j = 0; j < n_mine; ++j) {
         const int st = int(j % S);
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * st, uint32_t((j / S) & 1), wait_ns))) {
@@ -268,7 +276,7 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_items, in
         }
         const TileGeom g = geo[st];
         const uint32_t empty = empty0 + 8 * st;
-        sum += pol.consume(g, stage0 + int64_t(st) * stage_bytes, tid, [&] {
+        sum += pol.consume(g, stage0 + int64_t(st) * stage_bytes, tid, carry, [&] {
             __syncwarp();
             if (lane == 0) mbar_arrive(empty);
         });
@@ -277,69 +285,92 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_items, in
 }
 
 // ---- fused reduce-scatter + AdamW + cast ------------------------------------------
+// A tile's N replicas come in NG groups of Q (the last may be shorter); the partial
+// sums carry over in registers from group to group in rank order, and the last
+// group also stages the three state slices and does the update.  NG = 1 unless N
+// replicas and the state do not fit two stages.
+struct Sum4 {
+    float a0, a1, a2, a3;
+};
+
 template <typename GT, bool PARAM, bool GOUT>
 struct RsAdamw {
     static constexpr bool kGeomFirst = true;
     const Seg* segs;
     int64_t tile_base;
     GradPtrs gp;
-    int N;
+    int N, Q, NG;
     float *master, *exp_avg, *exp_avg_sq;
     uint16_t* param;
     float* gout;
     AdamScal sc;
 
-    __device__ TileGeom geom(int64_t i, int& cur) const {
-        const int64_t gt = tile_base + i;
+    using Carry = Sum4;
+    __device__ int groups() const { return NG; }
+    __device__ int q0(const TileGeom& g) const { return g.q * Q; }
+    __device__ int nq(const TileGeom& g) const { return (N - g.q * Q) < Q ? (N - g.q * Q) : Q; }
+    __device__ bool last(const TileGeom& g) const { return g.q == NG - 1; }
+    __device__ TileGeom geom(int64_t u, int k, int& cur) const {
+        const int64_t gt = tile_base + u;
         cur = advance_seg(segs, cur, gt);
-        return tile_geom<GT>(segs[cur], gt);
+        TileGeom g = tile_geom<GT>(segs[cur], gt);
+        g.q = k;
+        return g;
     }
     __device__ uint32_t bytes(const TileGeom& g) const {
-        const uint32_t sb = g.bs > g.as ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t sb = g.bs > g.as && last(g) ? uint32_t(g.bs - g.as) * 4u : 0u;
         const uint32_t gb = g.bg > g.ag ? uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
-        return 3u * sb + uint32_t(N) * gb;
+        return 3u * sb + uint32_t(nq(g)) * gb;
     }
     __device__ void issue(const TileGeom& g, uint32_t sbase, uint32_t bar, int lane) const {
-        const uint32_t sb = g.bs > g.as ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t sb = g.bs > g.as && last(g) ? uint32_t(g.bs - g.as) * 4u : 0u;
         const uint32_t gb = g.bg > g.ag ? uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
-        for (int k = lane; k < N + 3; k += 32) {
+        const int k0 = q0(g), n = nq(g);
+        for (int k = lane; k < n + 3; k += 32) {
             if (k < 3) {
                 const float* arr = k == 0 ? master : (k == 1 ? exp_avg : exp_avg_sq);
                 if (sb) bulk_g2s(sbase + k * kStateBytes + uint32_t(g.as - g.t0) * 4u, arr + g.as, sb, bar);
             } else if (gb) {
                 const int q = k - 3;
                 bulk_g2s(sbase + 3 * kStateBytes + q * grank_bytes<GT>() + uint32_t(g.ag - g.gbase) * uint32_t(sizeof(GT)),
-                         static_cast<const GT*>(gp.p[q]) + g.ag, gb, bar);
+                         static_cast<const GT*>(gp.p[k0 + q]) + g.ag, gb, bar);
             }
         }
     }
     template <class Release>
-    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Release release) const {
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry& carry, Release release) const {
         const int c = tid * 4;
         const int64_t x = g.t0 + c, f = x + g.delta;
         const bool live = x + 4 > g.s0 && x < g.s1;
         const bool fast = x >= g.s0 && x + 4 <= g.s1 && f >= g.ag && f + 4 <= g.bg;
+        const bool fin = last(g);
         float4 pv, mv, vv;
-        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+        if (g.q == 0) carry = Sum4{0.0f, 0.0f, 0.0f, 0.0f};
         if (fast) {
-            pv = lds4(sb + 0 * kStateBytes + c * 4);
-            mv = lds4(sb + 1 * kStateBytes + c * 4);
-            vv = lds4(sb + 2 * kStateBytes + c * 4);
-            const int o = int(f - g.gbase);
+            if (fin) {
+                pv = lds4(sb + 0 * kStateBytes + c * 4);
+                mv = lds4(sb + 1 * kStateBytes + c * 4);
+                vv = lds4(sb + 2 * kStateBytes + c * 4);
+            }
+            const int o = int(f - g.gbase), n = nq(g);
             const unsigned char* gs = sb + 3 * kStateBytes;
+            float a0 = carry.a0, a1 = carry.a1, a2 = carry.a2, a3 = carry.a3;
 #pragma unroll 4
-            for (int q = 0; q < N; ++q) {            // fixed rank order
+            for (int q = 0; q < n; ++q) {            // fixed rank order, continued from the last group
                 const float4 x4 = grad4<GT>(gs + q * grank_bytes<GT>(), o);
                 a0 = __fadd_rn(a0, x4.x); a1 = __fadd_rn(a1, x4.y);
                 a2 = __fadd_rn(a2, x4.z); a3 = __fadd_rn(a3, x4.w);
             }
+            carry = Sum4{a0, a1, a2, a3};
         }
         release();
+        if (!fin) return 0.0;
         if (fast) {
             float p[4] = {pv.x, pv.y, pv.z, pv.w};
             float m[4] = {mv.x, mv.y, mv.z, mv.w};
             float v[4] = {vv.x, vv.y, vv.z, vv.w};
-            float gg[4] = {__fdiv_rn(a0, sc.nf), __fdiv_rn(a1, sc.nf), __fdiv_rn(a2, sc.nf), __fdiv_rn(a3, sc.nf)};
+            float gg[4] = {__fdiv_rn(carry.a0, sc.nf), __fdiv_rn(carry.a1, sc.nf), __fdiv_rn(carry.a2, sc.nf),
+                           __fdiv_rn(carry.a3, sc.nf)};
 #pragma unroll
             for (int k = 0; k < 4; ++k) adamw1(sc, gg[k], p[k], m[k], v[k]);
             st4(master + x, make_float4(p[0], p[1], p[2], p[3]));
@@ -349,7 +380,7 @@ struct RsAdamw {
                 *reinterpret_cast<uint2*>(param + x) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
             if (GOUT) st4(gout + x, make_float4(gg[0], gg[1], gg[2], gg[3]));
         } else if (live) {
-            // segment edge: element by element from global memory
+            // segment edge: element by element from global memory, all N replicas at once
             const int64_t a = x > g.s0 ? x : g.s0;
             const int64_t b = (x + 4) < g.s1 ? (x + 4) : g.s1;
             for (int64_t e = a; e < b; ++e) {
@@ -383,8 +414,10 @@ struct HsdpAdamw {
     AdamScal sc;
     float rf;
 
-    __device__ TileGeom geom(int64_t i, int& cur) const {
-        const int64_t gt = tile_base + i;
+    using Carry = NoCarry;
+    __device__ int groups() const { return 1; }
+    __device__ TileGeom geom(int64_t u, int, int& cur) const {
+        const int64_t gt = tile_base + u;
         cur = advance_seg(segs, cur, gt);
         return tile_geom<GT>(segs[cur], gt);
     }
@@ -410,7 +443,7 @@ struct HsdpAdamw {
         }
     }
     template <class Release>
-    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Release release) const {
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry& carry, Release release) const {
         const int c = tid * 4;
         const int64_t x = g.t0 + c, f = x + g.delta;
         const bool live = x + 4 > g.s0 && x < g.s1;
@@ -493,8 +526,10 @@ struct RsNorm {
     float nf;
     double* part;
 
-    __device__ TileGeom geom(int64_t i, int& cur) const {
-        const int64_t gt = tile_base + i;
+    using Carry = NoCarry;
+    __device__ int groups() const { return 1; }
+    __device__ TileGeom geom(int64_t u, int, int& cur) const {
+        const int64_t gt = tile_base + u;
         cur = advance_seg(segs, cur, gt);
         return tile_geom<GT>(segs[cur], gt);
     }
@@ -509,7 +544,7 @@ struct RsNorm {
                      static_cast<const GT*>(gp.p[q]) + g.ag, gb, bar);
     }
     template <class Release>
-    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Release release) const {
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry& carry, Release release) const {
         const int c = tid * 4;
         const int64_t x = g.t0 + c, f = x + g.delta;
         const bool live = x + 4 > g.s0 && x < g.s1;
@@ -570,7 +605,9 @@ struct Accumulate {
 
     static constexpr int kMicroBytes = int(kTileElems * sizeof(MT));
     __device__ int nq(const TileGeom& g) const { return (N - g.q) < Q ? (N - g.q) : Q; }
-    __device__ TileGeom geom(int64_t i, int& cur) const {
+    using Carry = NoCarry;
+    __device__ int groups() const { return 1; }
+    __device__ TileGeom geom(int64_t i, int, int& cur) const {
         const int64_t gt = tile_base + i / NG;
         cur = advance_seg(segs, cur, gt);
         TileGeom g = tile_geom<MT>(segs[cur], gt);     // delta = 0: micro and acc share the index
@@ -597,7 +634,7 @@ struct Accumulate {
         }
     }
     template <class Release>
-    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Release release) const {
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry& carry, Release release) const {
         const int c = tid * 4;
         const int64_t x = g.t0 + c;
         const bool live = x + 4 > g.s0 && x < g.s1;
@@ -832,6 +869,15 @@ cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage
 }
 
 int rs_stage_bytes(int N, bool bf16) { return 3 * kStateBytes + N * (bf16 ? grank_bytes<uint16_t>() : grank_bytes<float>()); }
+
+// Replica groups of the fused step: one group when all N replicas and the state fit
+// two stages, else the fewest groups (of equal size, rounded up) that do.
+void rs_groups(int N, bool bf16, int dev, int* Q, int* NG) {
+    int ng = 1;
+    while (ng < N && stage_count(rs_stage_bytes((N + ng - 1) / ng, bf16), dev) < 2) ++ng;
+    *NG = ng;
+    *Q = (N + ng - 1) / ng;
+}
 int hsdp_stage_bytes(int N, int R, bool bf16) {
     return 3 * R * kStateBytes + R * N * (bf16 ? grank_bytes<uint16_t>() : grank_bytes<float>());
 }
@@ -846,7 +892,10 @@ bool fits(int stage_bytes) {
 
 }  // namespace
 
-bool staged_fits(int N, bool grad_bf16) { return fits(rs_stage_bytes(N, grad_bf16)); }
+bool staged_fits(int N, bool grad_bf16) {
+    // with replica groups, any N whose single-replica stage fits two stages
+    return N >= 1 && N <= kMaxRanks && fits(rs_stage_bytes(1, grad_bf16));
+}
 
 bool hsdp_staged_fits(int N, int R, bool grad_bf16, int64_t copy) {
     return R <= HsdpAdamw<float, false>::kMaxR && (copy & 3) == 0 && fits(hsdp_stage_bytes(N, R, grad_bf16));
@@ -865,11 +914,16 @@ int norm_staged_partials(int64_t n_tiles) {
 cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
                                    const GradPtrs& gp, int N, float* master, float* m, float* v, uint16_t* param,
                                    float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st) {
-    const int sb = rs_stage_bytes(N, grad_bf16);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int Q = N, NG = 1;
+    rs_groups(N, grad_bf16, dev, &Q, &NG);
+    const int sb = rs_stage_bytes(Q, grad_bf16);
     auto go = [&](auto tag_gt, auto tag_p, auto tag_g) {
         using GT = decltype(tag_gt);
         constexpr bool P = decltype(tag_p)::value, O = decltype(tag_g)::value;
-        RsAdamw<GT, P, O> pol{segs, tile_base, gp, N, master, m, v, param, gout, sc};
+        RsAdamw<GT, P, O> pol{segs, tile_base, gp, N, Q, NG, master, m, v, param, gout, sc};
         return launch_pipeline(k_rs_adamw_staged<GT, P, O>, pol, n_tiles, sb, wait_ns, st);
     };
     using T = std::true_type;

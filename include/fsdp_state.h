@@ -333,8 +333,9 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
  *                   pass keeps the direct kernel (measured as fast or faster).  A stage
  *                   holds 2048 elements of each array the call reads: for
  *                   fsdp_reduce_scatter_adamw the three fp32 state arrays and the N
- *                   gradient replicas (fits up to N = 16 with bf16 gradients, N = 8
- *                   with fp32); for HSDP 3R state arrays and R*N replicas (R <= 3,
+ *                   gradient replicas, the replicas in groups where all of them do
+ *                   not fit (bf16 N > 16, fp32 N > 8; always fits); for HSDP 3R
+ *                   state arrays and R*N replicas (R <= 3,
  *                   and N*stride a multiple of 4); for the clip pass the N replicas;
  *                   for accumulation one micro-batch replica and its accumulator
  *                   (always fits).  The default.

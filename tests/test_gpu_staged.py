@@ -2,7 +2,8 @@
 
 direct: 16-byte loads straight into registers, one launch per alignment class.
 staged: the bulk-copy engine stages each tile's state and gradient slices in
-shared memory (mbarrier pipeline), one launch for both classes.
+shared memory (mbarrier pipeline), one launch for both classes; beyond what two
+stages hold (bf16 N > 16, fp32 N > 8) the replicas come in groups.
 
 Each is compared with the oracle element by element on the same seeded inputs,
 and the two with each other bit for bit.  The bounded-wait exit of the staged
@@ -28,13 +29,6 @@ def rs_kernel():
     fs.fsdp_set_rs_kernel(prev)
 
 
-def staged_fits(N: int, grad_bytes: int) -> bool:
-    # a stage: 2048 elements of master/exp_avg/exp_avg_sq (fp32) + of N gradient replicas (+16 B each)
-    optin = torch.cuda.get_device_properties(0).shared_memory_per_block_optin
-    stage = 3 * 8192 + N * (2048 * grad_bytes + 16)
-    return (optin - 1024) // stage >= 2
-
-
 def W(shapes, units, N, mode, dtype, steps=2):
     return synth.Workload("staged_case", 9, list(shapes), list(units), N, mode, dtype, dtype, steps, 1e-3)
 
@@ -48,6 +42,9 @@ CASES = {
     "scalar": ([(), (2,), (1000,)], [0, 0, 0], 3, synth.FLAT),
     "n1": ([(4099,)], [0], 1, synth.FLAT),
     "n16": ([(2049, 3), (17,)], [0, 0], 16, synth.FLAT),
+    "n32": ([(5000, 3), (17,)], [0, 0], 32, synth.FLAT),         # replica groups
+    "n64": ([(2049, 7), (9,)], [0, 0], 64, synth.FLAT),
+    "n24_dim0": ([(700, 9), (33,), (50, 13)], [0, 0, 1], 24, synth.DIM0),
     "ragged": ([(1 << 16, 3)], [0], 7, synth.FLAT),
     "units": ([(300, 7), (5,), (64, 64), (33,)], [0, 1, 2, 2], 4, synth.FLAT),
 }
@@ -58,14 +55,13 @@ CASES = {
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_kernel_vs_oracle(oracle_lib, rs_kernel, kind, dtype, case):
     shapes, units, N, mode = CASES[case]
-    if kind == "staged" and not staged_fits(N, 2 if dtype == torch.bfloat16 else 4):
-        pytest.skip("staged kernel does not fit this N")
     rs_kernel(kind)
     pu.run_full_parity(W(shapes, units, N, mode, dtype))
 
 
 @pytest.mark.parametrize("kind", ["direct", "staged"])
-@pytest.mark.parametrize("P,N", [((1 << 20) + 1, 2), ((1 << 20) + 1, 8), (1 << 20, 16), ((1 << 20) + 3, 6)])
+@pytest.mark.parametrize("P,N", [((1 << 20) + 1, 2), ((1 << 20) + 1, 8), (1 << 20, 16), ((1 << 20) + 3, 6),
+                                 ((1 << 20) + 1, 32)])
 def test_sweep_vs_oracle(oracle_lib, rs_kernel, kind, P, N):
     rs_kernel(kind)
     w = synth.sweep(P, N)
@@ -96,7 +92,9 @@ def _run(w, kind, rs_kernel, steps=3):
     synth.dim0_n6(vocab=3200, hidden=512, ffn=1376, N=6),                # many misaligned rank views
     W([(1 << 18, 3), (7,), (999, 5)], [0, 1, 1], 8, synth.FLAT, torch.float32),
     synth.sweep((1 << 22) + 1, 4),
-], ids=["dim0_n6_small", "flat_f32_n8", "sweep_4M_n4"])
+    synth.sweep((1 << 21) + 1, 32),                                      # two replica groups
+    W([(1 << 18, 3), (7,)], [0, 0], 32, synth.FLAT, torch.float32),      # three replica groups
+], ids=["dim0_n6_small", "flat_f32_n8", "sweep_4M_n4", "sweep_2M_n32", "flat_f32_n32"])
 def test_direct_and_staged_agree_bitwise(rs_kernel, w):
     a = _run(w, "direct", rs_kernel)
     b = _run(w, "staged", rs_kernel)
@@ -108,13 +106,6 @@ def test_direct_and_staged_agree_bitwise(rs_kernel, w):
 
 def test_staged_refuses_what_does_not_fit(rs_kernel):
     rs_kernel("staged")
-    for N, dtype in ((64, torch.bfloat16), (32, torch.float32)):
-        w = W([(4096,)], [0], N, synth.FLAT, dtype)
-        st = pu.make_state(w)
-        grads = [torch.zeros(st.F, dtype=dtype, device="cuda") for _ in range(N)]
-        with pytest.raises(fs.FsdpError) as e:
-            st.reduce_scatter_adamw(grads, w.hp)
-        assert e.value.status == -1
     with pytest.raises(fs.FsdpError):
         fs.fsdp_set_rs_kernel(7)
     # HSDP with 4 replica groups: more state copies than the staged kernel holds
