@@ -604,13 +604,23 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* L, int32_t ub, int32_t ue, con
     const Seg* base = nullptr;
     if ((rc = device_tables(L, &base))) return rc;
     const Range D = range_of(L->data, base, ub, ue);
+    const bool bf = grad_dtype == FSDP_BF16;
+    bool staged = false;
+    // the automatic choice keeps the direct kernel: on GB300 the staged one was 3-4 %
+    // slower here (the N-way broadcast stores from one CTA per SM)
+    if ((rc = choose_staged(fsdp::zero1_staged_fits(L->N, bf), false, &staged))) return rc;
     if (D.n_tiles <= 0) return FSDP_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (staged) {
+        const cudaError_t e = fsdp::launch_zero1_adamw_staged(D.segs, D.tile_base, D.n_tiles, bf, gp, param_replicas,
+                                                              L->N, L->stride, master, exp_avg, exp_avg_sq, sc,
+                                                              kWaitNs, st);
+        return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "k_zero1_adamw_staged launch");
+    }
     auto launch = [&](auto k) {
         k<<<grid_of(k, D.n_tiles), kThreads, 0, st>>>(D.segs, D.tile_base, D.n_tiles, gp, L->N, L->stride, master,
                                                       exp_avg, exp_avg_sq, pp, sc);
     };
-    const bool bf = grad_dtype == FSDP_BF16;
     if (master) bf ? launch(k_zero1_adamw<uint16_t, true>) : launch(k_zero1_adamw<float, true>);
     else bf ? launch(k_zero1_adamw<uint16_t, false>) : launch(k_zero1_adamw<float, false>);
     const cudaError_t e = cudaGetLastError();

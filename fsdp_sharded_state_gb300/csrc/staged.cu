@@ -1,7 +1,7 @@
 // staged.cu -- kernels whose inputs the bulk-copy (TMA) engine stages in shared
 // memory (sm_103a).
 //
-// One pipeline, four uses.  A persistent CTA per SM walks its work items (a tile of
+// One pipeline, five uses.  A persistent CTA per SM walks its work items (a tile of
 // 2048 elements of one segment, or of one segment and one replica); per item, a
 // producer warp issues one cp.async.bulk global -> shared per input array into a
 // free stage and writes the item's geometry into the stage header, and a "full"
@@ -23,6 +23,9 @@
 //                        of squares, one partial per consumer warp.
 //   k_accumulate_staged  fp32 accumulation of one micro-batch into each replica's
 //                        gradient buffer ("第18章 FSDP" §18.26, no_sync).
+//   k_zero1_adamw_staged the ZeRO-1 owner step ("NCCL ZeRO/FSDP state sharding",
+//                        "ZeRO-1"): mean over the N replicas, AdamW on the owner's
+//                        state, the result stored into all N parameter replicas.
 //
 // Arithmetic and its order are those of the direct kernels (kernels.cu, rows.cu),
 // bit for bit.  A gradient piece whose full-layout offset is not congruent to its
@@ -512,6 +515,128 @@ struct HsdpAdamw {
     __device__ void finish(int, double) const {}
 };
 
+// ---- ZeRO-1: owner update + broadcast ------------------------------------------------
+// Parameters are whole and replicated; each tensor's optimizer state lives in its
+// owner's row.  g = mean over the N replicas; the owner's AdamW on its state (p from
+// the fp32 master in the row when the replicas are bf16, else from the owner's own
+// fp32 replica); the updated parameter is stored into all N replicas.  Owner rows
+// keep every tensor congruent to its full offset mod 8 (delta = 0 mod 8).
+struct ParamReplicas {
+    void* p[kMaxRanks];
+};
+
+template <typename GT, bool MASTER>
+struct Zero1Adamw {
+    static constexpr bool kGeomFirst = true;
+    const Seg* segs;
+    int64_t tile_base;
+    GradPtrs gp;
+    ParamReplicas pr;
+    int N;
+    int64_t stride;
+    float *master, *exp_avg, *exp_avg_sq;
+    AdamScal sc;
+
+    using Carry = NoCarry;
+    __device__ int groups() const { return 1; }
+    __device__ TileGeom geom(int64_t u, int, int& cur) const {
+        const int64_t gt = tile_base + u;
+        cur = advance_seg(segs, cur, gt);
+        const Seg sg = segs[cur];
+        TileGeom g = tile_geom<GT>(sg, gt);
+        g.q = int32_t(sg.shard / stride);            // the owner
+        return g;
+    }
+    __device__ uint32_t bytes(const TileGeom& g) const {
+        const uint32_t sb = g.bs > g.as ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t gb = g.bg > g.ag ? uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
+        const uint32_t pb = g.bg > g.ag && (g.delta & 7) == 0 ? uint32_t(g.bg - g.ag) * 4u : 0u;   // owner's replica
+        return (MASTER ? 3u * sb : 2u * sb + pb) + uint32_t(N) * gb;
+    }
+    __device__ void issue(const TileGeom& g, uint32_t sbase, uint32_t bar, int lane) const {
+        const uint32_t sb = g.bs > g.as ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t gb = g.bg > g.ag ? uint32_t(g.bg - g.ag) * uint32_t(sizeof(GT)) : 0u;
+        for (int k = lane; k < N + 3; k += 32) {
+            if (k == 0) {
+                if (MASTER) {
+                    if (sb) bulk_g2s(sbase + uint32_t(g.as - g.t0) * 4u, master + g.as, sb, bar);
+                } else if (g.bg > g.ag && (g.delta & 7) == 0) {
+                    // delta = 0 mod 8: gbase = t0 + delta, the slice fills the slot from its start
+                    bulk_g2s(sbase + uint32_t(g.ag - g.gbase) * 4u, static_cast<const float*>(pr.p[g.q]) + g.ag,
+                             uint32_t(g.bg - g.ag) * 4u, bar);
+                }
+            } else if (k < 3) {
+                const float* arr = k == 1 ? exp_avg : exp_avg_sq;
+                if (sb) bulk_g2s(sbase + k * kStateBytes + uint32_t(g.as - g.t0) * 4u, arr + g.as, sb, bar);
+            } else if (gb) {
+                const int q = k - 3;
+                bulk_g2s(sbase + 3 * kStateBytes + q * grank_bytes<GT>() + uint32_t(g.ag - g.gbase) * uint32_t(sizeof(GT)),
+                         static_cast<const GT*>(gp.p[q]) + g.ag, gb, bar);
+            }
+        }
+    }
+    template <class Release>
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry&, Release release) const {
+        const int c = tid * 4;
+        const int64_t x = g.t0 + c, f = x + g.delta;
+        const bool live = x + 4 > g.s0 && x < g.s1;
+        // owner rows keep delta = 0 mod 8; anything else goes element by element
+        const bool fast = x >= g.s0 && x + 4 <= g.s1 && f >= g.ag && f + 4 <= g.bg && (MASTER || (g.delta & 7) == 0);
+        float4 pv, mv, vv;
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+        if (fast) {
+            // p at the shard offset (master) or at the full offset (the owner's replica; gbase = t0 + delta)
+            pv = lds4(sb + c * 4);
+            mv = lds4(sb + 1 * kStateBytes + c * 4);
+            vv = lds4(sb + 2 * kStateBytes + c * 4);
+            const int o = int(f - g.gbase);
+            const unsigned char* gs = sb + 3 * kStateBytes;
+#pragma unroll 4
+            for (int q = 0; q < N; ++q) {
+                const float4 x4 = grad4<GT>(gs + q * grank_bytes<GT>(), o);
+                a0 = __fadd_rn(a0, x4.x); a1 = __fadd_rn(a1, x4.y);
+                a2 = __fadd_rn(a2, x4.z); a3 = __fadd_rn(a3, x4.w);
+            }
+        }
+        release();
+        if (fast) {
+            float p[4] = {pv.x, pv.y, pv.z, pv.w};
+            float m[4] = {mv.x, mv.y, mv.z, mv.w};
+            float v[4] = {vv.x, vv.y, vv.z, vv.w};
+            const float gg[4] = {__fdiv_rn(a0, sc.nf), __fdiv_rn(a1, sc.nf), __fdiv_rn(a2, sc.nf), __fdiv_rn(a3, sc.nf)};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) adamw1(sc, gg[k], p[k], m[k], v[k]);
+            if (MASTER) st4(master + x, make_float4(p[0], p[1], p[2], p[3]));
+            st4(exp_avg + x, make_float4(m[0], m[1], m[2], m[3]));
+            st4(exp_avg_sq + x, make_float4(v[0], v[1], v[2], v[3]));
+            if (MASTER) {                             // bf16 replicas
+                const uint2 w = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
+                for (int q = 0; q < N; ++q) *reinterpret_cast<uint2*>(static_cast<uint16_t*>(pr.p[q]) + f) = w;
+            } else {                                  // fp32 replicas
+                const float4 w = make_float4(p[0], p[1], p[2], p[3]);
+                for (int q = 0; q < N; ++q) st4(static_cast<float*>(pr.p[q]) + f, w);
+            }
+        } else if (live) {
+            const int64_t a = x > g.s0 ? x : g.s0;
+            const int64_t b = (x + 4) < g.s1 ? (x + 4) : g.s1;
+            for (int64_t e = a; e < b; ++e) {
+                const int64_t fe = e + g.delta;
+                float pp = MASTER ? master[e] : static_cast<const float*>(pr.p[g.q])[fe];
+                float mm = exp_avg[e], vv2 = exp_avg_sq[e];
+                adamw1(sc, __fdiv_rn(reduce1<GT>(gp, N, fe), sc.nf), pp, mm, vv2);
+                if (MASTER) master[e] = pp;
+                exp_avg[e] = mm; exp_avg_sq[e] = vv2;
+                for (int q = 0; q < N; ++q) {
+                    if (MASTER) static_cast<uint16_t*>(pr.p[q])[fe] = to_bf16(pp);
+                    else static_cast<float*>(pr.p[q])[fe] = pp;
+                }
+            }
+        }
+        return 0.0;
+    }
+    __device__ void finish(int, double) const {}
+};
+
 // ---- clip pass 1: reduce-scatter into the fp32 shard + sums of squares ---------------
 // Each 4-element chunk's squares are summed in fp32 (fma), the chunks in double; one
 // partial per consumer warp (warp tree, lane order), written to part[CTA * 16 + warp].
@@ -685,6 +810,12 @@ k_rs_adamw_staged(RsAdamw<GT, PARAM, GOUT> pol, int64_t n_items, int S, int stag
 template <typename GT, bool PARAM>
 __global__ void __launch_bounds__(kStThreads + 32, 1)
 k_hsdp_adamw_staged(HsdpAdamw<GT, PARAM> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+}
+
+template <typename GT, bool MASTER>
+__global__ void __launch_bounds__(kStThreads + 32, 1)
+k_zero1_adamw_staged(Zero1Adamw<GT, MASTER> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
     run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
 }
 
@@ -902,6 +1033,33 @@ bool hsdp_staged_fits(int N, int R, bool grad_bf16, int64_t copy) {
 }
 
 bool norm_staged_fits(int N, bool grad_bf16) { return fits(norm_stage_bytes(N, grad_bf16)); }
+
+bool zero1_staged_fits(int N, bool grad_bf16) { return fits(rs_stage_bytes(N, grad_bf16)); }
+
+cudaError_t launch_zero1_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
+                                      const GradPtrs& gp, void* const* replicas, int N, int64_t stride,
+                                      float* master, float* m, float* v, const AdamScal& sc, uint64_t wait_ns,
+                                      cudaStream_t st) {
+    const int sb = rs_stage_bytes(N, grad_bf16);
+    auto go = [&](auto tag_gt, auto tag_m) {
+        using GT = decltype(tag_gt);
+        constexpr bool M = decltype(tag_m)::value;
+        Zero1Adamw<GT, M> pol{};
+        pol.segs = segs;
+        pol.tile_base = tile_base;
+        pol.gp = gp;
+        for (int q = 0; q < N; ++q) pol.pr.p[q] = replicas[q];
+        pol.N = N;
+        pol.stride = stride;
+        pol.master = master;
+        pol.exp_avg = m;
+        pol.exp_avg_sq = v;
+        pol.sc = sc;
+        return launch_pipeline(k_zero1_adamw_staged<GT, M>, pol, n_tiles, sb, wait_ns, st);
+    };
+    if (grad_bf16) return master ? go(uint16_t{}, std::true_type{}) : go(uint16_t{}, std::false_type{});
+    return master ? go(float{}, std::true_type{}) : go(float{}, std::false_type{});
+}
 
 int norm_staged_partials(int64_t n_tiles) {
     int dev = 0, sms = 0;

@@ -18,6 +18,9 @@ bool staged_fits(int N, bool grad_bf16);
 bool hsdp_staged_fits(int N, int R, bool grad_bf16, int64_t copy);
 bool norm_staged_fits(int N, bool grad_bf16);
 
+// ZeRO-1: the owner state (3 slices) and the N replicas in one stage.
+bool zero1_staged_fits(int N, bool grad_bf16);
+
 // Partials k_rs_norm_staged writes for a launch over n_tiles tiles (one per
 // consumer warp of each CTA).
 int norm_staged_partials(int64_t n_tiles);
@@ -45,6 +48,13 @@ cudaError_t launch_rs_norm_staged(const Seg* segs, int64_t tile_base, int64_t n_
 cudaError_t launch_accumulate_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, int N, float* const* acc,
                                      const void* const* micro, bool micro_bf16, bool first, uint64_t wait_ns,
                                      cudaStream_t st);
+
+// ZeRO-1 owner step + broadcast: master (bf16 replicas) or NULL (fp32 replicas: the
+// owner's replica is its parameter); replicas is a host array of N device pointers.
+cudaError_t launch_zero1_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
+                                      const GradPtrs& gp, void* const* replicas, int N, int64_t stride,
+                                      float* master, float* m, float* v, const AdamScal& sc, uint64_t wait_ns,
+                                      cudaStream_t st);
 
 // All-gather (shard -> full, bitwise) of a segment range of the aligned class.
 cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16, const void* src,

@@ -326,11 +326,12 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
 /* Kernel choice of the calls that reduce over gradient replicas (process-wide;
  * the pages have no counterpart, the result is the same either way, bit for bit,
  * except the clip norm's last bits, see below): fsdp_reduce_scatter_adamw,
- * pass 1 of fsdp_reduce_scatter_clip_adamw, fsdp_hsdp_reduce_scatter_adamw and
- * fsdp_accumulate_grads.
+ * pass 1 of fsdp_reduce_scatter_clip_adamw, fsdp_hsdp_reduce_scatter_adamw,
+ * fsdp_accumulate_grads and fsdp_zero1_adamw_broadcast.
  *   FSDP_RS_AUTO    the staged kernel where at least two of its pipeline stages fit
  *                   in one CTA's shared memory, else the direct kernels; the clip
- *                   pass keeps the direct kernel (measured as fast or faster).  A stage
+ *                   pass and ZeRO-1 keep the direct kernel (measured as fast or
+ *                   faster).  A stage
  *                   holds 2048 elements of each array the call reads: for
  *                   fsdp_reduce_scatter_adamw the three fp32 state arrays and the N
  *                   gradient replicas, the replicas in groups where all of them do
@@ -338,7 +339,8 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
  *                   state arrays and R*N replicas (R <= 3,
  *                   and N*stride a multiple of 4); for the clip pass the N replicas;
  *                   for accumulation one micro-batch replica and its accumulator
- *                   (always fits).  The default.
+ *                   (always fits); for ZeRO-1 the owner's state and the N replicas.
+ *                   The default.
  *   FSDP_RS_DIRECT  the direct kernels: 16-byte loads straight into registers, one
  *                   launch per alignment class.
  *   FSDP_RS_STAGED  the staged kernels: the bulk-copy engine (cp.async.bulk) moves

@@ -185,7 +185,8 @@ def oracle_zero1_rows(sh, N, owners):
     return off, max(fill)
 
 
-@pytest.mark.parametrize("shapes,N", [(ZSHAPES, 3), (ZSHAPES, 4), ([(1 << 20,), (1000, 17), (333,)], 2)])
+@pytest.mark.parametrize("shapes,N", [(ZSHAPES, 3), (ZSHAPES, 4), ([(1 << 20,), (1000, 17), (333,)], 2),
+                                     (ZSHAPES + [(4096, 300), (77, 5)], 8)])
 @pytest.mark.parametrize("bf16", [False, True])
 def test_zero1_vs_oracle(oracle_lib, shapes, N, bf16):
     L = fs.Layout(shapes, None, N, fs.FSDP_ZERO1)
