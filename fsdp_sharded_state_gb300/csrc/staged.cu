@@ -1,7 +1,7 @@
 // staged.cu -- kernels whose inputs the bulk-copy (TMA) engine stages in shared
 // memory (sm_103a).
 //
-// One pipeline, five uses.  A persistent CTA per SM walks its work items (a tile of
+// One pipeline, six uses.  A persistent CTA per SM walks its work items (a tile of
 // 2048 elements of one segment, or of one segment and one replica); per item, a
 // producer warp issues one cp.async.bulk global -> shared per input array into a
 // free stage and writes the item's geometry into the stage header, and a "full"
@@ -21,6 +21,8 @@
 //   k_rs_norm_staged     pass 1 of the sharded clip_grad_norm_ ("第18章 FSDP" §18.18):
 //                        the reduce-scatter into the fp32 gradient shard plus the sum
 //                        of squares, one partial per consumer warp.
+//   k_adamw_scaled_staged  pass 3 of it: the clip coefficient times the gradient
+//                        shard, then AdamW and the cast.
 //   k_accumulate_staged  fp32 accumulation of one micro-batch into each replica's
 //                        gradient buffer ("第18章 FSDP" §18.26, no_sync).
 //   k_zero1_adamw_staged the ZeRO-1 owner step ("NCCL ZeRO/FSDP state sharding",
@@ -637,6 +639,84 @@ struct Zero1Adamw {
     __device__ void finish(int, double) const {}
 };
 
+// ---- clip pass 3: AdamW on the clipped fp32 gradient shard ----------------------------
+// g = gshard * coef (one fp32 multiplication; coef from device memory, written by the
+// norm pass), written back as the clipped gradient, then the AdamW and cast of the
+// fused step.  The gradient shard shares the state's (shard) index: four slices of
+// one tile per stage, no shift.
+template <bool PARAM>
+struct ScaledAdamw {
+    static constexpr bool kGeomFirst = true;
+    const Seg* segs;
+    int64_t tile_base;
+    float* gshard;
+    const float* coef_p;
+    float *master, *exp_avg, *exp_avg_sq;
+    uint16_t* param;
+    AdamScal sc;
+
+    using Carry = NoCarry;
+    __device__ int groups() const { return 1; }
+    __device__ TileGeom geom(int64_t u, int, int& cur) const {
+        const int64_t gt = tile_base + u;
+        cur = advance_seg(segs, cur, gt);
+        TileGeom g = tile_geom<float>(segs[cur], gt);
+        g.q = __float_as_int(*coef_p);                 // the clip coefficient, once per item
+        return g;
+    }
+    __device__ uint32_t bytes(const TileGeom& g) const {
+        return g.bs > g.as ? 4u * uint32_t(g.bs - g.as) * 4u : 0u;
+    }
+    __device__ void issue(const TileGeom& g, uint32_t sbase, uint32_t bar, int lane) const {
+        if (g.bs <= g.as || lane >= 4) return;
+        const float* arr = lane == 0 ? master : (lane == 1 ? exp_avg : (lane == 2 ? exp_avg_sq : gshard));
+        bulk_g2s(sbase + lane * kStateBytes + uint32_t(g.as - g.t0) * 4u, arr + g.as, uint32_t(g.bs - g.as) * 4u, bar);
+    }
+    template <class Release>
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry&, Release release) const {
+        const int c = tid * 4;
+        const int64_t x = g.t0 + c;
+        const bool live = x + 4 > g.s0 && x < g.s1;
+        const bool fast = x >= g.s0 && x + 4 <= g.s1;
+        const float coef = __int_as_float(g.q);
+        float4 pv, mv, vv, gv;
+        if (fast) {
+            pv = lds4(sb + 0 * kStateBytes + c * 4);
+            mv = lds4(sb + 1 * kStateBytes + c * 4);
+            vv = lds4(sb + 2 * kStateBytes + c * 4);
+            gv = lds4(sb + 3 * kStateBytes + c * 4);
+        }
+        release();
+        if (fast) {
+            float p[4] = {pv.x, pv.y, pv.z, pv.w};
+            float m[4] = {mv.x, mv.y, mv.z, mv.w};
+            float v[4] = {vv.x, vv.y, vv.z, vv.w};
+            const float gg[4] = {__fmul_rn(gv.x, coef), __fmul_rn(gv.y, coef), __fmul_rn(gv.z, coef),
+                                 __fmul_rn(gv.w, coef)};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) adamw1(sc, gg[k], p[k], m[k], v[k]);
+            st4(gshard + x, make_float4(gg[0], gg[1], gg[2], gg[3]));
+            st4(master + x, make_float4(p[0], p[1], p[2], p[3]));
+            st4(exp_avg + x, make_float4(m[0], m[1], m[2], m[3]));
+            st4(exp_avg_sq + x, make_float4(v[0], v[1], v[2], v[3]));
+            if (PARAM)
+                *reinterpret_cast<uint2*>(param + x) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
+        } else if (live) {
+            const int64_t a = x > g.s0 ? x : g.s0;
+            const int64_t b = (x + 4) < g.s1 ? (x + 4) : g.s1;
+            for (int64_t e = a; e < b; ++e) {
+                const float gg = __fmul_rn(gshard[e], coef);
+                float pp = master[e], mm = exp_avg[e], vv2 = exp_avg_sq[e];
+                adamw1(sc, gg, pp, mm, vv2);
+                gshard[e] = gg; master[e] = pp; exp_avg[e] = mm; exp_avg_sq[e] = vv2;
+                if (PARAM) param[e] = to_bf16(pp);
+            }
+        }
+        return 0.0;
+    }
+    __device__ void finish(int, double) const {}
+};
+
 // ---- clip pass 1: reduce-scatter into the fp32 shard + sums of squares ---------------
 // Each 4-element chunk's squares are summed in fp32 (fma), the chunks in double; one
 // partial per consumer warp (warp tree, lane order), written to part[CTA * 16 + warp].
@@ -816,6 +896,12 @@ k_hsdp_adamw_staged(HsdpAdamw<GT, PARAM> pol, int64_t n_items, int S, int stage_
 template <typename GT, bool MASTER>
 __global__ void __launch_bounds__(kStThreads + 32, 1)
 k_zero1_adamw_staged(Zero1Adamw<GT, MASTER> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+}
+
+template <bool PARAM>
+__global__ void __launch_bounds__(kStThreads + 32, 1)
+k_adamw_scaled_staged(ScaledAdamw<PARAM> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
     run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
 }
 
@@ -1035,6 +1121,18 @@ bool hsdp_staged_fits(int N, int R, bool grad_bf16, int64_t copy) {
 bool norm_staged_fits(int N, bool grad_bf16) { return fits(norm_stage_bytes(N, grad_bf16)); }
 
 bool zero1_staged_fits(int N, bool grad_bf16) { return fits(rs_stage_bytes(N, grad_bf16)); }
+
+cudaError_t launch_adamw_scaled_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, float* gshard,
+                                       const float* coef, float* master, float* m, float* v, uint16_t* param,
+                                       const AdamScal& sc, uint64_t wait_ns, cudaStream_t st) {
+    const int sb = 4 * kStateBytes;
+    if (param) {
+        ScaledAdamw<true> pol{segs, tile_base, gshard, coef, master, m, v, param, sc};
+        return launch_pipeline(k_adamw_scaled_staged<true>, pol, n_tiles, sb, wait_ns, st);
+    }
+    ScaledAdamw<false> pol{segs, tile_base, gshard, coef, master, m, v, param, sc};
+    return launch_pipeline(k_adamw_scaled_staged<false>, pol, n_tiles, sb, wait_ns, st);
+}
 
 cudaError_t launch_zero1_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
                                       const GradPtrs& gp, void* const* replicas, int N, int64_t stride,

@@ -49,6 +49,11 @@ cudaError_t launch_accumulate_staged(const Seg* segs, int64_t tile_base, int64_t
                                      const void* const* micro, bool micro_bf16, bool first, uint64_t wait_ns,
                                      cudaStream_t st);
 
+// Clip pass 3: g = gshard * (*coef), written back, then AdamW + cast (always fits).
+cudaError_t launch_adamw_scaled_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, float* gshard,
+                                       const float* coef, float* master, float* m, float* v, uint16_t* param,
+                                       const AdamScal& sc, uint64_t wait_ns, cudaStream_t st);
+
 // ZeRO-1 owner step + broadcast: master (bf16 replicas) or NULL (fp32 replicas: the
 // owner's replica is its parameter); replicas is a host array of N device pointers.
 cudaError_t launch_zero1_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,

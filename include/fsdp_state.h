@@ -326,11 +326,12 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
 /* Kernel choice of the calls that reduce over gradient replicas (process-wide;
  * the pages have no counterpart, the result is the same either way, bit for bit,
  * except the clip norm's last bits, see below): fsdp_reduce_scatter_adamw,
- * pass 1 of fsdp_reduce_scatter_clip_adamw, fsdp_hsdp_reduce_scatter_adamw,
- * fsdp_accumulate_grads and fsdp_zero1_adamw_broadcast.
+ * passes 1 and 3 of fsdp_reduce_scatter_clip_adamw,
+ * fsdp_hsdp_reduce_scatter_adamw, fsdp_accumulate_grads and
+ * fsdp_zero1_adamw_broadcast.
  *   FSDP_RS_AUTO    the staged kernel where at least two of its pipeline stages fit
  *                   in one CTA's shared memory, else the direct kernels; the clip
- *                   pass and ZeRO-1 keep the direct kernel (measured as fast or
+ *                   passes and ZeRO-1 keep the direct kernels (measured as fast or
  *                   faster).  A stage
  *                   holds 2048 elements of each array the call reads: for
  *                   fsdp_reduce_scatter_adamw the three fp32 state arrays and the N
