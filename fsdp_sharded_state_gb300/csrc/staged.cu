@@ -45,6 +45,7 @@
 // FSDP_ETIMEOUT in a device word that fsdp_check_status reads and returns (a
 // producer first waits, bounded, for the copies it has in flight), after which the
 // CTA's other waits run out in turn.  Nothing else in these kernels waits.
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <type_traits>
@@ -1029,9 +1030,15 @@ __global__ void k_wait_selftest(uint64_t wait_ns) {
 }
 
 // ---- host side ------------------------------------------------------------------
+// Opt-in shared memory per block of each device, queried once.
+std::atomic<int> g_optin[64];
+
 int optin_smem(int dev) {
-    int v = 0;
-    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (dev < 0 || dev >= 64) return 0;
+    int v = g_optin[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    g_optin[dev].store(v, std::memory_order_relaxed);
     return v;
 }
 
