@@ -31,8 +31,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sharded-step params/sec and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
 PEAK_FALLBACK_GBS = 6800.0
-KERNEL_SRC = {k: [os.path.join(ROOT, "fsdp_sharded_state_gb300", "csrc", f) for f in (src, "device_ops.cuh", "common.cuh")]
-              for k, src in (("k_rs_adamw", "kernels.cu"), ("k_rs_adamw_staged", "staged.cu"))}
+KERNEL_SRC = {k: [os.path.join(ROOT, "fsdp_sharded_state_gb300", "csrc", f) for f in srcs + ("device_ops.cuh", "common.cuh")]
+              for k, srcs in (("k_rs_adamw", ("kernels.cu",)), ("k_rs_adamw_staged", ("staged.cu", "pipeline.cuh")))}
 
 
 # ---------------------------------------------------------------------------

@@ -113,11 +113,13 @@ __device__ __forceinline__ void rs_tile_f32_split(const Seg& sg, int64_t gt, con
 // SHIFT = false: every segment has its full-layout offset congruent to its shard
 // offset mod 8 (plain 16-byte vectors on both sides).  SHIFT = true: none has, and
 // the gradients go through the warp realignment.
-// Occupancy: the aligned instances keep 3 CTAs (24 warps) per SM -- at 2 the
-// DRAM queue drains between tiles and a launch loses 5-20 % of bandwidth -- so
-// they are held to 85 registers; the shifted ones need more and keep 2.
+// Occupancy: the aligned instances of the main configurations keep 3 CTAs (24
+// warps) per SM -- at 2 the DRAM queue drains between tiles and a launch loses
+// 5-20 % of bandwidth -- so they are held to 85 registers; the shifted ones, those
+// that also write the gradient shard and bf16 gradients into fp32 parameters need
+// more and keep 2 (no spills).
 template <typename GT, bool PARAM, bool GOUT, bool SHIFT>
-__global__ void __launch_bounds__(kThreads, SHIFT ? 2 : 3)
+__global__ void __launch_bounds__(kThreads, (SHIFT || GOUT || (!PARAM && sizeof(GT) == 2)) ? 2 : 3)
 k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N, int64_t F,
            float* __restrict__ master, float* __restrict__ exp_avg, float* __restrict__ exp_avg_sq,
            uint16_t* __restrict__ param, float* __restrict__ gout, AdamScal sc) {

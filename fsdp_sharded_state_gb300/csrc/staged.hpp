@@ -1,4 +1,5 @@
-// staged.hpp -- host-side launchers of the bulk-copy staged kernels (staged.cu).
+// staged.hpp -- host-side launchers of the bulk-copy kernels (staged.cu, allgather.cu,
+// staged_rows.cu).
 #pragma once
 
 #include <cstdint>
@@ -68,7 +69,10 @@ cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_ti
 // One kernel whose only wait cannot complete: exercises the bounded-wait exit.
 cudaError_t launch_wait_selftest(uint64_t wait_ns, cudaStream_t st);
 
-// Reads and clears the device's "a bounded wait gave up" word (synchronous).
+// Reads and clears the "a bounded wait gave up" words of every staged translation
+// unit on the current device (synchronous).
 cudaError_t take_wait_error(unsigned int* flag);
+cudaError_t take_wait_error_allgather(unsigned int* flag);   // allgather.cu only
+cudaError_t take_wait_error_rows(unsigned int* flag);        // staged_rows.cu only
 
 }  // namespace fsdp
