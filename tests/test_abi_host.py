@@ -217,6 +217,26 @@ def test_error_strings():
     assert fs.fsdp_error_string(12345) == "unknown fsdp_status"
 
 
+def test_kernel_choice_is_process_wide_and_checked():
+    # the choice is host state: no GPU is touched
+    prev = fs.fsdp_set_rs_kernel("direct")
+    try:
+        assert fs.fsdp_set_rs_kernel("staged") == fs.FSDP_RS_DIRECT
+        assert fs.fsdp_set_rs_kernel("auto") == fs.FSDP_RS_STAGED
+        for bad in (-1, 3, 99):
+            assert fs.lib().fsdp_set_rs_kernel(bad) == -1          # FSDP_EINVAL, choice unchanged
+        assert fs.fsdp_set_rs_kernel(fs.FSDP_RS_AUTO) == fs.FSDP_RS_AUTO
+        with pytest.raises(KeyError):
+            fs.fsdp_set_rs_kernel("fastest")
+    finally:
+        fs.fsdp_set_rs_kernel(prev)
+
+
+def test_wait_selftest_validates_its_limit():
+    for bad in (0, -5, 10_000_000_001):
+        assert fs.lib().fsdp_wait_selftest(bad, None) == -1
+
+
 @pytest.mark.parametrize("P", [(1 << 20) + 1, (1 << 24) + 3, (1 << 28) + 1, 4099, 1000003])
 @pytest.mark.parametrize("N", [2, 3, 6, 8, 32])
 def test_single_unit_flat_views_line_up(P, N):
