@@ -25,6 +25,7 @@
 #include <atomic>
 #include <map>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include "common.cuh"
@@ -101,6 +102,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+
+// Shared -> global bulk copy in the current bulk async-group (16-byte aligned both
+// sides, bytes a multiple of 16), the group commit, and the waits on the groups.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ int64_t floor_to(int64_t x, int64_t a) { return x & ~(a - 1); }   // a: power of 2
 __device__ __forceinline__ int64_t ceil_to(int64_t x, int64_t a) { return (x + a - 1) & ~(a - 1); }
@@ -188,29 +199,122 @@ __host__ __device__ constexpr int grank_bytes() { return int(kTileElems * sizeof
 //                              of each consumer warp call it once) frees the stage;
 //                              returns the thread's contribution to a sum
 //   finish(tid, sum)           after the consumer's last item, with the thread's sum
+// A policy with an output ring (Pol::kOutSlotBytes > 0) also gets a store warp: the
+// consumers of item j write its results into output slot j mod kOutSlots (after
+// out.acquire(), then out.publish(header)), and the store warp issues the policy's
+// bulk stores from that slot (store(header, slot, lane)) and frees it once they
+// have read it.  Both sides wait on their own full/empty mbarriers, bounded.
 // ----------------------------------------------------------------------------
 struct NoCarry {};
+
+constexpr int kOutSlots = 2;
+
+// What the store warp needs about an item's output slot: the element range [a, b)
+// to store and the element at slot offset 0.
+struct OutHdr {
+    int64_t a, b, base;
+    int64_t pad;
+};
+
+template <class P, class = void>
+struct OutSlotBytes {
+    static constexpr int value = 0;
+};
+template <class P>
+struct OutSlotBytes<P, std::void_t<decltype(P::kOutSlotBytes)>> {
+    static constexpr int value = P::kOutSlotBytes;
+};
+
+// Front region: stage barriers, stage geometry, output barriers, output headers.
+constexpr int kGeoOff = 16 * kMaxStages;
+constexpr int kOutBarOff = kGeoOff + kMaxStages * int(sizeof(TileGeom));
+constexpr int kOutHdrOff = kOutBarOff + 16 * kOutSlots;
+static_assert(kOutHdrOff + kOutSlots * int(sizeof(OutHdr)) <= kFrontBytes, "front region");
+
+// The consumers' side of the output ring for one item.
+struct OutRing {
+    uint32_t full0, empty0;
+    unsigned char* slot0;
+    OutHdr* hdr;
+    int slot_bytes, lane, warp;
+    int64_t j;
+    uint64_t wait_ns;
+    bool ok;
+    // Waits (all lanes of the warp) until the item's slot is free; nullptr if the wait gave up.
+    __device__ unsigned char* acquire() {
+        const int k = int(j % kOutSlots);
+        const int64_t use = j / kOutSlots;
+        if (use > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * k, uint32_t((use - 1) & 1), wait_ns))) {
+            ok = false;
+            return nullptr;
+        }
+        return slot0 + k * slot_bytes;
+    }
+    // Hands the slot to the store warp (all lanes of the warp, after their writes).
+    __device__ void publish(const OutHdr& h) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the writes, to the bulk-copy engine
+        __syncwarp();
+        const int k = int(j % kOutSlots);
+        if (lane == 0) {
+            if (warp == 0) hdr[k] = h;                                 // released by the arrive
+            mbar_arrive(full0 + 8 * k);
+        }
+    }
+};
 
 template <class Pol>
 __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, int S, int stage_bytes, uint64_t wait_ns) {
     extern __shared__ __align__(128) unsigned char smem[];
-    static_assert(16 * kMaxStages + kMaxStages * sizeof(TileGeom) <= kFrontBytes, "front region");
+    constexpr int kOut = OutSlotBytes<Pol>::value;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t G = gridDim.x;
     const int NG = pol.groups();
     const int64_t n_mine = blockIdx.x < n_units ? (n_units - blockIdx.x + G - 1) / G * NG : 0;
     const uint32_t full0 = smem_addr(smem), empty0 = full0 + 8 * kMaxStages;
-    TileGeom* geo = reinterpret_cast<TileGeom*>(smem + 16 * kMaxStages);
+    TileGeom* geo = reinterpret_cast<TileGeom*>(smem + kGeoOff);
+    const uint32_t ofull0 = full0 + kOutBarOff, oempty0 = ofull0 + 8 * kOutSlots;
+    OutHdr* ohdr = reinterpret_cast<OutHdr*>(smem + kOutHdrOff);
     unsigned char* stage0 = smem + kFrontBytes;
+    unsigned char* out0 = stage0 + int64_t(S) * stage_bytes;
 
     if (tid == 0) {
         for (int k = 0; k < S; ++k) {
             mbar_init(full0 + 8 * k, 1);                      // the producer's arrive (+ bytes)
             mbar_init(empty0 + 8 * k, kConsumerWarps);        // one arrive per consumer warp
         }
+        if (kOut > 0)
+            for (int k = 0; k < kOutSlots; ++k) {
+                mbar_init(ofull0 + 8 * k, kConsumerWarps);    // one arrive per consumer warp
+                mbar_init(oempty0 + 8 * k, 1);                // the store warp's arrive
+            }
         mbar_fence_init();
     }
     __syncthreads();
+
+    if constexpr (kOut > 0) {
+        if (warp == kConsumerWarps + 1) {
+            // ---- store warp: the bulk stores of item j from output slot j mod kOutSlots ----
+            for (int64_t j = 0; j < n_mine; ++j) {
+                const int k = int(j % kOutSlots);
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(ofull0 + 8 * k, uint32_t((j / kOutSlots) & 1), wait_ns))) {
+                    if (lane == 0) atomicOr(&g_wait_error, 1u);
+                    break;
+                }
+                const OutHdr h = ohdr[k];
+                if (lane == 0) {
+                    pol.store(h, smem_addr(out0 + k * kOut));
+                    bulk_commit();
+                    bulk_wait_read_all();                     // the slot may be rewritten
+                    mbar_arrive(oempty0 + 8 * k);
+                }
+                __syncwarp();
+            }
+            if (lane == 0) bulk_wait_all();                   // the stores are complete
+            __syncwarp();
+            return;
+        }
+    }
 
     if (warp == kConsumerWarps) {
         // ---- producer warp: item j of this CTA into stage j mod S ----
@@ -256,10 +360,20 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, in
         }
         const TileGeom g = geo[st];
         const uint32_t empty = empty0 + 8 * st;
-        sum += pol.consume(g, stage0 + int64_t(st) * stage_bytes, tid, carry, [&] {
+        auto release = [&] {
             __syncwarp();
             if (lane == 0) mbar_arrive(empty);
-        });
+        };
+        if constexpr (kOut > 0) {
+            OutRing out{ofull0, oempty0, out0, ohdr, kOut, lane, warp, j, wait_ns, true};
+            sum += pol.consume(g, stage0 + int64_t(st) * stage_bytes, tid, carry, release, out);
+            if (!out.ok) {
+                if (lane == 0) atomicOr(&g_wait_error, 1u);
+                return;
+            }
+        } else {
+            sum += pol.consume(g, stage0 + int64_t(st) * stage_bytes, tid, carry, release);
+        }
     }
     pol.finish(tid, sum);
 }
@@ -282,8 +396,8 @@ int optin_smem(int dev) {
 // opt-in shared memory; 0 if two do not fit.  Measured on GB300 (fused step): about
 // 50-100 KB in flight per SM streams best; 3-4 stages of 57 KB lost up to 10 % of
 // the bandwidth, fewer than 40 KB in flight lost 8 %.
-int stage_count(int stage_bytes, int dev) {
-    const int avail = optin_smem(dev) - kFrontBytes;
+int stage_count(int stage_bytes, int dev, int extra_bytes = 0) {
+    const int avail = optin_smem(dev) - kFrontBytes - extra_bytes;
     const int fit = avail > 0 ? avail / stage_bytes : 0;
     int want = kInFlightBytes / stage_bytes + 1;
     want = want < 2 ? 2 : (want > kMaxStages ? kMaxStages : want);
@@ -294,7 +408,12 @@ int stage_count(int stage_bytes, int dev) {
 std::mutex g_st_mu;
 std::map<std::pair<const void*, int>, std::pair<int, int>> g_st_cache;   // (kernel, dev) -> (SMs, smem set)
 
-// One CTA of 544 threads per SM (at most one per item).
+// Threads of a pipeline CTA: the consumers, the producer warp, and the store warp
+// of a policy with an output ring.
+template <class Pol>
+constexpr int pipeline_threads() { return kStThreads + 32 + (OutSlotBytes<Pol>::value > 0 ? 32 : 0); }
+
+// One CTA of 544 (576 with a store warp) threads per SM (at most one per item).
 template <typename K, typename Pol>
 cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage_bytes, uint64_t wait_ns,
                             cudaStream_t st, int* grid_out = nullptr) {
@@ -303,9 +422,10 @@ cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int S = stage_count(stage_bytes, dev);
+    constexpr int kOutBytes = kOutSlots * OutSlotBytes<Pol>::value;
+    const int S = stage_count(stage_bytes, dev, kOutBytes);
     if (S < 2) return cudaErrorInvalidValue;
-    const int smem = kFrontBytes + S * stage_bytes;
+    const int smem = kFrontBytes + S * stage_bytes + kOutBytes;
     const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
     int sms = 0, set = 0;
     {
@@ -322,17 +442,17 @@ cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage
         g_st_cache[key] = std::make_pair(sms, smem);
     }
     const int64_t blocks = n_items < sms ? n_items : (sms > 0 ? sms : 1);
-    kernel<<<int(blocks), kStThreads + 32, smem, st>>>(pol, n_items, S, stage_bytes, wait_ns);
+    kernel<<<int(blocks), pipeline_threads<Pol>(), smem, st>>>(pol, n_items, S, stage_bytes, wait_ns);
     if (grid_out) *grid_out = int(blocks);
     return cudaGetLastError();
 }
 
 int rs_stage_bytes(int N, bool bf16) { return 3 * kStateBytes + N * (bf16 ? grank_bytes<uint16_t>() : grank_bytes<float>()); }
 
-bool fits(int stage_bytes) {
+bool fits(int stage_bytes, int extra_bytes = 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    return stage_count(stage_bytes, dev) >= 2;
+    return stage_count(stage_bytes, dev, extra_bytes) >= 2;
 }
 
 // Reads and clears this translation unit's wait word (synchronous).

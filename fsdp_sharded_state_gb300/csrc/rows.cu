@@ -614,9 +614,10 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* L, int32_t ub, int32_t ue, con
     const Range D = range_of(L->data, base, ub, ue);
     const bool bf = grad_dtype == FSDP_BF16;
     bool staged = false;
-    // the automatic choice keeps the direct kernel: on GB300 the staged one was 3-4 %
-    // slower here (the N-way broadcast stores from one CTA per SM)
-    if ((rc = choose_staged(fsdp::zero1_staged_fits(L->N, bf), false, &staged))) return rc;
+    // the automatic choice takes the staged kernel (bulk-store broadcast) for bf16
+    // replicas only: measured on GB300, 4-block Llama with bf16 replicas 0.96 of the
+    // copy peak against 0.95 direct, 128 MiB fp32 replicas 0.90 against 0.94
+    if ((rc = choose_staged(fsdp::zero1_staged_fits(L->N, bf), param_dtype == FSDP_BF16, &staged))) return rc;
     if (D.n_tiles <= 0) return FSDP_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (staged) {

@@ -187,8 +187,8 @@ def oracle_zero1_rows(sh, N, owners):
 
 @pytest.mark.parametrize("shapes,N", [(ZSHAPES, 3), (ZSHAPES, 4), ([(1 << 20,), (1000, 17), (333,)], 2),
                                      (ZSHAPES + [(4096, 300), (77, 5)], 8)])
-@pytest.mark.parametrize("bf16", [False, True])
-def test_zero1_vs_oracle(oracle_lib, shapes, N, bf16):
+@pytest.mark.parametrize("bf16,grad_bf16", [(False, False), (True, True), (False, True), (True, False)])
+def test_zero1_vs_oracle(oracle_lib, shapes, N, bf16, grad_bf16):
     L = fs.Layout(shapes, None, N, fs.FSDP_ZERO1)
     sh = oracle.Shapes(shapes)
     owners = oracle.zero1_owners(sh, N)
@@ -198,6 +198,7 @@ def test_zero1_vs_oracle(oracle_lib, shapes, N, bf16):
         assert (d["full_off"] - (owners[t] * L.stride + d["shard_off"])) % 8 == 0     # congruent placement
     P = L.info["numel"]
     w = W(shapes, [0] * len(shapes), N, synth.DIM0, torch.bfloat16 if bf16 else torch.float32)
+    w.grad_dtype = torch.bfloat16 if grad_bf16 else torch.float32
     offs = [L.tensor(t)["full_off"] for t in range(len(shapes))]
     full = synth.full_params(w, P, offs)
     stride = L.stride
