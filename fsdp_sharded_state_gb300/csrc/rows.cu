@@ -614,10 +614,11 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* L, int32_t ub, int32_t ue, con
     const Range D = range_of(L->data, base, ub, ue);
     const bool bf = grad_dtype == FSDP_BF16;
     bool staged = false;
-    // the automatic choice takes the staged kernel (bulk-store broadcast) for bf16
-    // replicas only: measured on GB300, 4-block Llama with bf16 replicas 0.96 of the
-    // copy peak against 0.95 direct, 128 MiB fp32 replicas 0.90 against 0.94
-    if ((rc = choose_staged(fsdp::zero1_staged_fits(L->N, bf), param_dtype == FSDP_BF16, &staged))) return rc;
+    // the automatic choice keeps the direct kernel: measured on GB300, the staged one
+    // (bulk-store broadcast) ran the 4-block Llama at 0.93-0.96 of the copy peak from
+    // one box to the next against a steady 0.95 direct, and 128 MiB of fp32 replicas
+    // at 0.90 against 0.94
+    if ((rc = choose_staged(fsdp::zero1_staged_fits(L->N, bf), false, &staged))) return rc;
     if (D.n_tiles <= 0) return FSDP_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (staged) {

@@ -331,8 +331,8 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
  * fsdp_zero1_adamw_broadcast.
  *   FSDP_RS_AUTO    the staged kernel where at least two of its pipeline stages fit
  *                   in one CTA's shared memory, else the direct kernels; the clip
- *                   passes, and ZeRO-1 with fp32 replicas, keep the direct kernels
- *                   (measured as fast or faster).  A stage
+ *                   passes and ZeRO-1 keep the direct kernels (measured as fast or
+ *                   steadier).  A stage
  *                   holds 2048 elements of each array the call reads: for
  *                   fsdp_reduce_scatter_adamw the three fp32 state arrays and the N
  *                   gradient replicas, the replicas in groups where all of them do
