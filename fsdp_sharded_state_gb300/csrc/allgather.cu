@@ -19,13 +19,21 @@ namespace {
 // 16-byte aligned on both sides, so the bulk-copy engine can move them without a
 // thread touching the data: per tile, one cp.async.bulk global->shared and one
 // cp.async.bulk shared->global of its aligned interior.  Each CTA is one warp with
-// a ring of 4 tile buffers and 2 loads ahead; 4 CTAs per SM.  Measured on GB300
+// a small ring of tile buffers (Ring below); 4 CTAs per SM.  Measured on GB300
 // (bf16, 1-3 GB): as fast as a device copy of the same bytes; 1 or 3 loads ahead,
 // 3, 5 or 8 CTAs per SM, or deeper rings were 2-8 % slower, and one CTA per SM
 // with 8 loads ahead ran at 40 %.  Lane 0 issues the copies; the at most 7
 // elements at each end of a segment that the copies leave out are copied by the
 // warp's lanes with plain loads and stores.
-constexpr int kURing = 4, kUAhead = 2, kUCtasPerSm = 4;
+constexpr int kUCtasPerSm = 4;
+// Loads ahead and ring buffers per CTA: about 32 KB in flight per SM for both element
+// sizes (bf16 tiles are 4 KB: 2 ahead; fp32 tiles 8 KB: 1 ahead).  Measured on GB300:
+// fp32 128 MiB all-gather 44.2 us with 1 ahead against 46.5 us with 2.
+template <int ES>
+struct Ring {
+    static constexpr int ahead = ES == 4 ? 1 : 2;
+    static constexpr int size = ahead + 2;
+};
 
 template <int ES>
 __global__ void __launch_bounds__(32)
@@ -33,14 +41,14 @@ k_unshard_bulk(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
                unsigned char* dst, uint64_t wait_ns) {
     constexpr int64_t E = 16 / ES;              // elements per 16 bytes
     using W = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
-    __shared__ __align__(128) unsigned char buf[kURing][kTileElems * ES];
-    __shared__ __align__(8) uint64_t bars[kURing];
+    __shared__ __align__(128) unsigned char buf[Ring<ES>::size][kTileElems * ES];
+    __shared__ __align__(8) uint64_t bars[Ring<ES>::size];
     const int lane = threadIdx.x;
     const int64_t G = gridDim.x;
     const int64_t n_mine = blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + G - 1) / G : 0;
     const uint32_t bar0 = smem_addr(&bars[0]);
     if (lane == 0) {
-        for (int k = 0; k < kURing; ++k) mbar_init(bar0 + 8 * k, 1);
+        for (int k = 0; k < Ring<ES>::size; ++k) mbar_init(bar0 + 8 * k, 1);
         mbar_fence_init();
     }
     __syncwarp();
@@ -64,24 +72,24 @@ k_unshard_bulk(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
     auto load = [&](int64_t j) {
         const Piece p = piece(load_cur, j);
         if (lane == 0) {
-            const int k = int(j % kURing);
+            const int k = int(j % Ring<ES>::size);
             const uint32_t bytes = p.b > p.a ? uint32_t(p.b - p.a) * ES : 0u;
             mbar_arrive_tx(bar0 + 8 * k, bytes);
             if (bytes) bulk_g2s(smem_addr(&buf[k][(p.a - p.t0) * ES]), src + p.a * ES, bytes, bar0 + 8 * k);
         }
     };
-    for (int64_t j = 0; j < n_mine && j < kUAhead; ++j) load(j);
+    for (int64_t j = 0; j < n_mine && j < Ring<ES>::ahead; ++j) load(j);
     int64_t j = 0;
     bool ok = true;
     for (; j < n_mine; ++j) {
-        if (j + kUAhead < n_mine) {
+        if (j + Ring<ES>::ahead < n_mine) {
             // buffer (j + ahead) mod ring was last stored from by tile j + ahead - ring
-            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kURing - kUAhead - 1) : "memory");
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(Ring<ES>::size - Ring<ES>::ahead - 1) : "memory");
             __syncwarp();
-            load(j + kUAhead);
+            load(j + Ring<ES>::ahead);
         }
-        const int k = int(j % kURing);
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * k, uint32_t((j / kURing) & 1), wait_ns));
+        const int k = int(j % Ring<ES>::size);
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * k, uint32_t((j / Ring<ES>::size) & 1), wait_ns));
         if (!ok) break;
         const Piece p = piece(store_cur, j);
         if (lane == 0) {
@@ -104,8 +112,8 @@ k_unshard_bulk(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
     if (!ok && lane == 0) {
         atomicOr(&g_wait_error, 1u);
         // loads already issued must land before the shared memory goes away
-        for (int64_t q = j + 1; q < n_mine && q < j + kUAhead; ++q)
-            mbar_wait_bounded(bar0 + 8 * int(q % kURing), uint32_t((q / kURing) & 1), wait_ns);
+        for (int64_t q = j + 1; q < n_mine && q <= j + Ring<ES>::ahead; ++q)
+            mbar_wait_bounded(bar0 + 8 * int(q % Ring<ES>::size), uint32_t((q / Ring<ES>::size) & 1), wait_ns);
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     __syncwarp();
