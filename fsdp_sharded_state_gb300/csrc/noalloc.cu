@@ -8,7 +8,8 @@
 // allocator (cudaMalloc can synchronize the device and may fail under memory
 // pressure mid-step), and embedders that forbid hidden allocations in a library.
 // This variant instead stages the table in one fixed array that lives in the
-// library image: `g_noalloc_segs` below, FSDP_NOALLOC_MAX_SEGMENTS entries of 32
+// library image (it runs the same kernel as fsdp_reduce_scatter_adamw, staged or
+// direct, neither of which allocates): `g_noalloc_segs` below, FSDP_NOALLOC_MAX_SEGMENTS entries of 32
 // bytes (256 KiB), present on every GPU that loads the library until the process
 // exits.  The entry point calls no cudaMalloc, cudaFree or other allocating
 // routine.
@@ -19,8 +20,10 @@
 #include <cuda_runtime.h>
 
 #include "../../include/fsdp_state.h"
+#include "internal.hpp"
 #include "kernels.hpp"
 #include "layout.hpp"
+#include "staged.hpp"
 
 namespace {
 
@@ -112,12 +115,30 @@ extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t u
     fsdp::GradPtrs gp{};
     for (int32_t q = 0; q < L->N; ++q) gp.p[q] = grads[q];
 
+    // The same kernel choice as fsdp_reduce_scatter_adamw (neither kernel allocates).
+    const bool bf16 = grad_dtype == FSDP_BF16;
+    bool staged = false;
+    if ((rc = fsdp::detail::choose_staged(fsdp::staged_fits(L->N, bf16), true, &staged))) return rc;
+
     // Stream-ordered: the table is written before this call's kernels read it.
     // Nothing in the scratch needs to start at zero: every entry read is written first.
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     Seg* next = scratch;
-    for (int c = 0; c < 2; ++c) {
+    if (staged) {
+        // one launch over the combined data list (fewer entries than the two classes)
+        const int32_t sb = L->data.unit_begin[ub], se = L->data.unit_begin[ue];
+        const int64_t n = int64_t(se - sb) + 1;
+        e = cudaMemcpyAsync(next, L->data.segs.data() + sb, size_t(n) * sizeof(Seg), cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return FSDP_ECUDA;
+        const int64_t t0 = L->data.segs[sb].tile0, t1 = L->data.segs[se].tile0;
+        e = fsdp::launch_rs_adamw_staged(next, t0, t1 - t0, bf16, gp, L->N, master, exp_avg, exp_avg_sq,
+                                         static_cast<uint16_t*>(param_shards), grad_shard_out, sc,
+                                         fsdp::detail::kWaitNs, st);
+        if (e != cudaSuccess) return FSDP_ECUDA;
+        next += n;
+    }
+    for (int c = 0; c < 2 && !staged; ++c) {
         const int32_t sb = cls[c]->unit_begin[ub], se = cls[c]->unit_begin[ue];
         e = cudaMemcpyAsync(next, cls[c]->segs.data() + sb, size_t(n_cls[c]) * sizeof(Seg), cudaMemcpyHostToDevice,
                             st);

@@ -371,7 +371,8 @@ int fsdp_rs_kernel_for(const fsdp_layout* layout, int32_t grad_dtype);
 int fsdp_wait_selftest(int64_t timeout_ns, fsdp_stream_t stream);
 
 /* fsdp_reduce_scatter_adamw_noalloc -- the pages have no counterpart of this call.
- * The same computation, arguments, checks and results as fsdp_reduce_scatter_adamw,
+ * The same computation, arguments, checks, kernel choice and results as
+ * fsdp_reduce_scatter_adamw,
  * for callers that cannot allocate device memory: a pre-sized pool or custom
  * allocator that owns all device memory, a step that must not enter the driver's
  * allocator (cudaMalloc may synchronize the device or fail under memory pressure),

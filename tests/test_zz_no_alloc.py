@@ -4,7 +4,7 @@ The no-allocation entry point serves callers that cannot call cudaMalloc (a
 pre-sized pool or custom allocator that owns device memory, a step that must not
 enter the driver's allocator, an embedder that forbids hidden allocations): its
 segment table lives in a fixed array inside the library.  It must give the same
-results as the allocating entry point, call after call.
+results as the allocating entry point, call after call, with either kernel.
 
 This file is named to be collected last: if it fails, a run that stops at the
 first failure has already run every other test.
@@ -40,7 +40,16 @@ def _pair(w, with_grad_out):
                     torch.float32, torch.float32, 2, 1e-3), [(0, 1), (1, 3)]),
 ])
 @pytest.mark.parametrize("with_grad_out", [False, True])
-def test_noalloc_matches_allocating_entry_point(w, ranges, with_grad_out):
+@pytest.mark.parametrize("kind", ["auto", "direct", "staged"])
+def test_noalloc_matches_allocating_entry_point(w, ranges, with_grad_out, kind):
+    prev = fs.fsdp_set_rs_kernel(kind)                 # both entry points follow the same choice
+    try:
+        _check_noalloc(w, ranges, with_grad_out)
+    finally:
+        fs.fsdp_set_rs_kernel(prev)
+
+
+def _check_noalloc(w, ranges, with_grad_out):
     a, b = _pair(w, with_grad_out)
     lib = fs.lib()
     stream = torch.cuda.current_stream().cuda_stream
