@@ -269,6 +269,7 @@ int fsdp_state_bytes(const fsdp_layout* L, int32_t stage, int32_t rank, int32_t 
 }
 
 int fsdp_layout_prepare(fsdp_layout* L) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_layout_prepare");
     if (!L) return FSDP_EINVAL;
     const Seg* base = nullptr;
     return device_tables(L, &base);
@@ -276,6 +277,7 @@ int fsdp_layout_prepare(fsdp_layout* L) {
 
 int fsdp_unshard(const fsdp_layout* L, int32_t ub, int32_t ue, const void* shards, void* full,
                  int32_t elem_dtype, fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_unshard");
     int rc = check_units(L, ub, ue);
     if (rc) return rc;
     if (elem_dtype != FSDP_F32 && elem_dtype != FSDP_BF16) return FSDP_EDTYPE;
@@ -299,6 +301,7 @@ int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, cons
                               int32_t grad_dtype, float* master, float* exp_avg, float* exp_avg_sq,
                               void* param_shards, float* grad_shard_out, const fsdp_adamw_hparams* hp,
                               int64_t step, fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_reduce_scatter_adamw");
     int rc = check_units(L, ub, ue);
     if (rc) return rc;
     if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
@@ -345,6 +348,7 @@ int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, cons
 
 int fsdp_reshard(const fsdp_layout* L, int32_t ub, int32_t ue, const void* full, int32_t full_dtype,
                  float* master, void* param_shards, fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_reshard");
     int rc = check_units(L, ub, ue);
     if (rc) return rc;
     if (!full) return FSDP_OK;   // release only: the full buffer is the caller's
@@ -366,6 +370,7 @@ int fsdp_reshard(const fsdp_layout* L, int32_t ub, int32_t ue, const void* full,
 }
 
 int fsdp_check_status(fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_check_status");
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     e = cudaGetLastError();
@@ -394,6 +399,7 @@ int fsdp_rs_kernel_for(const fsdp_layout* L, int32_t grad_dtype) {
 }
 
 int fsdp_wait_selftest(int64_t timeout_ns, fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_wait_selftest");
     if (timeout_ns <= 0 || timeout_ns > 10000000000LL) return FSDP_EINVAL;
     const cudaError_t e = fsdp::launch_wait_selftest(uint64_t(timeout_ns), reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "k_wait_selftest launch");

@@ -4,6 +4,7 @@
 #include <cstdint>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/fsdp_state.h"
 #include "common.cuh"
@@ -26,6 +27,15 @@ int check_units(const fsdp_layout* L, int32_t ub, int32_t ue);
 int check_ptr(const void* p);                            // non-NULL and 16-byte aligned
 int check_hparams(const fsdp_adamw_hparams* hp);
 AdamScal adam_scalars(const fsdp_adamw_hparams* hp, int64_t step, int32_t n_avg);
+
+// An NVTX range over one library call: the call's name on a profiler's timeline
+// (Nsight Systems, ncu --nvtx); without a tool attached the push and pop do nothing.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Time limit of each mbarrier wait in the staged kernels.
 constexpr uint64_t kWaitNs = 1000000000ull;

@@ -69,6 +69,7 @@ extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t u
                                                  float* exp_avg, float* exp_avg_sq, void* param_shards,
                                                  float* grad_shard_out, const fsdp_adamw_hparams* hp,
                                                  int64_t step, fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_reduce_scatter_adamw_noalloc");
     // ---- the same argument checks as fsdp_reduce_scatter_adamw ----
     if (!L || ub < 0 || ue > L->U || ub > ue) return FSDP_EINVAL;
     if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;

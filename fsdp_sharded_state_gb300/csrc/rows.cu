@@ -422,6 +422,7 @@ int fsdp_reduce_scatter_clip_adamw(const fsdp_layout* L, int32_t ub, int32_t ue,
                                    void* param_shards, float* grad_shard, float max_norm, void* workspace,
                                    float* norm_out, const fsdp_adamw_hparams* hp, int64_t step,
                                    fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_reduce_scatter_clip_adamw");
     int rc = check_units(L, ub, ue);
     if (rc) return rc;
     if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;
@@ -510,6 +511,7 @@ int fsdp_reduce_scatter_clip_adamw(const fsdp_layout* L, int32_t ub, int32_t ue,
 
 int fsdp_accumulate_grads(const fsdp_layout* L, int32_t ub, int32_t ue, float* const* acc,
                           const void* const* micro, int32_t micro_dtype, int32_t first, fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_accumulate_grads");
     int rc = check_units(L, ub, ue);
     if (rc) return rc;
     if (micro_dtype != FSDP_F32 && micro_dtype != FSDP_BF16) return FSDP_EDTYPE;
@@ -547,6 +549,7 @@ int fsdp_hsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue,
                                    const void* const* grads, int32_t grad_dtype, float* master, float* exp_avg,
                                    float* exp_avg_sq, void* param_shards, const fsdp_adamw_hparams* hp,
                                    int64_t step, fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_hsdp_reduce_scatter_adamw");
     int rc = check_units(L, ub, ue);
     if (rc) return rc;
     if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;
@@ -591,6 +594,7 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* L, int32_t ub, int32_t ue, con
                                int32_t grad_dtype, float* master, float* exp_avg, float* exp_avg_sq,
                                void* const* param_replicas, int32_t param_dtype, const fsdp_adamw_hparams* hp,
                                int64_t step, fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_zero1_adamw_broadcast");
     int rc = check_units(L, ub, ue);
     if (rc) return rc;
     if (L->mode != FSDP_ZERO1 || step < 1) return FSDP_EINVAL;
