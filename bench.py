@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -65,12 +66,20 @@ def load_peaks():
     return PEAK_FALLBACK_GBS, "fallback"
 
 
+def code_only(src: str) -> str:
+    """C/C++/CUDA source without comments and with whitespace collapsed: what the
+    compiler sees, so that an edit to a comment does not void a recorded capture."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_src_hash(kernel="k_rs_adamw"):
-    """Hash of the sources a core kernel compiles from."""
+    """Hash of the code (comments aside) of the sources a core kernel compiles from."""
     h = hashlib.sha256()
     for p in KERNEL_SRC[kernel]:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

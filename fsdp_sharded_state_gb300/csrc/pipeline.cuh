@@ -10,7 +10,9 @@
 // they do.  No CTA-wide barrier in the loop; the bytes in flight per SM do not
 // depend on registers.  A gradient piece whose full-layout offset is not congruent
 // to its shard offset mod 8 is copied as the 16-byte-aligned window around it and
-// read from shared memory at its offset: no warp shuffle.
+// read from shared memory at its offset: no warp shuffle.  A use may also take an
+// output ring: the consumers write an item's results once into a shared-memory slot
+// and a store warp sends them out with cp.async.bulk shared -> global copies.
 //
 // Every wait on an mbarrier is bounded in time; a warp that gives up records
 // FSDP_ETIMEOUT in this translation unit's device word (g_wait_error, read and

@@ -83,3 +83,11 @@ def test_launch_stats():
     assert s["median_ms"] == 1.0 and s["p95_ms"] == 1.0 and s["cv"] == 0.0 and not s["cv_flag"]
     s = bench.launch_stats([1.0, 2.0, 3.0, 4.0, 100.0])
     assert s["median_ms"] == 3.0 and s["p95_ms"] == 100.0 and s["cv_flag"] and s["n"] == 5
+
+
+def test_code_hash_ignores_comments():
+    import bench
+    a = "int f(int x) {  // comment\n  return x; /* block\n comment */ }\n"
+    b = "int f(int x) { return x; }"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only("int a;") != bench.code_only("int b;")
