@@ -394,14 +394,15 @@ int optin_smem(int dev) {
 }
 
 // Stages for a stage of `stage_bytes`: as many as keep about 96 KB in flight (the
-// stages beyond the one being consumed), between 2 and kMaxStages, within the
-// opt-in shared memory; 0 if two do not fit.  Measured on GB300 (fused step): about
-// 50-100 KB in flight per SM streams best; 3-4 stages of 57 KB lost up to 10 % of
-// the bandwidth, fewer than 40 KB in flight lost 8 %.
+// stages beyond the one being consumed), 4 for stages under 36 KB, between 2 and
+// kMaxStages, within the opt-in shared memory; 0 if two do not fit.  Measured on
+// GB300 (fused step): about 50-100 KB in flight per SM streams best; 3-4 stages of
+// 57 KB lost up to 10 % of the bandwidth, fewer than 40 KB in flight lost 8 %, and
+// stages of 33 KB (bf16, N = 2) ran best with 4.
 int stage_count(int stage_bytes, int dev, int extra_bytes = 0) {
     const int avail = optin_smem(dev) - kFrontBytes - extra_bytes;
     const int fit = avail > 0 ? avail / stage_bytes : 0;
-    int want = kInFlightBytes / stage_bytes + 1;
+    int want = stage_bytes < 36 * 1024 ? 4 : kInFlightBytes / stage_bytes + 1;
     want = want < 2 ? 2 : (want > kMaxStages ? kMaxStages : want);
     const int s = fit < want ? fit : want;
     return s >= 2 ? s : 0;

@@ -155,6 +155,7 @@ void rs_groups(int N, bool bf16, int dev, int* Q, int* NG) {
     *NG = ng;
     *Q = (N + ng - 1) / ng;
 }
+
 }  // namespace
 
 bool staged_fits(int N, bool grad_bf16) {
