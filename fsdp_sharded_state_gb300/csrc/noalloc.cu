@@ -55,13 +55,6 @@ int scratch_address(Seg** out) {
     return FSDP_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int ptr_ok(const void* p) {
-    if (!p) return FSDP_EINVAL;
-    return aligned16(p) ? FSDP_OK : FSDP_EALIGN;
-}
-
 }  // namespace
 
 extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t ub, int32_t ue,
@@ -71,21 +64,20 @@ extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t u
                                                  int64_t step, fsdp_stream_t stream) {
     fsdp::detail::NvtxRange nvtx_range("fsdp_reduce_scatter_adamw_noalloc");
     // ---- the same argument checks as fsdp_reduce_scatter_adamw ----
-    if (!L || ub < 0 || ue > L->U || ub > ue) return FSDP_EINVAL;
+    int rc;
+    if ((rc = fsdp::detail::check_units(L, ub, ue))) return rc;
     if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
     if (!grads || !hp || step < 1) return FSDP_EINVAL;
-    int rc;
     for (int32_t q = 0; q < L->N; ++q)
-        if ((rc = ptr_ok(grads[q]))) return rc;
-    if ((rc = ptr_ok(master)) || (rc = ptr_ok(exp_avg)) || (rc = ptr_ok(exp_avg_sq))) return rc;
-    if ((param_shards && !aligned16(param_shards)) || (grad_shard_out && !aligned16(grad_shard_out)))
+        if ((rc = fsdp::detail::check_ptr(grads[q]))) return rc;
+    if ((rc = fsdp::detail::check_ptr(master)) || (rc = fsdp::detail::check_ptr(exp_avg)) ||
+        (rc = fsdp::detail::check_ptr(exp_avg_sq)))
+        return rc;
+    if ((param_shards && !fsdp::detail::aligned16(param_shards)) ||
+        (grad_shard_out && !fsdp::detail::aligned16(grad_shard_out)))
         return FSDP_EALIGN;
-    const float lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
-    if (!std::isfinite(lr) || !std::isfinite(b1) || !std::isfinite(b2) || !std::isfinite(eps) || !std::isfinite(wd))
-        return FSDP_EINVAL;
-    if (lr < 0.f || b1 < 0.f || b1 >= 1.f || b2 < 0.f || b2 >= 1.f || eps <= 0.f || wd < 0.f ||
-        double(lr) * double(wd) > 1.0)
-        return FSDP_EINVAL;
+    if ((rc = fsdp::detail::check_hparams(hp))) return rc;
+    if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;
 
     // ---- the table entries this call reads: for each alignment class, the data
     //      segments of the unit range plus the entry after them (next unit's first
@@ -101,18 +93,7 @@ extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t u
     Seg* scratch = nullptr;
     if ((rc = scratch_address(&scratch))) return rc;
 
-    fsdp::AdamScal sc;
-    const double bc1 = 1.0 - std::pow(double(b1), double(step));
-    const double bc2 = 1.0 - std::pow(double(b2), double(step));
-    sc.decay = float(1.0 - double(lr) * double(wd));
-    sc.om1 = float(1.0 - double(b1));
-    sc.om2 = float(1.0 - double(b2));
-    sc.step_size = float(double(lr) / bc1);
-    sc.bc2s = float(std::sqrt(bc2));
-    sc.beta1 = b1;
-    sc.beta2 = b2;
-    sc.eps = eps;
-    sc.nf = float(L->N);
+    const fsdp::AdamScal sc = fsdp::detail::adam_scalars(hp, step, L->N);
     fsdp::GradPtrs gp{};
     for (int32_t q = 0; q < L->N; ++q) gp.p[q] = grads[q];
 
