@@ -1,4 +1,5 @@
-// kernels.cu -- the device side of libfsdpstate (sm_103a).
+// kernels.cu -- the direct (register) kernels of libfsdpstate (sm_103a); the
+// bulk-copy kernels are in staged.cu, allgather.cu and staged_rows.cu.
 //
 //   k_rs_adamw   fused reduce-scatter (fp32 mean over N gradient replicas, fixed
 //                rank order) + AdamW on the fp32 master/exp_avg/exp_avg_sq shard +
@@ -14,7 +15,8 @@
 // thread owns one 8-element vector per tile, aligned on the shard side; interior
 // vectors use 16-byte loads and stores, the (at most two) partial vectors of a
 // segment go element by element.  A segment whose full-layout offset is not
-// congruent to its shard offset mod 8 reads its gradients element by element.
+// congruent to its shard offset mod 8 (the "shifted" class) realigns its vectors
+// across the warp: each lane takes its neighbour's vector with a shuffle.
 // Memory-bound throughout: no tensor-core work (the path has no contraction).
 #include <map>
 #include <mutex>

@@ -1,7 +1,9 @@
 // rows.cu -- the rows beyond the core step: sharded clip_grad_norm_ before AdamW,
 // gradient accumulation without sync, HSDP (shard groups x replica groups) and the
-// ZeRO-1 owner step with its broadcast.  Same tile machinery, segment lists and
-// AdamW element as the core kernels (common.cuh, device_ops.cuh).
+// ZeRO-1 owner step with its broadcast.  Their entry points, and their direct
+// (register) kernels, with the same tile machinery, segment lists and AdamW element
+// as the core kernels (common.cuh, device_ops.cuh); the bulk-copy versions are in
+// staged_rows.cu and the entry points choose between the two (choose_staged).
 #include <cmath>
 #include <map>
 #include <mutex>
