@@ -52,6 +52,7 @@ k_unshard_bulk(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
         mbar_fence_init();
     }
     __syncwarp();
+    pdl_wait();
 
     struct Piece { int64_t t0, s0, s1, delta, a, b; };     // tile range, aligned interior [a, b)
     auto piece = [&](int& cur, int64_t j) {
@@ -133,9 +134,9 @@ cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_ti
     if (blocks > n_tiles) blocks = n_tiles;
     const auto* s8 = static_cast<const unsigned char*>(src);
     auto* d8 = static_cast<unsigned char*>(dst);
-    if (bf16) k_unshard_bulk<2><<<int(blocks), 32, 0, st>>>(segs, tile_base, n_tiles, s8, d8, wait_ns);
-    else k_unshard_bulk<4><<<int(blocks), 32, 0, st>>>(segs, tile_base, n_tiles, s8, d8, wait_ns);
-    return cudaGetLastError();
+    if (bf16) return launch(k_unshard_bulk<2>, dim3(unsigned(blocks)), dim3(32), 0, st, segs, tile_base, n_tiles, s8, d8,
+                            wait_ns);
+    return launch(k_unshard_bulk<4>, dim3(unsigned(blocks)), dim3(32), 0, st, segs, tile_base, n_tiles, s8, d8, wait_ns);
 }
 
 cudaError_t take_wait_error_allgather(unsigned int* flag) { return take_local_wait_error(flag); }

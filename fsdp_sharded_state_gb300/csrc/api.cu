@@ -82,7 +82,7 @@ int device_tables(const fsdp_layout* Lc, const Seg** base) {
 Range range_of(const SegList& l, const Seg* dev_base, int32_t ub, int32_t ue) {
     const int32_t sb = l.unit_begin[ub], se = l.unit_begin[ue];
     const int64_t t0 = l.segs[sb].tile0, t1 = l.segs[se].tile0;
-    return Range{dev_base + l.dev_off + sb, t0, t1 - t0};
+    return Range{dev_base + l.dev_off + sb, t0, t1 - t0, se - sb};
 }
 
 int check_units(const fsdp_layout* L, int32_t ub, int32_t ue) {

@@ -17,6 +17,7 @@ namespace detail {
 struct Range {
     const Seg* segs;
     int64_t tile_base, n_tiles;
+    int32_t n_segs;     // segments in the range (the sentinel after them not counted)
 };
 
 int cuda_fail(cudaError_t e, const char* where);        // records the error text, returns FSDP_ECUDA

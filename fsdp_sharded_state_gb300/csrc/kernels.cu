@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, (SHIFT || GOUT || (!PARAM && sizeof(
 k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N, int64_t F,
            float* __restrict__ master, float* __restrict__ exp_avg, float* __restrict__ exp_avg_sq,
            uint16_t* __restrict__ param, float* __restrict__ gout, AdamScal sc) {
+    pdl_wait();
     const bool lane31 = (threadIdx.x & 31) == 31;
     int s = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
@@ -270,6 +271,7 @@ template <typename ET>
 __global__ void __launch_bounds__(kThreads)
 k_unshard_shift(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, const ET* __restrict__ src,
                 ET* __restrict__ dst, int64_t src_limit) {
+    pdl_wait();
     const bool lane31 = (threadIdx.x & 31) == 31;
     int s = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
@@ -320,6 +322,7 @@ template <bool FULL_BF16, bool MASTER, bool PARAM>
 __global__ void __launch_bounds__(kThreads)
 k_reshard(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
           const void* __restrict__ full, float* __restrict__ master, uint16_t* __restrict__ param) {
+    pdl_wait();
     int s = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         const int64_t gt = tile_base + t;
@@ -365,6 +368,7 @@ template <bool F32OUT, bool BF16OUT>
 __global__ void __launch_bounds__(kThreads)
 k_zero_pad(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
            float* __restrict__ a32, uint16_t* __restrict__ a16) {
+    pdl_wait();
     int s = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         const int64_t gt = tile_base + t;
@@ -427,20 +431,25 @@ template <typename GT, bool SHIFT>
 static cudaError_t launch_rs_t(const Seg* segs, int64_t tile_base, int64_t n_tiles, const GradPtrs& gp,
                                int N, int64_t F, float* master, float* m, float* v, uint16_t* param, float* gout,
                                const AdamScal& sc, cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
     if (param && gout) {
         auto k = k_rs_adamw<GT, true, true, SHIFT>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, gp, N, F, master,
+                   m, v, param, gout, sc);
     } else if (param) {
         auto k = k_rs_adamw<GT, true, false, SHIFT>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, gp, N, F, master,
+                   m, v, param, gout, sc);
     } else if (gout) {
         auto k = k_rs_adamw<GT, false, true, SHIFT>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, gp, N, F, master,
+                   m, v, param, gout, sc);
     } else {
         auto k = k_rs_adamw<GT, false, false, SHIFT>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, gp, N, F, master, m, v, param, gout, sc);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, gp, N, F, master,
+                   m, v, param, gout, sc);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_rs_adamw(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool shifted, bool grad_bf16,
@@ -457,10 +466,11 @@ cudaError_t launch_rs_adamw(const Seg* segs, int64_t tile_base, int64_t n_tiles,
 template <typename ET>
 static cudaError_t launch_unshard_t(const Seg* segs, int64_t tile_base, int64_t n_tiles, const void* src, void* dst,
                                     int64_t src_limit, cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
     auto k = k_unshard_shift<ET>;
-    k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, static_cast<const ET*>(src),
+    e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, static_cast<const ET*>(src),
                                                   static_cast<ET*>(dst), src_limit);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_unshard_shifted(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16, const void* src,
@@ -473,17 +483,18 @@ cudaError_t launch_unshard_shifted(const Seg* segs, int64_t tile_base, int64_t n
 template <bool FB>
 static cudaError_t launch_reshard_t(const Seg* segs, int64_t tile_base, int64_t n_tiles, const void* full,
                                     float* master, uint16_t* param, cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
     if (master && param) {
         auto k = k_reshard<FB, true, true>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, full, master, param);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, full, master, param);
     } else if (master) {
         auto k = k_reshard<FB, true, false>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, full, master, param);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, full, master, param);
     } else {
         auto k = k_reshard<FB, false, true>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, full, master, param);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, full, master, param);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_reshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool full_bf16,
@@ -495,18 +506,19 @@ cudaError_t launch_reshard(const Seg* segs, int64_t tile_base, int64_t n_tiles, 
 
 cudaError_t launch_zero_pad(const Seg* segs, int64_t tile_base, int64_t n_tiles, float* a32, uint16_t* a16,
                             cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
     if (n_tiles <= 0 || (!a32 && !a16)) return cudaSuccess;
     if (a32 && a16) {
         auto k = k_zero_pad<true, true>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, a32, a16);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, a32, a16);
     } else if (a32) {
         auto k = k_zero_pad<true, false>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, a32, a16);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, a32, a16);
     } else {
         auto k = k_zero_pad<false, true>;
-        k<<<grid_for(k, n_tiles), kThreads, 0, st>>>(segs, tile_base, n_tiles, a32, a16);
+        e = launch(k, dim3(grid_for(k, n_tiles)), dim3(kThreads), 0, st, segs, tile_base, n_tiles, a32, a16);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace fsdp

@@ -293,6 +293,7 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, in
         mbar_fence_init();
     }
     __syncthreads();
+    pdl_wait();
 
     if constexpr (kOut > 0) {
         if (warp == kConsumerWarps + 1) {
@@ -445,9 +446,10 @@ cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage
         g_st_cache[key] = std::make_pair(sms, smem);
     }
     const int64_t blocks = n_items < sms ? n_items : (sms > 0 ? sms : 1);
-    kernel<<<int(blocks), pipeline_threads<Pol>(), smem, st>>>(pol, n_items, S, stage_bytes, wait_ns);
-    if (grid_out) *grid_out = int(blocks);
-    return cudaGetLastError();
+    e = launch(kernel, dim3(unsigned(blocks)), dim3(pipeline_threads<Pol>()), size_t(smem), st, pol, n_items, S,
+               stage_bytes, wait_ns);
+    if (e == cudaSuccess && grid_out) *grid_out = int(blocks);
+    return e;
 }
 
 int rs_stage_bytes(int N, bool bf16) { return 3 * kStateBytes + N * (bf16 ? grank_bytes<uint16_t>() : grank_bytes<float>()); }
