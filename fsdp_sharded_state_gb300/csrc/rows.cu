@@ -7,6 +7,7 @@
 #include <cmath>
 #include <map>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include "device_ops.cuh"
@@ -374,6 +375,80 @@ struct ParamPtrs {
     void* p[kMaxRanks];
 };
 
+// fp32 gradients and fp32 replicas, "split" lane mapping: within its warp's 256
+// elements lane l owns [4l, 4l+4) and [128+4l, 128+4l+4), so every 16-byte load or
+// store of the warp covers 512 contiguous bytes.  Same arithmetic, same order.
+__device__ __forceinline__ void zero1_tile_f32_split(const Seg& sg, int64_t gt, const GradPtrs& gp, int N,
+                                                     int64_t stride, float* __restrict__ exp_avg,
+                                                     float* __restrict__ exp_avg_sq, const ParamPtrs& pp,
+                                                     const AdamScal& sc) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t x0 = (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads) * kVec + warp * 256 + lane * 4;
+    const int64_t lo = sg.shard, hi = sg.shard + sg.len, delta = sg.full - sg.shard;
+    if (x0 >= hi) return;
+    const int64_t x1 = x0 + 128;
+    const float* own = static_cast<const float*>(pp.p[sg.shard / stride]);
+    if (x0 >= lo && x1 + 4 <= hi && (delta & 3) == 0) {
+        const float4 pa = ld4(own + x0 + delta), pb = ld4(own + x1 + delta);
+        const float4 ma = ld4(exp_avg + x0), mb = ld4(exp_avg + x1);
+        const float4 va = ld4(exp_avg_sq + x0), vb = ld4(exp_avg_sq + x1);
+        float acc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+#pragma unroll 1
+        for (int q0 = 0; q0 < N; q0 += 2) {                 // 2 replicas x 2 chunks in flight
+            uint4 ga[2], gb[2];
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+                if (q0 + b < N) {
+                    const float* g = static_cast<const float*>(gp.p[q0 + b]);
+                    ga[b] = ld_once(g + x0 + delta);
+                    gb[b] = ld_once(g + x1 + delta);
+                }
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+                if (q0 + b < N) {
+                    acc[0] = __fadd_rn(acc[0], __uint_as_float(ga[b].x));
+                    acc[1] = __fadd_rn(acc[1], __uint_as_float(ga[b].y));
+                    acc[2] = __fadd_rn(acc[2], __uint_as_float(ga[b].z));
+                    acc[3] = __fadd_rn(acc[3], __uint_as_float(ga[b].w));
+                    acc[4] = __fadd_rn(acc[4], __uint_as_float(gb[b].x));
+                    acc[5] = __fadd_rn(acc[5], __uint_as_float(gb[b].y));
+                    acc[6] = __fadd_rn(acc[6], __uint_as_float(gb[b].z));
+                    acc[7] = __fadd_rn(acc[7], __uint_as_float(gb[b].w));
+                }
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int64_t xc = c ? x1 : x0;
+            const float4 pc = c ? pb : pa, mc = c ? mb : ma, vc = c ? vb : va;
+            float p[4] = {pc.x, pc.y, pc.z, pc.w};
+            float m[4] = {mc.x, mc.y, mc.z, mc.w};
+            float v[4] = {vc.x, vc.y, vc.z, vc.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) adamw1(sc, __fdiv_rn(acc[4 * c + k], sc.nf), p[k], m[k], v[k]);
+            st4(exp_avg + xc, make_float4(m[0], m[1], m[2], m[3]));
+            st4(exp_avg_sq + xc, make_float4(v[0], v[1], v[2], v[3]));
+            const float4 pv = make_float4(p[0], p[1], p[2], p[3]);
+#pragma unroll 1
+            for (int q = 0; q < N; ++q) st4(static_cast<float*>(pp.p[q]) + xc + delta, pv);
+        }
+        return;
+    }
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {                           // a chunk at a segment edge
+        const int64_t xc = c ? x1 : x0;
+        const int64_t a = xc > lo ? xc : lo, b = (xc + 4) < hi ? (xc + 4) : hi;
+        for (int64_t e = a; e < b; ++e) {
+            const int64_t f = e + delta;
+            float p = own[f], m = exp_avg[e], v = exp_avg_sq[e];
+            adamw1(sc, __fdiv_rn(reduce1<float>(gp, N, f), sc.nf), p, m, v);
+            exp_avg[e] = m; exp_avg_sq[e] = v;
+            for (int q = 0; q < N; ++q) static_cast<float*>(pp.p[q])[f] = p;
+        }
+    }
+}
+
 template <typename GT, bool MASTER>
 __global__ void __launch_bounds__(kThreads, 2)
 k_zero1_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N,
@@ -385,6 +460,10 @@ k_zero1_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, 
         const int64_t gt = tile_base + t;
         s = advance_seg(segs, s, gt);
         const Seg sg = segs[s];
+        if (std::is_same<GT, float>::value && !MASTER) {
+            zero1_tile_f32_split(sg, gt, gp, N, stride, exp_avg, exp_avg_sq, pp, sc);
+            continue;
+        }
         const int64_t e0 = tile_e0(sg, gt);
         const int64_t lo = sg.shard, hi = sg.shard + sg.len, delta = sg.full - sg.shard;
         if (e0 >= hi) continue;
