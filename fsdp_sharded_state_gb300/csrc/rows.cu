@@ -79,6 +79,75 @@ __device__ __forceinline__ double block_sum(double x) {
 // and the coefficient itself (every CTA sums the partials in the same order),
 // which saves the launch of step (2).
 // ---------------------------------------------------------------------------
+// Sum, in rank order, of the N fp32 replicas at the two 4-element chunks a lane owns
+// under the "split" mapping (full-layout offsets fa and fb, 16-byte aligned): acc[0..3]
+// for fa, acc[4..7] for fb; 2 replicas x 2 chunks in flight.
+__device__ __forceinline__ void reduce_split_f32(const GradPtrs& gp, int N, int64_t fa, int64_t fb,
+                                                 float (&acc)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+#pragma unroll 1
+    for (int q0 = 0; q0 < N; q0 += 2) {
+        uint4 ga[2], gb[2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+            if (q0 + b < N) {
+                const float* g = static_cast<const float*>(gp.p[q0 + b]);
+                ga[b] = ld_once(g + fa);
+                gb[b] = ld_once(g + fb);
+            }
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+            if (q0 + b < N) {
+                acc[0] = __fadd_rn(acc[0], __uint_as_float(ga[b].x));
+                acc[1] = __fadd_rn(acc[1], __uint_as_float(ga[b].y));
+                acc[2] = __fadd_rn(acc[2], __uint_as_float(ga[b].z));
+                acc[3] = __fadd_rn(acc[3], __uint_as_float(ga[b].w));
+                acc[4] = __fadd_rn(acc[4], __uint_as_float(gb[b].x));
+                acc[5] = __fadd_rn(acc[5], __uint_as_float(gb[b].y));
+                acc[6] = __fadd_rn(acc[6], __uint_as_float(gb[b].z));
+                acc[7] = __fadd_rn(acc[7], __uint_as_float(gb[b].w));
+            }
+    }
+}
+
+// Pass 1 for fp32 gradients on aligned segments, split lane mapping (each 16-byte
+// load or store of a warp covers 512 contiguous bytes): the reduced gradient into
+// the shard, and the lane's sum of squares (fp32 over its 8 elements in order, then
+// double).
+__device__ __forceinline__ double norm_tile_f32_split(const Seg& sg, int64_t gt, const GradPtrs& gp, int N,
+                                                      float* __restrict__ gout, float nf) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t x0 = (seg_vec0(sg.shard) + (gt - sg.tile0) * kThreads) * kVec + warp * 256 + lane * 4;
+    const int64_t lo = sg.shard, hi = sg.shard + sg.len, delta = sg.full - sg.shard;
+    if (x0 >= hi) return 0.0;
+    const int64_t x1 = x0 + 128;
+    if (x0 >= lo && x1 + 4 <= hi && (delta & 3) == 0) {
+        float acc[8], g[8], sq = 0.0f;
+        reduce_split_f32(gp, N, x0 + delta, x1 + delta, acc);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            g[k] = __fdiv_rn(acc[k], nf);
+            sq = __fmaf_rn(g[k], g[k], sq);
+        }
+        st4(gout + x0, make_float4(g[0], g[1], g[2], g[3]));
+        st4(gout + x1, make_float4(g[4], g[5], g[6], g[7]));
+        return double(sq);
+    }
+    double ss = 0.0;
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {                           // a chunk at a segment edge
+        const int64_t xc = c ? x1 : x0;
+        const int64_t a = xc > lo ? xc : lo, b = (xc + 4) < hi ? (xc + 4) : hi;
+        for (int64_t e = a; e < b; ++e) {
+            const float g = __fdiv_rn(reduce1<float>(gp, N, e + delta), nf);
+            gout[e] = g;
+            ss += double(g) * double(g);
+        }
+    }
+    return ss;
+}
+
 template <typename GT, bool SHIFT>
 __global__ void __launch_bounds__(kThreads, 2)
 k_rs_norm(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N, int64_t F,
@@ -91,6 +160,10 @@ k_rs_norm(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, Grad
         const int64_t gt = tile_base + t;
         s = advance_seg(segs, s, gt);
         const Seg sg = segs[s];
+        if constexpr (std::is_same<GT, float>::value && !SHIFT) {
+            ss += norm_tile_f32_split(sg, gt, gp, N, gout, nf);
+            continue;
+        }
         const int64_t e0 = tile_e0(sg, gt);
         const int64_t lo = sg.shard, hi = sg.shard + sg.len, delta = sg.full - sg.shard;
         const int64_t f0 = e0 + delta;
@@ -393,31 +466,7 @@ __device__ __forceinline__ void zero1_tile_f32_split(const Seg& sg, int64_t gt, 
         const float4 ma = ld4(exp_avg + x0), mb = ld4(exp_avg + x1);
         const float4 va = ld4(exp_avg_sq + x0), vb = ld4(exp_avg_sq + x1);
         float acc[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-#pragma unroll 1
-        for (int q0 = 0; q0 < N; q0 += 2) {                 // 2 replicas x 2 chunks in flight
-            uint4 ga[2], gb[2];
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-                if (q0 + b < N) {
-                    const float* g = static_cast<const float*>(gp.p[q0 + b]);
-                    ga[b] = ld_once(g + x0 + delta);
-                    gb[b] = ld_once(g + x1 + delta);
-                }
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-                if (q0 + b < N) {
-                    acc[0] = __fadd_rn(acc[0], __uint_as_float(ga[b].x));
-                    acc[1] = __fadd_rn(acc[1], __uint_as_float(ga[b].y));
-                    acc[2] = __fadd_rn(acc[2], __uint_as_float(ga[b].z));
-                    acc[3] = __fadd_rn(acc[3], __uint_as_float(ga[b].w));
-                    acc[4] = __fadd_rn(acc[4], __uint_as_float(gb[b].x));
-                    acc[5] = __fadd_rn(acc[5], __uint_as_float(gb[b].y));
-                    acc[6] = __fadd_rn(acc[6], __uint_as_float(gb[b].z));
-                    acc[7] = __fadd_rn(acc[7], __uint_as_float(gb[b].w));
-                }
-        }
+        reduce_split_f32(gp, N, x0 + delta, x1 + delta, acc);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int64_t xc = c ? x1 : x0;
@@ -460,7 +509,7 @@ k_zero1_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, 
         const int64_t gt = tile_base + t;
         s = advance_seg(segs, s, gt);
         const Seg sg = segs[s];
-        if (std::is_same<GT, float>::value && !MASTER) {
+        if constexpr (std::is_same<GT, float>::value && !MASTER) {
             zero1_tile_f32_split(sg, gt, gp, N, stride, exp_avg, exp_avg_sq, pp, sc);
             continue;
         }
