@@ -1,0 +1,225 @@
+"""Calls that depend on one another, issued back to back on one stream with no host
+synchronisation between them, against the same chain in the oracle (GPU).
+
+Every kernel of the library is launched with programmatic stream serialization and
+waits for the grid before it before touching memory; these chains check that each
+call sees the complete result of the one before: the all-gather reads the shards the
+step before it wrote, the step reads the accumulators the accumulation wrote, the
+writeback reads the gathered buffer, ZeRO-1's owner reads the replica its previous
+call broadcast.  Each chain runs with the default kernel choice and with the direct
+and the staged kernels forced."""
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_state_gb300 as fs
+import oracle
+from fsdp_sharded_state_gb300 import synth
+
+import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, params=["auto", "direct", "staged"])
+def rs_kind(request):
+    prev = fs.fsdp_set_rs_kernel(request.param)
+    yield request.param
+    fs.fsdp_set_rs_kernel(prev)
+
+
+def W(shapes, units, N, mode, dtype=torch.bfloat16):
+    return synth.Workload("chain", 12, list(shapes), list(units), N, mode, dtype, dtype, 4, 1e-3)
+
+
+CHAINS = [W([(300, 37), (13,), (64, 65)], [0, 0, 1], 4, synth.FLAT),        # ragged tails, 2 units
+          W([(130, 64), (7,), (9, 3)], [0, 0, 0], 6, synth.DIM0),          # rows not divisible by N
+          W([((1 << 20) + 3,)], [0], 8, synth.FLAT),                       # many tiles, shifted ranks
+          W([(512, 96), (96,)], [0, 0], 4, synth.FLAT, torch.float32)]     # fp32 parameters
+
+
+@pytest.mark.parametrize("w", CHAINS)
+def test_step_chain_vs_oracle(oracle_lib, w):
+    """reshard -> unshard -> accumulate x2 -> step -> unshard -> writeback (reshard of
+    the gathered buffer) -> step -> unshard -> clipped step -> unshard, one sync at the end."""
+    st = pu.make_state(w, with_grad_out=True)
+    L, N, F, stride = st.layout, w.N, st.F, st.stride
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = pu.oracle_offsets(w)
+    bf16 = w.param_dtype == torch.bfloat16
+    gdt = torch.bfloat16 if bf16 else torch.float32
+    full0 = synth.full_params(w, F, O["t_full_off"])
+    micro1 = [g.to(gdt) for g in synth.grad_replicas(w, F, 1)]
+    micro2 = [g.to(gdt) for g in synth.grad_replicas(w, F, 2)]
+    g3 = [g.to(gdt) for g in synth.grad_replicas(w, F, 3)]
+    g4 = [g.to(gdt) for g in synth.grad_replicas(w, F, 4)]
+    acc = [torch.empty(F, dtype=torch.float32, device="cuda") for _ in range(N)]
+    gathered = [torch.empty(F, dtype=w.param_dtype, device="cuda") for _ in range(4)]
+    ws = torch.empty(fs.fsdp_clip_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    norm_out = torch.zeros(2, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+
+    # ---- the chain on the GPU: no synchronisation until the end ----
+    st.init_from_full(full0)
+    st.unshard(out=gathered[0])
+    fs.fsdp_accumulate_grads(L, 0, L.n_units, acc, micro1, first=True)
+    fs.fsdp_accumulate_grads(L, 0, L.n_units, acc, micro2, first=False)
+    st.reduce_scatter_adamw(acc, w.hp, step=1)
+    st.unshard(out=gathered[1])
+    fs.fsdp_reshard(L, 0, L.n_units, gathered[1], st.master, st.param)        # writeback of the gathered buffer
+    st.reduce_scatter_adamw(g3, w.hp, step=2)
+    st.unshard(out=gathered[2])
+    fs.fsdp_reduce_scatter_clip_adamw(L, 0, L.n_units, g4, st.master, st.exp_avg, st.exp_avg_sq, st.param,
+                                      st.grad_out, 2e-3, ws, norm_out, w.hp, 3)
+    st.unshard(out=gathered[3])
+
+    # ---- the same chain in the oracle ----
+    def gather(om, op):
+        return oracle.unshard(sh, N, w.mode, op if bf16 else om, stride, F)
+
+    om, op = oracle.reshard(sh, N, w.mode, pu.f32(full0), stride, True, bf16)
+    m, v, go = np.zeros_like(om), np.zeros_like(om), np.zeros_like(om)
+    ref = [gather(om, op)]
+    racc = [np.zeros(F, np.float32) for _ in range(N)]
+    for first, micro in ((True, micro1), (False, micro2)):
+        for q, x in enumerate(pu.grads_np(micro)):
+            oracle.accumulate(racc[q], x, first)
+    oracle.rs_adamw(sh, N, w.mode, racc, stride, om, m, v, param=op, grad_out=go, hp=w.hp, step=1)
+    ref.append(gather(om, op))
+    om, op = oracle.reshard(sh, N, w.mode, ref[1], stride, True, bf16)
+    oracle.rs_adamw(sh, N, w.mode, pu.grads_np(g3), stride, om, m, v, param=op, grad_out=go, hp=w.hp, step=2)
+    ref.append(gather(om, op))
+    ref_norm = oracle.rs_clip_adamw(sh, N, w.mode, pu.grads_np(g4), stride, om, m, v, 2e-3, param=op,
+                                    grad_out=go, hp=w.hp, step=3)
+    ref.append(gather(om, op))
+
+    torch.cuda.synchronize()
+    fs.fsdp_check_status()
+    for k in range(3):                 # before the clipped step: bit for bit
+        got = pu.u16(gathered[k]) if bf16 else pu.f32(gathered[k]).view(np.uint32)
+        exp = ref[k] if bf16 else ref[k].view(np.uint32)
+        assert np.array_equal(got, exp), f"gathered buffer {k}"
+    # the clip coefficient comes from a norm summed in another order: within tolerance
+    assert norm_out[0].item() == pytest.approx(ref_norm, rel=1e-6)
+    if bf16:
+        pu.assert_bf16_close(pu.u16(gathered[3]), ref[3], "gathered buffer 3")
+        pu.assert_bf16_close(pu.u16(st.param).reshape(-1), op, "param")
+    else:
+        pu.assert_f32_close(pu.f32(gathered[3]), ref[3], "gathered buffer 3")
+    pu.assert_f32_close(pu.f32(st.master).reshape(-1), om, "master")
+    pu.assert_f32_close(pu.f32(st.exp_avg).reshape(-1), m, "exp_avg")
+    pu.assert_f32_close(pu.f32(st.exp_avg_sq).reshape(-1), v, "exp_avg_sq")
+    pu.assert_f32_close(pu.f32(st.grad_out).reshape(-1), go, "clipped gradient shard")
+
+
+@pytest.mark.parametrize("w,R", [(W([(300, 37), (13,), (64, 65)], [0, 0, 1], 4, synth.FLAT), 2),
+                                 (W([(512, 96), (96,)], [0, 0], 2, synth.FLAT, torch.float32), 3)])
+def test_hsdp_chain_vs_oracle(oracle_lib, rs_kind, w, R):
+    """HSDP step -> unshard of replica group 0 -> HSDP step -> unshard of group 0, one sync (the
+    views of the other groups need not start on a 16-byte boundary)."""
+    L = fs.Layout(w.shapes, w.unit_ids, w.N, w.mode)
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = pu.oracle_offsets(w)
+    N, stride, F = w.N, L.stride, L.info["full_numel"]
+    bf16 = w.param_dtype == torch.bfloat16
+    full = synth.full_params(w, F, O["t_full_off"])
+    master = torch.zeros(R, N, stride, dtype=torch.float32, device="cuda")
+    param = torch.zeros(R, N, stride, dtype=torch.bfloat16, device="cuda") if bf16 else None
+    fs.fsdp_reshard(L, 0, L.n_units, full, master[0], param[0] if bf16 else None)
+    for rho in range(1, R):
+        master[rho].copy_(master[0])
+        if bf16:
+            param[rho].copy_(param[0])
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    grads = [[synth.grad_replica(w, F, t, k) for k in range(R * N)] for t in (1, 2)]
+    outs = [torch.empty(F, dtype=w.param_dtype, device="cuda") for _ in range(2)]
+    src = param if bf16 else master
+    torch.cuda.synchronize()
+    try:
+        fs.fsdp_hsdp_reduce_scatter_adamw(L, 0, L.n_units, R, grads[0], master, m, v, param, w.hp, 1)
+    except fs.FsdpError as e:
+        if rs_kind == "staged" and e.status == -1:
+            pytest.skip("the staged HSDP kernel does not hold this case")
+        raise
+    fs.fsdp_unshard(L, 0, L.n_units, src[0], outs[0])
+    fs.fsdp_hsdp_reduce_scatter_adamw(L, 0, L.n_units, R, grads[1], master, m, v, param, w.hp, 2)
+    fs.fsdp_unshard(L, 0, L.n_units, src[0], outs[1])
+
+    om1, op1 = oracle.reshard(sh, N, w.mode, pu.f32(full), stride, True, bf16)
+    om = np.concatenate([om1] * R)
+    op = np.concatenate([op1] * R) if bf16 else None
+    rm, rv = np.zeros_like(om), np.zeros_like(om)
+    ref = []
+    for t in (1, 2):
+        oracle.hsdp_adamw(sh, N, w.mode, R, pu.grads_np(grads[t - 1]), stride, om, rm, rv, param=op, hp=w.hp,
+                          step=t)
+        rows = (op if bf16 else om).reshape(R, -1)[0]
+        ref.append(oracle.unshard(sh, N, w.mode, rows, stride, F))
+    torch.cuda.synchronize()
+    fs.fsdp_check_status()
+    for k in range(2):
+        got = pu.u16(outs[k]) if bf16 else pu.f32(outs[k]).view(np.uint32)
+        exp = ref[k] if bf16 else ref[k].view(np.uint32)
+        assert np.array_equal(got, exp), f"gathered buffer {k}"
+    pu.assert_f32_close(pu.f32(master).reshape(-1), om, "master")
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_zero1_chain_vs_oracle(oracle_lib, bf16):
+    """Three ZeRO-1 steps back to back: each owner's update reads what the step before
+    broadcast (its own fp32 replica) or wrote (its master), one sync."""
+    shapes, N = [(7, 5), (3,), (9, 2), (4, 4), (11,), (6, 6), (257, 33), (1 << 16,)], 4
+    L = fs.Layout(shapes, None, N, fs.FSDP_ZERO1)
+    sh = oracle.Shapes(shapes)
+    w = W(shapes, [0] * len(shapes), N, synth.DIM0, torch.bfloat16 if bf16 else torch.float32)
+    F, stride = L.info["full_numel"], L.stride
+    offs = [L.tensor(t)["full_off"] for t in range(len(shapes))]
+    full = synth.full_params(w, F, offs)
+    master = torch.zeros(N, stride, dtype=torch.float32, device="cuda") if bf16 else None
+    if bf16:
+        fs.fsdp_reshard(L, 0, L.n_units, full, master, None)
+    m = torch.zeros(N, stride, dtype=torch.float32, device="cuda")
+    v = torch.zeros_like(m)
+    params = [full.to(w.param_dtype).clone() for _ in range(N)]
+    grads = [synth.grad_replicas(w, F, t) for t in (1, 2, 3)]
+    ref_params = [pu.u16(p) if bf16 else pu.f32(p) for p in params]
+    rmaster = None
+    if bf16:
+        rmaster = pu.f32(master).reshape(-1).copy()
+    torch.cuda.synchronize()
+    for t in (1, 2, 3):
+        fs.fsdp_zero1_adamw_broadcast(L, 0, L.n_units, grads[t - 1], master, m, v, params, w.hp, t)
+    rm = np.zeros(N * stride, np.float32)
+    rv = np.zeros_like(rm)
+    owners = oracle.zero1_owners(sh, N)
+    assert [L.owner(t) for t in range(len(shapes))] == list(owners)
+    ometa = [L.tensor(t) for t in range(len(shapes))]
+    # the oracle packs each owner's tensors back to back; the library keeps each at an
+    # offset congruent to its full offset: map the library's rows onto the oracle's
+    sizes = [int(np.prod(s)) for s in shapes]
+    fill, o_off = [0] * N, []
+    for t, o in enumerate(owners):
+        o_off.append(fill[o])
+        fill[o] += sizes[t]
+    ostride = max(max(fill), 1)
+    om = np.zeros(N * ostride, np.float32) if bf16 else None
+    if bf16:
+        for t, o in enumerate(owners):
+            a = o * stride + ometa[t]["shard_off"]
+            om[o * ostride + o_off[t]:o * ostride + o_off[t] + sizes[t]] = rmaster[a:a + sizes[t]]
+    orm, orv = np.zeros(N * ostride, np.float32), np.zeros(N * ostride, np.float32)
+    for t in (1, 2, 3):
+        ref_params = oracle.zero1_adamw(sh, N, pu.grads_np(grads[t - 1]), ostride, om, orm, orv, ref_params,
+                                        hp=w.hp, step=t)
+    torch.cuda.synchronize()
+    fs.fsdp_check_status()
+    for q in range(N):
+        if bf16:
+            pu.assert_bf16_close(pu.u16(params[q]), ref_params[q], f"replica {q}")
+        else:
+            pu.assert_f32_close(pu.f32(params[q]), ref_params[q], f"replica {q}")
+    got_m = pu.f32(m).reshape(-1)
+    for t, o in enumerate(owners):
+        a = o * stride + ometa[t]["shard_off"]
+        b = o * ostride + o_off[t]
+        pu.assert_f32_close(got_m[a:a + sizes[t]], orm[b:b + sizes[t]], f"exp_avg of tensor {t}")
