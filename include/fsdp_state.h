@@ -33,7 +33,10 @@
  *     small per-device copy of its segment tables.
  *   - Streams: fsdp_stream_t is a cudaStream_t (NULL = legacy default stream).
  *     Launch calls are asynchronous and never synchronize; only
- *     fsdp_check_status and fsdp_layout_prepare block.
+ *     fsdp_check_status and fsdp_layout_prepare block.  Kernels are launched as
+ *     programmatic dependents of the work before them on the stream: each waits,
+ *     before touching memory, for that work to complete, so stream order is kept
+ *     exactly; only the launch latency between consecutive kernels is hidden.
  *   - Shard arrays are [N][stride] row-major: rank r's shard starts at element
  *     r*stride; stride = fsdp_layout_info.shard_stride >= S.  The layout picks
  *     stride mod 8 so that as many rank views as possible sit at a shard index
@@ -260,10 +263,11 @@ int fsdp_layout_owner(const fsdp_layout* layout, int32_t tensor, int32_t* rank);
  * coef = min(1, max_norm / (norm + 1e-6)), formed in double and rounded to fp32
  * once; each reduced gradient is multiplied by it (one fp32 rounding) and then
  * goes through the AdamW and bf16 steps of fsdp_reduce_scatter_adamw.
- * Three kernels on `stream`: the reduce-scatter writes the fp32 gradient shard and
+ * Two passes on `stream`: the reduce-scatter writes the fp32 gradient shard and
  * per-CTA partial sums of squares (fixed order, so the norm is reproducible on a
- * given GPU), one CTA adds the partials in double, the update pass scales the
- * shard and runs AdamW.
+ * given GPU); the update pass adds the partials in double (every CTA in the same
+ * order), forms the coefficient, scales the shard and runs AdamW.  (With the
+ * staged kernels forced, one extra single-CTA kernel forms the norm between them.)
  *   grad_shard  required device [N][stride] fp32: receives the CLIPPED reduced
  *               gradient (padding +0); it is also the working buffer.
  *   max_norm    > 0 and finite.
