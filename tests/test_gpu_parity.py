@@ -2,9 +2,11 @@
 
 Small layouts are compared element by element over the whole state after every
 step; the full-size 4-block Llama (809.5M parameters, N=8) and the FSDP2 dim-0
-group (243M, N=6) are run at full size in the bench's launch configuration and
-compared on sampled positions (every edge of every rank's view, plus 200k random
-positions) that the oracle tracks across the steps.
+group (243M, N=6) are run at full size and compared on sampled positions (every
+edge of every rank's view, plus 200k random positions) that the oracle tracks
+across the steps.  Most runs also request the reduced-gradient output; the last
+tests run the configurations bench.py times (no such output, so the kernel
+instance the bench launches) at full size.
 """
 import pytest
 import torch
@@ -65,3 +67,19 @@ def test_sweep_small_full_compare(oracle_lib, P, N):
 @pytest.mark.parametrize("P,N", [((1 << 26) + 1, 8), ((1 << 29) + 1, 32), (1 << 29, 2)])
 def test_sweep_large_sampled(oracle_lib, P, N):
     pu.run_sampled_parity(synth.sweep(P, N), n_random=100_000)
+
+
+# ---------------------------------------------------------------------------
+# The configurations bench.py times: no reduced-gradient output (the kernel instance
+# without it), the default kernel choice, FULL_SHARD.
+def test_mlp128m_bench_config(oracle_lib):
+    w = synth.mlp128m()
+    _, ulps = pu.run_full_parity(w, steps=3, with_grad_out=False)
+    print("mlp128m (bench configuration) ulps per step", ulps)
+
+
+@pytest.mark.parametrize("name", ["llama4", "dim0_n6", "sweep_P268435457_N8", "sweep_P67108865_N32"])
+def test_bench_config_full_size_sampled(oracle_lib, name):
+    w = synth.workload(name)
+    _, ulps = pu.run_sampled_parity(w, steps=min(w.steps, 2), n_random=100_000, with_grad_out=False)
+    print(name, "(bench configuration) ulps per step", ulps)
