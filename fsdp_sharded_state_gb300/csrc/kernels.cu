@@ -49,27 +49,7 @@ __device__ __forceinline__ void rs_tile_f32_split(const Seg& sg, int64_t gt, con
         const float4 ma = ld4(exp_avg + x0), mb = ld4(exp_avg + x1);
         const float4 va = ld4(exp_avg_sq + x0), vb = ld4(exp_avg_sq + x1);
         float acc[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-#pragma unroll 1
-        for (int q0 = 0; q0 < N; q0 += 2) {                 // 2 replicas x 2 chunks in flight
-            uint4 ga[2], gb[2];
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-                if (q0 + b < N) {
-                    const float* g = static_cast<const float*>(gp.p[q0 + b]);
-                    ga[b] = ld_once(g + x0 + delta);
-                    gb[b] = ld_once(g + x1 + delta);
-                }
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-                if (q0 + b < N) {
-                    acc[0] = __fadd_rn(acc[0], __uint_as_float(ga[b].x)); acc[1] = __fadd_rn(acc[1], __uint_as_float(ga[b].y));
-                    acc[2] = __fadd_rn(acc[2], __uint_as_float(ga[b].z)); acc[3] = __fadd_rn(acc[3], __uint_as_float(ga[b].w));
-                    acc[4] = __fadd_rn(acc[4], __uint_as_float(gb[b].x)); acc[5] = __fadd_rn(acc[5], __uint_as_float(gb[b].y));
-                    acc[6] = __fadd_rn(acc[6], __uint_as_float(gb[b].z)); acc[7] = __fadd_rn(acc[7], __uint_as_float(gb[b].w));
-                }
-        }
+        reduce_split_f32(gp, N, x0 + delta, x1 + delta, acc);
         // compute and store one 4-element chunk at a time (fewer live registers)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {

@@ -79,38 +79,6 @@ __device__ __forceinline__ double block_sum(double x) {
 // and the coefficient itself (every CTA sums the partials in the same order),
 // which saves the launch of step (2).
 // ---------------------------------------------------------------------------
-// Sum, in rank order, of the N fp32 replicas at the two 4-element chunks a lane owns
-// under the "split" mapping (full-layout offsets fa and fb, 16-byte aligned): acc[0..3]
-// for fa, acc[4..7] for fb; 2 replicas x 2 chunks in flight.
-__device__ __forceinline__ void reduce_split_f32(const GradPtrs& gp, int N, int64_t fa, int64_t fb,
-                                                 float (&acc)[8]) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-#pragma unroll 1
-    for (int q0 = 0; q0 < N; q0 += 2) {
-        uint4 ga[2], gb[2];
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-            if (q0 + b < N) {
-                const float* g = static_cast<const float*>(gp.p[q0 + b]);
-                ga[b] = ld_once(g + fa);
-                gb[b] = ld_once(g + fb);
-            }
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-            if (q0 + b < N) {
-                acc[0] = __fadd_rn(acc[0], __uint_as_float(ga[b].x));
-                acc[1] = __fadd_rn(acc[1], __uint_as_float(ga[b].y));
-                acc[2] = __fadd_rn(acc[2], __uint_as_float(ga[b].z));
-                acc[3] = __fadd_rn(acc[3], __uint_as_float(ga[b].w));
-                acc[4] = __fadd_rn(acc[4], __uint_as_float(gb[b].x));
-                acc[5] = __fadd_rn(acc[5], __uint_as_float(gb[b].y));
-                acc[6] = __fadd_rn(acc[6], __uint_as_float(gb[b].z));
-                acc[7] = __fadd_rn(acc[7], __uint_as_float(gb[b].w));
-            }
-    }
-}
-
 // Pass 1 for fp32 gradients on aligned segments, split lane mapping (each 16-byte
 // load or store of a warp covers 512 contiguous bytes): the reduced gradient into
 // the shard, and the lane's sum of squares (fp32 over its 8 elements in order, then
