@@ -378,5 +378,5 @@ def fsdp_error_string(status: int) -> str:
     return lib().fsdp_error_string(status).decode()
 
 
-from .state import ShardedState  # noqa: E402  (harness over the calls above)
+from .state import ShardedState, step_schedule  # noqa: E402  (harness over the calls above)
 from .hostfeed import HostFeed  # noqa: E402  (host-fed steps over ShardedState)

@@ -24,6 +24,24 @@ from . import (FSDP_BF16, FSDP_F32, FSDP_FLAT, Layout, fsdp_reduce_scatter_adamw
 STRATEGIES = {"full_shard": 2, "shard_grad_op": 1}   # all-gathers per step
 
 
+def step_schedule(n_units: int, strategy: str = "full_shard"):
+    """The per-unit collectives of one step, in the order FSDP issues them, as
+    ("all_gather", u) / ("reduce_scatter", u) pairs.  Forward gathers every unit in
+    order; backward visits the units in reverse, and under FULL_SHARD gathers each
+    one again first (the forward freed it), then reduce-scatters its gradient;
+    SHARD_GRAD_OP keeps the forward gather through backward ("NCCL ZeRO/FSDP state
+    sharding", sections "ZeRO-2 方向" and "ZeRO-3 方向": with 8 wrap units, 8 + 0
+    all-gathers and 8 reduce-scatters, and 8 + 8 all-gathers and 8 reduce-scatters)."""
+    if strategy not in STRATEGIES:
+        raise ValueError(f"unknown strategy {strategy!r}")
+    sched = [("all_gather", u) for u in range(n_units)]
+    for u in reversed(range(n_units)):
+        if strategy == "full_shard":
+            sched.append(("all_gather", u))
+        sched.append(("reduce_scatter", u))
+    return sched
+
+
 class ShardedState:
     def __init__(self, shapes: Sequence[Sequence[int]], unit_ids: Optional[Sequence[int]], n_ranks: int,
                  mode: int = FSDP_FLAT, param_dtype: torch.dtype = torch.bfloat16, device="cuda",
@@ -78,6 +96,19 @@ class ShardedState:
         for _ in range(STRATEGIES[strategy]):
             self.unshard(stream=stream)
         self.reduce_scatter_adamw(grads, hp, stream=stream)
+
+    def step_per_unit(self, grads, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), strategy: str = "full_shard",
+                      stream=None) -> None:
+        """The same step issued unit by unit, in step_schedule's order: one library call
+        per collective of the pages' per-unit FSDP schedule, every reduce-scatter with
+        the same step number.  Same results as step(), bit for bit."""
+        t = self.t + 1
+        for kind, u in step_schedule(self.layout.n_units, strategy):
+            if kind == "all_gather":
+                self.unshard(u, u + 1, stream=stream)
+            else:
+                self.reduce_scatter_adamw(grads, hp, step=t, ub=u, ue=u + 1, stream=stream)
+        self.t = t
 
     def launch_counts(self, grad_dtype: torch.dtype = torch.bfloat16) -> dict:
         """Kernels one call launches.  The all-gather and the direct reduce-scatter

@@ -223,3 +223,29 @@ def test_zero1_chain_vs_oracle(oracle_lib, bf16):
         a = o * stride + ometa[t]["shard_off"]
         b = o * ostride + o_off[t]
         pu.assert_f32_close(got_m[a:a + sizes[t]], orm[b:b + sizes[t]], f"exp_avg of tensor {t}")
+
+
+@pytest.mark.parametrize("strategy", ["full_shard", "shard_grad_op"])
+@pytest.mark.parametrize("w", [W([(256, 64)] * 8, list(range(8)), 4, synth.FLAT, torch.float32),
+                               W([(300, 37), (13,), (64, 65), (129, 7), (5,)], [0, 1, 1, 2, 3], 8, synth.FLAT),
+                               W([(130, 64), (7,), (9, 3)], [0, 0, 0], 6, synth.DIM0)])
+def test_per_unit_step_equals_whole_range(oracle_lib, w, strategy):
+    """The step issued unit by unit in FSDP's collective order (ShardedState.step_per_unit)
+    gives the whole-range step's results bit for bit, over two steps."""
+    a, b = pu.make_state(w), pu.make_state(w)
+    O = pu.oracle_offsets(w)
+    full = synth.full_params(w, a.F, O["t_full_off"])
+    a.init_from_full(full)
+    b.init_from_full(full)
+    for t in (1, 2):
+        grads = [g.to(w.grad_dtype) for g in synth.grad_replicas(w, a.F, t)]
+        a.step(grads, w.hp, strategy=strategy)
+        b.step_per_unit(grads, w.hp, strategy=strategy)
+    torch.cuda.synchronize()
+    assert a.t == b.t == 2
+    for x, y, what in ((a.master, b.master, "master"), (a.exp_avg, b.exp_avg, "exp_avg"),
+                       (a.exp_avg_sq, b.exp_avg_sq, "exp_avg_sq"), (a.full, b.full, "gathered buffer")):
+        assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16),
+                           y.view(torch.int32) if y.dtype == torch.float32 else y.view(torch.int16)), what
+    if a.param is not None:
+        assert torch.equal(a.param.view(torch.int16), b.param.view(torch.int16)), "param"
