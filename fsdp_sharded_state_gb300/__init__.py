@@ -33,7 +33,8 @@ EXPORTS = ("fsdp_layout_create", "fsdp_layout_destroy", "fsdp_layout_query", "fs
            "fsdp_error_string", "fsdp_last_cuda_error", "fsdp_reduce_scatter_adamw_noalloc",
            "fsdp_layout_owner", "fsdp_clip_workspace_bytes", "fsdp_reduce_scatter_clip_adamw",
            "fsdp_accumulate_grads", "fsdp_hsdp_reduce_scatter_adamw", "fsdp_zero1_adamw_broadcast",
-           "fsdp_set_rs_kernel", "fsdp_rs_kernel_for", "fsdp_wait_selftest")
+           "fsdp_set_rs_kernel", "fsdp_rs_kernel_for", "fsdp_wait_selftest", "fsdp_adamw_step_consts_make",
+           "fsdp_reduce_scatter_adamw_consts", "fsdp_adamw_step_consts_upload")
 
 
 class FsdpError(RuntimeError):
@@ -54,6 +55,13 @@ class LayoutInfo(C.Structure):
 class AdamWHparams(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
                 ("weight_decay", C.c_float)]
+
+
+class AdamWStepConsts(C.Structure):
+    """The 48-byte block of per-step AdamW constants (fsdp_adamw_step_consts)."""
+    _fields_ = [("decay", C.c_float), ("om1", C.c_float), ("om2", C.c_float), ("step_size", C.c_float),
+                ("bc2s", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
+                ("n_avg", C.c_float), ("reserved", C.c_float * 3)]
 
 
 _lib: Optional[C.CDLL] = None
@@ -96,6 +104,9 @@ def lib() -> C.CDLL:
         L.fsdp_set_rs_kernel.argtypes = [i32]
         L.fsdp_rs_kernel_for.argtypes = [vp, i32]
         L.fsdp_wait_selftest.argtypes = [i64, vp]
+        L.fsdp_adamw_step_consts_make.argtypes = [vp, C.POINTER(AdamWHparams), i64, C.POINTER(AdamWStepConsts)]
+        L.fsdp_reduce_scatter_adamw_consts.argtypes = [vp, i32, i32, C.POINTER(vp), i32, vp, vp, vp, vp, vp, vp, vp]
+        L.fsdp_adamw_step_consts_upload.argtypes = [vp, vp, vp]
         L.fsdp_error_string.argtypes = [C.c_int]
         L.fsdp_error_string.restype = C.c_char_p
         L.fsdp_last_cuda_error.argtypes = []
@@ -270,6 +281,38 @@ def fsdp_reduce_scatter_adamw_noalloc(layout: Layout, unit_begin: int, unit_end:
                                                    _stream(stream)), "fsdp_reduce_scatter_adamw_noalloc")
 
 
+def fsdp_adamw_step_consts_make(layout: Layout, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step: int = 1) -> AdamWStepConsts:
+    """The step's AdamW constants as the fused step forms them (host only)."""
+    out = AdamWStepConsts()
+    h = hp if isinstance(hp, AdamWHparams) else AdamWHparams(*hp)
+    _check(lib().fsdp_adamw_step_consts_make(layout.handle, C.byref(h), step, C.byref(out)),
+           "fsdp_adamw_step_consts_make")
+    return out
+
+
+def fsdp_adamw_step_consts_upload(dev_dst, host_src, stream=None) -> None:
+    """Copies a 48-byte block of step constants from (pinned) host memory to the device
+    block on the stream; inside a CUDA graph capture it reads host_src at every replay."""
+    _check(lib().fsdp_adamw_step_consts_upload(_ptr(dev_dst), _ptr(host_src), _stream(stream)),
+           "fsdp_adamw_step_consts_upload")
+
+
+def fsdp_reduce_scatter_adamw_consts(layout: Layout, unit_begin: int, unit_end: int, grad_replicas, master,
+                                     exp_avg, exp_avg_sq, param_shards=None, grad_shard_out=None, consts=None,
+                                     stream=None, grad_dtype: Optional[int] = None) -> None:
+    """fsdp_reduce_scatter_adamw with the step constants read on the device from `consts`
+    (a 48-byte device buffer, e.g. a float32 tensor of 12 elements)."""
+    if len(grad_replicas) != layout.N:
+        raise ValueError(f"need {layout.N} gradient replicas, got {len(grad_replicas)}")
+    if grad_dtype is None:
+        grad_dtype = _dtype_code(grad_replicas[0])
+    arr = (C.c_void_p * layout.N)(*[_ptr(g) for g in grad_replicas])
+    _check(lib().fsdp_reduce_scatter_adamw_consts(layout.handle, unit_begin, unit_end, arr, grad_dtype,
+                                                  _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+                                                  _ptr(param_shards), _ptr(grad_shard_out), _ptr(consts),
+                                                  _stream(stream)), "fsdp_reduce_scatter_adamw_consts")
+
+
 def _ptr_array(xs):
     return (C.c_void_p * len(xs))(*[_ptr(x) for x in xs])
 
@@ -378,5 +421,5 @@ def fsdp_error_string(status: int) -> str:
     return lib().fsdp_error_string(status).decode()
 
 
-from .state import ShardedState, step_schedule  # noqa: E402  (harness over the calls above)
+from .state import ShardedState, StepGraph, step_schedule  # noqa: E402  (harness over the calls above)
 from .hostfeed import HostFeed  # noqa: E402  (host-fed steps over ShardedState)

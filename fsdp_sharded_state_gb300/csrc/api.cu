@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -126,6 +127,37 @@ AdamScal adam_scalars(const fsdp_adamw_hparams* hp, int64_t step, int32_t n_avg)
     sc.nf = float(n_avg);
     return sc;
 }
+
+// The buffer and layout checks of the fused step (hyper-parameters aside), in the
+// order the fused entry points apply them.
+int check_rs_buffers(const fsdp_layout* L, int32_t ub, int32_t ue, const void* const* grads, int32_t grad_dtype,
+                     const float* master, const float* exp_avg, const float* exp_avg_sq, const void* param_shards,
+                     const float* grad_shard_out) {
+    int rc = check_units(L, ub, ue);
+    if (rc) return rc;
+    if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if (!grads) return FSDP_EINVAL;
+    for (int32_t q = 0; q < L->N; ++q)
+        if ((rc = check_ptr(grads[q]))) return rc;
+    if ((rc = check_ptr(master)) || (rc = check_ptr(exp_avg)) || (rc = check_ptr(exp_avg_sq))) return rc;
+    if (param_shards && !aligned16(param_shards)) return FSDP_EALIGN;
+    if (grad_shard_out && !aligned16(grad_shard_out)) return FSDP_EALIGN;
+    if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;
+    return FSDP_OK;
+}
+
+// The device block of the step constants is read by the kernels as an AdamScal.
+static_assert(sizeof(fsdp_adamw_step_consts) == 48, "step constants block");
+static_assert(offsetof(fsdp_adamw_step_consts, decay) == offsetof(AdamScal, decay) &&
+                  offsetof(fsdp_adamw_step_consts, om1) == offsetof(AdamScal, om1) &&
+                  offsetof(fsdp_adamw_step_consts, om2) == offsetof(AdamScal, om2) &&
+                  offsetof(fsdp_adamw_step_consts, step_size) == offsetof(AdamScal, step_size) &&
+                  offsetof(fsdp_adamw_step_consts, bc2s) == offsetof(AdamScal, bc2s) &&
+                  offsetof(fsdp_adamw_step_consts, beta1) == offsetof(AdamScal, beta1) &&
+                  offsetof(fsdp_adamw_step_consts, beta2) == offsetof(AdamScal, beta2) &&
+                  offsetof(fsdp_adamw_step_consts, eps) == offsetof(AdamScal, eps) &&
+                  offsetof(fsdp_adamw_step_consts, n_avg) == offsetof(AdamScal, nf),
+              "step constants block matches AdamScal");
 
 }  // namespace detail
 }  // namespace fsdp
@@ -302,17 +334,11 @@ int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, cons
                               void* param_shards, float* grad_shard_out, const fsdp_adamw_hparams* hp,
                               int64_t step, fsdp_stream_t stream) {
     fsdp::detail::NvtxRange nvtx_range("fsdp_reduce_scatter_adamw");
-    int rc = check_units(L, ub, ue);
+    int rc = check_rs_buffers(L, ub, ue, grads, grad_dtype, master, exp_avg, exp_avg_sq, param_shards,
+                              grad_shard_out);
     if (rc) return rc;
-    if (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16) return FSDP_EDTYPE;
-    if (!grads || !hp || step < 1) return FSDP_EINVAL;
-    for (int32_t q = 0; q < L->N; ++q)
-        if ((rc = check_ptr(grads[q]))) return rc;
-    if ((rc = check_ptr(master)) || (rc = check_ptr(exp_avg)) || (rc = check_ptr(exp_avg_sq))) return rc;
-    if (param_shards && !aligned16(param_shards)) return FSDP_EALIGN;
-    if (grad_shard_out && !aligned16(grad_shard_out)) return FSDP_EALIGN;
+    if (!hp || step < 1) return FSDP_EINVAL;
     if ((rc = check_hparams(hp))) return rc;
-    if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;
     const fsdp::AdamScal sc = adam_scalars(hp, step, L->N);
 
     fsdp::GradPtrs gp{};
@@ -338,6 +364,66 @@ int fsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, cons
             if (e != cudaSuccess) return cuda_fail(e, "k_rs_adamw launch");
         }
     }
+    if (grad_shard_out) {
+        const Range P = range_of(L->pad, base, ub, ue);
+        e = fsdp::launch_zero_pad(P.segs, P.tile_base, P.n_tiles, grad_shard_out, nullptr, st);
+        if (e != cudaSuccess) return cuda_fail(e, "k_zero_pad launch");
+    }
+    return FSDP_OK;
+}
+
+int fsdp_adamw_step_consts_make(const fsdp_layout* L, const fsdp_adamw_hparams* hp, int64_t step,
+                                fsdp_adamw_step_consts* out) {
+    if (!L || !hp || !out || step < 1) return FSDP_EINVAL;
+    const int rc = check_hparams(hp);
+    if (rc) return rc;
+    const fsdp::AdamScal sc = adam_scalars(hp, step, L->N);
+    fsdp_adamw_step_consts c{};
+    c.decay = sc.decay;
+    c.om1 = sc.om1;
+    c.om2 = sc.om2;
+    c.step_size = sc.step_size;
+    c.bc2s = sc.bc2s;
+    c.beta1 = sc.beta1;
+    c.beta2 = sc.beta2;
+    c.eps = sc.eps;
+    c.n_avg = sc.nf;
+    *out = c;
+    return FSDP_OK;
+}
+
+int fsdp_adamw_step_consts_upload(fsdp_adamw_step_consts* dev_dst, const fsdp_adamw_step_consts* host_src,
+                                  fsdp_stream_t stream) {
+    int rc = check_ptr(dev_dst);
+    if (rc) return rc;
+    if (!host_src) return FSDP_EINVAL;
+    const cudaError_t e = cudaMemcpyAsync(dev_dst, host_src, sizeof(fsdp_adamw_step_consts), cudaMemcpyHostToDevice,
+                                          reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "cudaMemcpyAsync(step constants)");
+}
+
+int fsdp_reduce_scatter_adamw_consts(const fsdp_layout* L, int32_t ub, int32_t ue, const void* const* grads,
+                                     int32_t grad_dtype, float* master, float* exp_avg, float* exp_avg_sq,
+                                     void* param_shards, float* grad_shard_out, const fsdp_adamw_step_consts* consts,
+                                     fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_reduce_scatter_adamw_consts");
+    int rc = check_rs_buffers(L, ub, ue, grads, grad_dtype, master, exp_avg, exp_avg_sq, param_shards,
+                              grad_shard_out);
+    if (rc) return rc;
+    if ((rc = check_ptr(consts))) return rc;
+    const bool bf16 = grad_dtype == FSDP_BF16;
+    if (!fsdp::staged_fits(L->N, bf16)) return FSDP_EINVAL;
+    fsdp::GradPtrs gp{};
+    for (int32_t q = 0; q < L->N; ++q) gp.p[q] = grads[q];
+    const Seg* base = nullptr;
+    if ((rc = device_tables(L, &base))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const Range R = range_of(L->data, base, ub, ue);
+    const fsdp::AdamScal unused{};   // the kernel reads the device block instead
+    cudaError_t e = fsdp::launch_rs_adamw_staged(R.segs, R.tile_base, R.n_tiles, bf16, gp, L->N, master, exp_avg,
+                                                 exp_avg_sq, static_cast<uint16_t*>(param_shards), grad_shard_out,
+                                                 unused, kWaitNs, st, reinterpret_cast<const fsdp::AdamScal*>(consts));
+    if (e != cudaSuccess) return cuda_fail(e, "k_rs_adamw_staged launch");
     if (grad_shard_out) {
         const Range P = range_of(L->pad, base, ub, ue);
         e = fsdp::launch_zero_pad(P.segs, P.tile_base, P.n_tiles, grad_shard_out, nullptr, st);

@@ -25,7 +25,18 @@ struct Sum4 {
     float a0, a1, a2, a3;
 };
 
-template <typename GT, bool PARAM, bool GOUT>
+// A consumer thread's carry when the step constants come from device memory: the
+// partial sums, and the constants, read once at the thread's first item.
+struct SumConsts {
+    Sum4 sum;
+    AdamScal s;
+    int ready;
+};
+
+// DC: the step's AdamW constants are read from device memory (dsc), once per
+// consumer thread, instead of taken from the kernel argument (sc), so that a
+// captured CUDA graph can replay the launch with the constants rewritten in between.
+template <typename GT, bool PARAM, bool GOUT, bool DC = false>
 struct RsAdamw {
     static constexpr bool kGeomFirst = true;
     const Seg* segs;
@@ -36,8 +47,9 @@ struct RsAdamw {
     uint16_t* param;
     float* gout;
     AdamScal sc;
+    const AdamScal* dsc;
 
-    using Carry = Sum4;
+    using Carry = typename std::conditional<DC, SumConsts, Sum4>::type;
     __device__ int groups() const { return NG; }
     __device__ int q0(const TileGeom& g) const { return g.q * Q; }
     __device__ int nq(const TileGeom& g) const { return (N - g.q * Q) < Q ? (N - g.q * Q) : Q; }
@@ -71,6 +83,19 @@ struct RsAdamw {
     }
     template <class Release>
     __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry& carry, Release release) const {
+        if constexpr (DC) {
+            if (!carry.ready) {
+                carry.s = *dsc;
+                carry.ready = 1;
+            }
+            return consume_with(carry.s, g, sb, tid, carry.sum, release);
+        } else {
+            return consume_with(sc, g, sb, tid, carry, release);
+        }
+    }
+    template <class Release>
+    __device__ double consume_with(const AdamScal& sc, const TileGeom& g, const unsigned char* sb, int tid,
+                                   Sum4& carry, Release release) const {
         const int c = tid * 4;
         const int64_t x = g.t0 + c, f = x + g.delta;
         const bool live = x + 4 > g.s0 && x < g.s1;
@@ -129,9 +154,9 @@ struct RsAdamw {
     __device__ void finish(int, double) const {}
 };
 
-template <typename GT, bool PARAM, bool GOUT>
+template <typename GT, bool PARAM, bool GOUT, bool DC>
 __global__ void __launch_bounds__(kStThreads + 32, 1)
-k_rs_adamw_staged(RsAdamw<GT, PARAM, GOUT> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
+k_rs_adamw_staged(RsAdamw<GT, PARAM, GOUT, DC> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
     run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
 }
 
@@ -165,7 +190,8 @@ bool staged_fits(int N, bool grad_bf16) {
 
 cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
                                    const GradPtrs& gp, int N, float* master, float* m, float* v, uint16_t* param,
-                                   float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st) {
+                                   float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st,
+                                   const AdamScal* dsc) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -175,8 +201,12 @@ cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n
     auto go = [&](auto tag_gt, auto tag_p, auto tag_g) {
         using GT = decltype(tag_gt);
         constexpr bool P = decltype(tag_p)::value, O = decltype(tag_g)::value;
-        RsAdamw<GT, P, O> pol{segs, tile_base, gp, N, Q, NG, master, m, v, param, gout, sc};
-        return launch_pipeline(k_rs_adamw_staged<GT, P, O>, pol, n_tiles, sb, wait_ns, st);
+        if (dsc) {
+            RsAdamw<GT, P, O, true> pol{segs, tile_base, gp, N, Q, NG, master, m, v, param, gout, sc, dsc};
+            return launch_pipeline(k_rs_adamw_staged<GT, P, O, true>, pol, n_tiles, sb, wait_ns, st);
+        }
+        RsAdamw<GT, P, O, false> pol{segs, tile_base, gp, N, Q, NG, master, m, v, param, gout, sc, nullptr};
+        return launch_pipeline(k_rs_adamw_staged<GT, P, O, false>, pol, n_tiles, sb, wait_ns, st);
     };
     using T = std::true_type;
     using F = std::false_type;

@@ -30,7 +30,8 @@ int norm_staged_partials(int64_t n_tiles);
 // bounds every mbarrier wait.
 cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
                                    const GradPtrs& gp, int N, float* master, float* m, float* v, uint16_t* param,
-                                   float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st);
+                                   float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st,
+                                   const AdamScal* dsc = nullptr);   // dsc: constants read on the device
 
 // HSDP: replicas gp.p[rho*N + q]; state copy rho at element offset rho * copy; rf = R.
 cudaError_t launch_hsdp_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,

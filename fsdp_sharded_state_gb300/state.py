@@ -14,12 +14,14 @@ are given as N full-layout replicas, one per simulated rank.
 """
 from __future__ import annotations
 
+import ctypes
 from typing import Optional, Sequence
 
 import torch
 
-from . import (FSDP_BF16, FSDP_F32, FSDP_FLAT, Layout, fsdp_reduce_scatter_adamw, fsdp_reshard,
-               fsdp_rs_kernel_for, fsdp_unshard)
+from . import (FSDP_BF16, FSDP_F32, FSDP_FLAT, Layout, fsdp_adamw_step_consts_make, fsdp_adamw_step_consts_upload,
+               fsdp_reduce_scatter_adamw, fsdp_reduce_scatter_adamw_consts, fsdp_reshard, fsdp_rs_kernel_for,
+               fsdp_unshard)
 
 STRATEGIES = {"full_shard": 2, "shard_grad_op": 1}   # all-gathers per step
 
@@ -141,3 +143,77 @@ class ShardedState:
         """Kernel launches of one step (for a launch count)."""
         c = self.launch_counts(grad_dtype)
         return STRATEGIES[strategy] * c["unshard"] + c["reduce_scatter_adamw"]
+
+
+class StepGraph:
+    """One sharded step captured in CUDA graphs and replayed step after step.
+
+    For layouts small enough that issuing a step's library calls takes the host longer
+    than the GPU takes to run them (the 4,192-parameter MLP: about 33 us of host work
+    for a step the GPU runs in about 10 us), the step's kernels are captured once and
+    each step is one graph launch.  The fused update reads its AdamW step constants
+    from a 48-byte device block (fsdp_reduce_scatter_adamw_consts); each graph starts
+    with a copy of that block from a pinned host block (fsdp_adamw_step_consts_upload), which step() fills with the
+    step's constants (fsdp_adamw_step_consts_make) before the replay.  n_blocks host
+    blocks, each with its own graph, take turns, so the host rewrites a block only once
+    the replay that copied it has run: it runs at most n_blocks steps ahead.
+
+    The first step() runs the same calls eagerly (it also sets up the library's
+    per-kernel launch state, which must not happen during capture); the graphs are
+    captured right after it.  Buffers are fixed at construction: the step reads
+    `grads` every time, as a training loop that refills them in place would.  Same
+    results as ShardedState.step, bit for bit."""
+
+    def __init__(self, state: ShardedState, grads, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), strategy: str = "full_shard",
+                 n_blocks: int = 3):
+        if strategy not in STRATEGIES:
+            raise ValueError(f"unknown strategy {strategy!r}")
+        if n_blocks < 1:
+            raise ValueError("n_blocks must be >= 1")
+        self.st, self.grads, self.hp, self.strategy = state, list(grads), hp, strategy
+        dev = state.full.device
+        self.dev_consts = torch.zeros(12, dtype=torch.float32, device=dev)
+        self.host = [torch.zeros(12, dtype=torch.float32).pin_memory() for _ in range(n_blocks)]
+        self.done = [None] * n_blocks
+        self.graphs = None
+        self.k = 0
+        state.layout.prepare()
+
+    def _calls(self, b: int) -> None:
+        st = self.st
+        fsdp_adamw_step_consts_upload(self.dev_consts, self.host[b])
+        for _ in range(STRATEGIES[self.strategy]):
+            st.unshard()
+        fsdp_reduce_scatter_adamw_consts(st.layout, 0, st.layout.n_units, self.grads, st.master, st.exp_avg,
+                                         st.exp_avg_sq, st.param, st.grad_out, consts=self.dev_consts)
+
+    def _capture(self) -> None:
+        torch.cuda.synchronize(self.st.full.device)
+        graphs = []
+        for b in range(len(self.host)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                self._calls(b)
+            graphs.append(g)
+        self.graphs = graphs
+
+    def step(self) -> None:
+        """One step: the next step number's constants into a host block, then the graph
+        that copies that block and runs the step (on the current stream)."""
+        b = self.k % len(self.host)
+        if self.done[b] is not None:
+            self.done[b].synchronize()           # the replay that last read block b has run
+        t = self.st.t + 1
+        c = fsdp_adamw_step_consts_make(self.st.layout, self.hp, t)
+        ctypes.memmove(self.host[b].data_ptr(), ctypes.addressof(c), ctypes.sizeof(c))
+        if self.graphs is None:
+            self._calls(b)
+            torch.cuda.current_stream().synchronize()
+            self._capture()
+        else:
+            self.graphs[b].replay()
+        ev = torch.cuda.Event()
+        ev.record()
+        self.done[b] = ev
+        self.st.t = t
+        self.k += 1

@@ -374,6 +374,49 @@ int fsdp_rs_kernel_for(const fsdp_layout* layout, int32_t grad_dtype);
  * records a wait that gives up the same way (limit: 1 s per wait). */
 int fsdp_wait_selftest(int64_t timeout_ns, fsdp_stream_t stream);
 
+/* The step constants of the fused update, in device memory, for CUDA graphs.
+ * The pages have no counterpart of these two calls.  fsdp_reduce_scatter_adamw
+ * forms its per-step AdamW constants on the host and passes them as kernel
+ * arguments, so a CUDA graph that captured it would replay one step's bias
+ * corrections forever.  fsdp_reduce_scatter_adamw_consts runs the same step with
+ * those constants read on the device from `consts`; a captured graph copies the
+ * next step's block there (for instance from pinned host memory, captured as a
+ * memcpy node) before the call, and replays.
+ *
+ * fsdp_adamw_step_consts_make fills the 48-byte block for `step` exactly as
+ * fsdp_reduce_scatter_adamw forms it (each constant in double from the fp32
+ * hyper-parameters, rounded to fp32 once): decay = 1 - lr*wd, om1 = 1 - beta1,
+ * om2 = 1 - beta2, step_size = lr / (1 - beta1^step), bc2s = sqrt(1 - beta2^step),
+ * beta1, beta2, eps, n_avg = N.  Host only; hp and step are checked as in
+ * fsdp_reduce_scatter_adamw (FSDP_EINVAL).
+ *
+ * fsdp_reduce_scatter_adamw_consts: arguments, checks and results as
+ * fsdp_reduce_scatter_adamw (bit for bit, given the block of the same step), with
+ *   consts   device pointer, 16-byte aligned (else FSDP_EALIGN), to a block the
+ *            kernel reads when it runs; it must stay valid until then.
+ * It always runs the staged kernel (the default of fsdp_reduce_scatter_adamw),
+ * whatever fsdp_set_rs_kernel chose.  Launching it during stream capture needs
+ * the layout's device tables to exist already (fsdp_layout_prepare, or any
+ * earlier call on the device). */
+typedef struct {
+    float decay, om1, om2, step_size, bc2s, beta1, beta2, eps, n_avg;
+    float reserved[3];
+} fsdp_adamw_step_consts;
+int fsdp_adamw_step_consts_make(const fsdp_layout* layout, const fsdp_adamw_hparams* hp, int64_t step,
+                                fsdp_adamw_step_consts* out);
+int fsdp_reduce_scatter_adamw_consts(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                                     const void* const* grad_replicas, int32_t grad_dtype,
+                                     float* master, float* exp_avg, float* exp_avg_sq,
+                                     void* param_shards, float* grad_shard_out,
+                                     const fsdp_adamw_step_consts* consts, fsdp_stream_t stream);
+/* Copies a block of step constants from host memory into the device block, on
+ * `stream` (cudaMemcpyAsync, 48 bytes).  Captured in a CUDA graph it becomes a copy
+ * that reads host_src when the graph runs, so host_src must be page-locked (pinned)
+ * there and must not be rewritten before that replay has run.  dev_dst 16-byte
+ * aligned (else FSDP_EALIGN); host_src non-NULL. */
+int fsdp_adamw_step_consts_upload(fsdp_adamw_step_consts* dev_dst, const fsdp_adamw_step_consts* host_src,
+                                  fsdp_stream_t stream);
+
 /* fsdp_reduce_scatter_adamw_noalloc -- the pages have no counterpart of this call.
  * The same computation, arguments, checks, kernel choice and results as
  * fsdp_reduce_scatter_adamw,

@@ -305,3 +305,29 @@ def test_zero1_layout_vs_oracle_owners(oracle_lib):
             for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
                 assert a1 <= b0
             assert not spans or spans[-1][1] <= L.stride
+
+
+# ---------------------------------------------------------------------------
+# The step-constants block (host only)
+def test_step_consts_block():
+    import ctypes
+    L = fs.Layout([(8, 3), (5,)], [0, 0], 6, fs.FSDP_FLAT)
+    hp = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+    assert ctypes.sizeof(fs.AdamWStepConsts) == 48
+    c1 = fs.fsdp_adamw_step_consts_make(L, hp, 1)
+    assert c1.n_avg == 6.0
+    assert c1.beta1 == np.float32(0.9) and c1.beta2 == np.float32(0.999) and c1.eps == np.float32(1e-8)
+    b1, b2 = float(np.float32(0.9)), float(np.float32(0.999))
+    lr, wd = float(np.float32(1e-3)), float(np.float32(0.01))
+    # at step 1 the bias corrections are 1 - beta: step_size = lr / (1 - b1), bc2s = sqrt(1 - b2)
+    assert c1.step_size == pytest.approx(lr / (1 - b1), rel=1e-6)
+    assert c1.bc2s == pytest.approx((1 - b2) ** 0.5, rel=1e-6)
+    assert c1.decay == pytest.approx(1 - lr * wd, rel=1e-7)
+    assert c1.om1 == pytest.approx(1 - b1, rel=1e-6) and c1.om2 == pytest.approx(1 - b2, rel=1e-5)
+    # late steps: the corrections go to 1
+    c9 = fs.fsdp_adamw_step_consts_make(L, hp, 100000)
+    assert c9.step_size == pytest.approx(lr, rel=1e-6) and c9.bc2s == pytest.approx(1.0, rel=1e-6)
+    for bad_step, bad_hp in ((0, hp), (1, (1e-3, 1.0, 0.999, 1e-8, 0.01)), (1, (1e-3, 0.9, 0.999, 0.0, 0.01))):
+        with pytest.raises(fs.FsdpError) as e:
+            fs.fsdp_adamw_step_consts_make(L, bad_hp, bad_step)
+        assert e.value.status == -1
