@@ -411,6 +411,18 @@ int fsdp_reduce_scatter_adamw_consts(const fsdp_layout* L, int32_t ub, int32_t u
                               grad_shard_out);
     if (rc) return rc;
     if ((rc = check_ptr(consts))) return rc;
+    // the block may be device, managed or page-locked host memory: the kernel reads it
+    // through the address the device sees; other host memory is refused
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, consts) != cudaSuccess) {
+        (void)cudaGetLastError();   // not sticky: clear it
+        return FSDP_EINVAL;
+    }
+    if ((pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeHost && pa.type != cudaMemoryTypeManaged) ||
+        !pa.devicePointer)
+        return FSDP_EINVAL;
+    const fsdp::AdamScal* dconsts = static_cast<const fsdp::AdamScal*>(pa.devicePointer);
+    if (!aligned16(dconsts)) return FSDP_EALIGN;
     const bool bf16 = grad_dtype == FSDP_BF16;
     if (!fsdp::staged_fits(L->N, bf16)) return FSDP_EINVAL;
     fsdp::GradPtrs gp{};
@@ -422,7 +434,7 @@ int fsdp_reduce_scatter_adamw_consts(const fsdp_layout* L, int32_t ub, int32_t u
     const fsdp::AdamScal unused{};   // the kernel reads the device block instead
     cudaError_t e = fsdp::launch_rs_adamw_staged(R.segs, R.tile_base, R.n_tiles, bf16, gp, L->N, master, exp_avg,
                                                  exp_avg_sq, static_cast<uint16_t*>(param_shards), grad_shard_out,
-                                                 unused, kWaitNs, st, reinterpret_cast<const fsdp::AdamScal*>(consts));
+                                                 unused, kWaitNs, st, dconsts);
     if (e != cudaSuccess) return cuda_fail(e, "k_rs_adamw_staged launch");
     if (grad_shard_out) {
         const Range P = range_of(L->pad, base, ub, ue);

@@ -227,11 +227,31 @@ struct OutSlotBytes<P, std::void_t<decltype(P::kOutSlotBytes)>> {
     static constexpr int value = P::kOutSlotBytes;
 };
 
+// A policy with `static constexpr bool kPrologue = true` gets prologue(tid) called by
+// every consumer thread once, before its first item, followed by a barrier among the
+// consumer warps only (the producer is not held): for per-launch data the consumers
+// need, read once per CTA into shared memory.
+template <class P, class = void>
+struct PrologueOf {
+    static constexpr bool value = false;
+};
+template <class P>
+struct PrologueOf<P, std::void_t<decltype(P::kPrologue)>> {
+    static constexpr bool value = P::kPrologue;
+};
+
 // Front region: stage barriers, stage geometry, output barriers, output headers.
 constexpr int kGeoOff = 16 * kMaxStages;
 constexpr int kOutBarOff = kGeoOff + kMaxStages * int(sizeof(TileGeom));
 constexpr int kOutHdrOff = kOutBarOff + 16 * kOutSlots;
-static_assert(kOutHdrOff + kOutSlots * int(sizeof(OutHdr)) <= kFrontBytes, "front region");
+// and, at its end, 64 bytes a policy may use for per-launch data (policy_front())
+constexpr int kPolicyFrontOff = kFrontBytes - 64;
+static_assert(kOutHdrOff + kOutSlots * int(sizeof(OutHdr)) <= kPolicyFrontOff, "front region");
+
+__device__ __forceinline__ unsigned char* policy_front() {
+    extern __shared__ __align__(128) unsigned char smem[];
+    return smem + kPolicyFrontOff;
+}
 
 // The consumers' side of the output ring for one item.
 struct OutRing {
@@ -353,6 +373,10 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, in
     }
 
     // ---- consumer warps ----
+    if constexpr (PrologueOf<Pol>::value) {
+        pol.prologue(tid);
+        asm volatile("bar.sync 1, %0;" ::"n"(kStThreads) : "memory");   // the consumer warps only
+    }
     double sum = 0.0;
     typename Pol::Carry carry{};
     for (int64_t j = 0; j < n_mine; ++j) {

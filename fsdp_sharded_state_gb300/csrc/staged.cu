@@ -25,17 +25,49 @@ struct Sum4 {
     float a0, a1, a2, a3;
 };
 
-// A consumer thread's carry when the step constants come from device memory: the
-// partial sums, and the constants, read once at the thread's first item.
+// A consumer thread's carry when the step constants come from memory: the partial
+// sums, and the constants, taken from shared memory at the thread's first item.
 struct SumConsts {
     Sum4 sum;
     AdamScal s;
     int ready;
 };
 
-// DC: the step's AdamW constants are read from device memory (dsc), once per
-// consumer thread, instead of taken from the kernel argument (sc), so that a
-// captured CUDA graph can replay the launch with the constants rewritten in between.
+// The CTA's copy of the constants block (read by one consumer thread per CTA), in
+// the pipeline's policy area of shared memory.
+__device__ __forceinline__ AdamScal& consts_shared() {
+    static_assert(sizeof(AdamScal) <= 64, "policy area");
+    return *reinterpret_cast<AdamScal*>(policy_front());
+}
+
+// The constants block (16-byte aligned; device or page-locked host memory), read
+// with .cv loads: no cached copy is used, so a replayed launch sees what the host
+// wrote into a host block since the last one.
+__device__ __forceinline__ AdamScal ld_consts_fresh(const AdamScal* p) {
+    float v[12];
+    const float* f = reinterpret_cast<const float*>(p);
+    asm volatile("ld.global.cv.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+                 : "l"(f) : "memory");
+    asm volatile("ld.global.cv.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+                 : "l"(f + 4) : "memory");
+    asm volatile("ld.global.cv.f32 %0, [%1];" : "=f"(v[8]) : "l"(f + 8) : "memory");
+    AdamScal s;
+    s.decay = v[0];
+    s.om1 = v[1];
+    s.om2 = v[2];
+    s.step_size = v[3];
+    s.bc2s = v[4];
+    s.beta1 = v[5];
+    s.beta2 = v[6];
+    s.eps = v[7];
+    s.nf = v[8];
+    return s;
+}
+
+// DC: the step's AdamW constants are read from a block in memory (dsc: device or
+// page-locked host memory), once per CTA into shared memory, instead of taken from
+// the kernel argument (sc), so that a captured CUDA graph can replay the launch with
+// the constants rewritten in between.
 template <typename GT, bool PARAM, bool GOUT, bool DC = false>
 struct RsAdamw {
     static constexpr bool kGeomFirst = true;
@@ -50,6 +82,10 @@ struct RsAdamw {
     const AdamScal* dsc;
 
     using Carry = typename std::conditional<DC, SumConsts, Sum4>::type;
+    static constexpr bool kPrologue = DC;
+    __device__ void prologue(int tid) const {
+        if (tid == 0) consts_shared() = ld_consts_fresh(dsc);   // one read of the block per CTA
+    }
     __device__ int groups() const { return NG; }
     __device__ int q0(const TileGeom& g) const { return g.q * Q; }
     __device__ int nq(const TileGeom& g) const { return (N - g.q * Q) < Q ? (N - g.q * Q) : Q; }
@@ -85,7 +121,7 @@ struct RsAdamw {
     __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry& carry, Release release) const {
         if constexpr (DC) {
             if (!carry.ready) {
-                carry.s = *dsc;
+                carry.s = consts_shared();
                 carry.ready = 1;
             }
             return consume_with(carry.s, g, sb, tid, carry.sum, release);

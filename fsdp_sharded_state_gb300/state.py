@@ -19,9 +19,8 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (FSDP_BF16, FSDP_F32, FSDP_FLAT, Layout, fsdp_adamw_step_consts_make, fsdp_adamw_step_consts_upload,
-               fsdp_reduce_scatter_adamw, fsdp_reduce_scatter_adamw_consts, fsdp_reshard, fsdp_rs_kernel_for,
-               fsdp_unshard)
+from . import (FSDP_BF16, FSDP_F32, FSDP_FLAT, Layout, fsdp_adamw_step_consts_make, fsdp_reduce_scatter_adamw,
+               fsdp_reduce_scatter_adamw_consts, fsdp_reshard, fsdp_rs_kernel_for, fsdp_unshard)
 
 STRATEGIES = {"full_shard": 2, "shard_grad_op": 1}   # all-gathers per step
 
@@ -149,14 +148,14 @@ class StepGraph:
     """One sharded step captured in CUDA graphs and replayed step after step.
 
     For layouts small enough that issuing a step's library calls takes the host longer
-    than the GPU takes to run them (the 4,192-parameter MLP: about 33 us of host work
+    than the GPU takes to run them (the 4,192-parameter MLP: about 30 us of host work
     for a step the GPU runs in about 10 us), the step's kernels are captured once and
     each step is one graph launch.  The fused update reads its AdamW step constants
-    from a 48-byte device block (fsdp_reduce_scatter_adamw_consts); each graph starts
-    with a copy of that block from a pinned host block (fsdp_adamw_step_consts_upload), which step() fills with the
-    step's constants (fsdp_adamw_step_consts_make) before the replay.  n_blocks host
-    blocks, each with its own graph, take turns, so the host rewrites a block only once
-    the replay that copied it has run: it runs at most n_blocks steps ahead.
+    from a 48-byte block in page-locked host memory (fsdp_reduce_scatter_adamw_consts),
+    which step() fills with the step's constants (fsdp_adamw_step_consts_make) before
+    the replay; the graph holds no copy.  n_blocks host blocks, each with its own
+    graph, take turns, so the host rewrites a block only once the replay that read it
+    has run: it runs at most n_blocks steps ahead.
 
     The first step() runs the same calls eagerly (it also sets up the library's
     per-kernel launch state, which must not happen during capture); the graphs are
@@ -171,8 +170,6 @@ class StepGraph:
         if n_blocks < 1:
             raise ValueError("n_blocks must be >= 1")
         self.st, self.grads, self.hp, self.strategy = state, list(grads), hp, strategy
-        dev = state.full.device
-        self.dev_consts = torch.zeros(12, dtype=torch.float32, device=dev)
         self.host = [torch.zeros(12, dtype=torch.float32).pin_memory() for _ in range(n_blocks)]
         self.done = [None] * n_blocks
         self.graphs = None
@@ -181,11 +178,10 @@ class StepGraph:
 
     def _calls(self, b: int) -> None:
         st = self.st
-        fsdp_adamw_step_consts_upload(self.dev_consts, self.host[b])
         for _ in range(STRATEGIES[self.strategy]):
             st.unshard()
         fsdp_reduce_scatter_adamw_consts(st.layout, 0, st.layout.n_units, self.grads, st.master, st.exp_avg,
-                                         st.exp_avg_sq, st.param, st.grad_out, consts=self.dev_consts)
+                                         st.exp_avg_sq, st.param, st.grad_out, consts=self.host[b])
 
     def _capture(self) -> None:
         torch.cuda.synchronize(self.st.full.device)
@@ -199,7 +195,7 @@ class StepGraph:
 
     def step(self) -> None:
         """One step: the next step number's constants into a host block, then the graph
-        that copies that block and runs the step (on the current stream)."""
+        that reads that block (on the current stream)."""
         b = self.k % len(self.host)
         if self.done[b] is not None:
             self.done[b].synchronize()           # the replay that last read block b has run

@@ -374,14 +374,15 @@ int fsdp_rs_kernel_for(const fsdp_layout* layout, int32_t grad_dtype);
  * records a wait that gives up the same way (limit: 1 s per wait). */
 int fsdp_wait_selftest(int64_t timeout_ns, fsdp_stream_t stream);
 
-/* The step constants of the fused update, in device memory, for CUDA graphs.
- * The pages have no counterpart of these two calls.  fsdp_reduce_scatter_adamw
- * forms its per-step AdamW constants on the host and passes them as kernel
- * arguments, so a CUDA graph that captured it would replay one step's bias
- * corrections forever.  fsdp_reduce_scatter_adamw_consts runs the same step with
- * those constants read on the device from `consts`; a captured graph copies the
- * next step's block there (for instance from pinned host memory, captured as a
- * memcpy node) before the call, and replays.
+/* The step constants of the fused update in memory, for CUDA graphs.  The pages
+ * have no counterpart of these three calls.  fsdp_reduce_scatter_adamw forms its
+ * per-step AdamW constants on the host and passes them as kernel arguments, so a
+ * CUDA graph that captured it would replay one step's bias corrections forever.
+ * fsdp_reduce_scatter_adamw_consts runs the same step with those constants read
+ * from a block in memory when the kernel runs; a captured graph is replayed after
+ * the next step's block has been written there.  The block may be page-locked host
+ * memory, which the host rewrites between replays with no copy in the graph, or
+ * device memory filled on the stream (fsdp_adamw_step_consts_upload).
  *
  * fsdp_adamw_step_consts_make fills the 48-byte block for `step` exactly as
  * fsdp_reduce_scatter_adamw forms it (each constant in double from the fp32
@@ -392,8 +393,11 @@ int fsdp_wait_selftest(int64_t timeout_ns, fsdp_stream_t stream);
  *
  * fsdp_reduce_scatter_adamw_consts: arguments, checks and results as
  * fsdp_reduce_scatter_adamw (bit for bit, given the block of the same step), with
- *   consts   device pointer, 16-byte aligned (else FSDP_EALIGN), to a block the
- *            kernel reads when it runs; it must stay valid until then.
+ *   consts   16-byte aligned (else FSDP_EALIGN) block in device, managed or
+ *            page-locked host memory (pageable host memory: FSDP_EINVAL).  The
+ *            kernel reads it when it runs, once per thread, with loads that use no
+ *            cached copy; it must hold the step's constants then and must not be
+ *            rewritten until the kernel has finished.
  * It always runs the staged kernel (the default of fsdp_reduce_scatter_adamw),
  * whatever fsdp_set_rs_kernel chose.  Launching it during stream capture needs
  * the layout's device tables to exist already (fsdp_layout_prepare, or any

@@ -46,9 +46,12 @@ def _pair(w, with_grad_out):
     return a, b
 
 
+@pytest.mark.parametrize("block", ["device", "pinned_host"])
 @pytest.mark.parametrize("with_grad_out", [False, True])
 @pytest.mark.parametrize("w", CASES)
-def test_consts_call_equals_fused_call(oracle_lib, w, with_grad_out):
+def test_consts_call_equals_fused_call(oracle_lib, w, with_grad_out, block):
+    """The block in device memory (uploaded on the stream) or read by the kernel from
+    page-locked host memory."""
     a, b = _pair(w, with_grad_out)
     L = b.layout
     dev = torch.zeros(12, dtype=torch.float32, device="cuda")
@@ -59,9 +62,10 @@ def test_consts_call_equals_fused_call(oracle_lib, w, with_grad_out):
         c = fs.fsdp_adamw_step_consts_make(L, w.hp, t)
         torch.cuda.synchronize()                      # host block free to rewrite
         ctypes.memmove(host.data_ptr(), ctypes.addressof(c), 48)
-        fs.fsdp_adamw_step_consts_upload(dev, host)
+        if block == "device":
+            fs.fsdp_adamw_step_consts_upload(dev, host)
         fs.fsdp_reduce_scatter_adamw_consts(L, 0, L.n_units, grads, b.master, b.exp_avg, b.exp_avg_sq, b.param,
-                                            b.grad_out, consts=dev)
+                                            b.grad_out, consts=dev if block == "device" else host)
         torch.cuda.synchronize()
         for x, y, what in ((a.master, b.master, "master"), (a.exp_avg, b.exp_avg, "exp_avg"),
                            (a.exp_avg_sq, b.exp_avg_sq, "exp_avg_sq"), (a.param, b.param, "param"),
@@ -123,6 +127,13 @@ def test_consts_rejects_bad_arguments(oracle_lib):
     assert e.value.status == -1
     with pytest.raises(fs.FsdpError) as e:                          # no host source
         fs.fsdp_adamw_step_consts_upload(dev, None)
+    assert e.value.status == -1
+    pageable = np.zeros(16, np.float32)                             # not page-locked: refused
+    addr = pageable.ctypes.data
+    addr += (-addr) % 16
+    with pytest.raises(fs.FsdpError) as e:
+        fs.fsdp_reduce_scatter_adamw_consts(L, 0, L.n_units, grads, st.master, st.exp_avg, st.exp_avg_sq,
+                                            st.param, None, consts=addr)
     assert e.value.status == -1
     torch.cuda.synchronize()
     assert not np.any(pu.f32(st.exp_avg))                           # nothing was launched
