@@ -216,6 +216,20 @@ def oracle_step(w, st, t, strategy):
                     param=st["param"], hp=w.hp, step=t, ub=0, ue=st["u_end"])
 
 
+def host_cpu():
+    """The host's CPU model (lscpu) and logical core count, recorded beside the oracle's timing."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"model": model, "nproc": os.cpu_count()}
+
+
 def cpu_baseline(w, strategy, min_seconds=10.0):
     st = oracle_sample_setup(w, target_s=1.0)
     t0 = time.perf_counter()
@@ -228,7 +242,7 @@ def cpu_baseline(w, strategy, min_seconds=10.0):
             break
     return {"value": st["numel"] * steps / el, "unit": "params/s", "cores": 1, "kind": "oracle",
             "sample": f"units [0,{st['u_end']}) of {w.name} ({st['numel']} params), {steps} oracle steps "
-                      f"({strategy}), single thread, {el:.1f} s"}
+                      f"({strategy}), single thread, {el:.1f} s", "host": host_cpu()}
 
 
 # ---------------------------------------------------------------------------
@@ -524,7 +538,7 @@ def main():
             "config": {"workload": w.name, "strategy": args.strategy},
             "cpu_baseline": {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
                              "sample": f"units [0,{st['u_end']}) of {w.name} ({st['numel']} params) per step, "
-                                       "single thread"},
+                                       "single thread", "host": host_cpu()},
             "e2e": {"value": v, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
         return
