@@ -99,16 +99,40 @@ class ShardedState:
         self.reduce_scatter_adamw(grads, hp, stream=stream)
 
     def step_per_unit(self, grads, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), strategy: str = "full_shard",
-                      stream=None) -> None:
+                      stream=None, gather_stream=None) -> None:
         """The same step issued unit by unit, in step_schedule's order: one library call
         per collective of the pages' per-unit FSDP schedule, every reduce-scatter with
-        the same step number.  Same results as step(), bit for bit."""
+        the same step number.  Same results as step(), bit for bit.
+
+        With gather_stream, the all-gathers go on that stream and the reduce-scatters on
+        `stream` (the current one by default), as FSDP keeps its all-gathers on a
+        stream of their own ([FSDP-ch18] §18.3, prefetch): a unit's reduce-scatter
+        waits for that unit's last all-gather (it rewrites the shards the gather reads),
+        and the step's gathers wait for all work queued on `stream` before the step (the
+        previous step's updates).  So the gather of unit u-1 runs beside the
+        reduce-scatter of unit u.  When the call returns, `stream` holds the whole step."""
         t = self.t + 1
+        if gather_stream is None:
+            for kind, u in step_schedule(self.layout.n_units, strategy):
+                if kind == "all_gather":
+                    self.unshard(u, u + 1, stream=stream)
+                else:
+                    self.reduce_scatter_adamw(grads, hp, step=t, ub=u, ue=u + 1, stream=stream)
+            self.t = t
+            return
+        main = stream if stream is not None else torch.cuda.current_stream(self.full.device)
+        gather_stream.wait_stream(main)
+        gathered = {}
         for kind, u in step_schedule(self.layout.n_units, strategy):
             if kind == "all_gather":
-                self.unshard(u, u + 1, stream=stream)
+                self.unshard(u, u + 1, stream=gather_stream)
+                ev = torch.cuda.Event()
+                ev.record(gather_stream)
+                gathered[u] = ev                  # the unit's latest gather
             else:
-                self.reduce_scatter_adamw(grads, hp, step=t, ub=u, ue=u + 1, stream=stream)
+                main.wait_event(gathered[u])
+                self.reduce_scatter_adamw(grads, hp, step=t, ub=u, ue=u + 1, stream=main)
+        main.wait_stream(gather_stream)           # the step's last gathers, for the caller
         self.t = t
 
     def launch_counts(self, grad_dtype: torch.dtype = torch.bfloat16) -> dict:

@@ -225,24 +225,28 @@ def test_zero1_chain_vs_oracle(oracle_lib, bf16):
         pu.assert_f32_close(got_m[a:a + sizes[t]], orm[b:b + sizes[t]], f"exp_avg of tensor {t}")
 
 
+@pytest.mark.parametrize("gather_stream", [False, True])
 @pytest.mark.parametrize("strategy", ["full_shard", "shard_grad_op"])
 @pytest.mark.parametrize("w", [W([(256, 64)] * 8, list(range(8)), 4, synth.FLAT, torch.float32),
                                W([(300, 37), (13,), (64, 65), (129, 7), (5,)], [0, 1, 1, 2, 3], 8, synth.FLAT),
-                               W([(130, 64), (7,), (9, 3)], [0, 0, 0], 6, synth.DIM0)])
-def test_per_unit_step_equals_whole_range(oracle_lib, w, strategy):
-    """The step issued unit by unit in FSDP's collective order (ShardedState.step_per_unit)
-    gives the whole-range step's results bit for bit, over two steps."""
+                               W([(130, 64), (7,), (9, 3)], [0, 0, 0], 6, synth.DIM0),
+                               W([(1 << 18, 8)] * 4, list(range(4)), 4, synth.FLAT)])
+def test_per_unit_step_equals_whole_range(oracle_lib, w, strategy, gather_stream):
+    """The step issued unit by unit in FSDP's collective order (ShardedState.step_per_unit),
+    with the all-gathers on the current stream or on a stream of their own beside the
+    reduce-scatters, gives the whole-range step's results bit for bit, over three steps."""
     a, b = pu.make_state(w), pu.make_state(w)
     O = pu.oracle_offsets(w)
     full = synth.full_params(w, a.F, O["t_full_off"])
     a.init_from_full(full)
     b.init_from_full(full)
-    for t in (1, 2):
+    side = torch.cuda.Stream() if gather_stream else None
+    for t in (1, 2, 3):
         grads = [g.to(w.grad_dtype) for g in synth.grad_replicas(w, a.F, t)]
         a.step(grads, w.hp, strategy=strategy)
-        b.step_per_unit(grads, w.hp, strategy=strategy)
+        b.step_per_unit(grads, w.hp, strategy=strategy, gather_stream=side)
     torch.cuda.synchronize()
-    assert a.t == b.t == 2
+    assert a.t == b.t == 3
     for x, y, what in ((a.master, b.master, "master"), (a.exp_avg, b.exp_avg, "exp_avg"),
                        (a.exp_avg_sq, b.exp_avg_sq, "exp_avg_sq"), (a.full, b.full, "gathered buffer")):
         assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16),
