@@ -73,12 +73,14 @@ def test_consts_call_equals_fused_call(oracle_lib, w, with_grad_out, block):
             _same(x, y, f"{what} step {t}")
 
 
+@pytest.mark.parametrize("with_grad_out", [False, True])
 @pytest.mark.parametrize("strategy", ["full_shard", "shard_grad_op"])
 @pytest.mark.parametrize("w", [synth.tiny_mlp()] + CASES[:3])
-def test_step_graph_equals_eager(oracle_lib, w, strategy):
+def test_step_graph_equals_eager(oracle_lib, w, strategy, with_grad_out):
     """Six steps: the first runs eagerly and captures the graphs, five replay them
-    (the three host blocks each come round twice)."""
-    a, b = _pair(w, False)
+    (the three host blocks each come round twice).  With the reduced-gradient output,
+    the graphs also hold the zero-fill of its padding."""
+    a, b = _pair(w, with_grad_out)
     grads = [g.to(w.grad_dtype) for g in synth.grad_replicas(w, a.F, 1)]
     g = fs.StepGraph(b, grads, w.hp, strategy, n_blocks=3)
     for t in range(1, 7):
@@ -88,7 +90,7 @@ def test_step_graph_equals_eager(oracle_lib, w, strategy):
         assert a.t == b.t == t
         for x, y, what in ((a.master, b.master, "master"), (a.exp_avg, b.exp_avg, "exp_avg"),
                            (a.exp_avg_sq, b.exp_avg_sq, "exp_avg_sq"), (a.param, b.param, "param"),
-                           (a.full, b.full, "gathered buffer")):
+                           (a.full, b.full, "gathered buffer"), (a.grad_out, b.grad_out, "grad_out")):
             _same(x, y, f"{what} step {t}")
     fs.fsdp_check_status()
 
