@@ -470,15 +470,24 @@ def run_row(args, w):
         grads = synth.grad_replicas(w, F, 1, device=dev)
         call = lambda t: fs.fsdp_zero1_adamw_broadcast(L, 0, L.n_units, grads, master, m, v, params, w.hp, t)
     del full
-    for k in range(args.warmup):
-        call(k + 1)
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for k, (a, b) in enumerate(evs):
-        a.record()
-        call(args.warmup + k + 1)
-        b.record()
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t = 0
+        t_end = time.time() + args.soak          # untimed: clocks to their working point, samples taken
+        while time.time() < t_end:
+            t += 1
+            call(t)
+            torch.cuda.synchronize()
+        for k in range(args.warmup):
+            t += 1
+            call(t)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in evs:
+            t += 1
+            a.record()
+            call(t)
+            b.record()
+        torch.cuda.synchronize()
     fs.fsdp_check_status()
     ms = [a.elapsed_time(b) for a, b in evs]
     med = statistics.median(ms)
@@ -490,7 +499,8 @@ def run_row(args, w):
             "data": "synthetic", "config": {"workload": w.name, "n_ranks_simulated": N,
                                             "groups": R if args.row == "hsdp" else None},
             "roofline": {"call": args.row, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_call": nbytes}}
+                         "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_call": nbytes},
+            "clocks": parse_clocks(clk.out)}
 
 
 def main():
