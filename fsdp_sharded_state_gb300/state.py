@@ -184,8 +184,9 @@ class StepGraph:
     The first step() runs the same calls eagerly (it also sets up the library's
     per-kernel launch state, which must not happen during capture); the graphs are
     captured right after it.  Buffers are fixed at construction: the step reads
-    `grads` every time, as a training loop that refills them in place would.  Same
-    results as ShardedState.step, bit for bit."""
+    `grads` every time, as a training loop that refills them in place would.  Call
+    step() with one current stream throughout: replays on two streams would update the
+    same state concurrently.  Same results as ShardedState.step, bit for bit."""
 
     def __init__(self, state: ShardedState, grads, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), strategy: str = "full_shard",
                  n_blocks: int = 3):
