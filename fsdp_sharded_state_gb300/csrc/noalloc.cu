@@ -35,20 +35,26 @@ using fsdp::Seg;
 static __device__ __align__(256) Seg g_noalloc_segs[FSDP_NOALLOC_MAX_SEGMENTS];
 
 constexpr int kMaxDevices = 64;
+// Held by a call from its first table copy to its last launch, so that the copies and
+// launches of two host threads on one stream are queued call by call, never
+// interleaved (a kernel always reads the table its own call wrote).
 std::mutex g_mu;
-Seg* g_addr[kMaxDevices] = {};   // device address of g_noalloc_segs, per device
+Seg* g_addr[kMaxDevices] = {};   // device address of g_noalloc_segs, per device (under g_mu)
 
 // Set-up, once per device, with that device current: the device address of the
-// scratch array.  (It loads the library's module on that device if needed.)
+// scratch array.  (It loads the library's module on that device if needed.)  The
+// cached address belongs to the device's current context: a cudaDeviceReset ends
+// that context, so no call may follow one in this process.  Called under g_mu.
 int scratch_address(Seg** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FSDP_ECUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return FSDP_EINVAL;
-    std::lock_guard<std::mutex> lk(g_mu);
     if (!g_addr[dev]) {
         Seg* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_segs);
-        if (e != cudaSuccess || !p) return FSDP_ECUDA;
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_segs);
+        if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+        if (!p) return FSDP_ECUDA;
         g_addr[dev] = p;
     }
     *out = g_addr[dev];
@@ -90,6 +96,7 @@ extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t u
     const int64_t n_pad = grad_shard_out ? int64_t(pe - pb) + 1 : 0;
     if (n_cls[0] + n_cls[1] + n_pad > FSDP_NOALLOC_MAX_SEGMENTS) return FSDP_EINVAL;   // beyond the fixed scratch
 
+    std::lock_guard<std::mutex> lk(g_mu);             // through the last launch of this call
     Seg* scratch = nullptr;
     if ((rc = scratch_address(&scratch))) return rc;
 
@@ -112,32 +119,32 @@ extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t u
         const int32_t sb = L->data.unit_begin[ub], se = L->data.unit_begin[ue];
         const int64_t n = int64_t(se - sb) + 1;
         e = cudaMemcpyAsync(next, L->data.segs.data() + sb, size_t(n) * sizeof(Seg), cudaMemcpyHostToDevice, st);
-        if (e != cudaSuccess) return FSDP_ECUDA;
+        if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "cudaMemcpyAsync(no-allocation table)");
         const int64_t t0 = L->data.segs[sb].tile0, t1 = L->data.segs[se].tile0;
         e = fsdp::launch_rs_adamw_staged(next, t0, t1 - t0, bf16, gp, L->N, master, exp_avg, exp_avg_sq,
                                          static_cast<uint16_t*>(param_shards), grad_shard_out, sc,
                                          fsdp::detail::kWaitNs, st);
-        if (e != cudaSuccess) return FSDP_ECUDA;
+        if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "k_rs_adamw_staged launch");
         next += n;
     }
     for (int c = 0; c < 2 && !staged; ++c) {
         const int32_t sb = cls[c]->unit_begin[ub], se = cls[c]->unit_begin[ue];
         e = cudaMemcpyAsync(next, cls[c]->segs.data() + sb, size_t(n_cls[c]) * sizeof(Seg), cudaMemcpyHostToDevice,
                             st);
-        if (e != cudaSuccess) return FSDP_ECUDA;
+        if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "cudaMemcpyAsync(no-allocation table)");
         const int64_t t0 = cls[c]->segs[sb].tile0, t1 = cls[c]->segs[se].tile0;
         e = fsdp::launch_rs_adamw(next, t0, t1 - t0, c == 1, grad_dtype == FSDP_BF16, gp, L->N, L->F, master, exp_avg,
                                   exp_avg_sq, static_cast<uint16_t*>(param_shards), grad_shard_out, sc, st);
-        if (e != cudaSuccess) return FSDP_ECUDA;
+        if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "k_rs_adamw launch");
         next += n_cls[c];
     }
     if (grad_shard_out) {
         Seg* pad = next;
         e = cudaMemcpyAsync(pad, L->pad.segs.data() + pb, size_t(n_pad) * sizeof(Seg), cudaMemcpyHostToDevice, st);
-        if (e != cudaSuccess) return FSDP_ECUDA;
+        if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "cudaMemcpyAsync(no-allocation pad table)");
         const int64_t q0 = L->pad.segs[pb].tile0, q1 = L->pad.segs[pe].tile0;
         e = fsdp::launch_zero_pad(pad, q0, q1 - q0, grad_shard_out, nullptr, st);
-        if (e != cudaSuccess) return FSDP_ECUDA;
+        if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "k_zero_pad launch");
     }
     return FSDP_OK;
 }

@@ -128,6 +128,12 @@ int fsdp_layout_create(int32_t n_tensors, const int32_t* ndim, const int64_t* di
  * reads its tables. */
 void fsdp_layout_destroy(fsdp_layout* layout);
 
+/* The layout's sizes ([ZeRO-state] "FlatParameter 与 Padding": the padded physical
+ * numel N*ceil(P/N) against the logical P, and the shard numel each rank holds;
+ * "Canonical ZeRO 状态公式": the per-rank element counts the state formulas use):
+ * P, S, the row stride of the shard arrays, the full-layout size, the padding over
+ * all ranks and the number of (tensor or unit, rank) pieces.  Host only.
+ * FSDP_EINVAL when an argument is NULL. */
 int fsdp_layout_query(const fsdp_layout* layout, fsdp_layout_info* out);
 
 /* Unit u: its shard offset and size S_u inside a rank row, its offset and size
@@ -241,10 +247,11 @@ int fsdp_reshard(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end
                  const void* full, int32_t full_dtype, float* master, void* param_shards,
                  fsdp_stream_t stream);
 
-/* Blocks until `stream` is idle and reports any CUDA error seen there
- * (FSDP_ECUDA) -- the analogue of a collective's error check -- or, failing that,
- * a bounded device-side wait that gave up on the current device since the last
- * check (FSDP_ETIMEOUT; the record is cleared). */
+/* The pages have no counterpart of this call: their collectives report errors
+ * through NCCL and the process group, which this library replaces with kernels.
+ * Blocks until `stream` is idle and reports any CUDA error seen there
+ * (FSDP_ECUDA), or, failing that, a bounded device-side wait that gave up on the
+ * current device since the last check (FSDP_ETIMEOUT; the record is cleared). */
 int fsdp_check_status(fsdp_stream_t stream);
 
 /* Static text for a status code; never NULL. */
@@ -437,11 +444,16 @@ int fsdp_adamw_step_consts_upload(fsdp_adamw_step_consts* dev_dst, const fsdp_ad
  *     its padding pieces + 1.  A larger range returns FSDP_EINVAL with nothing
  *     launched; split it into smaller unit ranges.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.  The
+ *     address is kept for the rest of the process: after a cudaDeviceReset of that
+ *     device it is stale, so do not call this entry point after one.
  *   - All calls share the one array and each call rewrites the entries it reads
  *     before its kernels run, so no state carries over between calls.  Calls whose
  *     work overlaps on the GPU race on the array: issue them on one stream, or order
- *     them with events. */
+ *     them with events.  Host threads may call it at the same time: a lock held from
+ *     a call's table copy to its last launch keeps each call's copy and kernels
+ *     together on the stream.
+ *   - A CUDA error is recorded for fsdp_last_cuda_error, as by the other calls. */
 #define FSDP_NOALLOC_MAX_SEGMENTS 8192
 int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
                                       const void* const* grad_replicas, int32_t grad_dtype,

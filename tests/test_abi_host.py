@@ -6,6 +6,7 @@ Every rejected call below carries exactly one invalid argument, so validation
 fails before any CUDA call; no call here can reach a kernel.
 """
 import ctypes as C
+import functools
 import os
 import re
 import subprocess
@@ -165,15 +166,21 @@ def test_unshard_validation(lay):
 
 
 def rs(lay, grads=None, gdt=1, master=A, m=A, v=A, param=None, gout=None, hp=(1e-3, 0.9, 0.999, 1e-8, 0.01),
-       step=1, ub=0, ue=2):
+       step=1, ub=0, ue=2, fn="fsdp_reduce_scatter_adamw"):
     lib = fs.lib()
-    arr = (C.c_void_p * 4)(*(grads or [A] * 4))
+    arr = (C.c_void_p * lay.N)(*(grads or [A] * lay.N))
     h = fs.AdamWHparams(*hp)
-    return lib.fsdp_reduce_scatter_adamw(lay.handle, ub, ue, arr, gdt, master, m, v, param, gout, C.byref(h),
-                                         step, None)
+    return getattr(lib, fn)(lay.handle, ub, ue, arr, gdt, master, m, v, param, gout, C.byref(h), step, None)
 
 
-def test_reduce_scatter_adamw_validation(lay):
+# The allocating entry point and the one that allocates nothing make the same checks,
+# all before any CUDA call: every rejection below runs on a machine with no GPU.
+RS_ENTRY_POINTS = ["fsdp_reduce_scatter_adamw", "fsdp_reduce_scatter_adamw_noalloc"]
+
+
+@pytest.mark.parametrize("fn", RS_ENTRY_POINTS)
+def test_reduce_scatter_adamw_validation(lay, fn):
+    rs = functools.partial(globals()["rs"], fn=fn)
     assert rs(lay, ue=3) == -1
     assert rs(lay, gdt=4) == -2
     assert rs(lay, step=0) == -1
@@ -187,6 +194,14 @@ def test_reduce_scatter_adamw_validation(lay):
                 (1e-3, .9, .999, 0.0, .01), (1e-3, .9, .999, 1e-8, -1.0), (float("nan"), .9, .999, 1e-8, .01),
                 (1e-3, .9, float("inf"), 1e-8, .01), (2.0, .9, .999, 1e-8, 0.6)]:
         assert rs(lay, hp=bad) == -1, bad
+    assert rs(lay, ub=-1) == -1
+
+
+@pytest.mark.parametrize("fn", RS_ENTRY_POINTS)
+def test_reduce_scatter_adamw_rejects_zero1_layouts(fn):
+    # a ZeRO-1 layout keeps parameters whole: the reduce-scatter step does not apply
+    z = fs.Layout([(64, 32), (64,)], None, 4, fs.FSDP_ZERO1)
+    assert rs(z, fn=fn) == -1
 
 
 def test_reshard_validation(lay):
