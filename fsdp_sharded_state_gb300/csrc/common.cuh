@@ -71,11 +71,14 @@ __device__ __forceinline__ uint16_t to_bf16(float x) {
 }
 
 // ---- 16-byte memory operations ---------------------------------------------------
-// Gradient replicas are read exactly once per step: stream them past L1.
+// Gradient replicas are read exactly once per step: stream them past L1.  The asm
+// is volatile with a memory clobber, so the compiler keeps it after pdl_wait() (and
+// in order with every other memory access) whatever the address depends on: a
+// replica written by the grid before this one is never read ahead of the wait.
 __device__ __forceinline__ uint4 ld_once(const void* p) {
     uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
     return r;
 }
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
