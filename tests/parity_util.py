@@ -206,7 +206,55 @@ def run_sampled_parity(w: synth.Workload, steps=None, strategy="full_shard", n_r
             u.append(assert_bf16_close(u16(st.param.reshape(-1)[lin]), par, f"param step {t}"))
         ulps.append(max(u))
         del grads
-    # padding stays +0 (sampled padding positions went through the oracle with g = 0 too)
+    # padding stays +0 (sampled padding positions went through the oracle with g = 0 too),
+    # and so does every padding position of every state array, found from the oracle's layout
     pad = ~real
     assert not f32(st.master.reshape(-1)[lin])[pad].view(np.uint32).any()
+    pads = torch.from_numpy(padding_positions(w, O, st.stride)).cuda()
+    arrays = [("master", st.master), ("exp_avg", st.exp_avg), ("exp_avg_sq", st.exp_avg_sq), ("param", st.param),
+              ("grad_out", st.grad_out)]
+    for name, a in arrays:
+        if a is not None and pads.numel():
+            x = a.reshape(-1)[pads]
+            assert not x.view(torch.int16 if x.dtype == torch.bfloat16 else torch.int32).any(), f"{name} padding"
     return st, ulps
+
+
+def padding_positions(w: synth.Workload, O, stride):
+    """Linear indices (rank * stride + j) of every padding element of the shard arrays,
+    from the oracle's layout: FLAT -- the tail of each unit past its logical elements
+    (on the last ranks); DIM0 -- each rank slot's rows past the rows it owns."""
+    out = []
+    for r in range(w.N):
+        if w.mode == oracle.FLAT:
+            for u in range(O["U"]):
+                S_u, P_u, a = int(O["u_S"][u]), int(O["u_numel"][u]), int(O["u_shard_off"][u])
+                own = min(max(P_u - r * S_u, 0), S_u)
+                out.append(r * stride + np.arange(a + own, a + S_u, dtype=np.int64))
+        else:
+            for t, shp in enumerate(w.shapes):
+                d0 = shp[0] if shp else 1
+                inner = int(np.prod(shp[1:])) if len(shp) > 1 else 1
+                c, a = int(O["t_rows"][t]), int(O["t_shard_off"][t])
+                own = min(max(d0 - r * c, 0), c)
+                out.append(r * stride + np.arange(a + own * inner, a + c * inner, dtype=np.int64))
+    return np.concatenate(out) if out else np.zeros(0, np.int64)
+
+
+def logical(O, shapes):
+    """Mask of the full-layout positions that hold a tensor element (FLAT padding False)."""
+    mask = np.zeros(O["F"], bool)
+    for t, s in enumerate(shapes):
+        mask[O["t_full_off"][t]:O["t_full_off"][t] + int(np.prod(s) if s else 1)] = True
+    return mask
+
+
+def oracle_zero1_rows(sh, N, owners):
+    """The oracle's ZeRO-1 packing: each owner's tensors back to back, in tensor order;
+    returns each tensor's offset in its owner's row and the row length."""
+    sizes = [int(np.prod(s) if s else 1) for s in sh.shapes]
+    off, fill = [], [0] * N
+    for t, o in enumerate(owners):
+        off.append(fill[o])
+        fill[o] += sizes[t]
+    return off, max(fill)

@@ -91,3 +91,13 @@ def test_code_hash_ignores_comments():
     b = "int f(int x) { return x; }"
     assert bench.code_only(a) == bench.code_only(b)
     assert bench.code_only("int a;") != bench.code_only("int b;")
+
+
+def test_oracle_host_run_spawns_one_process_per_core():
+    # the host-wide CPU baseline: spawned processes, each the unmodified oracle on one
+    # unit of its own copy of the workload, timed together behind a barrier
+    import oracle
+    oracle.build()
+    r = bench.oracle_host_run(synth.tiny_mlp(), "full_shard", procs=3, warmup=1, steps=2)
+    assert r["cores"] == 3 and r["kind"] == "oracle" and r["value"] > 0
+    assert "3 processes" in r["sample"] and "2-2 oracle steps" in r["sample"]

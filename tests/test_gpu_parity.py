@@ -1,6 +1,7 @@
 """CUDA path vs oracle on the five workloads (GPU).
 
-Small layouts are compared element by element over the whole state after every
+Small layouts, and the one-unit sweep up to 2^26+1 parameters (bf16 and fp32
+parameters), are compared element by element over the whole state after every
 step; the full-size 4-block Llama (809.5M parameters, N=8) and the FSDP2 dim-0
 group (243M, N=6) are run at full size and compared on sampled positions (every
 edge of every rank's view, plus 200k random positions) that the oracle tracks
@@ -62,6 +63,24 @@ def test_dim0_n6_full_size_sampled(oracle_lib):
 def test_sweep_small_full_compare(oracle_lib, P, N):
     w = synth.sweep(P, N)
     pu.run_full_parity(w, strategy="full_shard" if P % 2 else "shard_grad_op")
+
+
+@pytest.mark.parametrize("N", [2, 8, 32])
+@pytest.mark.parametrize("P", [(1 << 22) + 1, (1 << 24) + 1, (1 << 26) + 1])
+def test_sweep_full_compare_to_2_26(oracle_lib, P, N):
+    # the sweep compared over the whole state up to 2^26+1 parameters (odd sizes:
+    # padding in the last rank, views off their 16-byte congruence)
+    pu.run_full_parity(synth.sweep(P, N), strategy="full_shard")
+
+
+@pytest.mark.parametrize("N", [2, 4, 8, 16, 32])
+@pytest.mark.parametrize("P", [(1 << 20) + 1, (1 << 24) + 1])
+@pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float32], ids=["bf16grad", "f32grad"])
+def test_sweep_fp32_params_full_compare(oracle_lib, P, N, grad_dtype):
+    # fp32 parameters (the master is the parameter, no bf16 copy); fp32 gradients
+    # beyond N = 8 and bf16 ones beyond N = 16 are staged in replica groups
+    w = synth.sweep(P, N, param_dtype=torch.float32, grad_dtype=grad_dtype)
+    pu.run_full_parity(w, strategy="full_shard" if N % 4 else "shard_grad_op")
 
 
 @pytest.mark.parametrize("P,N", [((1 << 26) + 1, 8), ((1 << 29) + 1, 32), (1 << 29, 2)])

@@ -1,7 +1,8 @@
 """Seeded random layouts (GPU): the staged and the direct kernels of every call
 that has both (the fused step, HSDP, accumulation, ZeRO-1) must agree bit for
-bit, and every fifth layout of the fused step is also compared with the oracle
-element by element.
+bit, and every fifth layout of the fused step, and every fifth layout of the
+rows (HSDP, accumulation, ZeRO-1), is also compared with the oracle element by
+element.
 
 The layouts mix FLAT and DIM0 units, odd and empty tensors, row counts below N,
 1..64 ranks, bf16 and fp32, so that pieces of both alignment classes, ragged
@@ -12,6 +13,7 @@ import pytest
 import torch
 
 import fsdp_sharded_state_gb300 as fs
+import oracle
 from fsdp_sharded_state_gb300 import synth
 
 import parity_util as pu
@@ -129,21 +131,115 @@ def run_rows(w, kind, R):
         fs.fsdp_set_rs_kernel(prev)
 
 
+def _bits(x):
+    return x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16)
+
+
+_ROWS_CACHE = {}
+
+
+def rows_runs(seed):
+    """The layout of `seed`, its R, and the direct and staged runs of its rows (kept for
+    the three row tests of the seed; only the latest seed is held)."""
+    if seed not in _ROWS_CACHE:
+        _ROWS_CACHE.clear()
+        w = random_workload(seed)
+        if w.N > 16:
+            w.N = 16                 # R * N <= 64 replicas for the HSDP call
+        R = 2 + (seed // 2) % 2
+        _ROWS_CACHE[seed] = (w, R, run_rows(w, "direct", R), run_rows(w, "staged", R))
+    return _ROWS_CACHE[seed]
+
+
+@pytest.mark.parametrize("row", ["hsdp", "acc", "zero1"])
 @pytest.mark.parametrize("seed", list(range(0, 40, 2)))
-def test_staged_rows_equal_direct_on_random_layouts(seed):
-    w = random_workload(seed)
-    if w.N > 16:
-        w.N = 16                     # R * N <= 64 replicas for the HSDP call
-    R = 2 + (seed // 2) % 2
-    a = run_rows(w, "direct", R)
-    b = run_rows(w, "staged", R)
-    if "hsdp" in b:
-        for x, y in zip(a["hsdp"], b["hsdp"]):
-            if x is not None:
-                assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16),
-                                   y.view(torch.int32) if y.dtype == torch.float32 else y.view(torch.int16))
-    for x, y in zip(a["acc"], b["acc"]):
-        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
-    for x, y in zip(a["zero1"], b.get("zero1", a["zero1"])):
-        assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16),
-                           y.view(torch.int32) if y.dtype == torch.float32 else y.view(torch.int16))
+def test_staged_rows_equal_direct_on_random_layouts(oracle_lib, seed, row):
+    w, R, a, b = rows_runs(seed)
+    if (seed // 2) % 5 == 0:         # every fifth layout: the direct results against the oracle
+        rows_vs_oracle(w, R, a, row)
+    if row not in b:
+        # the staged kernel does not hold this layout: the call refused it (FSDP_EINVAL)
+        pytest.skip(f"staged {row} kernel refused the layout (N={w.N}, R={R}); nothing to compare")
+    for x, y in zip(a[row], b[row]):
+        if x is not None:
+            assert torch.equal(_bits(x), _bits(y)), (row, w.shapes, w.N)
+
+
+def rows_vs_oracle(w, R, out, row):
+    """One row's results of run_rows (HSDP, accumulation or ZeRO-1) against the oracle,
+    on the same seeded inputs."""
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = pu.oracle_offsets(w)
+    N, F = w.N, O["F"]
+    stride = fs.Layout(w.shapes, w.unit_ids, N, w.mode).stride
+    bf16 = w.param_dtype == torch.bfloat16
+    full = pu.f32(synth.full_params(w, F, O["t_full_off"], device="cuda"))
+    if row == "hsdp":
+        return _hsdp_vs_oracle(w, R, out, sh, O, N, F, stride, bf16, full)
+    if row == "acc":
+        return _acc_vs_oracle(w, out, O, N, F)
+    return _zero1_vs_oracle(w, out, N, bf16)
+
+
+def _hsdp_vs_oracle(w, R, out, sh, O, N, F, stride, bf16, full):
+    # R groups start from the same shards, one step
+    om1, op1 = oracle.reshard(sh, N, w.mode, full, stride, True, bf16)
+    om = np.concatenate([om1] * R)
+    op = np.concatenate([op1] * R) if bf16 else None
+    m, v = np.zeros_like(om), np.zeros_like(om)
+    grads = [synth.grad_replica(w, F, 1, rho * N + q) for rho in range(R) for q in range(N)]
+    oracle.hsdp_adamw(sh, N, w.mode, R, pu.grads_np(grads), stride, om, m, v, param=op, hp=w.hp, step=1)
+    master, gm, gv, param = out["hsdp"]
+    pu.assert_f32_close(pu.f32(master).reshape(-1), om, "hsdp master")
+    pu.assert_f32_close(pu.f32(gm).reshape(-1), m, "hsdp exp_avg")
+    pu.assert_f32_close(pu.f32(gv).reshape(-1), v, "hsdp exp_avg_sq")
+    if bf16:
+        pu.assert_bf16_close(pu.u16(param).reshape(-1), op, "hsdp param")
+
+
+def _acc_vs_oracle(w, out, O, N, F):
+    # 3 micro-batches, logical positions (FLAT padding is not touched)
+    mask = pu.logical(O, w.shapes)
+    ref = [np.zeros(F, np.float32) for _ in range(N)]
+    for mi in range(3):
+        micro = pu.grads_np(synth.grad_replicas(w, F, 10 + mi))
+        for q in range(N):
+            oracle.accumulate(ref[q], micro[q], first=(mi == 0))
+    for q in range(N):
+        assert np.array_equal(pu.f32(out["acc"][q])[mask].view(np.uint32), ref[q][mask].view(np.uint32)), f"acc {q}"
+
+
+def _zero1_vs_oracle(w, out, N, bf16):
+    # the same tensors in a ZeRO-1 layout, two steps
+    zsh = oracle.Shapes(w.shapes)
+    Z = fs.Layout(w.shapes, None, N, fs.FSDP_ZERO1)
+    P = Z.info["numel"]
+    zoffs = [Z.tensor(t)["full_off"] for t in range(len(w.shapes))]
+    zfull = synth.full_params(w, P, zoffs, device="cuda")
+    owners = oracle.zero1_owners(zsh, N)
+    ooff, ostride = pu.oracle_zero1_rows(zsh, N, owners)
+    sizes = [int(np.prod(s) if s else 1) for s in w.shapes]
+    rm = np.zeros(N * max(ostride, 1), np.float32)
+    rv = np.zeros_like(rm)
+    rmaster = None
+    f = pu.f32(zfull)
+    if bf16:
+        rmaster = np.zeros_like(rm)
+        for t, o in enumerate(owners):
+            rmaster[o * ostride + ooff[t]:o * ostride + ooff[t] + sizes[t]] = f[zoffs[t]:zoffs[t] + sizes[t]]
+    rparams = [pu.u16(zfull.to(torch.bfloat16)) if bf16 else f.copy() for _ in range(N)]
+    for t in range(1, 3):
+        g = pu.grads_np(synth.grad_replicas(w, P, 20 + t))
+        rparams = oracle.zero1_adamw(zsh, N, g, ostride, rmaster, rm, rv, rparams, hp=w.hp, step=t)
+    reps, zm, zv = out["zero1"][:N], out["zero1"][N], out["zero1"][N + 1]
+    for q in range(N):
+        if bf16:
+            pu.assert_bf16_close(pu.u16(reps[q]), rparams[q], f"zero1 replica {q}")
+        else:
+            pu.assert_f32_close(pu.f32(reps[q]), rparams[q], f"zero1 replica {q}")
+    gm, gv = pu.f32(zm).reshape(-1), pu.f32(zv).reshape(-1)
+    for k, o in enumerate(owners):
+        a = o * Z.stride + Z.tensor(k)["shard_off"]
+        b = o * ostride + ooff[k]
+        pu.assert_f32_close(gm[a:a + sizes[k]], rm[b:b + sizes[k]], f"zero1 exp_avg t{k}")
+        pu.assert_f32_close(gv[a:a + sizes[k]], rv[b:b + sizes[k]], f"zero1 exp_avg_sq t{k}")

@@ -29,11 +29,7 @@ def W(shapes, units, N, mode, dtype=torch.bfloat16, name="rows"):
     return synth.Workload(name, 11, list(shapes), list(units), N, mode, dtype, dtype, 3, 1e-3)
 
 
-def logical(O, shapes):
-    mask = np.zeros(O["F"], bool)
-    for t, s in enumerate(shapes):
-        mask[O["t_full_off"][t]:O["t_full_off"][t] + int(np.prod(s) if s else 1)] = True
-    return mask
+logical = pu.logical
 
 
 # ---------------------------------------------------------------------------
@@ -175,14 +171,7 @@ def test_hsdp_vs_oracle(oracle_lib, rs_kind, w, R):
 ZSHAPES = [(7, 5), (3,), (9, 2), (4, 4), (11,), (6, 6), (257, 33)]
 
 
-def oracle_zero1_rows(sh, N, owners):
-    """The oracle's packing: each owner's tensors back to back, in tensor order."""
-    sizes = [int(np.prod(s) if s else 1) for s in sh.shapes]
-    off, fill = [], [0] * N
-    for t, o in enumerate(owners):
-        off.append(fill[o])
-        fill[o] += sizes[t]
-    return off, max(fill)
+oracle_zero1_rows = pu.oracle_zero1_rows
 
 
 @pytest.mark.parametrize("shapes,N", [(ZSHAPES, 3), (ZSHAPES, 4), ([(1 << 20,), (1000, 17), (333,)], 2),
