@@ -171,8 +171,8 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample_setup(w, target_s=1.0):
-    """Host inputs for a bounded sample of workload w: the units [0, u_end) whose
+def oracle_sample_setup(w, target_s=1.0, unit=0):
+    """Host inputs for a bounded sample of workload w: the units [unit, u_end) whose
     oracle step takes about target_s seconds (at least one unit)."""
     import numpy as np
 
@@ -180,15 +180,15 @@ def oracle_sample_setup(w, target_s=1.0):
     sh = oracle.Shapes(w.shapes, w.unit_ids)
     O = oracle.layout(sh, w.N, w.mode)
     stride = O["S"]
-    rng = np.random.default_rng(0)
-    u_end = 1
-    numel = int(O["u_numel"][0])
+    rng = np.random.default_rng(unit)
+    u_end = unit + 1
+    numel = int(O["u_numel"][unit])
     # about 2.5e7 elements per second of single-core oracle work at N=4 (measured order)
     budget = int(2.5e7 * target_s * 4 / max(w.N, 1))
     while u_end < O["U"] and numel + int(O["u_numel"][u_end]) <= budget:
         numel += int(O["u_numel"][u_end])
         u_end += 1
-    lo = int(O["u_full_off"][0])
+    lo = int(O["u_full_off"][unit])
     hi = int(O["u_full_off"][u_end - 1] + (w.N * O["u_S"][u_end - 1] if w.mode == 0 else O["u_numel"][u_end - 1]))
     full = np.zeros(O["F"], np.float32)
     full[lo:hi] = rng.normal(0, 0.02, hi - lo)
@@ -207,13 +207,13 @@ def oracle_sample_setup(w, target_s=1.0):
     return st
 
 
-def oracle_step(w, st, t, strategy):
+def oracle_step(w, st, t, strategy, ub=0):
     import oracle
     src = st["param"] if st["param"] is not None else st["master"]
     for _ in range(2 if strategy == "full_shard" else 1):
-        oracle.unshard(st["sh"], w.N, w.mode, src, st["stride"], st["O"]["F"], 0, st["u_end"], out=st["out"])
+        oracle.unshard(st["sh"], w.N, w.mode, src, st["stride"], st["O"]["F"], ub, st["u_end"], out=st["out"])
     oracle.rs_adamw(st["sh"], w.N, w.mode, st["grads"], st["stride"], st["master"], st["m"], st["v"],
-                    param=st["param"], hp=w.hp, step=t, ub=0, ue=st["u_end"])
+                    param=st["param"], hp=w.hp, step=t, ub=ub, ue=st["u_end"])
 
 
 def host_cpu():
@@ -231,6 +231,7 @@ def host_cpu():
 
 
 def cpu_baseline(w, strategy, min_seconds=10.0):
+    """The oracle on one host core: the step on a prefix of the workload's units."""
     st = oracle_sample_setup(w, target_s=1.0)
     t0 = time.perf_counter()
     steps = 0
@@ -245,18 +246,107 @@ def cpu_baseline(w, strategy, min_seconds=10.0):
                       f"({strategy}), single thread, {el:.1f} s", "host": host_cpu()}
 
 
+def _oracle_proc(name, strategy, unit, warmup, steps, min_seconds, barrier, out):
+    """One process of the host-wide oracle run: the unmodified single-threaded oracle
+    step on one unit of its own copy of the workload.  After set-up and `warmup` steps
+    every process waits at the barrier, so the timed steps of all processes overlap;
+    then `steps` steps (or, with steps = 0, as many as fill min_seconds)."""
+    try:
+        import oracle
+        from fsdp_sharded_state_gb300 import synth
+        w = synth.workload(name)
+        st = oracle_sample_setup(w, target_s=0.0, unit=unit)
+        for k in range(warmup):
+            oracle_step(w, st, k + 1, strategy, ub=unit)
+        barrier.wait(timeout=600)
+        t0 = time.perf_counter()
+        k = 0
+        while True:
+            k += 1
+            oracle_step(w, st, warmup + k, strategy, ub=unit)
+            el = time.perf_counter() - t0
+            if (steps and k >= steps) or (not steps and el >= min_seconds):
+                break
+        out.put((unit, st["numel"], k, el, None))
+    except Exception as e:          # reported by the parent
+        try:
+            barrier.abort()
+        except Exception:
+            pass
+        out.put((unit, 0, 0, 0.0, repr(e)))
+
+
+def oracle_host_run(w, strategy, procs=None, warmup=1, steps=0, min_seconds=10.0):
+    """The oracle on every host core: `procs` processes (default: the core count,
+    capped by host memory), each running the unmodified single-threaded oracle step
+    on one unit of its own copy of the workload (process i takes unit i mod U, so
+    the processes cover the units in turn).  The processes start with `spawn` (a
+    fresh interpreter: nothing of this process's CUDA state is inherited) and time
+    their steps together; the aggregate is the parameters all processes stepped over
+    the slowest process's time."""
+    import multiprocessing as mpr
+
+    import oracle
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = oracle.layout(sh, w.N, w.mode)
+    U = O["U"]
+    n = int(O["u_numel"].max())
+    gb = 2 if str(w.grad_dtype).endswith("bfloat16") else 4
+    # host bytes of one process (oracle_sample_setup keeps full-layout buffers): the fp32
+    # full parameters, N gradient replicas, master/m/v and the bf16 copy, the gathered output
+    F, NS = int(O["F"]), w.N * int(O["S"])
+    per_proc = 4 * F + w.N * gb * F + 14 * NS + 4 * F
+    try:
+        host_mem = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    except (ValueError, OSError, AttributeError):
+        host_mem = 16 << 30
+    ncpu = os.cpu_count() or 1
+    if procs is None:
+        procs = max(1, min(ncpu, int(0.4 * host_mem // max(per_proc, 1))))
+    ctx = mpr.get_context("spawn")
+    barrier = ctx.Barrier(procs)
+    out = ctx.Queue()
+    ps = [ctx.Process(target=_oracle_proc, args=(w.name, strategy, i % U, warmup, steps, min_seconds, barrier, out))
+          for i in range(procs)]
+    for p in ps:
+        p.start()
+    import queue
+    res, t_give_up = [], time.time() + 1800
+    while len(res) < len(ps):
+        try:
+            res.append(out.get(timeout=1.0))
+        except queue.Empty:
+            dead = [p.exitcode for p in ps if p.exitcode not in (None, 0)]
+            if dead or time.time() > t_give_up:      # a process died before reporting
+                for p in ps:
+                    if p.is_alive():
+                        p.terminate()
+                raise RuntimeError(f"oracle processes failed (exit codes {dead})")
+    for p in ps:
+        p.join(timeout=60)
+    errs = [r[4] for r in res if r[4]]
+    if errs:
+        raise RuntimeError(f"oracle process failed: {errs[0]}")
+    params = sum(r[1] * r[2] for r in res)
+    el = max(r[3] for r in res)
+    return {"value": params / el, "unit": "params/s", "cores": procs, "kind": "oracle",
+            "sample": f"{procs} processes, process i one unit (i mod {U}) of its own copy of {w.name} "
+                      f"({n} params per unit), {min(r[2] for r in res)}-{max(r[2] for r in res)} oracle steps "
+                      f"({strategy}) each, single-threaded oracle in every process, {el:.1f} s",
+            "host": host_cpu(), "elapsed_s": el}
+
+
 # ---------------------------------------------------------------------------
 # the CUDA path
 # ---------------------------------------------------------------------------
-def run_ours(args, w, rank, world, dist):
+def setup_state(w, dev, rs_kernel="auto"):
+    """The workload's sharded state on the device, resharded from its seeded full
+    parameters, and its N seeded gradient replicas."""
     import torch
 
     import fsdp_sharded_state_gb300 as fs
     from fsdp_sharded_state_gb300 import synth
-
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    fs.fsdp_set_rs_kernel(args.rs_kernel)
+    fs.fsdp_set_rs_kernel(rs_kernel)
     st = fs.ShardedState(w.shapes, w.unit_ids, w.N, w.mode, param_dtype=w.param_dtype, device=dev)
     st.layout.prepare()
     L = st.layout
@@ -265,12 +355,22 @@ def run_ours(args, w, rank, world, dist):
     st.init_from_full(full)
     del full
     grads = synth.grad_replicas(w, st.F, 1, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    info = L.info
+    torch.cuda.synchronize(dev)
+    return st, grads
+
+
+def time_steps(w, st, grads, dev, stream, strategy, steps, warmup, soak, dist=None):
+    """Times `steps` sharded steps after an untimed clock soak and `warmup` steps, then
+    the same number again with events around each fused launch.  Returns the timed
+    region's ms, the per-launch ms of the fused kernel, the algorithmic bytes, whether
+    L2 was flushed between steps, and the clock samples of the whole run."""
+    import torch
+
+    info = st.layout.info
     gb = 2 if w.grad_dtype == torch.bfloat16 else 4
     pb = 2 if w.param_dtype == torch.bfloat16 else 4
     ab = algorithmic_bytes(w.N, info["numel"], info["shard_numel"], info["full_numel"], w.mode, gb, pb)
-    n_unshard = 2 if args.strategy == "full_shard" else 1
+    n_unshard = 2 if strategy == "full_shard" else 1
 
     def step(ev=None):
         for _ in range(n_unshard):
@@ -289,26 +389,25 @@ def run_ours(args, w, rank, world, dist):
     flush = step_bytes < 4 * l2
     scratch = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev) if flush else None
 
-    # clock soak (untimed): bring the clocks to their working point
     with ClockSampler(dev.index) as clk:
-        t_end = time.time() + args.soak
+        t_end = time.time() + soak             # clock soak (untimed): clocks to their working point
         while time.time() < t_end:
             step()
             torch.cuda.synchronize(dev)
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step()
         torch.cuda.synchronize(dev)
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize(dev)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         # the timed steps: no event between the kernels of a step (an event recorded
         # between two kernels ends the programmatic overlap of the second's launch)
         t0.record(stream)
-        for k in range(args.steps):
+        for k in range(steps):
             if flush:
                 scratch.fill_(float(k))
                 sevs[k][0].record(stream)
@@ -321,15 +420,80 @@ def run_ours(args, w, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize(dev)
         # the same steps again with events around the fused kernel: its launch times
-        for k in range(args.steps):
+        for k in range(steps):
             if flush:
                 scratch.fill_(float(k))
             step(evs[k])
         torch.cuda.synchronize(dev)
-    fs.fsdp_check_status(stream)
     ms = sum(a.elapsed_time(b) for a, b in sevs) if flush else t0.elapsed_time(t1)
     rs_ms = [a.elapsed_time(b) for a, b in evs]
-    ms_max = aggregate_max(ms, world, dist)
+    l2_note = ("L2 flushed before every step (a %.0f MB write; the step touches %.3f GB)" % (2 * l2 / 1e6, step_bytes / 1e9)
+               if flush else "inputs larger than L2 (step touches %.2f GB)" % (step_bytes / 1e9))
+    return {"ms": ms, "rs_ms": rs_ms, "ab": ab, "step_bytes": step_bytes, "flush": flush, "l2": l2_note,
+            "n_unshard": n_unshard, "clocks": parse_clocks(clk.out)}
+
+
+def fused_roofline(fs, st, w, meas, workload_name):
+    """The roofline object of the fused kernel from a time_steps() measurement."""
+    peak, peak_kind = load_peaks()
+    rs_avg = statistics.mean(meas["rs_ms"])
+    rs_bytes = meas["ab"]["rs_adamw"]
+    achieved = rs_bytes / (rs_avg * 1e-3) / 1e9
+    kname = "k_rs_adamw_staged" if fs.fsdp_rs_kernel_for(st.layout, w.grad_dtype) == "staged" else "k_rs_adamw"
+    return {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_launch": rs_bytes, "launch_ms": rs_avg,
+            "traffic": profiled_traffic(kname, workload_name), "launch_stats": launch_stats(meas["rs_ms"])}
+
+
+# The configurations timed beside the headline one (the pages' other workloads), one
+# after the other, each freed before the next: the 4-block Llama and the FSDP2 dim-0
+# group as the fused kernel's HBM rate, the tiny MLP as the latency of a step.
+SIDE_CONFIGS = ("llama4", "dim0_n6", "tiny_mlp")
+GATE_GBS = 8000.0 * 0.75          # the pages' target: 75 % of ~8 TB/s
+
+
+def side_config(args, name, dev, stream):
+    import torch
+
+    import fsdp_sharded_state_gb300 as fs
+    from fsdp_sharded_state_gb300 import synth
+    w = synth.workload(name)
+    st, grads = setup_state(w, dev, args.rs_kernel)
+    steps = max(args.steps, 20)
+    meas = time_steps(w, st, grads, dev, stream, args.strategy, steps, max(args.warmup, 3), args.soak)
+    fs.fsdp_check_status(stream)
+    roof = fused_roofline(fs, st, w, meas, name)
+    P = st.P
+    out = {"workload": name, "params": P, "n_ranks_simulated": w.N,
+           "layout": "flat" if w.mode == 0 else "dim0", "strategy": args.strategy,
+           "param_dtype": str(w.param_dtype).replace("torch.", ""),
+           "grad_dtype": str(w.grad_dtype).replace("torch.", ""), "steps": steps,
+           "ms_per_step": meas["ms"] / steps, "params_per_s": P * steps / (meas["ms"] * 1e-3),
+           "step_bytes": meas["step_bytes"], "step_hbm_gbs": meas["step_bytes"] / (meas["ms"] / steps * 1e-3) / 1e9,
+           "l2": meas["l2"], "kernel": roof["kernel"], "launch_ms": roof["launch_ms"],
+           "bytes_per_launch": roof["bytes_per_launch"], "achieved_gbs": roof["achieved"], "frac": roof["frac"],
+           "peak_kind": roof["peak_kind"], "frac_of_8tbs": roof["achieved"] / 8000.0,
+           "gate_75pct_of_8tbs": roof["achieved"] >= GATE_GBS, "launch_stats": roof["launch_stats"],
+           "clocks": meas["clocks"]}
+    if meas["flush"]:
+        out["us_per_step"] = meas["ms"] / steps * 1e3        # latency-bound: the step's time is the figure
+    del st, grads
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, w, rank, world, dist):
+    import torch
+
+    import fsdp_sharded_state_gb300 as fs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    st, grads = setup_state(w, dev, args.rs_kernel)
+    meas = time_steps(w, st, grads, dev, stream, args.strategy, args.steps, args.warmup, args.soak, dist)
+    fs.fsdp_check_status(stream)
+    ms_max = aggregate_max(meas["ms"], world, dist)
 
     # e2e through the public API with host buffers (pinned): every step copies its N
     # gradient replicas host -> device and its updated parameter shards back
@@ -354,14 +518,10 @@ def run_ours(args, w, rank, world, dist):
     torch.cuda.synchronize(dev)
     e2e_ms = aggregate_max(e0.elapsed_time(e1), world, dist)
     del feed
-    clocks = parse_clocks(clk.out)
-    peak, peak_kind = load_peaks()
-    rs_avg = statistics.mean(rs_ms)
-    rs_bytes = ab["rs_adamw"]
-    achieved = rs_bytes / (rs_avg * 1e-3) / 1e9
+    roof = fused_roofline(fs, st, w, meas, w.name)
+    info = st.layout.info
     P = info["numel"]
     launches_per_step = st.launches_per_step(args.strategy, w.grad_dtype)
-    kname = "k_rs_adamw_staged" if fs.fsdp_rs_kernel_for(L, w.grad_dtype) == "staged" else "k_rs_adamw"
     res = {
         "metric": METRIC,
         "value": world * P * args.steps / (ms_max * 1e-3),
@@ -379,20 +539,22 @@ def run_ours(args, w, rank, world, dist):
                    "layout": "flat" if w.mode == 0 else "dim0", "strategy": args.strategy,
                    "param_dtype": str(w.param_dtype).replace("torch.", ""),
                    "grad_dtype": str(w.grad_dtype).replace("torch.", ""),
-                   "master_moments": "float32", "step_bytes": ab["rs_adamw"] + n_unshard * ab["unshard"],
-                   "l2": ("L2 flushed before every step (a %.0f MB write; the step touches %.3f GB)" % (2 * l2 / 1e6, step_bytes / 1e9)
-                          if flush else "inputs larger than L2 (step touches %.2f GB)" % (step_bytes / 1e9)),
+                   "master_moments": "float32", "step_bytes": meas["step_bytes"], "l2": meas["l2"],
                    "clock_soak_s": args.soak, "parallelism": f"replicas x{world}"},
-        "step_hbm_gbs": (ab["rs_adamw"] + n_unshard * ab["unshard"]) / (ms_max / args.steps * 1e-3) / 1e9,
-        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_launch": rs_bytes,
-                     "launch_ms": rs_avg, "traffic": profiled_traffic(kname, w.name),
-                     "launch_stats": launch_stats(rs_ms)},
+        "step_hbm_gbs": meas["step_bytes"] / (ms_max / args.steps * 1e-3) / 1e9,
+        "roofline": roof,
         "e2e": {"value": world * P * args.steps / (e2e_ms * 1e-3), "unit": "params/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+        "clocks": meas["clocks"],
     }
+    del st, grads, host_grads, out_host
+    torch.cuda.empty_cache()
+    if world == 1 and args.side_configs:
+        res["configs"] = {}
+        for name in SIDE_CONFIGS:
+            if name != w.name:
+                res["configs"][name] = side_config(args, name, dev, stream)
     return res
 
 
@@ -503,6 +665,11 @@ def run_row(args, w):
             "clocks": parse_clocks(clk.out)}
 
 
+def torch_dtype_f32():
+    import torch
+    return torch.float32
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -514,6 +681,10 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before warm-up")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-side-configs", dest="side_configs", action="store_false",
+                    help="time the headline workload only (no 'configs' object)")
+    ap.add_argument("--cpu-procs", type=int, default=None,
+                    help="oracle processes of the host-wide CPU baseline (default: the core count)")
     ap.add_argument("--row", choices=["step", "clip", "accum", "hsdp", "zero1"], default="step",
                     help="time a row beyond the core step instead (one JSON line, no cpu baseline)")
     ap.add_argument("--groups", type=int, default=2, help="HSDP replica groups for --row hsdp")
@@ -533,22 +704,17 @@ def main():
             return
         import oracle
         oracle.build()
-        st = oracle_sample_setup(w, target_s=1.0)
-        for k in range(args.warmup):
-            oracle_step(w, st, k + 1, args.strategy)
-        t0 = time.perf_counter()
-        for k in range(args.steps):
-            oracle_step(w, st, args.warmup + k + 1, args.strategy)
-        el = time.perf_counter() - t0
-        v = st["numel"] * args.steps / el
+        # the oracle on every host core: one process per core, each stepping one unit
+        # of its own copy of the workload; a step = one oracle step in every process
+        cb = oracle_host_run(w, args.strategy, procs=args.cpu_procs, warmup=args.warmup, steps=args.steps)
+        v = cb["value"]
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": v, "unit": "params/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["elapsed_s"] * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if w.param_dtype == torch_dtype_f32() else "bf16+f32", "data": "synthetic",
             "config": {"workload": w.name, "strategy": args.strategy},
-            "cpu_baseline": {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
-                             "sample": f"units [0,{st['u_end']}) of {w.name} ({st['numel']} params) per step, "
-                                       "single thread", "host": host_cpu()},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "host")},
             "e2e": {"value": v, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
         return
@@ -565,7 +731,11 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        res["cpu_baseline"] = cpu_baseline(w, args.strategy, args.cpu_seconds)
+        # the host's figure (every core, one oracle process each), with one core's beside it
+        host = oracle_host_run(w, args.strategy, procs=args.cpu_procs, min_seconds=args.cpu_seconds)
+        one = cpu_baseline(w, args.strategy, args.cpu_seconds)
+        res["cpu_baseline"] = {k: host[k] for k in ("value", "unit", "cores", "kind", "sample", "host")}
+        res["cpu_baseline"]["single_core"] = {k: one[k] for k in ("value", "cores", "sample")}
     if rank == 0:
         print(json.dumps(res))
     if dist is not None:
