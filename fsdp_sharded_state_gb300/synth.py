@@ -107,7 +107,16 @@ def sweep(P: int, N: int, param_dtype=torch.bfloat16, grad_dtype=torch.bfloat16)
     return Workload(f"sweep_P{P}_N{N}{suffix}", 5, [(P,)], [0], N, FLAT, param_dtype, grad_dtype, 1, 1e-3)
 
 
-WORKLOADS = {"tiny_mlp": tiny_mlp, "mlp128m": mlp128m, "llama4": llama4, "dim0_n6": dim0_n6}
+def dim0_n6_h2048() -> Workload:
+    """The dim-0 group at hidden 2048 (ffn 5504, vocab 32000; 93.6M parameters): the same
+    dtypes, N and placement rule on a layout small enough for a profiler capture."""
+    w = dim0_n6(hidden=2048, ffn=5504)
+    w.name = "dim0_n6_h2048"
+    return w
+
+
+WORKLOADS = {"tiny_mlp": tiny_mlp, "mlp128m": mlp128m, "llama4": llama4, "dim0_n6": dim0_n6,
+             "dim0_n6_h2048": dim0_n6_h2048}
 
 
 def workload(name: str) -> Workload:
