@@ -84,3 +84,58 @@ def test_noalloc_rejects_tables_beyond_its_scratch():
     rc = fs.lib().fsdp_reduce_scatter_adamw_noalloc(L.handle, 0, 1, ptrs, fs.FSDP_BF16, A, A, A, A, None,
                                                     C.byref(h), 1, None)
     assert rc == -1
+
+
+def test_noalloc_two_host_threads_on_one_stream():
+    # Two host threads call the entry point at the same time on one stream, each for its
+    # own layout and state.  Every call queues its table copy and its kernels together,
+    # so each state ends as the allocating entry point leaves it, bit for bit.
+    import threading
+    wa = synth.Workload("noalloc_a", 7, [(300, 7), (5,), (64, 64)], [0, 1, 1], 4, synth.FLAT,
+                        torch.bfloat16, torch.bfloat16, 2, 1e-3)
+    wb = synth.Workload("noalloc_b", 8, [(37, 5), (3,), (130, 64)], [0, 0, 1], 6, synth.DIM0,
+                        torch.float32, torch.float32, 2, 1e-3)
+    K = 12
+    side = torch.cuda.Stream()
+    jobs = []
+    for w in (wa, wb):
+        ref, got = _pair(w, with_grad_out=True)
+        grads = [synth.grad_replicas(w, ref.F, t) for t in range(1, K + 1)]
+        for t in range(1, K + 1):
+            ref.reduce_scatter_adamw(grads[t - 1], w.hp, step=t)
+        jobs.append((w, ref, got, grads))
+    torch.cuda.synchronize()
+    lib = fs.lib()
+    errors = []
+    start = threading.Barrier(2)
+
+    def worker(w, st, grads):
+        try:
+            h = fs.AdamWHparams(*w.hp)
+            gdt = fs.FSDP_BF16 if w.grad_dtype == torch.bfloat16 else fs.FSDP_F32
+            ptrs = [(C.c_void_p * w.N)(*[g.data_ptr() for g in gs]) for gs in grads]
+            start.wait()
+            for t in range(1, K + 1):
+                rc = lib.fsdp_reduce_scatter_adamw_noalloc(
+                    st.layout.handle, 0, st.layout.n_units, ptrs[t - 1], gdt, st.master.data_ptr(),
+                    st.exp_avg.data_ptr(), st.exp_avg_sq.data_ptr(),
+                    st.param.data_ptr() if st.param is not None else None, st.grad_out.data_ptr(), C.byref(h), t,
+                    side.cuda_stream)
+                assert rc == 0, fs.fsdp_error_string(rc)
+        except BaseException as e:          # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(w, got, grads)) for w, _, got, grads in jobs]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    side.synchronize()
+    fs.fsdp_check_status(side)
+    assert not errors, errors
+    for w, ref, got, _ in jobs:
+        for name in ("master", "exp_avg", "exp_avg_sq", "grad_out", "param"):
+            a, b = getattr(ref, name), getattr(got, name)
+            if a is not None:
+                assert torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+                                   b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32)), (w.name, name)
