@@ -83,17 +83,28 @@ def kernel_src_hash(kernel="k_rs_adamw"):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel, workload):
+def profiled_traffic(kernel, workload, with_source=False):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, or None when there is none or the kernel source changed since."""
+    workload, or None when there is none or the kernel source changed since.  A
+    summary taken on a smaller case of the same layout class carries `scaled_from`:
+    its bytes were scaled to this workload by the ratio of logical parameters.
+    with_source=True also returns where the figure comes from."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
-    if not os.path.exists(p):
-        return None
-    with open(p) as f:
-        d = json.load(f)
-    if d.get("kernel_src_sha256_16") != kernel_src_hash(kernel):
-        return None
-    return d.get("dram_bytes_per_launch")
+    d = None
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("kernel_src_sha256_16") != kernel_src_hash(kernel):
+            d = None
+    v = d.get("dram_bytes_per_launch") if d else None
+    if not with_source:
+        return v
+    src = None
+    if d is not None:
+        sf = d.get("scaled_from")
+        src = (f"ncu on {sf['workload']}, scaled x{d['scale']:.4f} by logical parameters" if sf
+               else f"ncu on {workload}")
+    return v, src
 
 
 def launch_stats(ms):
@@ -440,9 +451,10 @@ def fused_roofline(fs, st, w, meas, workload_name):
     rs_bytes = meas["ab"]["rs_adamw"]
     achieved = rs_bytes / (rs_avg * 1e-3) / 1e9
     kname = "k_rs_adamw_staged" if fs.fsdp_rs_kernel_for(st.layout, w.grad_dtype) == "staged" else "k_rs_adamw"
+    traffic, traffic_src = profiled_traffic(kname, workload_name, with_source=True)
     return {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_kind": peak_kind, "bytes_per_launch": rs_bytes, "launch_ms": rs_avg,
-            "traffic": profiled_traffic(kname, workload_name), "launch_stats": launch_stats(meas["rs_ms"])}
+            "traffic": traffic, "traffic_source": traffic_src, "launch_stats": launch_stats(meas["rs_ms"])}
 
 
 # The configurations timed beside the headline one (the pages' other workloads), one
@@ -472,6 +484,7 @@ def side_config(args, name, dev, stream):
            "step_bytes": meas["step_bytes"], "step_hbm_gbs": meas["step_bytes"] / (meas["ms"] / steps * 1e-3) / 1e9,
            "l2": meas["l2"], "kernel": roof["kernel"], "launch_ms": roof["launch_ms"],
            "bytes_per_launch": roof["bytes_per_launch"], "achieved_gbs": roof["achieved"], "frac": roof["frac"],
+           "traffic": roof["traffic"], "traffic_source": roof["traffic_source"],
            "peak_kind": roof["peak_kind"], "frac_of_8tbs": roof["achieved"] / 8000.0,
            "gate_75pct_of_8tbs": roof["achieved"] >= GATE_GBS, "launch_stats": roof["launch_stats"],
            "clocks": meas["clocks"]}
