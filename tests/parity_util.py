@@ -127,32 +127,52 @@ def run_full_parity(w: synth.Workload, steps=None, strategy="full_shard", with_g
     return st, ulps
 
 
-def sample_points(w: synth.Workload, O, n_random=200_000, seed=0):
-    """(rank, j) sample of shard positions: the edges of every rank's view of every
-    unit/tensor plus a seeded random set; padding positions kept (checked for +0)."""
+TILE = 2048          # elements of one kernel tile (256 threads x 8)
+
+
+def sample_points(w: synth.Workload, O, n_random=200_000, seed=0, tile_frac=0.01):
+    """(rank, j) sample of shard positions, with each one's full-layout index (-1 for
+    padding, which is checked for +0): for every rank, the whole tile windows touching each
+    boundary of every unit (FLAT) or tensor slot (DIM0) -- so every segment, rank and padding
+    edge; a seeded random `tile_frac` of all tile windows, every element of each; and
+    n_random seeded random positions."""
     sh = oracle.Shapes(w.shapes, w.unit_ids)
     rng = np.random.default_rng(seed)
-    ranks, js = [], []
-    S = O["S"]
-    edges = set()
+    S = int(O["S"])
+    bounds = set()
     if w.mode == oracle.FLAT:
         for u in range(O["U"]):
-            a, n = O["u_shard_off"][u], O["u_S"][u]
-            for j in list(range(a, min(a + 9, a + n))) + list(range(max(a, a + n - 9), a + n)):
-                edges.add(j)
+            a, n = int(O["u_shard_off"][u]), int(O["u_S"][u])
+            own_last = int(O["u_numel"][u]) - (w.N - 1) * n           # logical elements of the last rank
+            bounds.update((a, a + n, a + min(max(own_last, 0), n)))
     else:
-        for t in range(len(w.shapes)):
-            a, n = O["t_shard_off"][t], O["t_slot"][t]
-            for j in list(range(a, min(a + 9, a + n))) + list(range(max(a, a + n - 9), a + n)):
-                edges.add(j)
+        for t, shp in enumerate(w.shapes):
+            a, n = int(O["t_shard_off"][t]), int(O["t_slot"][t])
+            bounds.update((a, a + n))
+            d0 = shp[0] if shp else 1
+            inner = n // max(int(O["t_rows"][t]), 1) if n else 0
+            for r in range(w.N):                                     # each rank's first padding row
+                own = min(max(d0 - r * int(O["t_rows"][t]), 0), int(O["t_rows"][t]))
+                bounds.add(a + own * inner)
+    win = []
+    for b in sorted(bounds):                                          # tiles touching a boundary
+        lo = (max(b - 1, 0) // TILE) * TILE
+        win.append(np.arange(lo, min(lo + 2 * TILE, S), dtype=np.int64))
+    edge_j = np.unique(np.concatenate(win)) if win else np.zeros(0, np.int64)
+    ranks, js = [], []
     for r in range(w.N):
-        e = np.array(sorted(edges), np.int64)
-        ranks.append(np.full(e.size, r))
-        js.append(e)
-    rr = rng.integers(0, w.N, n_random)
-    jj = rng.integers(0, S, n_random)
-    ranks.append(rr)
-    js.append(jj)
+        ranks.append(np.full(edge_j.size, r, np.int64))
+        js.append(edge_j)
+    n_tiles = (S + TILE - 1) // TILE
+    k = max(1, int(round(tile_frac * w.N * n_tiles)))
+    pick = rng.choice(w.N * n_tiles, size=min(k, w.N * n_tiles), replace=False)
+    for p in pick:                                                     # whole random tiles
+        r, t = divmod(int(p), n_tiles)
+        j = np.arange(t * TILE, min((t + 1) * TILE, S), dtype=np.int64)
+        ranks.append(np.full(j.size, r, np.int64))
+        js.append(j)
+    ranks.append(rng.integers(0, w.N, n_random))
+    js.append(rng.integers(0, S, n_random))
     r = np.concatenate(ranks)
     j = np.concatenate(js)
     fi = np.empty_like(j)

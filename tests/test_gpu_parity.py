@@ -3,9 +3,10 @@
 Small layouts, and the one-unit sweep up to 2^26+1 parameters (bf16 and fp32
 parameters), are compared element by element over the whole state after every
 step; the full-size 4-block Llama (809.5M parameters, N=8) and the FSDP2 dim-0
-group (243M, N=6) are run at full size and compared on sampled positions (every
-edge of every rank's view, plus 200k random positions) that the oracle tracks
-across the steps.  Most runs also request the reduced-gradient output; the last
+group (243M, N=6) are run at full size and compared on sampled positions that the
+oracle tracks across the steps: every element of each tile touching a unit, tensor,
+rank or padding boundary, every element of a seeded 1 % of all tiles, and random
+positions; every padding element of every state array is checked for +0.  Most runs also request the reduced-gradient output; the last
 tests run the configurations bench.py times (no such output, so the kernel
 instance the bench launches) at full size.
 """
