@@ -108,11 +108,15 @@ struct HsdpAdamw {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) adamw1(sc, gg[k], p[k], m[k], v[k]);
                 const int64_t e = rho * copy + x;
-                st4(master + e, make_float4(p[0], p[1], p[2], p[3]));
-                st4(exp_avg + e, make_float4(m[0], m[1], m[2], m[3]));
-                st4(exp_avg_sq + e, make_float4(v[0], v[1], v[2], v[3]));
+                // streaming stores (st.global.cs, evict-first in L2): fewer of this call's
+                // dirty lines are left in L2 for the next call to write back (measured on
+                // GB300, calls back to back on the 128 MiB fp32 layout, R = 2: 430 -> 413 us;
+                // the 4-block Llama unchanged)
+                __stcs(reinterpret_cast<float4*>(master + e), make_float4(p[0], p[1], p[2], p[3]));
+                __stcs(reinterpret_cast<float4*>(exp_avg + e), make_float4(m[0], m[1], m[2], m[3]));
+                __stcs(reinterpret_cast<float4*>(exp_avg_sq + e), make_float4(v[0], v[1], v[2], v[3]));
                 if (PARAM)
-                    *reinterpret_cast<uint2*>(param + e) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
+                    __stcs(reinterpret_cast<uint2*>(param + e), make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])));
             }
         } else if (live) {
             const int64_t a = x > g.s0 ? x : g.s0;
@@ -511,10 +515,12 @@ struct Accumulate {
         }
         release();
         if (fast) {
+            // streaming stores (st.global.cs): measured on GB300, accumulation calls back to
+            // back on the 128 MiB fp32 layout 246 -> 242 us, the 4-block Llama unchanged
 #pragma unroll
             for (int r = 0; r < kMaxQ; ++r) {
                 if (r >= k) break;
-                st4(acc[g.q + r] + x, out[r]);
+                __stcs(reinterpret_cast<float4*>(acc[g.q + r] + x), out[r]);
             }
         } else if (live) {
             const int64_t lo = x > g.s0 ? x : g.s0;
