@@ -182,6 +182,15 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
+def _normal_block(rng, n, std, block=1 << 22):
+    """n fp32 values N(0, std): one seeded block of up to 4M draws, repeated (the oracle's
+    speed does not depend on the values, and drawing hundreds of millions of normals
+    would take the host longer than the steps it times)."""
+    import numpy as np
+    x = rng.standard_normal(min(n, block), dtype=np.float32) * np.float32(std)
+    return np.resize(x, n)
+
+
 def oracle_sample_setup(w, target_s=1.0, unit=0):
     """Host inputs for a bounded sample of workload w: the units [unit, u_end) whose
     oracle step takes about target_s seconds (at least one unit)."""
@@ -202,18 +211,18 @@ def oracle_sample_setup(w, target_s=1.0, unit=0):
     lo = int(O["u_full_off"][unit])
     hi = int(O["u_full_off"][u_end - 1] + (w.N * O["u_S"][u_end - 1] if w.mode == 0 else O["u_numel"][u_end - 1]))
     full = np.zeros(O["F"], np.float32)
-    full[lo:hi] = rng.normal(0, 0.02, hi - lo)
+    full[lo:hi] = _normal_block(rng, hi - lo, 0.02)
     gdt = np.uint16 if str(w.grad_dtype).endswith("bfloat16") else np.float32
     grads = []
     for _ in range(w.N):
         g = np.zeros(O["F"], gdt)
-        x = rng.normal(0, w.grad_std, hi - lo).astype(np.float32)
+        x = _normal_block(rng, hi - lo, w.grad_std)
         g[lo:hi] = oracle.bf16_rne(x) if gdt == np.uint16 else x
         grads.append(g)
     bf16 = gdt == np.uint16 or str(w.param_dtype).endswith("bfloat16")
     master, param = oracle.reshard(sh, w.N, w.mode, full, stride, True, bf16)
     st = {"sh": sh, "O": O, "stride": stride, "grads": grads, "master": master, "param": param,
-          "m": np.zeros_like(master), "v": np.zeros_like(master), "u_end": u_end, "numel": numel,
+          "m": np.full_like(master, 0.0), "v": np.full_like(master, 0.0), "u_end": u_end, "numel": numel,
           "out": np.zeros(O["F"], np.uint16 if bf16 else np.float32)}
     return st
 
@@ -257,6 +266,19 @@ def cpu_baseline(w, strategy, min_seconds=10.0):
                       f"({strategy}), single thread, {el:.1f} s", "host": host_cpu()}
 
 
+def unit_workload(w, unit):
+    """The tensors of one unit of w as a workload of its own (one unit, the same N, mode,
+    dtypes and hyper-parameters): a FLAT unit's layout, and so the oracle's arithmetic on
+    it, does not depend on the other units, and its buffers are the unit's size."""
+    import copy
+    idx = [t for t, u in enumerate(w.unit_ids) if u == unit]
+    ws = copy.copy(w)
+    ws.shapes = [w.shapes[t] for t in idx]
+    ws.unit_ids = [0] * len(idx)
+    ws.ones = [k for k, t in enumerate(idx) if t in set(w.ones)]
+    return ws
+
+
 def _oracle_proc(name, strategy, unit, warmup, steps, min_seconds, barrier, out):
     """One process of the host-wide oracle run: the unmodified single-threaded oracle
     step on one unit of its own copy of the workload.  After set-up and `warmup` steps
@@ -265,16 +287,16 @@ def _oracle_proc(name, strategy, unit, warmup, steps, min_seconds, barrier, out)
     try:
         import oracle
         from fsdp_sharded_state_gb300 import synth
-        w = synth.workload(name)
-        st = oracle_sample_setup(w, target_s=0.0, unit=unit)
+        w = unit_workload(synth.workload(name), unit)
+        st = oracle_sample_setup(w, target_s=0.0)
         for k in range(warmup):
-            oracle_step(w, st, k + 1, strategy, ub=unit)
-        barrier.wait(timeout=600)
+            oracle_step(w, st, k + 1, strategy)
+        barrier.wait(timeout=1800)
         t0 = time.perf_counter()
         k = 0
         while True:
             k += 1
-            oracle_step(w, st, warmup + k, strategy, ub=unit)
+            oracle_step(w, st, warmup + k, strategy)
             el = time.perf_counter() - t0
             if (steps and k >= steps) or (not steps and el >= min_seconds):
                 break
@@ -291,10 +313,10 @@ def oracle_host_run(w, strategy, procs=None, warmup=1, steps=0, min_seconds=10.0
     """The oracle on every host core: `procs` processes (default: the core count,
     capped by host memory), each running the unmodified single-threaded oracle step
     on one unit of its own copy of the workload (process i takes unit i mod U, so
-    the processes cover the units in turn).  The processes start with `spawn` (a
-    fresh interpreter: nothing of this process's CUDA state is inherited) and time
-    their steps together; the aggregate is the parameters all processes stepped over
-    the slowest process's time."""
+    the processes cover the units in turn; each builds only that unit's tensors).  The
+    processes start with `spawn` (a fresh interpreter: nothing of this process's CUDA
+    state is inherited) and time their steps together; the aggregate is the parameters
+    all processes stepped over the slowest process's time."""
     import multiprocessing as mpr
 
     import oracle
@@ -303,17 +325,21 @@ def oracle_host_run(w, strategy, procs=None, warmup=1, steps=0, min_seconds=10.0
     U = O["U"]
     n = int(O["u_numel"].max())
     gb = 2 if str(w.grad_dtype).endswith("bfloat16") else 4
-    # host bytes of one process (oracle_sample_setup keeps full-layout buffers): the fp32
-    # full parameters, N gradient replicas, master/m/v and the bf16 copy, the gathered output
-    F, NS = int(O["F"]), w.N * int(O["S"])
-    per_proc = 4 * F + w.N * gb * F + 14 * NS + 4 * F
+    # host bytes of one process (its unit's full-layout buffers): the fp32 full parameters,
+    # N gradient replicas, master/m/v and the bf16 copy, the gathered output
+    per_proc = 0
+    for u in range(U):
+        ws = unit_workload(w, u)
+        Ou = oracle.layout(oracle.Shapes(ws.shapes, ws.unit_ids), ws.N, ws.mode)
+        F, NS = int(Ou["F"]), w.N * int(Ou["S"])
+        per_proc = max(per_proc, 4 * F + w.N * gb * F + 14 * NS + 4 * F)
     try:
         host_mem = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
     except (ValueError, OSError, AttributeError):
         host_mem = 16 << 30
     ncpu = os.cpu_count() or 1
     if procs is None:
-        procs = max(1, min(ncpu, int(0.4 * host_mem // max(per_proc, 1))))
+        procs = max(1, min(ncpu, int(0.55 * host_mem // max(per_proc, 1))))
     ctx = mpr.get_context("spawn")
     barrier = ctx.Barrier(procs)
     out = ctx.Queue()
@@ -322,7 +348,7 @@ def oracle_host_run(w, strategy, procs=None, warmup=1, steps=0, min_seconds=10.0
     for p in ps:
         p.start()
     import queue
-    res, t_give_up = [], time.time() + 1800
+    res, t_give_up = [], time.time() + 3600
     while len(res) < len(ps):
         try:
             res.append(out.get(timeout=1.0))
@@ -342,7 +368,8 @@ def oracle_host_run(w, strategy, procs=None, warmup=1, steps=0, min_seconds=10.0
     el = max(r[3] for r in res)
     return {"value": params / el, "unit": "params/s", "cores": procs, "kind": "oracle",
             "sample": f"{procs} processes, process i one unit (i mod {U}) of its own copy of {w.name} "
-                      f"({n} params per unit), {min(r[2] for r in res)}-{max(r[2] for r in res)} oracle steps "
+                      f"({n} params per unit; inputs N(0, sigma) from a repeated block of 4M seeded draws), "
+                      f"{min(r[2] for r in res)}-{max(r[2] for r in res)} oracle steps "
                       f"({strategy}) each, single-threaded oracle in every process, {el:.1f} s",
             "host": host_cpu(), "elapsed_s": el}
 
@@ -492,6 +519,13 @@ def side_config(args, name, dev, stream):
         out["us_per_step"] = meas["ms"] / steps * 1e3        # latency-bound: the step's time is the figure
     del st, grads
     torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        # the oracle on this workload, on every host core (one oracle process per core)
+        import oracle
+        oracle.build()
+        cb = oracle_host_run(w, args.strategy, procs=args.cpu_procs, warmup=0, min_seconds=args.cpu_seconds_side)
+        out["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        out["cpu_baseline"]["per_process"] = cb["value"] / cb["cores"]
     return out
 
 
@@ -696,6 +730,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-side-configs", dest="side_configs", action="store_false",
                     help="time the headline workload only (no 'configs' object)")
+    ap.add_argument("--cpu-seconds-side", type=float, default=8.0,
+                    help="seconds of host-wide oracle steps for each side configuration")
     ap.add_argument("--cpu-procs", type=int, default=None,
                     help="oracle processes of the host-wide CPU baseline (default: the core count)")
     ap.add_argument("--row", choices=["step", "clip", "accum", "hsdp", "zero1"], default="step",

@@ -101,3 +101,37 @@ def test_oracle_host_run_spawns_one_process_per_core():
     r = bench.oracle_host_run(synth.tiny_mlp(), "full_shard", procs=3, warmup=1, steps=2)
     assert r["cores"] == 3 and r["kind"] == "oracle" and r["value"] > 0
     assert "3 processes" in r["sample"] and "2-2 oracle steps" in r["sample"]
+
+
+def test_unit_workload_steps_like_its_unit_of_the_whole():
+    # A host-wide oracle process builds one unit's tensors only: its step must give that
+    # unit's shard of the whole workload's step, bit for bit (a FLAT unit's layout and
+    # arithmetic do not depend on the other units).
+    import numpy as np
+    import oracle
+    oracle.build()
+    w = synth.llama4(blocks=3, hidden=64, ffn=176, N=8)
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = oracle.layout(sh, w.N, w.mode)
+    rng = np.random.default_rng(3)
+    full = rng.normal(0, 0.02, O["F"]).astype(np.float32)
+    grads = [oracle.bf16_rne(rng.normal(0, 1e-3, O["F"]).astype(np.float32)) for _ in range(w.N)]
+    S = O["S"]
+    master, param = oracle.reshard(sh, w.N, w.mode, full, S, True, True)
+    m, v = np.zeros_like(master), np.zeros_like(master)
+    oracle.rs_adamw(sh, w.N, w.mode, grads, S, master, m, v, param=param, hp=w.hp, step=1)
+    for u in range(O["U"]):
+        ws = bench.unit_workload(w, u)
+        shu = oracle.Shapes(ws.shapes, ws.unit_ids)
+        Ou = oracle.layout(shu, ws.N, ws.mode)
+        a, n, f0 = int(O["u_shard_off"][u]), int(O["u_S"][u]), int(O["u_full_off"][u])
+        assert Ou["U"] == 1 and Ou["S"] == n and Ou["F"] == w.N * n
+        fu = full[f0:f0 + Ou["F"]].copy()
+        gu = [g[f0:f0 + Ou["F"]].copy() for g in grads]
+        mu, pu_ = oracle.reshard(shu, ws.N, ws.mode, fu, n, True, True)
+        mm, vv = np.zeros_like(mu), np.zeros_like(mu)
+        oracle.rs_adamw(shu, ws.N, ws.mode, gu, n, mu, mm, vv, param=pu_, hp=w.hp, step=1)
+        for r in range(w.N):
+            assert np.array_equal(mu[r * n:(r + 1) * n].view(np.uint32),
+                                  master[r * S + a:r * S + a + n].view(np.uint32))
+            assert np.array_equal(pu_[r * n:(r + 1) * n], param[r * S + a:r * S + a + n])
