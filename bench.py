@@ -374,6 +374,36 @@ def oracle_host_run(w, strategy, procs=None, warmup=1, steps=0, min_seconds=10.0
             "host": host_cpu(), "elapsed_s": el}
 
 
+def oracle_one_run(w, strategy, warmup=1, steps=0, min_seconds=10.0):
+    """The single-process form of oracle_host_run: this process, one core, one unit."""
+    ws = unit_workload(w, 0)
+    st = oracle_sample_setup(ws, target_s=0.0)
+    for k in range(warmup):
+        oracle_step(ws, st, k + 1, strategy)
+    t0 = time.perf_counter()
+    k = 0
+    while True:
+        k += 1
+        oracle_step(ws, st, warmup + k, strategy)
+        el = time.perf_counter() - t0
+        if (steps and k >= steps) or (not steps and el >= min_seconds):
+            break
+    return {"value": st["numel"] * k / el, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": f"1 process, unit 0 of {w.name} ({st['numel']} params), {k} oracle steps ({strategy}), "
+                      f"single thread, {el:.1f} s", "host": host_cpu(), "elapsed_s": el}
+
+
+def oracle_host_or_one(w, strategy, procs=None, warmup=1, steps=0, min_seconds=10.0):
+    """oracle_host_run; if that fails (a process died, the host ran short of memory),
+    the same run in this process on one core, with the failure recorded beside it."""
+    try:
+        return oracle_host_run(w, strategy, procs=procs, warmup=warmup, steps=steps, min_seconds=min_seconds)
+    except Exception as e:
+        r = oracle_one_run(w, strategy, warmup=warmup, steps=steps, min_seconds=min_seconds)
+        r["host_run_failed"] = repr(e)[:300]
+        return r
+
+
 # ---------------------------------------------------------------------------
 # the CUDA path
 # ---------------------------------------------------------------------------
@@ -523,8 +553,9 @@ def side_config(args, name, dev, stream):
         # the oracle on this workload, on every host core (one oracle process per core)
         import oracle
         oracle.build()
-        cb = oracle_host_run(w, args.strategy, procs=args.cpu_procs, warmup=0, min_seconds=args.cpu_seconds_side)
-        out["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cb = oracle_host_or_one(w, args.strategy, procs=args.cpu_procs, warmup=0, min_seconds=args.cpu_seconds_side)
+        out["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "host_run_failed")
+                               if k in cb}
         out["cpu_baseline"]["per_process"] = cb["value"] / cb["cores"]
     return out
 
@@ -755,7 +786,7 @@ def main():
         oracle.build()
         # the oracle on every host core: one process per core, each stepping one unit
         # of its own copy of the workload; a step = one oracle step in every process
-        cb = oracle_host_run(w, args.strategy, procs=args.cpu_procs, warmup=args.warmup, steps=args.steps)
+        cb = oracle_host_or_one(w, args.strategy, procs=args.cpu_procs, warmup=args.warmup, steps=args.steps)
         v = cb["value"]
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": v, "unit": "params/s", "n_gpus": args.gpus,
@@ -763,7 +794,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if w.param_dtype == torch_dtype_f32() else "bf16+f32", "data": "synthetic",
             "config": {"workload": w.name, "strategy": args.strategy},
-            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "host")},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "host", "host_run_failed")
+                             if k in cb},
             "e2e": {"value": v, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
         return
@@ -781,9 +813,10 @@ def main():
         import oracle
         oracle.build()
         # the host's figure (every core, one oracle process each), with one core's beside it
-        host = oracle_host_run(w, args.strategy, procs=args.cpu_procs, min_seconds=args.cpu_seconds)
+        host = oracle_host_or_one(w, args.strategy, procs=args.cpu_procs, min_seconds=args.cpu_seconds)
         one = cpu_baseline(w, args.strategy, args.cpu_seconds)
-        res["cpu_baseline"] = {k: host[k] for k in ("value", "unit", "cores", "kind", "sample", "host")}
+        res["cpu_baseline"] = {k: host[k] for k in ("value", "unit", "cores", "kind", "sample", "host", "host_run_failed")
+                               if k in host}
         res["cpu_baseline"]["single_core"] = {k: one[k] for k in ("value", "cores", "sample")}
     if rank == 0:
         print(json.dumps(res))

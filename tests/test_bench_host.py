@@ -135,3 +135,19 @@ def test_unit_workload_steps_like_its_unit_of_the_whole():
             assert np.array_equal(mu[r * n:(r + 1) * n].view(np.uint32),
                                   master[r * S + a:r * S + a + n].view(np.uint32))
             assert np.array_equal(pu_[r * n:(r + 1) * n], param[r * S + a:r * S + a + n])
+
+
+def test_oracle_host_run_failure_falls_back_to_one_process():
+    # a child that fails (here: its workload name is unknown, so it cannot rebuild it) is
+    # noticed at once; the bench then times the oracle in its own process and says why
+    import time
+    import oracle
+    oracle.build()
+    w = synth.tiny_mlp()
+    w.name = "no_such_workload"
+    t0 = time.time()
+    with pytest.raises(RuntimeError):
+        bench.oracle_host_run(w, "full_shard", procs=2, warmup=0, steps=1)
+    assert time.time() - t0 < 120
+    r = bench.oracle_host_or_one(w, "full_shard", procs=2, warmup=0, steps=2)
+    assert r["cores"] == 1 and r["value"] > 0 and "KeyError" in r["host_run_failed"]
