@@ -451,11 +451,11 @@ def time_steps(w, st, grads, dev, stream, strategy, steps, warmup, soak, dist=No
 
     # A step that touches less than 4x L2 would partly run from L2 if steps ran back to
     # back: then every timed step is bracketed by its own events and preceded by a write
-    # of a scratch buffer twice the L2 (outside the step's events).
+    # of a scratch buffer four times the L2 (outside the step's events).
     step_bytes = ab["rs_adamw"] + n_unshard * ab["unshard"]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = step_bytes < 4 * l2
-    scratch = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev) if flush else None
+    scratch = torch.empty(4 * l2 // 4 + 1, dtype=torch.float32, device=dev) if flush else None
 
     with ClockSampler(dev.index) as clk:
         t_end = time.time() + soak             # clock soak (untimed): clocks to their working point
@@ -495,7 +495,7 @@ def time_steps(w, st, grads, dev, stream, strategy, steps, warmup, soak, dist=No
         torch.cuda.synchronize(dev)
     ms = sum(a.elapsed_time(b) for a, b in sevs) if flush else t0.elapsed_time(t1)
     rs_ms = [a.elapsed_time(b) for a, b in evs]
-    l2_note = ("L2 flushed before every step (a %.0f MB write; the step touches %.3f GB)" % (2 * l2 / 1e6, step_bytes / 1e9)
+    l2_note = ("L2 flushed before every step (a %.0f MB write; the step touches %.3f GB)" % (4 * l2 / 1e6, step_bytes / 1e9)
                if flush else "inputs larger than L2 (step touches %.2f GB)" % (step_bytes / 1e9))
     return {"ms": ms, "rs_ms": rs_ms, "ab": ab, "step_bytes": step_bytes, "flush": flush, "l2": l2_note,
             "n_unshard": n_unshard, "clocks": parse_clocks(clk.out)}
