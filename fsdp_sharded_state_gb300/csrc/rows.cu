@@ -570,12 +570,20 @@ k_zero1_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, 
 // reads 509 MB from DRAM instead of 515 MB (537 MB algorithmic), and pass 1 leaves fewer
 // lines to write back.
 constexpr double kClipKeepFrac = 0.25;
+std::map<int, int64_t> g_keep_cache;             // per device, under g_grid_mu
 int64_t clip_keep_tiles() {
     int dev = 0, l2 = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0)
-        return 0;
-    return int64_t(kClipKeepFrac * double(l2)) / (kTileElems * int64_t(sizeof(float)));
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    {
+        std::lock_guard<std::mutex> lk(g_grid_mu);
+        auto it = g_keep_cache.find(dev);
+        if (it != g_keep_cache.end()) return it->second;
+    }
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0) return 0;
+    const int64_t tiles = int64_t(kClipKeepFrac * double(l2)) / (kTileElems * int64_t(sizeof(float)));
+    std::lock_guard<std::mutex> lk(g_grid_mu);
+    g_keep_cache[dev] = tiles;
+    return tiles;
 }
 
 int ptrs_ok(const void* const* v, int n) {
