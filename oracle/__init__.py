@@ -187,6 +187,22 @@ def state_bytes(sh, N, mode, stage, rank, physical, pb, gb, ob, step_bytes=0):
     return tuple(int(x) for x in out)
 
 
+NO_SHARD, ZERO1_OPT, SHARD_GRAD_OP, FULL_SHARD, HYBRID_SHARD = 0, 1, 2, 3, 4
+
+
+def collective_payload(sh, N, mode, strategy, R=1):
+    """Per-rank collective payload of one step: (elems, bus) with elems = all-reduce
+    input, forward all-gather, backward all-gather, reduce-scatter input, broadcast
+    (logical elements) and bus = elements a rank sends under ring algorithms."""
+    elems = np.zeros(5, np.int64)
+    bus = C.c_double()
+    rc = lib().oracle_collective_payload(*sh.args(), C.c_int32(N), C.c_int32(mode), C.c_int32(strategy),
+                                         C.c_int32(R), _p(elems), C.byref(bus))
+    if rc != 0:
+        raise ValueError("oracle_collective_payload rejected the arguments")
+    return [int(x) for x in elems], bus.value
+
+
 def rs_clip_adamw(sh, N, mode, grads, stride, master, m, v, max_norm, param=None, grad_out=None,
                   hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step=1, ub=0, ue=None):
     """Reduce-scatter, sharded clip_grad_norm_, AdamW; in place.  Returns the norm."""

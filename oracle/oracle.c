@@ -459,6 +459,47 @@ int oracle_state_bytes(int32_t T, const int32_t* ndim, const int64_t* dims, cons
     return 0;
 }
 
+/* Collective payload of one training step, per rank ([ZeRO-state] "Logical Payload
+ * 模型": the logical total of each collective's input buffer, in elements, not the
+ * bytes a ring algorithm moves over links).  strategy: 0 NO_SHARD (DDP: one all-reduce
+ * of the gradient), 1 ZeRO-1 (ZeroRedundancyOptimizer: the same all-reduce, then the
+ * updated parameters synchronised by broadcast, about P), 2 SHARD_GRAD_OP (forward
+ * all-gather, gradient reduce-scatter), 3 FULL_SHARD (forward and backward all-gather,
+ * reduce-scatter), 4 HYBRID_SHARD with R replica groups of N ranks ([FSDP-ch18] §18.9:
+ * the FULL_SHARD collectives inside a group, then one all-reduce of the reduced shard,
+ * S elements, across the groups).  R must be 1 for the other strategies.
+ * elems[0..4] = all-reduce input, forward all-gather, backward all-gather,
+ * reduce-scatter input, broadcast.
+ * *bus = elements one rank sends (and receives) under ring algorithms: an all-reduce
+ * over n ranks 2(n-1)/n times its input (the same page section); an all-gather or a
+ * reduce-scatter over N ranks (N-1)/N times the full buffer (each rank passes on N-1 of
+ * the N chunks); the broadcast: each rank receives the parameters it does not own,
+ * (N-1)/N of P when owners hold equal shares (a reading: the page gives only the
+ * logical size). */
+int oracle_collective_payload(int32_t T, const int32_t* ndim, const int64_t* dims, const int32_t* unit_id,
+                              int32_t N, int32_t mode, int32_t strategy, int32_t R, int64_t* elems, double* bus) {
+    olayout L;
+    if (strategy < 0 || strategy > 4 || R < 1 || (strategy != 4 && R != 1)) return -1;
+    if (ol_build(&L, T, ndim, dims, unit_id, N, mode)) return -1;
+    int64_t P = L.P, S = L.S;
+    for (int k = 0; k < 5; ++k) elems[k] = 0;
+    if (strategy == 0 || strategy == 1) elems[0] = P;
+    if (strategy == 1) elems[4] = P;
+    if (strategy >= 2) { elems[1] = P; elems[3] = P; }
+    if (strategy >= 3) elems[2] = P;
+    double chunk = (double)(N - 1) / (double)N;            /* ring share over the N ranks */
+    double b = chunk * (double)(elems[1] + elems[2] + elems[3] + elems[4]);
+    if (strategy == 4) {
+        elems[0] = S;
+        b += 2.0 * (double)(R - 1) / (double)R * (double)S;
+    } else {
+        b += 2.0 * chunk * (double)elems[0];
+    }
+    *bus = b;
+    ol_free(&L);
+    return 0;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Rows beyond the core step                                                  */
 /* ------------------------------------------------------------------------- */
