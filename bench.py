@@ -618,7 +618,8 @@ def run_ours(args, w, rank, world, dist):
                    "param_dtype": str(w.param_dtype).replace("torch.", ""),
                    "grad_dtype": str(w.grad_dtype).replace("torch.", ""),
                    "master_moments": "float32", "step_bytes": meas["step_bytes"], "l2": meas["l2"],
-                   "clock_soak_s": args.soak, "parallelism": f"replicas x{world}"},
+                   "clock_soak_s": args.soak, "parallelism": f"replicas x{world}",
+                   "collectives_per_rank": st.layout.collective_payload(args.strategy)},
         "step_hbm_gbs": meas["step_bytes"] / (ms_max / args.steps * 1e-3) / 1e9,
         "roofline": roof,
         "e2e": {"value": world * P * args.steps / (e2e_ms * 1e-3), "unit": "params/s",

@@ -34,7 +34,7 @@ EXPORTS = ("fsdp_layout_create", "fsdp_layout_destroy", "fsdp_layout_query", "fs
            "fsdp_layout_owner", "fsdp_clip_workspace_bytes", "fsdp_reduce_scatter_clip_adamw",
            "fsdp_accumulate_grads", "fsdp_hsdp_reduce_scatter_adamw", "fsdp_zero1_adamw_broadcast",
            "fsdp_set_rs_kernel", "fsdp_rs_kernel_for", "fsdp_wait_selftest", "fsdp_adamw_step_consts_make",
-           "fsdp_reduce_scatter_adamw_consts", "fsdp_adamw_step_consts_upload")
+           "fsdp_reduce_scatter_adamw_consts", "fsdp_adamw_step_consts_upload", "fsdp_collective_payload")
 
 
 class FsdpError(RuntimeError):
@@ -50,6 +50,17 @@ class LayoutInfo(C.Structure):
     _fields_ = [("n_tensors", C.c_int32), ("n_units", C.c_int32), ("n_ranks", C.c_int32), ("mode", C.c_int32),
                 ("numel", C.c_int64), ("shard_numel", C.c_int64), ("shard_stride", C.c_int64),
                 ("full_numel", C.c_int64), ("pad_numel", C.c_int64), ("n_segments", C.c_int64)]
+
+
+FSDP_NO_SHARD, FSDP_ZERO1_OPT, FSDP_SHARD_GRAD_OP, FSDP_FULL_SHARD, FSDP_HYBRID_SHARD = 0, 1, 2, 3, 4
+STRATEGIES = {"no_shard": FSDP_NO_SHARD, "zero1": FSDP_ZERO1_OPT, "shard_grad_op": FSDP_SHARD_GRAD_OP,
+              "full_shard": FSDP_FULL_SHARD, "hybrid_shard": FSDP_HYBRID_SHARD}
+
+
+class CollectivePayload(C.Structure):
+    _fields_ = [("allreduce_input", C.c_int64), ("forward_allgather", C.c_int64),
+                ("backward_allgather", C.c_int64), ("reducescatter_input", C.c_int64), ("broadcast", C.c_int64),
+                ("bus_elements", C.c_double)]
 
 
 class AdamWHparams(C.Structure):
@@ -84,6 +95,7 @@ def lib() -> C.CDLL:
         L.fsdp_layout_tensor.argtypes = [vp, i32, C.POINTER(i32)] + [C.POINTER(i64)] * 4
         L.fsdp_layout_segment.argtypes = [vp, i32, i32] + [C.POINTER(i64)] * 4
         L.fsdp_state_bytes.argtypes = [vp, i32, i32, i32, i64, i64, i64, i64, C.POINTER(i64)]
+        L.fsdp_collective_payload.argtypes = [vp, i32, i32, C.POINTER(CollectivePayload)]
         L.fsdp_layout_prepare.argtypes = [vp]
         L.fsdp_unshard.argtypes = [vp, i32, i32, vp, vp, i32, vp]
         L.fsdp_reduce_scatter_adamw.argtypes = [vp, i32, i32, C.POINTER(vp), i32, vp, vp, vp, vp, vp,
@@ -219,6 +231,14 @@ class Layout:
         _check(lib().fsdp_state_bytes(self._h, stage, rank, int(physical), param_bytes, grad_bytes, optim_bytes,
                                       step_bytes, out), "fsdp_state_bytes")
         return tuple(out)
+
+    def collective_payload(self, strategy, n_groups: int = 1) -> dict:
+        """Per-rank collective payload of one step (fsdp_collective_payload): logical
+        input elements of each collective and the ring bus elements a rank sends."""
+        code = STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
+        out = CollectivePayload()
+        _check(lib().fsdp_collective_payload(self._h, code, n_groups, C.byref(out)), "fsdp_collective_payload")
+        return {f: getattr(out, f) for f, _ in CollectivePayload._fields_}
 
     def prepare(self) -> None:
         _check(lib().fsdp_layout_prepare(self._h), "fsdp_layout_prepare")

@@ -300,6 +300,41 @@ int fsdp_state_bytes(const fsdp_layout* L, int32_t stage, int32_t rank, int32_t 
     return FSDP_OK;
 }
 
+int fsdp_collective_payload(const fsdp_layout* L, int32_t strategy, int32_t n_groups,
+                            fsdp_collective_payload_info* out) {
+    if (!L || !out || strategy < FSDP_NO_SHARD || strategy > FSDP_HYBRID_SHARD || n_groups < 1) return FSDP_EINVAL;
+    if (strategy != FSDP_HYBRID_SHARD && n_groups != 1) return FSDP_EINVAL;
+    // Collectives of one step per strategy, as multiples of the layout's P: all-reduce,
+    // forward all-gather, backward all-gather, reduce-scatter, broadcast.
+    static const int8_t kUses[5][5] = {
+        {1, 0, 0, 0, 0},   // NO_SHARD: the gradient all-reduce
+        {1, 0, 0, 0, 1},   // ZeRO-1: the same, then the updated parameters broadcast by their owners
+        {0, 1, 0, 1, 0},   // SHARD_GRAD_OP
+        {0, 1, 1, 1, 0},   // FULL_SHARD
+        {0, 1, 1, 1, 0},   // HYBRID_SHARD inside a group; its all-reduce across groups is added below
+    };
+    const int8_t* u = kUses[strategy];
+    out->allreduce_input = u[0] * L->P;
+    out->forward_allgather = u[1] * L->P;
+    out->backward_allgather = u[2] * L->P;
+    out->reducescatter_input = u[3] * L->P;
+    out->broadcast = u[4] * L->P;
+    // Ring algorithms, elements one rank sends: all-gather, reduce-scatter and the
+    // owners' broadcast pass on (N-1) of N chunks of the buffer; an all-reduce is a
+    // reduce-scatter followed by an all-gather, twice that.
+    const double N = double(L->N);
+    const double gather_like = double(out->forward_allgather + out->backward_allgather + out->reducescatter_input +
+                                      out->broadcast);
+    double bus = gather_like * (N - 1.0) / N + 2.0 * double(out->allreduce_input) * (N - 1.0) / N;
+    if (strategy == FSDP_HYBRID_SHARD) {
+        // the reduced shard of each rank, all-reduced across the n_groups replica groups
+        out->allreduce_input = L->S;
+        bus += 2.0 * double(L->S) * double(n_groups - 1) / double(n_groups);
+    }
+    out->bus_elements = bus;
+    return FSDP_OK;
+}
+
 int fsdp_layout_prepare(fsdp_layout* L) {
     fsdp::detail::NvtxRange nvtx_range("fsdp_layout_prepare");
     if (!L) return FSDP_EINVAL;

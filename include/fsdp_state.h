@@ -14,7 +14,9 @@
  *     shard, fused into one pass:  fsdp_reduce_scatter_adamw;
  *   - initial sharding, summon_full_params(writeback) and the release of the
  *     full buffer after use:  fsdp_reshard;
- *   - per-rank model-state bytes of ZeRO stages 0-3:  fsdp_state_bytes.
+ *   - per-rank model-state bytes of ZeRO stages 0-3:  fsdp_state_bytes; per-rank
+ *     collective payload of a step under each sharding strategy:
+ *     fsdp_collective_payload.
  *
  * Sources (titles and sections of the pages this restates):
  *   [FSDP-ch18]  "第18章 FSDP：ZeRO 风格的参数分片" (yangyitao.com PyTorch book)
@@ -173,6 +175,34 @@ int fsdp_layout_segment(const fsdp_layout* layout, int32_t tensor, int32_t rank,
 int fsdp_state_bytes(const fsdp_layout* layout, int32_t stage, int32_t rank, int32_t physical,
                      int64_t param_bytes, int64_t grad_bytes, int64_t optim_bytes,
                      int64_t step_bytes, int64_t out[3]);
+
+/* Collective payload of one training step, per rank ([ZeRO-state] "Logical Payload
+ * 模型": the logical total of each collective's input buffer, in elements, not the bytes
+ * a ring algorithm moves; the ring all-reduce moves 2(N-1)/N of its input per rank.
+ * [FSDP-ch18] §18.2: one all-reduce about 2 Psi for DDP, reduce-scatter plus
+ * all-gather 2 Psi, FULL_SHARD 3 Psi).
+ *   strategy   FSDP_NO_SHARD (DDP: the gradient all-reduce), FSDP_ZERO1_OPT (the same
+ *              all-reduce, then each owner broadcasts its updated parameters, about P),
+ *              FSDP_SHARD_GRAD_OP (forward all-gather, reduce-scatter), FSDP_FULL_SHARD
+ *              (forward and backward all-gather, reduce-scatter), FSDP_HYBRID_SHARD
+ *              (FULL_SHARD inside each of n_groups groups of N ranks, then an all-reduce
+ *              of each rank's reduced shard, S elements, across the groups; [FSDP-ch18]
+ *              §18.9)
+ *   n_groups   replica groups: >= 1 for FSDP_HYBRID_SHARD, else 1 (else FSDP_EINVAL)
+ * out: the logical inputs (P = the layout's logical elements) and bus_elements, the
+ * elements one rank sends, and receives, under ring algorithms: (N-1)/N of the buffer
+ * for an all-gather, a reduce-scatter or the owners' broadcast (equal shares), 2(N-1)/N
+ * for an all-reduce (2(R-1)/R of S across R groups).  Multiply by the element size of
+ * each collective's dtype for bytes.  Host only. */
+typedef enum {
+    FSDP_NO_SHARD = 0, FSDP_ZERO1_OPT = 1, FSDP_SHARD_GRAD_OP = 2, FSDP_FULL_SHARD = 3, FSDP_HYBRID_SHARD = 4
+} fsdp_strategy;
+typedef struct {
+    int64_t allreduce_input, forward_allgather, backward_allgather, reducescatter_input, broadcast;
+    double bus_elements;
+} fsdp_collective_payload_info;
+int fsdp_collective_payload(const fsdp_layout* layout, int32_t strategy, int32_t n_groups,
+                            fsdp_collective_payload_info* out);
 
 /* Allocates and uploads the layout's segment tables on the current CUDA device
  * and blocks until they are there.  Launch calls do this themselves on their

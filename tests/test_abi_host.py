@@ -121,6 +121,31 @@ def test_state_bytes_vs_oracle(oracle_lib, case, stage):
                                                                                       2, 4, 12, 4)
 
 
+@pytest.mark.parametrize("case", small_cases()[:40])
+def test_collective_payload_vs_oracle(oracle_lib, case):
+    shapes, units, N, mode = case
+    L = fs.Layout(shapes, units, N, mode)
+    sh = oracle.Shapes(shapes, units)
+    keys = ("allreduce_input", "forward_allgather", "backward_allgather", "reducescatter_input", "broadcast")
+    for strategy in range(5):
+        for R in ((1, 2, 3) if strategy == fs.FSDP_HYBRID_SHARD else (1,)):
+            got = L.collective_payload(strategy, R)
+            elems, bus = oracle.collective_payload(sh, N, mode, strategy, R)
+            assert [got[k] for k in keys] == elems, (strategy, R)
+            assert got["bus_elements"] == pytest.approx(bus, rel=1e-12, abs=1e-9), (strategy, R)
+
+
+def test_collective_payload_validation(lay):
+    lib = fs.lib()
+    out = fs.CollectivePayload()
+    assert lib.fsdp_collective_payload(None, 3, 1, C.byref(out)) == -1
+    assert lib.fsdp_collective_payload(lay.handle, 5, 1, C.byref(out)) == -1
+    assert lib.fsdp_collective_payload(lay.handle, -1, 1, C.byref(out)) == -1
+    assert lib.fsdp_collective_payload(lay.handle, 3, 2, C.byref(out)) == -1     # groups only with HSDP
+    assert lib.fsdp_collective_payload(lay.handle, 4, 0, C.byref(out)) == -1
+    assert lib.fsdp_collective_payload(lay.handle, 4, 2, None) == -1
+
+
 # ---------------------------------------------------------------------------
 # validation
 # ---------------------------------------------------------------------------
