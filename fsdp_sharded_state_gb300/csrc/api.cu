@@ -37,6 +37,8 @@ int choose_staged(bool fits, bool preferred, bool* staged) {
     return FSDP_OK;
 }
 
+int rs_kernel_choice() { return g_rs_kernel.load(); }
+
 int cuda_fail(cudaError_t e, const char* where) {
     std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s (%s)", where, cudaGetErrorName(e),
                   cudaGetErrorString(e));

@@ -47,5 +47,8 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 // FSDP_EINVAL when the staged kernel is forced but does not fit.
 int choose_staged(bool fits, bool preferred, bool* staged);
 
+// The process-wide kernel choice (fsdp_set_rs_kernel): FSDP_RS_AUTO, _DIRECT or _STAGED.
+int rs_kernel_choice();
+
 }  // namespace detail
 }  // namespace fsdp

@@ -630,11 +630,32 @@ int fsdp_reduce_scatter_clip_adamw(const fsdp_layout* L, int32_t ub, int32_t ue,
     char* ws = static_cast<char*>(workspace);
     double* ws_norm = reinterpret_cast<double*>(ws);
     float* ws_coef = reinterpret_cast<float*>(ws + 8);
+    unsigned int* counter = reinterpret_cast<unsigned int*>(ws + 16);
     double* part = reinterpret_cast<double*>(ws + kClipHeader);
+    const bool bf = grad_dtype == FSDP_BF16;
+
+    // The automatic choice runs the whole step in one cooperative launch when every piece
+    // of the range is in the aligned class (clip_coop.cu): each CTA keeps the gradient of
+    // its last tiles in shared memory across the grid-wide barrier, so that part of the
+    // shard is neither written to nor read back from memory between the two phases.
+    if (rs_kernel_choice() == FSDP_RS_AUTO) {
+        const Range Dsh = range_of(L->data_sh, base, ub, ue);
+        const Range Dc = range_of(L->data, base, ub, ue);
+        if (Dsh.n_tiles == 0 && Dc.n_tiles > 0) {
+            const Range P = range_of(L->pad, base, ub, ue);
+            cudaError_t e = fsdp::launch_zero_pad(P.segs, P.tile_base, P.n_tiles, grad_shard, nullptr, st);
+            if (e != cudaSuccess) return cuda_fail(e, "k_zero_pad launch");
+            bool launched = false;
+            e = fsdp::launch_clip_coop(Dc.segs, Dc.n_segs, Dc.tile_base, Dc.n_tiles, bf, gp, L->N, grad_shard, master,
+                                       exp_avg, exp_avg_sq, static_cast<uint16_t*>(param_shards), part, kMaxPartials,
+                                       counter, ws_norm, ws_coef, norm_out, max_norm, sc, kWaitNs, st, &launched);
+            if (e != cudaSuccess) return cuda_fail(e, "k_clip_coop launch");
+            if (launched) return FSDP_OK;
+        }
+    }
 
     // (1) reduce-scatter + sums of squares: staged (one partial per consumer warp, one
     // launch) or direct (one partial per CTA, one launch per alignment class)
-    const bool bf = grad_dtype == FSDP_BF16;
     const Range D1 = range_of(L->data, base, ub, ue);
     bool staged = false;
     // the automatic choice keeps the direct kernel here: on GB300 the staged pass was

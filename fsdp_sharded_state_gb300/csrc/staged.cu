@@ -260,11 +260,12 @@ cudaError_t launch_wait_selftest(uint64_t wait_ns, cudaStream_t st) {
 }
 
 cudaError_t take_wait_error(unsigned int* flag) {
-    unsigned int a = 0, b = 0, c = 0;
+    unsigned int a = 0, b = 0, c = 0, d = 0;
     cudaError_t e = take_local_wait_error(&a);
     if (e == cudaSuccess) e = take_wait_error_allgather(&b);
     if (e == cudaSuccess) e = take_wait_error_rows(&c);
-    *flag = a | b | c;
+    if (e == cudaSuccess) e = take_wait_error_coop(&d);
+    *flag = a | b | c | d;
     return e;
 }
 

@@ -70,10 +70,25 @@ cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_ti
 // One kernel whose only wait cannot complete: exercises the bounded-wait exit.
 cudaError_t launch_wait_selftest(uint64_t wait_ns, cudaStream_t st);
 
+// The sharded clip step in one cooperative launch (clip_coop.cu) over a segment range
+// of the aligned class: the reduce-scatter into gshard (its last tiles per CTA held in
+// shared memory), the sums of squares into part[0 .. grid), a grid-wide barrier on
+// *counter (cleared on the stream first; bounded by wait_ns), the norm and coefficient
+// (CTA 0 stores them in ws_norm, ws_coef and norm_out), AdamW on the clipped shard.
+// *launched is false, with nothing queued but the counter's clear, when the device
+// cannot hold the whole grid at once or its grid would need more than max_part partials:
+// the caller then runs the two-pass form.
+cudaError_t launch_clip_coop(const Seg* segs, int n_segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
+                             const GradPtrs& gp, int N, float* gshard, float* master, float* m, float* v,
+                             uint16_t* param, double* part, int max_part, unsigned int* counter, double* ws_norm,
+                             float* ws_coef, float* norm_out, float max_norm, const AdamScal& sc, uint64_t wait_ns,
+                             cudaStream_t st, bool* launched);
+
 // Reads and clears the "a bounded wait gave up" words of every staged translation
 // unit on the current device (synchronous).
 cudaError_t take_wait_error(unsigned int* flag);
 cudaError_t take_wait_error_allgather(unsigned int* flag);   // allgather.cu only
 cudaError_t take_wait_error_rows(unsigned int* flag);        // staged_rows.cu only
+cudaError_t take_wait_error_coop(unsigned int* flag);        // clip_coop.cu only
 
 }  // namespace fsdp

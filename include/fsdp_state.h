@@ -300,11 +300,19 @@ int fsdp_layout_owner(const fsdp_layout* layout, int32_t tensor, int32_t* rank);
  * coef = min(1, max_norm / (norm + 1e-6)), formed in double and rounded to fp32
  * once; each reduced gradient is multiplied by it (one fp32 rounding) and then
  * goes through the AdamW and bf16 steps of fsdp_reduce_scatter_adamw.
- * Two passes on `stream`: the reduce-scatter writes the fp32 gradient shard and
- * per-CTA partial sums of squares (fixed order, so the norm is reproducible on a
- * given GPU); the update pass adds the partials in double (every CTA in the same
- * order), forms the coefficient, scales the shard and runs AdamW.  (With the
- * staged kernels forced, one extra single-CTA kernel forms the norm between them.)
+ * Under the automatic kernel choice, when every rank view of the unit range sits at
+ * a shard index congruent to its full-layout index mod 8, one cooperative launch on
+ * `stream` runs the whole step: each CTA reduce-scatters a fixed block of tiles into
+ * the fp32 gradient shard -- holding the last of them in shared memory -- and writes
+ * its partial sum of squares; after a grid-wide barrier (bounded: it gives up after
+ * 1 s and records FSDP_ETIMEOUT for fsdp_check_status) every CTA adds the partials in
+ * double in the same order, forms the coefficient, scales its tiles and runs AdamW.
+ * Otherwise (or when the device cannot hold the whole grid at once), two passes: the
+ * reduce-scatter writes the fp32 gradient shard and per-CTA partial sums of squares
+ * (fixed order, so the norm is reproducible on a given GPU); the update pass adds the
+ * partials in double (every CTA in the same order), forms the coefficient, scales the
+ * shard and runs AdamW.  (With the staged kernels forced, one extra single-CTA kernel
+ * forms the norm between them.)
  *   grad_shard  required device [N][stride] fp32: receives the CLIPPED reduced
  *               gradient (padding +0); it is also the working buffer.
  *   max_norm    > 0 and finite.
@@ -372,8 +380,9 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
  * fsdp_zero1_adamw_broadcast.
  *   FSDP_RS_AUTO    the staged kernel where at least two of its pipeline stages fit
  *                   in one CTA's shared memory, else the direct kernels; the clip
- *                   passes and ZeRO-1 keep the direct kernels (measured as fast or
- *                   steadier).  A stage
+ *                   runs as one cooperative launch where its unit range has no
+ *                   misaligned rank view, else as the direct passes, and ZeRO-1 keeps
+ *                   the direct kernel (measured as fast or steadier).  A stage
  *                   holds 2048 elements of each array the call reads: for
  *                   fsdp_reduce_scatter_adamw the three fp32 state arrays and the N
  *                   gradient replicas, the replicas in groups where all of them do
@@ -390,8 +399,9 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
  *                   per stage counts the bytes, one launch for both alignment
  *                   classes.  A call whose staged kernel does not fit returns
  *                   FSDP_EINVAL.
- * The clip norm is a double sum whose grouping differs between the two (one
- * partial per CTA or per warp); both are deterministic run to run.
+ * The clip norm is a double sum whose grouping differs between the forms (one
+ * partial per CTA of the passes, per warp of the staged pass, per CTA of the
+ * cooperative launch over other tiles); all are deterministic run to run.
  * Returns the previous choice, or FSDP_EINVAL for an unknown one.  Not ordered
  * with calls in flight on other threads. */
 typedef enum { FSDP_RS_AUTO = 0, FSDP_RS_DIRECT = 1, FSDP_RS_STAGED = 2 } fsdp_rs_kernel;
