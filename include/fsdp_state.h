@@ -317,7 +317,10 @@ int fsdp_layout_owner(const fsdp_layout* layout, int32_t tensor, int32_t* rank);
  *               gradient (padding +0); it is also the working buffer.
  *   max_norm    > 0 and finite.
  *   workspace   device scratch of fsdp_clip_workspace_bytes() bytes, 16-byte
- *               aligned, owned by the caller; no initial contents needed.
+ *               aligned, owned by the caller; no initial contents needed.  It holds
+ *               the call's partial sums (and the cooperative launch's barrier count)
+ *               until the call's work has run: calls whose work may overlap on the GPU
+ *               (other streams) need workspaces of their own.
  *   norm_out    optional device float[2] (8-byte aligned): total norm, coef.
  * Other arguments and errors as fsdp_reduce_scatter_adamw. */
 size_t fsdp_clip_workspace_bytes(void);
