@@ -42,7 +42,19 @@ CLIP_CASES = [
 ]
 
 
-@pytest.mark.parametrize("w,max_norm", CLIP_CASES)
+# Layouts whose rank views are all congruent to their full-layout positions mod 8, with
+# many segments and tens of tiles per CTA: under the automatic choice the clip runs as one
+# cooperative launch, whose thread groups then meet tiles kept in shared memory, tiles
+# stored with the evict-last policy and plain ones, across segment boundaries.
+CLIP_COOP_CASES = [
+    (W([(4096, 1024), (2048, 2048), (1024, 1024), (8, 4096), (512, 520), (4096, 2048)], [0] * 6, 4, synth.DIM0,
+       torch.float32), 1e-2),
+    (W([(2048, 2048), (4096, 512), (16, 1024), (1024, 4096)], [0] * 4, 8, synth.DIM0), 5e-3),
+    (W([(1 << 22,), (1 << 21,), (1 << 20,)], [0, 1, 2], 8, synth.FLAT), 1e3),     # clip not active
+]
+
+
+@pytest.mark.parametrize("w,max_norm", CLIP_CASES + CLIP_COOP_CASES)
 def test_clip_vs_oracle(oracle_lib, w, max_norm):
     st = pu.make_state(w, with_grad_out=True)
     sh = oracle.Shapes(w.shapes, w.unit_ids)
