@@ -149,7 +149,7 @@ __device__ __forceinline__ double coop_phase1(const Seg& sg, int64_t gt, const G
             reduce_split_f32(gp, N, x0 + delta, x1 + delta, acc);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                g[k] = __fdiv_rn(acc[k], nf);
+                g[k] = mean_div(acc[k], nf);
                 sq = __fmaf_rn(g[k], g[k], sq);
             }
             const float4 a = make_float4(g[0], g[1], g[2], g[3]), b = make_float4(g[4], g[5], g[6], g[7]);
@@ -167,7 +167,7 @@ __device__ __forceinline__ double coop_phase1(const Seg& sg, int64_t gt, const G
             const int64_t xc = c ? x1 : x0;
             const int64_t a = xc > lo ? xc : lo, b = (xc + 4) < hi ? (xc + 4) : hi;
             for (int64_t e = a; e < b; ++e) {
-                const float g = __fdiv_rn(reduce1<float>(gp, N, e + delta), nf);
+                const float g = mean_div(reduce1<float>(gp, N, e + delta), nf);
                 if (keep) keep[e - base] = g;
                 else gout[e] = g;
                 ss += double(g) * double(g);
@@ -183,7 +183,7 @@ __device__ __forceinline__ double coop_phase1(const Seg& sg, int64_t gt, const G
             coop_reduce8_bf16(gp, N, e0 + delta, acc);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                g[k] = __fdiv_rn(acc[k], nf);
+                g[k] = mean_div(acc[k], nf);
                 sq = __fmaf_rn(g[k], g[k], sq);
             }
             const float4 a = make_float4(g[0], g[1], g[2], g[3]), b = make_float4(g[4], g[5], g[6], g[7]);
@@ -198,7 +198,7 @@ __device__ __forceinline__ double coop_phase1(const Seg& sg, int64_t gt, const G
         }
         const int64_t a = e0 > lo ? e0 : lo, b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
         for (int64_t e = a; e < b; ++e) {
-            const float g = __fdiv_rn(reduce1<GT>(gp, N, e + delta), nf);
+            const float g = mean_div(reduce1<GT>(gp, N, e + delta), nf);
             if (keep) keep[e - base] = g;
             else gout[e] = g;
             ss += double(g) * double(g);

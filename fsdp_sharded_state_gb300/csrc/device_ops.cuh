@@ -23,6 +23,19 @@ __device__ __forceinline__ void adamw1(const AdamScal& s, float g, float& p, flo
     v = vv;
 }
 
+// ----------------------------------------------------------------------------
+// The mean's division x / n by the rank count n (a float holding an integer >= 1).
+// When n is a power of two, 1/n is exact, so x * (1/n) is the same real number as
+// x / n and rounds to the same float -- subnormal results, zeros and infinities
+// included -- for far fewer instructions than an IEEE division.  Otherwise the
+// division.  (n is the same for a whole launch: the test and the reciprocal are loop
+// invariants.)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float mean_div(float x, float n) {
+    const bool pow2 = (__float_as_uint(n) & 0x807FFFFFu) == 0u && n >= 1.0f;
+    return pow2 ? __fmul_rn(x, __frcp_rn(n)) : __fdiv_rn(x, n);
+}
+
 template <typename GT> struct GradIO;
 
 // bf16 gradients: one 16-byte load per replica covers the 8 elements.

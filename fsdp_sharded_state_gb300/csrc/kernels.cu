@@ -61,7 +61,7 @@ __device__ __forceinline__ void rs_tile_f32_split(const Seg& sg, int64_t gt, con
             float g[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                g[k] = __fdiv_rn(acc[4 * c + k], sc.nf);
+                g[k] = mean_div(acc[4 * c + k], sc.nf);
                 adamw1(sc, g[k], p[k], m[k], v[k]);
             }
             st4(master + xc, make_float4(p[0], p[1], p[2], p[3]));
@@ -82,7 +82,7 @@ __device__ __forceinline__ void rs_tile_f32_split(const Seg& sg, int64_t gt, con
         for (int64_t e = a; e < b; ++e) {
             float acc = 0.0f;
             for (int q = 0; q < N; ++q) acc = __fadd_rn(acc, static_cast<const float*>(gp.p[q])[e + delta]);
-            const float gg = __fdiv_rn(acc, sc.nf);
+            const float gg = mean_div(acc, sc.nf);
             float pp = master[e], mm = exp_avg[e], vv = exp_avg_sq[e];
             adamw1(sc, gg, pp, mm, vv);
             master[e] = pp; exp_avg[e] = mm; exp_avg_sq[e] = vv;
@@ -152,7 +152,7 @@ k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, Gra
             float g[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                g[k] = __fdiv_rn(acc[k], sc.nf);
+                g[k] = mean_div(acc[k], sc.nf);
                 adamw1(sc, g[k], p[k], m[k], v[k]);
             }
             st4(master + e0, make_float4(p[0], p[1], p[2], p[3]));
@@ -173,7 +173,7 @@ k_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, Gra
             const int64_t a = e0 > lo ? e0 : lo;
             const int64_t b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
             for (int64_t e = a; e < b; ++e) {
-                const float g = __fdiv_rn(reduce1<GT>(gp, N, e + delta), sc.nf);
+                const float g = mean_div(reduce1<GT>(gp, N, e + delta), sc.nf);
                 float p = master[e], m = exp_avg[e], v = exp_avg_sq[e];
                 adamw1(sc, g, p, m, v);
                 master[e] = p; exp_avg[e] = m; exp_avg_sq[e] = v;

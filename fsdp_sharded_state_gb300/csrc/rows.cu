@@ -112,7 +112,7 @@ __device__ __forceinline__ double norm_tile_f32_split(const Seg& sg, int64_t gt,
         reduce_split_f32(gp, N, x0 + delta, x1 + delta, acc);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            g[k] = __fdiv_rn(acc[k], nf);
+            g[k] = mean_div(acc[k], nf);
             sq = __fmaf_rn(g[k], g[k], sq);
         }
         st4_hint(gout + x0, make_float4(g[0], g[1], g[2], g[3]), keep, pol);
@@ -125,7 +125,7 @@ __device__ __forceinline__ double norm_tile_f32_split(const Seg& sg, int64_t gt,
         const int64_t xc = c ? x1 : x0;
         const int64_t a = xc > lo ? xc : lo, b = (xc + 4) < hi ? (xc + 4) : hi;
         for (int64_t e = a; e < b; ++e) {
-            const float g = __fdiv_rn(reduce1<float>(gp, N, e + delta), nf);
+            const float g = mean_div(reduce1<float>(gp, N, e + delta), nf);
             gout[e] = g;
             ss += double(g) * double(g);
         }
@@ -172,7 +172,7 @@ k_rs_norm(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, Grad
             float g[8], sq = 0.0f;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                g[k] = __fdiv_rn(acc[k], nf);
+                g[k] = mean_div(acc[k], nf);
                 sq = __fmaf_rn(g[k], g[k], sq);
             }
             st4_hint(gout + e0, make_float4(g[0], g[1], g[2], g[3]), keep, pol);
@@ -181,7 +181,7 @@ k_rs_norm(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, Grad
         } else {
             const int64_t a = e0 > lo ? e0 : lo, b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
             for (int64_t e = a; e < b; ++e) {
-                const float g = __fdiv_rn(reduce1<GT>(gp, N, e + delta), nf);
+                const float g = mean_div(reduce1<GT>(gp, N, e + delta), nf);
                 gout[e] = g;
                 ss += double(g) * double(g);
             }
@@ -378,10 +378,10 @@ k_hsdp_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, G
                 float acc[8];
                 reduce8_vec<GT>(gp, N, e0 + delta, acc, rho * N);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) outer[k] = __fadd_rn(outer[k], __fdiv_rn(acc[k], sc.nf));
+                for (int k = 0; k < 8; ++k) outer[k] = __fadd_rn(outer[k], mean_div(acc[k], sc.nf));
             }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) g[k] = __fdiv_rn(outer[k], rf);
+            for (int k = 0; k < 8; ++k) g[k] = mean_div(outer[k], rf);
 #pragma unroll 1
             for (int rho = 0; rho < R; ++rho) {
                 const int64_t e = rho * copy + e0;
@@ -410,9 +410,9 @@ k_hsdp_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, G
                 for (int rho = 0; rho < R; ++rho) {
                     float acc = 0.0f;
                     for (int q = 0; q < N; ++q) acc = __fadd_rn(acc, GradIO<GT>::load1(gp.p[rho * N + q], e + delta));
-                    outer = __fadd_rn(outer, __fdiv_rn(acc, sc.nf));
+                    outer = __fadd_rn(outer, mean_div(acc, sc.nf));
                 }
-                const float g = __fdiv_rn(outer, rf);
+                const float g = mean_div(outer, rf);
                 for (int rho = 0; rho < R; ++rho) {
                     const int64_t x = rho * copy + e;
                     float p = master[x], m = exp_avg[x], v = exp_avg_sq[x];
@@ -462,7 +462,7 @@ __device__ __forceinline__ void zero1_tile_f32_split(const Seg& sg, int64_t gt, 
             float m[4] = {mc.x, mc.y, mc.z, mc.w};
             float v[4] = {vc.x, vc.y, vc.z, vc.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) adamw1(sc, __fdiv_rn(acc[4 * c + k], sc.nf), p[k], m[k], v[k]);
+            for (int k = 0; k < 4; ++k) adamw1(sc, mean_div(acc[4 * c + k], sc.nf), p[k], m[k], v[k]);
             st4(exp_avg + xc, make_float4(m[0], m[1], m[2], m[3]));
             st4(exp_avg_sq + xc, make_float4(v[0], v[1], v[2], v[3]));
             const float4 pv = make_float4(p[0], p[1], p[2], p[3]);
@@ -478,7 +478,7 @@ __device__ __forceinline__ void zero1_tile_f32_split(const Seg& sg, int64_t gt, 
         for (int64_t e = a; e < b; ++e) {
             const int64_t f = e + delta;
             float p = own[f], m = exp_avg[e], v = exp_avg_sq[e];
-            adamw1(sc, __fdiv_rn(reduce1<float>(gp, N, f), sc.nf), p, m, v);
+            adamw1(sc, mean_div(reduce1<float>(gp, N, f), sc.nf), p, m, v);
             exp_avg[e] = m; exp_avg_sq[e] = v;
             for (int q = 0; q < N; ++q) static_cast<float*>(pp.p[q])[f] = p;
         }
@@ -522,7 +522,7 @@ k_zero1_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, 
             float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
             float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-            for (int k = 0; k < 8; ++k) adamw1(sc, __fdiv_rn(acc[k], sc.nf), p[k], m[k], v[k]);
+            for (int k = 0; k < 8; ++k) adamw1(sc, mean_div(acc[k], sc.nf), p[k], m[k], v[k]);
             if (MASTER) {
                 st4(master + e0, make_float4(p[0], p[1], p[2], p[3]));
                 st4(master + e0 + 4, make_float4(p[4], p[5], p[6], p[7]));
@@ -550,7 +550,7 @@ k_zero1_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, 
                 const int64_t f = e + delta;
                 float p = MASTER ? master[e] : static_cast<const float*>(pp.p[owner])[f];
                 float m = exp_avg[e], v = exp_avg_sq[e];
-                adamw1(sc, __fdiv_rn(reduce1<GT>(gp, N, f), sc.nf), p, m, v);
+                adamw1(sc, mean_div(reduce1<GT>(gp, N, f), sc.nf), p, m, v);
                 if (MASTER) master[e] = p;
                 exp_avg[e] = m; exp_avg_sq[e] = v;
                 for (int q = 0; q < N; ++q) {

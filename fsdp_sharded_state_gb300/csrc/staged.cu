@@ -162,8 +162,8 @@ struct RsAdamw {
             float p[4] = {pv.x, pv.y, pv.z, pv.w};
             float m[4] = {mv.x, mv.y, mv.z, mv.w};
             float v[4] = {vv.x, vv.y, vv.z, vv.w};
-            float gg[4] = {__fdiv_rn(carry.a0, sc.nf), __fdiv_rn(carry.a1, sc.nf), __fdiv_rn(carry.a2, sc.nf),
-                           __fdiv_rn(carry.a3, sc.nf)};
+            float gg[4] = {mean_div(carry.a0, sc.nf), mean_div(carry.a1, sc.nf), mean_div(carry.a2, sc.nf),
+                           mean_div(carry.a3, sc.nf)};
 #pragma unroll
             for (int k = 0; k < 4; ++k) adamw1(sc, gg[k], p[k], m[k], v[k]);
             st4(master + x, make_float4(p[0], p[1], p[2], p[3]));
@@ -177,7 +177,7 @@ struct RsAdamw {
             const int64_t a = x > g.s0 ? x : g.s0;
             const int64_t b = (x + 4) < g.s1 ? (x + 4) : g.s1;
             for (int64_t e = a; e < b; ++e) {
-                const float gg = __fdiv_rn(reduce1<GT>(gp, N, e + g.delta), sc.nf);
+                const float gg = mean_div(reduce1<GT>(gp, N, e + g.delta), sc.nf);
                 float pp = master[e], mm = exp_avg[e], vv2 = exp_avg_sq[e];
                 adamw1(sc, gg, pp, mm, vv2);
                 master[e] = pp; exp_avg[e] = mm; exp_avg_sq[e] = vv2;

@@ -92,13 +92,13 @@ struct HsdpAdamw {
                     a0 = __fadd_rn(a0, x4.x); a1 = __fadd_rn(a1, x4.y);
                     a2 = __fadd_rn(a2, x4.z); a3 = __fadd_rn(a3, x4.w);
                 }
-                o0 = __fadd_rn(o0, __fdiv_rn(a0, sc.nf)); o1 = __fadd_rn(o1, __fdiv_rn(a1, sc.nf));
-                o2 = __fadd_rn(o2, __fdiv_rn(a2, sc.nf)); o3 = __fadd_rn(o3, __fdiv_rn(a3, sc.nf));
+                o0 = __fadd_rn(o0, mean_div(a0, sc.nf)); o1 = __fadd_rn(o1, mean_div(a1, sc.nf));
+                o2 = __fadd_rn(o2, mean_div(a2, sc.nf)); o3 = __fadd_rn(o3, mean_div(a3, sc.nf));
             }
         }
         release();
         if (fast) {
-            const float gg[4] = {__fdiv_rn(o0, rf), __fdiv_rn(o1, rf), __fdiv_rn(o2, rf), __fdiv_rn(o3, rf)};
+            const float gg[4] = {mean_div(o0, rf), mean_div(o1, rf), mean_div(o2, rf), mean_div(o3, rf)};
 #pragma unroll
             for (int rho = 0; rho < kMaxR; ++rho) {
                 if (rho >= R) break;
@@ -127,9 +127,9 @@ struct HsdpAdamw {
                     float acc = 0.0f;
                     for (int q = 0; q < N; ++q)
                         acc = __fadd_rn(acc, GradIO<GT>::load1(gp.p[rho * N + q], e + g.delta));
-                    outer = __fadd_rn(outer, __fdiv_rn(acc, sc.nf));
+                    outer = __fadd_rn(outer, mean_div(acc, sc.nf));
                 }
-                const float gg = __fdiv_rn(outer, rf);
+                const float gg = mean_div(outer, rf);
                 for (int rho = 0; rho < R; ++rho) {
                     const int64_t y = rho * copy + e;
                     float pp = master[y], mm = exp_avg[y], vv = exp_avg_sq[y];
@@ -253,7 +253,7 @@ struct Zero1Adamw {
             float p[4] = {pv.x, pv.y, pv.z, pv.w};
             float m[4] = {mv.x, mv.y, mv.z, mv.w};
             float v[4] = {vv.x, vv.y, vv.z, vv.w};
-            const float gg[4] = {__fdiv_rn(a0, sc.nf), __fdiv_rn(a1, sc.nf), __fdiv_rn(a2, sc.nf), __fdiv_rn(a3, sc.nf)};
+            const float gg[4] = {mean_div(a0, sc.nf), mean_div(a1, sc.nf), mean_div(a2, sc.nf), mean_div(a3, sc.nf)};
 #pragma unroll
             for (int k = 0; k < 4; ++k) adamw1(sc, gg[k], p[k], m[k], v[k]);
             if (MASTER) st4(master + x, make_float4(p[0], p[1], p[2], p[3]));
@@ -278,7 +278,7 @@ struct Zero1Adamw {
                 const int64_t fe = e + g.delta;
                 float pp = MASTER ? master[e] : static_cast<const float*>(pr.p[g.q])[fe];
                 float mm = exp_avg[e], vv2 = exp_avg_sq[e];
-                adamw1(sc, __fdiv_rn(reduce1<GT>(gp, N, fe), sc.nf), pp, mm, vv2);
+                adamw1(sc, mean_div(reduce1<GT>(gp, N, fe), sc.nf), pp, mm, vv2);
                 if (MASTER) master[e] = pp;
                 exp_avg[e] = mm; exp_avg_sq[e] = vv2;
                 for (int q = 0; q < N; ++q) {
@@ -421,7 +421,7 @@ struct RsNorm {
         }
         release();
         if (fast) {
-            const float g0 = __fdiv_rn(a0, nf), g1 = __fdiv_rn(a1, nf), g2 = __fdiv_rn(a2, nf), g3 = __fdiv_rn(a3, nf);
+            const float g0 = mean_div(a0, nf), g1 = mean_div(a1, nf), g2 = mean_div(a2, nf), g3 = mean_div(a3, nf);
             st4(gout + x, make_float4(g0, g1, g2, g3));
             float sq = __fmul_rn(g0, g0);
             sq = __fmaf_rn(g1, g1, sq);
@@ -432,7 +432,7 @@ struct RsNorm {
             const int64_t a = x > g.s0 ? x : g.s0;
             const int64_t b = (x + 4) < g.s1 ? (x + 4) : g.s1;
             for (int64_t e = a; e < b; ++e) {
-                const float gg = __fdiv_rn(reduce1<GT>(gp, N, e + g.delta), nf);
+                const float gg = mean_div(reduce1<GT>(gp, N, e + g.delta), nf);
                 gout[e] = gg;
                 ss += double(gg) * double(gg);
             }
