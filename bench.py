@@ -515,9 +515,16 @@ def fused_roofline(fs, st, w, meas, workload_name):
 
 
 # The configurations timed beside the headline one (the pages' other workloads), one
-# after the other, each freed before the next: the 4-block Llama and the FSDP2 dim-0
-# group as the fused kernel's HBM rate, the tiny MLP as the latency of a step.
-SIDE_CONFIGS = ("llama4", "dim0_n6", "tiny_mlp")
+# after the other, each freed before the next: the 4-block Llama, the FSDP2 dim-0 group
+# and the largest points of the one-unit sweep (2^29+1 parameters at N = 32 and N = 2) as
+# the fused kernel's HBM rate, the tiny MLP as the latency of a step.
+SIDE_CONFIGS = ("llama4", "dim0_n6", "tiny_mlp", "sweep_P536870913_N32", "sweep_P536870913_N2")
+# Side configurations whose oracle step is not timed in the bench: one unit of 537M
+# parameters per oracle process would take the host minutes to set up and step.
+NO_CPU_SIDE = {"sweep_P536870913_N32": "not timed: one 537M-parameter unit per oracle process exceeds the bench's "
+                                       "CPU time (about 20 GB of host buffers and minutes per step)",
+               "sweep_P536870913_N2": "not timed: one 537M-parameter unit per oracle process exceeds the bench's "
+                                      "CPU time (about 20 GB of host buffers and minutes per step)"}
 GATE_GBS = 8000.0 * 0.75          # the pages' target: 75 % of ~8 TB/s
 
 
@@ -549,7 +556,9 @@ def side_config(args, name, dev, stream):
         out["us_per_step"] = meas["ms"] / steps * 1e3        # latency-bound: the step's time is the figure
     del st, grads
     torch.cuda.empty_cache()
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and name in NO_CPU_SIDE:
+        out["cpu_baseline"] = {"kind": "oracle", "value": None, "note": NO_CPU_SIDE[name]}
+    elif not args.no_cpu_baseline:
         # the oracle on this workload, on every host core (one oracle process per core)
         import oracle
         oracle.build()
