@@ -651,6 +651,8 @@ def row_bytes(row, w, P, N, R=2):
     clip:  N replicas read; fp32 gradient shard written, re-read and rewritten
            (clipped); master/m/v read + written; bf16 params written.
     accum: per replica the micro-gradient read and the fp32 accumulator read + written.
+    accum_step: the last micro-batch fused with the step: per replica the fp32
+           accumulator and the micro-gradient read; master/m/v read + written; bf16 params.
     hsdp:  R*N replicas read; R copies of master/m/v read + written (+ bf16 params).
     zero1: N replicas read; the owner's m/v (and master, or its own fp32 replica)
            read + written; the updated parameter written into all N replicas."""
@@ -661,6 +663,10 @@ def row_bytes(row, w, P, N, R=2):
         return N * P * gb + 4 * P + 8 * P + 24 * P + (2 * P if bf else 0)
     if row == "accum":
         return N * P * (gb + 8)
+    if row == "accum_step":
+        # the last micro-batch fused with the step: per replica the fp32 accumulator and
+        # the micro-batch gradient read (nothing written back to them); the state as in the step
+        return N * P * (4 + gb) + 24 * P + (2 * P if bf else 0)
     if row == "hsdp":
         return R * N * P * gb + R * P * (24 + (2 if bf else 0))
     if row == "zero1":
@@ -687,7 +693,7 @@ def run_row(args, w):
     full = synth.full_params(w, F, offs, device=dev)
     bf = w.param_dtype == torch.bfloat16
     z = lambda *shape, dt=torch.float32: torch.zeros(*shape, dtype=dt, device=dev)
-    if args.row in ("clip", "accum"):
+    if args.row in ("clip", "accum", "accum_step"):
         st = fs.ShardedState(w.shapes, w.unit_ids, N, w.mode, param_dtype=w.param_dtype, device=dev,
                              with_grad_out=True)
         st.init_from_full(full)
@@ -697,9 +703,15 @@ def run_row(args, w):
             call = lambda t: fs.fsdp_reduce_scatter_clip_adamw(st.layout, 0, st.layout.n_units, grads,
                                                                st.master, st.exp_avg, st.exp_avg_sq, st.param,
                                                                st.grad_out, 1e-2, ws, None, w.hp, t)
-        else:
+        elif args.row == "accum":
             acc = [z(F) for _ in range(N)]
             call = lambda t: fs.fsdp_accumulate_grads(st.layout, 0, st.layout.n_units, acc, grads, first=False)
+        else:
+            acc = [z(F) for _ in range(N)]
+            fs.fsdp_accumulate_grads(st.layout, 0, st.layout.n_units, acc, grads, first=True)
+            call = lambda t: fs.fsdp_accumulate_reduce_scatter_adamw(st.layout, 0, st.layout.n_units, acc, grads,
+                                                                    st.master, st.exp_avg, st.exp_avg_sq, st.param,
+                                                                    None, w.hp, t)
     elif args.row == "hsdp":
         master = z(R, N, stride)
         param = z(R, N, stride, dt=torch.bfloat16) if bf else None
@@ -775,7 +787,7 @@ def main():
                     help="seconds of host-wide oracle steps for each side configuration")
     ap.add_argument("--cpu-procs", type=int, default=None,
                     help="oracle processes of the host-wide CPU baseline (default: the core count)")
-    ap.add_argument("--row", choices=["step", "clip", "accum", "hsdp", "zero1"], default="step",
+    ap.add_argument("--row", choices=["step", "clip", "accum", "accum_step", "hsdp", "zero1"], default="step",
                     help="time a row beyond the core step instead (one JSON line, no cpu baseline)")
     ap.add_argument("--groups", type=int, default=2, help="HSDP replica groups for --row hsdp")
     ap.add_argument("--rs-kernel", choices=["auto", "direct", "staged"], default="auto",

@@ -34,7 +34,8 @@ EXPORTS = ("fsdp_layout_create", "fsdp_layout_destroy", "fsdp_layout_query", "fs
            "fsdp_layout_owner", "fsdp_clip_workspace_bytes", "fsdp_reduce_scatter_clip_adamw",
            "fsdp_accumulate_grads", "fsdp_hsdp_reduce_scatter_adamw", "fsdp_zero1_adamw_broadcast",
            "fsdp_set_rs_kernel", "fsdp_rs_kernel_for", "fsdp_wait_selftest", "fsdp_adamw_step_consts_make",
-           "fsdp_reduce_scatter_adamw_consts", "fsdp_adamw_step_consts_upload", "fsdp_collective_payload")
+           "fsdp_reduce_scatter_adamw_consts", "fsdp_adamw_step_consts_upload", "fsdp_collective_payload",
+           "fsdp_accumulate_reduce_scatter_adamw")
 
 
 class FsdpError(RuntimeError):
@@ -108,6 +109,8 @@ def lib() -> C.CDLL:
         L.fsdp_reduce_scatter_clip_adamw.argtypes = [vp, i32, i32, C.POINTER(vp), i32, vp, vp, vp, vp, vp, C.c_float,
                                                      vp, vp, C.POINTER(AdamWHparams), i64, vp]
         L.fsdp_accumulate_grads.argtypes = [vp, i32, i32, C.POINTER(vp), C.POINTER(vp), i32, i32, vp]
+        L.fsdp_accumulate_reduce_scatter_adamw.argtypes = [vp, i32, i32, C.POINTER(vp), C.POINTER(vp), i32, vp, vp,
+                                                           vp, vp, vp, C.POINTER(AdamWHparams), i64, vp]
         L.fsdp_hsdp_reduce_scatter_adamw.argtypes = [vp, i32, i32, i32, C.POINTER(vp), i32, vp, vp, vp, vp,
                                                      C.POINTER(AdamWHparams), i64, vp]
         L.fsdp_zero1_adamw_broadcast.argtypes = [vp, i32, i32, C.POINTER(vp), i32, vp, vp, vp, C.POINTER(vp), i32,
@@ -368,6 +371,24 @@ def fsdp_accumulate_grads(layout: Layout, unit_begin: int, unit_end: int, acc, m
         micro_dtype = _dtype_code(micro[0])
     _check(lib().fsdp_accumulate_grads(layout.handle, unit_begin, unit_end, _ptr_array(acc), _ptr_array(micro),
                                        micro_dtype, int(bool(first)), _stream(stream)), "fsdp_accumulate_grads")
+
+
+def fsdp_accumulate_reduce_scatter_adamw(layout: Layout, unit_begin: int, unit_end: int, acc, micro, master,
+                                         exp_avg, exp_avg_sq, param_shards=None, grad_shard_out=None,
+                                         hp=(1e-3, 0.9, 0.999, 1e-8, 0.01), step: int = 1, stream=None,
+                                         micro_dtype: Optional[int] = None) -> None:
+    """The last micro-batch of a no_sync accumulation fused with the step: acc (N fp32
+    accumulators, read only) plus micro (N micro-batch gradients), reduce-scattered, AdamW, cast."""
+    if len(acc) != layout.N or len(micro) != layout.N:
+        raise ValueError(f"need {layout.N} accumulators and micro-gradients")
+    if micro_dtype is None:
+        micro_dtype = _dtype_code(micro[0])
+    h = hp if isinstance(hp, AdamWHparams) else AdamWHparams(*hp)
+    _check(lib().fsdp_accumulate_reduce_scatter_adamw(layout.handle, unit_begin, unit_end, _ptr_array(acc),
+                                                      _ptr_array(micro), micro_dtype, _ptr(master), _ptr(exp_avg),
+                                                      _ptr(exp_avg_sq), _ptr(param_shards), _ptr(grad_shard_out),
+                                                      C.byref(h), step, _stream(stream)),
+           "fsdp_accumulate_reduce_scatter_adamw")
 
 
 def fsdp_hsdp_reduce_scatter_adamw(layout: Layout, unit_begin: int, unit_end: int, n_groups: int, grad_replicas,

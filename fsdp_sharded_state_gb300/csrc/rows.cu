@@ -347,6 +347,86 @@ k_accumulate(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, A
 }
 
 // ---------------------------------------------------------------------------
+// The last micro-batch of a no_sync accumulation fused with the step, direct: per
+// replica q its fp32 accumulator plus its micro-batch gradient at the same full-layout
+// element (the accumulation's own fp32 addition), those sums in rank order, the mean,
+// AdamW and the cast.  The accumulators are read only.  Vectors where the view's
+// full-layout position is congruent to its shard position mod 8, else element by element.
+// ---------------------------------------------------------------------------
+template <typename MT, bool PARAM, bool GOUT>
+__global__ void __launch_bounds__(kThreads, 2)
+k_acc_rs_adamw(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, GradPtrs acc, GradPtrs micro, int N,
+               float* __restrict__ master, float* __restrict__ exp_avg, float* __restrict__ exp_avg_sq,
+               uint16_t* __restrict__ param, float* __restrict__ gout, AdamScal sc) {
+    pdl_wait();
+    int s = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const int64_t gt = tile_base + t;
+        s = advance_seg(segs, s, gt);
+        const Seg sg = segs[s];
+        const int64_t e0 = tile_e0(sg, gt);
+        const int64_t lo = sg.shard, hi = sg.shard + sg.len, delta = sg.full - sg.shard;
+        if (e0 >= hi) continue;
+        if (e0 >= lo && e0 + kVec <= hi && (delta & (kVec - 1)) == 0) {
+            const int64_t f0 = e0 + delta;
+            const float4 p0 = ld4(master + e0), p1 = ld4(master + e0 + 4);
+            const float4 m0 = ld4(exp_avg + e0), m1 = ld4(exp_avg + e0 + 4);
+            const float4 v0 = ld4(exp_avg_sq + e0), v1 = ld4(exp_avg_sq + e0 + 4);
+            float sum[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sum[k] = 0.0f;
+#pragma unroll 1
+            for (int q = 0; q < N; ++q) {
+                const float* a = static_cast<const float*>(acc.p[q]) + f0;
+                const uint4 x0 = ld_once(a), x1 = ld_once(a + 4);
+                const typename GradIO<MT>::Vec mv = GradIO<MT>::load(micro.p[q], f0);
+                const uint32_t aw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    sum[k] = __fadd_rn(sum[k], __fadd_rn(__uint_as_float(aw[k]), GradIO<MT>::elem(mv, mv, k)));
+            }
+            float g[8];
+            float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                g[k] = mean_div(sum[k], sc.nf);
+                adamw1(sc, g[k], p[k], m[k], v[k]);
+            }
+            st4(master + e0, make_float4(p[0], p[1], p[2], p[3]));
+            st4(master + e0 + 4, make_float4(p[4], p[5], p[6], p[7]));
+            st4(exp_avg + e0, make_float4(m[0], m[1], m[2], m[3]));
+            st4(exp_avg + e0 + 4, make_float4(m[4], m[5], m[6], m[7]));
+            st4(exp_avg_sq + e0, make_float4(v[0], v[1], v[2], v[3]));
+            st4(exp_avg_sq + e0 + 4, make_float4(v[4], v[5], v[6], v[7]));
+            if (PARAM)
+                stu4(param + e0, make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                                            pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7])));
+            if (GOUT) {
+                st4(gout + e0, make_float4(g[0], g[1], g[2], g[3]));
+                st4(gout + e0 + 4, make_float4(g[4], g[5], g[6], g[7]));
+            }
+        } else {
+            const int64_t a = e0 > lo ? e0 : lo, b = (e0 + kVec) < hi ? (e0 + kVec) : hi;
+            for (int64_t e = a; e < b; ++e) {
+                const int64_t f = e + delta;
+                float sum = 0.0f;
+                for (int q = 0; q < N; ++q)
+                    sum = __fadd_rn(sum, __fadd_rn(static_cast<const float*>(acc.p[q])[f],
+                                                   GradIO<MT>::load1(micro.p[q], f)));
+                const float g = mean_div(sum, sc.nf);
+                float pp = master[e], mm = exp_avg[e], vv = exp_avg_sq[e];
+                adamw1(sc, g, pp, mm, vv);
+                master[e] = pp; exp_avg[e] = mm; exp_avg_sq[e] = vv;
+                if (PARAM) param[e] = to_bf16(pp);
+                if (GOUT) gout[e] = g;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // HSDP: g = (sum over groups rho of (sum over q of G[rho*N + q]) / N) / R, then
 // the same AdamW on each group's copy of the state (copy rho at rho*copy).
 // Aligned segments take 16-byte vectors; shifted ones go element by element.
@@ -750,6 +830,61 @@ int fsdp_accumulate_grads(const fsdp_layout* L, int32_t ub, int32_t ue, float* c
     };
     const cudaError_t e = micro_dtype == FSDP_BF16 ? go(k_accumulate<uint16_t>) : go(k_accumulate<float>);
     return e == cudaSuccess ? FSDP_OK : cuda_fail(e, "k_accumulate launch");
+}
+
+int fsdp_accumulate_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, const float* const* acc,
+                                         const void* const* micro, int32_t micro_dtype, float* master,
+                                         float* exp_avg, float* exp_avg_sq, void* param_shards, float* grad_shard_out,
+                                         const fsdp_adamw_hparams* hp, int64_t step, fsdp_stream_t stream) {
+    fsdp::detail::NvtxRange nvtx_range("fsdp_accumulate_reduce_scatter_adamw");
+    int rc = check_units(L, ub, ue);
+    if (rc) return rc;
+    if (L->mode == FSDP_ZERO1) return FSDP_EINVAL;
+    if (micro_dtype != FSDP_F32 && micro_dtype != FSDP_BF16) return FSDP_EDTYPE;
+    if (step < 1) return FSDP_EINVAL;
+    if ((rc = ptrs_ok(reinterpret_cast<const void* const*>(acc), L->N)) || (rc = ptrs_ok(micro, L->N)) ||
+        (rc = check_ptr(master)) || (rc = check_ptr(exp_avg)) || (rc = check_ptr(exp_avg_sq)))
+        return rc;
+    if ((param_shards && !aligned16(param_shards)) || (grad_shard_out && !aligned16(grad_shard_out)))
+        return FSDP_EALIGN;
+    if ((rc = check_hparams(hp))) return rc;
+    const AdamScal sc = adam_scalars(hp, step, L->N);
+    GradPtrs ga{}, gm{};
+    for (int32_t q = 0; q < L->N; ++q) {
+        ga.p[q] = acc[q];
+        gm.p[q] = micro[q];
+    }
+    const Seg* base = nullptr;
+    if ((rc = device_tables(L, &base))) return rc;
+    const bool bf = micro_dtype == FSDP_BF16;
+    bool staged = false;
+    if ((rc = choose_staged(fsdp::acc_rs_staged_fits(bf), true, &staged))) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const Range D = range_of(L->data, base, ub, ue);
+    uint16_t* par = static_cast<uint16_t*>(param_shards);
+    if (D.n_tiles > 0 && staged) {
+        const cudaError_t e = fsdp::launch_acc_rs_adamw_staged(D.segs, D.tile_base, D.n_tiles, bf, ga, gm, L->N, master,
+                                                               exp_avg, exp_avg_sq, par, grad_shard_out, sc, kWaitNs,
+                                                               st);
+        if (e != cudaSuccess) return cuda_fail(e, "k_acc_rs_adamw_staged launch");
+    } else if (D.n_tiles > 0) {
+        auto go = [&](auto k) {
+            return launch(k, dim3(grid_of(k, D.n_tiles)), dim3(kThreads), 0, st, D.segs, D.tile_base, D.n_tiles, ga, gm,
+                          L->N, master, exp_avg, exp_avg_sq, par, grad_shard_out, sc);
+        };
+        cudaError_t e;
+        if (bf) e = par ? (grad_shard_out ? go(k_acc_rs_adamw<uint16_t, true, true>) : go(k_acc_rs_adamw<uint16_t, true, false>))
+                        : (grad_shard_out ? go(k_acc_rs_adamw<uint16_t, false, true>) : go(k_acc_rs_adamw<uint16_t, false, false>));
+        else e = par ? (grad_shard_out ? go(k_acc_rs_adamw<float, true, true>) : go(k_acc_rs_adamw<float, true, false>))
+                     : (grad_shard_out ? go(k_acc_rs_adamw<float, false, true>) : go(k_acc_rs_adamw<float, false, false>));
+        if (e != cudaSuccess) return cuda_fail(e, "k_acc_rs_adamw launch");
+    }
+    if (grad_shard_out) {                         // its padding: +0
+        const Range P = range_of(L->pad, base, ub, ue);
+        const cudaError_t e = fsdp::launch_zero_pad(P.segs, P.tile_base, P.n_tiles, grad_shard_out, nullptr, st);
+        if (e != cudaSuccess) return cuda_fail(e, "k_zero_pad launch");
+    }
+    return FSDP_OK;
 }
 
 int fsdp_hsdp_reduce_scatter_adamw(const fsdp_layout* L, int32_t ub, int32_t ue, int32_t n_groups,

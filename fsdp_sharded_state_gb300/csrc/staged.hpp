@@ -33,6 +33,16 @@ cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n
                                    float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st,
                                    const AdamScal* dsc = nullptr);   // dsc: constants read on the device
 
+// The last micro-batch of a no_sync accumulation fused with the step: replica q
+// contributes acc.p[q] (fp32 accumulator) + micro.p[q] (micro_bf16 ? bf16 : fp32),
+// full layout; the accumulators are read only.  Replicas come in groups where all N
+// pairs and the state do not fit two stages.  acc_rs_staged_fits: one pair does.
+cudaError_t launch_acc_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool micro_bf16,
+                                       const GradPtrs& acc, const GradPtrs& micro, int N, float* master, float* m,
+                                       float* v, uint16_t* param, float* gout, const AdamScal& sc, uint64_t wait_ns,
+                                       cudaStream_t st);
+bool acc_rs_staged_fits(bool micro_bf16);
+
 // HSDP: replicas gp.p[rho*N + q]; state copy rho at element offset rho * copy; rf = R.
 cudaError_t launch_hsdp_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
                                      const GradPtrs& gp, int N, int R, int64_t copy, float* master, float* m,

@@ -14,6 +14,8 @@
 //   k_zero1_adamw_staged  the ZeRO-1 owner step ("NCCL ZeRO/FSDP state sharding",
 //                         "ZeRO-1"): mean over the N replicas, AdamW on the owner's
 //                         state, the result stored into all N parameter replicas.
+//   k_acc_rs_adamw_staged the last micro-batch of a no_sync accumulation ("第18章
+//                         FSDP" §18.26) fused with the reduce-scatter + AdamW + cast.
 //
 // Arithmetic and its order are those of the direct kernels (rows.cu), bit for bit
 // (the clip norm's double sum is grouped per warp instead of per CTA).
@@ -566,6 +568,159 @@ k_accumulate_staged(Accumulate<MT, FIRST> pol, int64_t n_items, int S, int stage
     run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
 }
 
+// Running sums of a thread's four elements, carried from one replica group to the next.
+struct AccSum4 {
+    float a0, a1, a2, a3;
+};
+
+// ---- the last micro-batch of a no_sync accumulation, fused with the step -----------
+// ("第18章 FSDP" §18.26.)  Replica q contributes acc_q + micro_q: its fp32 accumulator
+// and its micro-batch gradient (MT) at the same full-layout element, added in fp32 --
+// the accumulation's own addition -- and the sums join the running mean's sum in rank
+// order, as the fused step would read accumulators that had been updated first.  The
+// accumulators are read only.  A stage holds the three state slices and, per replica of
+// the group, its accumulator slice then its micro-batch slice; each slice is the
+// 16-byte-aligned window of its own element size around the tile's full-layout range.
+template <typename MT, bool PARAM, bool GOUT>
+struct AccRsAdamw {
+    static constexpr bool kGeomFirst = true;
+    static constexpr int kPair = grank_bytes<float>() + grank_bytes<MT>();   // one replica's slices
+    const Seg* segs;
+    int64_t tile_base;
+    GradPtrs acc, micro;
+    int N, Q, NG;
+    float *master, *exp_avg, *exp_avg_sq;
+    uint16_t* param;
+    float* gout;
+    AdamScal sc;
+
+    using Carry = AccSum4;
+    __device__ int groups() const { return NG; }
+    __device__ int q0(const TileGeom& g) const { return g.q * Q; }
+    __device__ int nq(const TileGeom& g) const { return (N - g.q * Q) < Q ? (N - g.q * Q) : Q; }
+    __device__ bool last(const TileGeom& g) const { return g.q == NG - 1; }
+    // the fp32 accumulators' window is the geometry's (ag, bg, gbase); the micro-batch's
+    // window, for MT elements, is formed here
+    __device__ static void mwin(const TileGeom& g, int64_t& a, int64_t& b, int64_t& base) {
+        constexpr int64_t E = 16 / sizeof(MT);
+        a = ceil_to(g.s0 + g.delta, E);
+        b = floor_to(g.s1 + g.delta, E);
+        base = floor_to(g.t0 + g.delta, E);
+    }
+    __device__ TileGeom geom(int64_t u, int k, int& cur) const {
+        const int64_t gt = tile_base + u;
+        cur = advance_seg(segs, cur, gt);
+        TileGeom g = tile_geom<float>(segs[cur], gt);
+        g.q = k;
+        return g;
+    }
+    __device__ uint32_t bytes(const TileGeom& g) const {
+        int64_t ma, mb, mbase;
+        mwin(g, ma, mb, mbase);
+        const uint32_t sb = g.bs > g.as && last(g) ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t ab = g.bg > g.ag ? uint32_t(g.bg - g.ag) * 4u : 0u;
+        const uint32_t mbytes = mb > ma ? uint32_t(mb - ma) * uint32_t(sizeof(MT)) : 0u;
+        return 3u * sb + uint32_t(nq(g)) * (ab + mbytes);
+    }
+    __device__ void issue(const TileGeom& g, uint32_t sbase, uint32_t bar, int lane) const {
+        int64_t ma, mb, mbase;
+        mwin(g, ma, mb, mbase);
+        const uint32_t sb = g.bs > g.as && last(g) ? uint32_t(g.bs - g.as) * 4u : 0u;
+        const uint32_t ab = g.bg > g.ag ? uint32_t(g.bg - g.ag) * 4u : 0u;
+        const uint32_t mbytes = mb > ma ? uint32_t(mb - ma) * uint32_t(sizeof(MT)) : 0u;
+        const int k0 = q0(g), n = nq(g);
+        for (int k = lane; k < 3 + 2 * n; k += 32) {
+            if (k < 3) {
+                const float* arr = k == 0 ? master : (k == 1 ? exp_avg : exp_avg_sq);
+                if (sb) bulk_g2s(sbase + k * kStateBytes + uint32_t(g.as - g.t0) * 4u, arr + g.as, sb, bar);
+            } else {
+                const int q = (k - 3) >> 1;
+                const uint32_t slot = sbase + 3 * kStateBytes + q * kPair;
+                if ((k - 3) & 1) {
+                    if (mbytes)
+                        bulk_g2s(slot + grank_bytes<float>() + uint32_t(ma - mbase) * uint32_t(sizeof(MT)),
+                                 static_cast<const MT*>(micro.p[k0 + q]) + ma, mbytes, bar);
+                } else if (ab) {
+                    bulk_g2s(slot + uint32_t(g.ag - g.gbase) * 4u, static_cast<const float*>(acc.p[k0 + q]) + g.ag,
+                             ab, bar);
+                }
+            }
+        }
+    }
+    template <class Release>
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry& carry, Release release) const {
+        int64_t ma, mb, mbase;
+        mwin(g, ma, mb, mbase);
+        const int c = tid * 4;
+        const int64_t x = g.t0 + c, f = x + g.delta;
+        const bool live = x + 4 > g.s0 && x < g.s1;
+        const bool fast = x >= g.s0 && x + 4 <= g.s1 && f >= g.ag && f + 4 <= g.bg && f >= ma && f + 4 <= mb;
+        const bool fin = last(g);
+        float4 pv, mv, vv;
+        if (g.q == 0) carry = AccSum4{0.0f, 0.0f, 0.0f, 0.0f};
+        if (fast) {
+            if (fin) {
+                pv = lds4(sb + 0 * kStateBytes + c * 4);
+                mv = lds4(sb + 1 * kStateBytes + c * 4);
+                vv = lds4(sb + 2 * kStateBytes + c * 4);
+            }
+            const int oa = int(f - g.gbase), om = int(f - mbase), n = nq(g);
+            const unsigned char* gs = sb + 3 * kStateBytes;
+            float a0 = carry.a0, a1 = carry.a1, a2 = carry.a2, a3 = carry.a3;
+#pragma unroll 2
+            for (int q = 0; q < n; ++q) {            // rank order, continued from the last group
+                const float4 y = grad4<float>(gs + q * kPair, oa);
+                const float4 z = grad4<MT>(gs + q * kPair + grank_bytes<float>(), om);
+                a0 = __fadd_rn(a0, __fadd_rn(y.x, z.x)); a1 = __fadd_rn(a1, __fadd_rn(y.y, z.y));
+                a2 = __fadd_rn(a2, __fadd_rn(y.z, z.z)); a3 = __fadd_rn(a3, __fadd_rn(y.w, z.w));
+            }
+            carry = AccSum4{a0, a1, a2, a3};
+        }
+        release();
+        if (!fin) return 0.0;
+        if (fast) {
+            float p[4] = {pv.x, pv.y, pv.z, pv.w};
+            float m[4] = {mv.x, mv.y, mv.z, mv.w};
+            float v[4] = {vv.x, vv.y, vv.z, vv.w};
+            float gg[4] = {mean_div(carry.a0, sc.nf), mean_div(carry.a1, sc.nf), mean_div(carry.a2, sc.nf),
+                           mean_div(carry.a3, sc.nf)};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) adamw1(sc, gg[k], p[k], m[k], v[k]);
+            st4(master + x, make_float4(p[0], p[1], p[2], p[3]));
+            st4(exp_avg + x, make_float4(m[0], m[1], m[2], m[3]));
+            st4(exp_avg_sq + x, make_float4(v[0], v[1], v[2], v[3]));
+            if (PARAM)
+                *reinterpret_cast<uint2*>(param + x) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
+            if (GOUT) st4(gout + x, make_float4(gg[0], gg[1], gg[2], gg[3]));
+        } else if (live) {
+            // segment edge, or a window edge: element by element from global memory
+            const int64_t a = x > g.s0 ? x : g.s0;
+            const int64_t b = (x + 4) < g.s1 ? (x + 4) : g.s1;
+            for (int64_t e = a; e < b; ++e) {
+                const int64_t fe = e + g.delta;
+                float sum = 0.0f;
+                for (int q = 0; q < N; ++q)
+                    sum = __fadd_rn(sum, __fadd_rn(static_cast<const float*>(acc.p[q])[fe],
+                                                   GradIO<MT>::load1(micro.p[q], fe)));
+                const float gg = mean_div(sum, sc.nf);
+                float pp = master[e], mm = exp_avg[e], vv2 = exp_avg_sq[e];
+                adamw1(sc, gg, pp, mm, vv2);
+                master[e] = pp; exp_avg[e] = mm; exp_avg_sq[e] = vv2;
+                if (PARAM) param[e] = to_bf16(pp);
+                if (GOUT) gout[e] = gg;
+            }
+        }
+        return 0.0;
+    }
+    __device__ void finish(int, double) const {}
+};
+
+template <typename MT, bool PARAM, bool GOUT>
+__global__ void __launch_bounds__(kStThreads + 32, 1)
+k_acc_rs_adamw_staged(AccRsAdamw<MT, PARAM, GOUT> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+}
+
 int hsdp_stage_bytes(int N, int R, bool bf16) {
     return 3 * R * kStateBytes + R * N * (bf16 ? grank_bytes<uint16_t>() : grank_bytes<float>());
 }
@@ -573,6 +728,40 @@ int norm_stage_bytes(int N, bool bf16) { return N * (bf16 ? grank_bytes<uint16_t
 int acc_stage_bytes(int Q, bool bf16, bool first) { return Q * (int(kTileElems) * (bf16 ? 2 : 4) + (first ? 0 : kStateBytes)); }
 
 }  // namespace
+
+cudaError_t launch_acc_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool micro_bf16,
+                                       const GradPtrs& acc, const GradPtrs& micro, int N, float* master, float* m,
+                                       float* v, uint16_t* param, float* gout, const AdamScal& sc, uint64_t wait_ns,
+                                       cudaStream_t st) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int pair = micro_bf16 ? AccRsAdamw<uint16_t, false, false>::kPair : AccRsAdamw<float, false, false>::kPair;
+    auto stage = [&](int q) { return 3 * kStateBytes + q * pair; };
+    int NG = 1;                          // the fewest equal groups whose stage fits twice
+    while (NG < N && stage_count(stage((N + NG - 1) / NG), dev) < 2) ++NG;
+    const int Q = (N + NG - 1) / NG;
+    if (stage_count(stage(Q), dev) < 2) return cudaErrorInvalidValue;
+    auto go = [&](auto tag_mt, auto tag_p, auto tag_g) {
+        using MT = decltype(tag_mt);
+        constexpr bool P = decltype(tag_p)::value, O = decltype(tag_g)::value;
+        AccRsAdamw<MT, P, O> pol{segs, tile_base, acc, micro, N, Q, NG, master, m, v, param, gout, sc};
+        return launch_pipeline(k_acc_rs_adamw_staged<MT, P, O>, pol, n_tiles, stage(Q), wait_ns, st);
+    };
+    using T = std::true_type;
+    using F = std::false_type;
+    if (micro_bf16) {
+        if (param) return gout ? go(uint16_t{}, T{}, T{}) : go(uint16_t{}, T{}, F{});
+        return gout ? go(uint16_t{}, F{}, T{}) : go(uint16_t{}, F{}, F{});
+    }
+    if (param) return gout ? go(float{}, T{}, T{}) : go(float{}, T{}, F{});
+    return gout ? go(float{}, F{}, T{}) : go(float{}, F{}, F{});
+}
+
+bool acc_rs_staged_fits(bool micro_bf16) {
+    const int pair = micro_bf16 ? AccRsAdamw<uint16_t, false, false>::kPair : AccRsAdamw<float, false, false>::kPair;
+    return fits(3 * kStateBytes + pair);
+}
 
 bool hsdp_staged_fits(int N, int R, bool grad_bf16, int64_t copy) {
     return R <= HsdpAdamw<float, false>::kMaxR && (copy & 3) == 0 && fits(hsdp_stage_bytes(N, R, grad_bf16));

@@ -344,6 +344,29 @@ int fsdp_accumulate_grads(const fsdp_layout* layout, int32_t unit_begin, int32_t
                           float* const* acc, const void* const* micro, int32_t micro_dtype,
                           int32_t first, fsdp_stream_t stream);
 
+/* The last micro-batch of a gradient accumulation without synchronisation, fused with
+ * the reduce-scatter + AdamW + cast ([FSDP-ch18] §18.26: the micro-batches before the
+ * last accumulate their unsharded gradients locally; the last one runs with
+ * synchronisation, its gradients added to the accumulated ones and reduce-scattered).
+ * For rank r and shard element j with full-layout index f:
+ *   g = (sum over q = 0..N-1, in that order, of (acc[q][f] + micro[q][f])) / N
+ * in fp32 (each acc + micro one fp32 addition, as fsdp_accumulate_grads makes it), then
+ * AdamW and the cast exactly as fsdp_reduce_scatter_adamw.  Bit for bit the results of
+ * fsdp_accumulate_grads(first = 0) followed by fsdp_reduce_scatter_adamw(FSDP_F32) on
+ * the accumulators, in one pass that reads each accumulator once and writes none: the
+ * accumulators are read only (FSDP frees the unsharded gradients after the
+ * reduce-scatter).
+ *   acc    host array of N device pointers: fp32 full-layout accumulators
+ *   micro  host array of N device pointers: the last micro-batch, micro_dtype
+ * Other arguments, checks and results as fsdp_reduce_scatter_adamw (grad_shard_out
+ * optional; the kernel choice of fsdp_set_rs_kernel applies: staged by default, with
+ * the replicas in groups where all N pairs of slices do not fit). */
+int fsdp_accumulate_reduce_scatter_adamw(const fsdp_layout* layout, int32_t unit_begin, int32_t unit_end,
+                                         const float* const* acc, const void* const* micro, int32_t micro_dtype,
+                                         float* master, float* exp_avg, float* exp_avg_sq, void* param_shards,
+                                         float* grad_shard_out, const fsdp_adamw_hparams* hp, int64_t step,
+                                         fsdp_stream_t stream);
+
 /* HSDP step ([FSDP-ch18] §18.9: shard inside a group, replicate across groups;
  * reduce-scatter in the shard dimension, then one all-reduce across the replica
  * groups; torchtitan article §3).  R = n_groups groups of N ranks (R*N <=

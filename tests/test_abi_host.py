@@ -222,6 +222,31 @@ def test_reduce_scatter_adamw_validation(lay, fn):
     assert rs(lay, ub=-1) == -1
 
 
+def test_accumulate_reduce_scatter_adamw_validation(lay):
+    lib = fs.lib()
+    h = fs.AdamWHparams(1e-3, 0.9, 0.999, 1e-8, 0.01)
+
+    def call(acc=None, micro=None, mdt=1, master=A, m=A, v=A, param=None, gout=None, hp=h, step=1, ub=0, ue=2,
+             L=lay):
+        a = (C.c_void_p * L.N)(*(acc or [A] * L.N))
+        mi = (C.c_void_p * L.N)(*(micro or [A] * L.N))
+        return lib.fsdp_accumulate_reduce_scatter_adamw(L.handle, ub, ue, a, mi, mdt, master, m, v, param, gout,
+                                                        C.byref(hp), step, None)
+    assert call(ue=3) == -1
+    assert call(mdt=2) == -2
+    assert call(step=0) == -1
+    assert call(acc=[A, None, A, A]) == -1
+    assert call(micro=[A, A, A + 2, A]) == -4
+    assert call(acc=[A, A, A, A + 4]) == -4
+    assert call(master=None) == -1
+    assert call(v=A + 4) == -4
+    assert call(param=A + 2) == -4
+    assert call(gout=A + 8) == -4
+    assert call(hp=fs.AdamWHparams(1e-3, 1.0, 0.999, 1e-8, 0.01)) == -1
+    z = fs.Layout([(64, 32), (64,)], None, 4, fs.FSDP_ZERO1)
+    assert call(L=z, ue=1) == -1
+
+
 @pytest.mark.parametrize("fn", RS_ENTRY_POINTS)
 def test_reduce_scatter_adamw_rejects_zero1_layouts(fn):
     # a ZeRO-1 layout keeps parameters whole: the reduce-scatter step does not apply

@@ -99,6 +99,9 @@ def _run(w):
     acc = [A.make(f"acc{q}", F, torch.float32) for q in range(N)]
     for mi in range(2):
         fs.fsdp_accumulate_grads(L, 0, L.n_units, acc, synth.grad_replicas(w, F, 10 + mi), first=(mi == 0))
+    # the last micro-batch fused with the step, reading the guarded accumulators
+    fs.fsdp_accumulate_reduce_scatter_adamw(L, 0, L.n_units, acc, synth.grad_replicas(w, F, 12), master, m, v, param,
+                                            gout, w.hp, 5)
     # HSDP with two replica groups (the staged kernel may refuse a layout: then nothing runs)
     R = 2
     hm = A.make("hsdp_master", R * N * stride, torch.float32)

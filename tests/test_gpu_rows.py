@@ -136,6 +136,63 @@ def test_accumulate_then_step_vs_oracle(oracle_lib, w, micro_dtype):
 
 
 # ---------------------------------------------------------------------------
+# The last micro-batch fused with the step: against the oracle (accumulate every
+# micro-batch, then the step on the accumulators), against the unfused calls bit for
+# bit, and the accumulators left as they were.
+ACC_RS_CASES = [
+    (W([(37, 5), (3,), (11, 13)], [0, 1, 1], 6, synth.FLAT), torch.bfloat16),       # views off their congruence
+    (W([(130, 64), (7,), (9, 3)], [0, 0, 1], 4, synth.DIM0), torch.float32),
+    (W([(1 << 22,)], [0], 4, synth.FLAT, torch.float32), torch.float32),
+    (W([(300, 40), (9,)], [0, 0], 8, synth.FLAT, torch.float32), torch.float32),    # replica groups
+    (W([(5000,), (33,)], [0, 0], 16, synth.FLAT), torch.bfloat16),                  # replica groups
+]
+
+
+@pytest.mark.parametrize("w,micro_dtype", ACC_RS_CASES)
+def test_accumulate_reduce_scatter_vs_oracle(oracle_lib, w, micro_dtype):
+    M = 3
+    sh = oracle.Shapes(w.shapes, w.unit_ids)
+    O = pu.oracle_offsets(w)
+    a, b = pu.make_state(w, with_grad_out=True), pu.make_state(w, with_grad_out=True)
+    full = synth.full_params(w, a.F, O["t_full_off"])
+    a.init_from_full(full)
+    b.init_from_full(full)
+    bf16 = w.param_dtype == torch.bfloat16
+    om, op = oracle.reshard(sh, w.N, w.mode, pu.f32(full), a.stride, True, bf16)
+    m, v, go = np.zeros_like(om), np.zeros_like(om), np.zeros_like(om)
+    acc_a = [torch.zeros(a.F, dtype=torch.float32, device="cuda") for _ in range(w.N)]
+    acc_b = [torch.zeros(a.F, dtype=torch.float32, device="cuda") for _ in range(w.N)]
+    ref_acc = [np.zeros(a.F, np.float32) for _ in range(w.N)]
+    micros = [[g.to(micro_dtype) for g in synth.grad_replicas(w, a.F, 10 + mi)] for mi in range(M)]
+    for mi in range(M):
+        for q in range(w.N):
+            oracle.accumulate(ref_acc[q], pu.grads_np([micros[mi][q]])[0], first=(mi == 0))
+    for mi in range(M - 1):
+        fs.fsdp_accumulate_grads(a.layout, 0, a.layout.n_units, acc_a, micros[mi], first=(mi == 0))
+        fs.fsdp_accumulate_grads(b.layout, 0, b.layout.n_units, acc_b, micros[mi], first=(mi == 0))
+    before = [x.clone() for x in acc_a]
+    # fused: the last micro-batch and the step in one call
+    fs.fsdp_accumulate_reduce_scatter_adamw(a.layout, 0, a.layout.n_units, acc_a, micros[M - 1], a.master, a.exp_avg,
+                                            a.exp_avg_sq, a.param, a.grad_out, w.hp, 1)
+    # unfused: the accumulation, then the step on the accumulators
+    fs.fsdp_accumulate_grads(b.layout, 0, b.layout.n_units, acc_b, micros[M - 1], first=False)
+    b.reduce_scatter_adamw(acc_b, w.hp, step=1)
+    oracle.rs_adamw(sh, w.N, w.mode, ref_acc, a.stride, om, m, v, param=op, grad_out=go, hp=w.hp, step=1)
+    torch.cuda.synchronize()
+    for x, y in zip(acc_a, before):                       # read only
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    for name in ("master", "exp_avg", "exp_avg_sq", "grad_out"):
+        assert torch.equal(getattr(a, name).view(torch.int32), getattr(b, name).view(torch.int32)), name
+    if bf16:
+        assert torch.equal(a.param.view(torch.int16), b.param.view(torch.int16))
+        pu.assert_bf16_close(pu.u16(a.param).reshape(-1), op, "param")
+    pu.assert_f32_close(pu.f32(a.master).reshape(-1), om, "master")
+    pu.assert_f32_close(pu.f32(a.exp_avg).reshape(-1), m, "exp_avg")
+    pu.assert_f32_close(pu.f32(a.exp_avg_sq).reshape(-1), v, "exp_avg_sq")
+    pu.assert_f32_close(pu.f32(a.grad_out).reshape(-1), go, "grad_out")
+
+
+# ---------------------------------------------------------------------------
 @pytest.mark.parametrize("w,R", [(W([(37, 5), (3,), (11, 13)], [0, 1, 1], 3, synth.FLAT), 2),
                                  (W([(130, 64), (7,), (9, 3)], [0, 0, 0], 4, synth.DIM0), 2),
                                  (W([(1 << 22,)], [0], 4, synth.FLAT), 4),
