@@ -5,15 +5,20 @@
 // full-layout position mod 8).
 //
 // The two-pass form (rows.cu) writes the whole fp32 gradient shard in pass 1 and reads
-// it back in pass 3.  Here every CTA owns one contiguous block of tiles for both
-// phases, split among its four 256-thread groups: phase 1 walks a group's tiles
-// forward (reduce-scatter, sum of squares) and keeps the reduced gradient of its last
-// kKeepSmem tiles in shared memory instead of storing it; the tiles before those are
-// stored with an L2 evict-last policy.  After a grid-wide barrier (bounded in time)
-// every CTA forms the norm and the clip coefficient from the per-CTA partials, in one
-// fixed order, and phase 3 walks the group's tiles backward: the kept tiles first, from
-// shared memory, then the ones most likely still in L2.  The kept tiles' gradient never
-// makes the write-and-read-back round trip through DRAM.
+// it back in pass 3.  Here CTA b of G takes tiles b, b + G, b + 2G, ... of the range in
+// phase 1 (reduce-scatter, sum of squares), spread over its four 256-thread groups, and
+// keeps the reduced gradient of its last kKeepTotal tiles in shared memory instead of
+// storing it (over the grid: the top kKeepTotal G tiles of the range); the kKeepTotal
+// before those are stored with an L2 evict-last policy.  After a grid-wide barrier
+// (bounded in time) every CTA forms the norm and the clip coefficient from the per-CTA
+// partials, in one fixed order.  In phase 3 each group first updates its kept tiles
+// from shared memory, then claims the other tiles one at a time from a grid-wide
+// counter, from the top of the range down (the evict-last tiles first).  The kept
+// tiles' gradient never makes the write-and-read-back round trip through DRAM, and the
+// claims let the SMs that stream faster take more tiles: measured on GB300, a static
+// split of phase 3 left the fastest SMs idle for up to 13 % of it.  Phase 1 stays a
+// static split, so that the norm's grouping, and with it the norm, is the same in
+// every run.
 //
 // The arithmetic per element is that of the two-pass kernels (rows.cu), operation for
 // operation; the norm's double sum is grouped per CTA over other tile sets, so its last
@@ -29,7 +34,7 @@ namespace {
 constexpr int kCoopGroups = 4;                          // 256-thread tile groups per CTA
 constexpr int kCoopThreads = kThreads * kCoopGroups;    // 1024
 constexpr int kKeepSmem = 6;                            // tiles kept in shared memory per group
-constexpr int kKeepL2 = 6;                              // the tiles before them: evict-last stores
+constexpr int kKeepTotal = kKeepSmem * kCoopGroups;     // per CTA; as many before them: evict-last stores
 constexpr size_t kCoopSmem = size_t(kCoopGroups) * kKeepSmem * size_t(kTileElems) * sizeof(float);  // 192 KB
 
 __device__ __forceinline__ int64_t coop_tile_x0(const Seg& sg, int64_t gt) {
@@ -209,7 +214,8 @@ __device__ __forceinline__ double coop_phase1(const Seg& sg, int64_t gt, const G
 
 // Phase 3 on one tile (split lane mapping, as the two-pass kernel's pass 3): the clipped
 // gradient g = shard * coef -- the shard read from the tile's shared-memory slot `keep`
-// when it has one, else from memory -- written back, then AdamW and the cast.
+// when it has one, else from L2 (another SM may have written it in phase 1) -- written
+// back, then AdamW and the cast.
 template <bool PARAM>
 __device__ __forceinline__ void coop_phase3(const Seg& sg, int64_t gt, const float* keep, float coef,
                                             float* __restrict__ gshard, float* __restrict__ master,
@@ -223,7 +229,7 @@ __device__ __forceinline__ void coop_phase3(const Seg& sg, int64_t gt, const flo
     for (int c = 0; c < 2; ++c) {
         const int64_t xc = x0 + 128 * c;
         if (xc >= lo && xc + 4 <= hi) {
-            const float4 gq = keep ? *reinterpret_cast<const float4*>(keep + (xc - base)) : ld4(gshard + xc);
+            const float4 gq = keep ? *reinterpret_cast<const float4*>(keep + (xc - base)) : __ldcg(reinterpret_cast<const float4*>(gshard + xc));
             const float4 pq = ld4(master + xc), mq = ld4(exp_avg + xc), vq = ld4(exp_avg_sq + xc);
             float g[4] = {gq.x, gq.y, gq.z, gq.w}, p[4] = {pq.x, pq.y, pq.z, pq.w};
             float m[4] = {mq.x, mq.y, mq.z, mq.w}, v[4] = {vq.x, vq.y, vq.z, vq.w};
@@ -241,7 +247,7 @@ __device__ __forceinline__ void coop_phase3(const Seg& sg, int64_t gt, const flo
         } else {
             const int64_t a = xc > lo ? xc : lo, b = (xc + 4) < hi ? (xc + 4) : hi;
             for (int64_t e = a; e < b; ++e) {
-                const float g = __fmul_rn(keep ? keep[e - base] : gshard[e], coef);
+                const float g = __fmul_rn(keep ? keep[e - base] : __ldcg(gshard + e), coef);
                 float p = master[e], m = exp_avg[e], v = exp_avg_sq[e];
                 adamw1(sc, g, p, m, v);
                 gshard[e] = g; master[e] = p; exp_avg[e] = m; exp_avg_sq[e] = v;
@@ -251,10 +257,8 @@ __device__ __forceinline__ void coop_phase3(const Seg& sg, int64_t gt, const flo
     }
 }
 
-// The whole clip step.  CTA b owns tiles [n*b/G, n*(b+1)/G) of the range; its group w
-// (256 threads) takes every fourth of them from the w-th on, nw in all.  A group keeps
-// its last kKeepSmem tiles in its shared-memory slots and stores the kKeepL2 before those
-// with the evict-last policy.
+// The whole clip step.  counter[0] counts the CTAs in at the grid barrier, counter[1]
+// hands out the phase-3 tiles; both start at 0 (the launcher clears them).
 template <typename GT, bool PARAM>
 __global__ void __launch_bounds__(kCoopThreads, 1)
 k_clip_coop(const Seg* __restrict__ segs, int n_segs, int64_t tile_base, int64_t n_tiles, GradPtrs gp, int N,
@@ -264,43 +268,46 @@ k_clip_coop(const Seg* __restrict__ segs, int n_segs, int64_t tile_base, int64_t
             float* __restrict__ norm_out, float max_norm, AdamScal sc, uint64_t wait_ns) {
     extern __shared__ __align__(16) float keep_sm[];
     __shared__ double warp_part[kCoopThreads / 32];
+    __shared__ int claim_sh[kCoopGroups][2];
     __shared__ float coef_sh;
     __shared__ int ok_sh;
     const int grp = threadIdx.x / kThreads, t = threadIdx.x % kThreads;
-    const int64_t b0 = n_tiles * blockIdx.x / gridDim.x, b1 = n_tiles * (blockIdx.x + 1) / gridDim.x;
-    const int64_t nw = b1 - b0 > grp ? (b1 - b0 - grp + kCoopGroups - 1) / kCoopGroups : 0;
-    const int64_t first_keep = nw > kKeepSmem ? nw - kKeepSmem : 0;
-    const int64_t first_hint = first_keep > kKeepL2 ? first_keep - kKeepL2 : 0;
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    // this CTA's list: tiles b + k G, k < n1 (a list length fits in an int: the launcher
+    // takes ranges of fewer than 2^31 tiles); group grp takes k = grp, grp + 4, ...
+    const int n1 = b < n_tiles ? int((n_tiles - b + G - 1) / G) : 0;
+    const int keep_from = n1 - kKeepTotal;              // k >= keep_from: kept (slot (k - keep_from) / 4)
+    const int hint_from = keep_from - kKeepTotal;       // k in [hint_from, keep_from): evict-last stores
     float* my_keep = keep_sm + size_t(grp) * kKeepSmem * size_t(kTileElems);
     const uint64_t pol = coop_policy_evict_last();
 
     // ---- phase 1: reduce-scatter and sums of squares, the group's tiles forward ----
     double ss = 0.0;
-    if (nw > 0) {
-        int s = coop_find_seg(segs, n_segs, tile_base + b0 + grp);
+    if (grp < n1) {
+        int s = coop_find_seg(segs, n_segs, tile_base + b + grp * G);
 #pragma unroll 1
-        for (int64_t k = 0; k < nw; ++k) {
-            const int64_t gt = tile_base + b0 + grp + k * kCoopGroups;
+        for (int k = grp; k < n1; k += kCoopGroups) {
+            const int64_t gt = tile_base + b + int64_t(k) * G;
             s = advance_seg(segs, s, gt);
             const Seg sg = segs[s];
-            float* keep = k >= first_keep ? my_keep + (k - first_keep) * kTileElems : nullptr;
-            ss += coop_phase1<GT>(sg, gt, gp, N, nf, gshard, keep, k >= first_hint, pol, t);
+            float* keep = k >= keep_from ? my_keep + ((k - keep_from) >> 2) * kTileElems : nullptr;
+            ss += coop_phase1<GT>(sg, gt, gp, N, nf, gshard, keep, k >= hint_from, pol, t);
         }
     }
     const double tot = coop_block_sum(ss, warp_part);
-    if (threadIdx.x == 0) part[blockIdx.x] = tot;
+    if (threadIdx.x == 0) part[b] = tot;
 
     // ---- the grid barrier, then the norm and the clip coefficient in every CTA ----
     if (!coop_grid_barrier(counter, wait_ns, &ok_sh)) return;
     double x = 0.0;
-    for (int i = threadIdx.x; i < int(gridDim.x); i += kCoopThreads) x += __ldcg(part + i);
+    for (int i = threadIdx.x; i < int(G); i += kCoopThreads) x += __ldcg(part + i);
     const double all = coop_block_sum(x, warp_part);
     if (threadIdx.x == 0) {
         const double norm = sqrt(all);
         double c = double(max_norm) / (norm + 1e-6);
         if (c > 1.0) c = 1.0;
         coef_sh = float(c);
-        if (blockIdx.x == 0) {
+        if (b == 0) {
             *ws_norm = norm;
             *ws_coef = float(c);
             if (norm_out) {
@@ -312,16 +319,38 @@ k_clip_coop(const Seg* __restrict__ segs, int n_segs, int64_t tile_base, int64_t
     __syncthreads();
     const float coef = coef_sh;
 
-    // ---- phase 3: AdamW on the clipped shard, the group's tiles backward ----
-    if (nw > 0) {
-        int s = coop_find_seg(segs, n_segs, tile_base + b0 + grp + (nw - 1) * kCoopGroups);
+    // ---- phase 3 (a): the group's kept tiles, from shared memory, last first ----
+    if (grp < n1) {
+        int k = grp + (n1 - 1 - grp) / kCoopGroups * kCoopGroups;         // the group's last list entry
+        if (k >= keep_from) {
+            int s = coop_find_seg(segs, n_segs, tile_base + b + int64_t(k) * G);
 #pragma unroll 1
-        for (int64_t k = nw - 1; k >= 0; --k) {
-            const int64_t gt = tile_base + b0 + grp + k * kCoopGroups;
+            for (; k >= 0 && k >= keep_from; k -= kCoopGroups) {
+                const int64_t gt = tile_base + b + int64_t(k) * G;
+                while (segs[s].tile0 > gt) --s;
+                coop_phase3<PARAM>(segs[s], gt, my_keep + ((k - keep_from) >> 2) * kTileElems, coef, gshard, master,
+                                   exp_avg, exp_avg_sq, param, sc, t);
+            }
+        }
+    }
+    // ---- phase 3 (b): the other tiles, [0, nd), claimed one at a time from the top down ----
+    // The group's thread 0 takes the next claim while the group updates the current tile;
+    // the claim reaches the group through a two-slot shared word and one group barrier.
+    const int nd = n_tiles > kKeepTotal * G ? int(n_tiles - kKeepTotal * G) : 0;
+    if (nd > 0) {
+        unsigned int nxt = 0;
+        if (t == 0) nxt = atomicAdd(counter + 1, 1u);
+        int s = n_segs - 1;                                 // claims come from the top down
+#pragma unroll 1
+        for (unsigned int par = 0;; par ^= 1u) {
+            if (t == 0) claim_sh[grp][par] = nxt < unsigned(nd) ? nd - 1 - int(nxt) : -1;
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kThreads) : "memory");
+            const int tt = claim_sh[grp][par];
+            if (tt < 0) break;
+            const int64_t gt = tile_base + tt;
+            if (t == 0) nxt = atomicAdd(counter + 1, 1u);
             while (segs[s].tile0 > gt) --s;
-            const Seg sg = segs[s];
-            const float* keep = k >= first_keep ? my_keep + (k - first_keep) * kTileElems : nullptr;
-            coop_phase3<PARAM>(sg, gt, keep, coef, gshard, master, exp_avg, exp_avg_sq, param, sc, t);
+            coop_phase3<PARAM>(segs[s], gt, nullptr, coef, gshard, master, exp_avg, exp_avg_sq, param, sc, t);
         }
     }
 }
@@ -363,8 +392,9 @@ cudaError_t launch_clip_coop(const Seg* segs, int n_segs, int64_t tile_base, int
     *launched = false;
     auto go = [&](auto kernel) -> cudaError_t {
         const int grid = coop_grid_of(kernel);
-        if (grid <= 0 || grid > max_part) return cudaSuccess;          // not here: the caller falls back
-        cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned int), st);
+        // not here: the caller falls back (the kernel's tile indices are ints)
+        if (grid <= 0 || grid > max_part || n_tiles >= (int64_t(1) << 31)) return cudaSuccess;
+        cudaError_t e = cudaMemsetAsync(counter, 0, 2 * sizeof(unsigned int), st);
         if (e != cudaSuccess) return e;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeCooperative;

@@ -302,11 +302,14 @@ int fsdp_layout_owner(const fsdp_layout* layout, int32_t tensor, int32_t* rank);
  * goes through the AdamW and bf16 steps of fsdp_reduce_scatter_adamw.
  * Under the automatic kernel choice, when every rank view of the unit range sits at
  * a shard index congruent to its full-layout index mod 8, one cooperative launch on
- * `stream` runs the whole step: each CTA reduce-scatters a fixed block of tiles into
+ * `stream` runs the whole step: each CTA reduce-scatters a fixed set of tiles into
  * the fp32 gradient shard -- holding the last of them in shared memory -- and writes
  * its partial sum of squares; after a grid-wide barrier (bounded: it gives up after
  * 1 s and records FSDP_ETIMEOUT for fsdp_check_status) every CTA adds the partials in
- * double in the same order, forms the coefficient, scales its tiles and runs AdamW.
+ * double in the same order, forms the coefficient, scales and updates the tiles it
+ * holds, then takes the other tiles one at a time from a shared counter in the
+ * workspace and scales and updates them (the tile sets of the sums are fixed, so the
+ * norm is the same in every run).
  * Otherwise (or when the device cannot hold the whole grid at once), two passes: the
  * reduce-scatter writes the fp32 gradient shard and per-CTA partial sums of squares
  * (fixed order, so the norm is reproducible on a given GPU); the update pass adds the
@@ -318,7 +321,7 @@ int fsdp_layout_owner(const fsdp_layout* layout, int32_t tensor, int32_t* rank);
  *   max_norm    > 0 and finite.
  *   workspace   device scratch of fsdp_clip_workspace_bytes() bytes, 16-byte
  *               aligned, owned by the caller; no initial contents needed.  It holds
- *               the call's partial sums (and the cooperative launch's barrier count)
+ *               the call's partial sums (and the cooperative launch's barrier and tile counters)
  *               until the call's work has run: calls whose work may overlap on the GPU
  *               (other streams) need workspaces of their own.
  *   norm_out    optional device float[2] (8-byte aligned): total norm, coef.

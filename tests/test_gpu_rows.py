@@ -3,7 +3,7 @@ sharded clip_grad_norm_, gradient accumulation without sync, HSDP, ZeRO-1.
 
 Every test runs three times: with the default kernel choice (the bulk-copy
 staged kernels where they fit and are preferred), with the direct kernels forced
-and with the staged kernels forced (an HSDP case they do not hold is skipped)."""
+and with the staged kernels forced (an HSDP or clip case they do not hold is skipped)."""
 import numpy as np
 import pytest
 import torch
@@ -45,17 +45,20 @@ CLIP_CASES = [
 # Layouts whose rank views are all congruent to their full-layout positions mod 8, with
 # many segments and tens of tiles per CTA: under the automatic choice the clip runs as one
 # cooperative launch, whose thread groups then meet tiles kept in shared memory, tiles
-# stored with the evict-last policy and plain ones, across segment boundaries.
+# stored with the evict-last policy and plain ones, across segment boundaries, and in the
+# update phase claim the remaining tiles one by one.  The last case has misaligned rank
+# views: the two passes.
 CLIP_COOP_CASES = [
     (W([(4096, 1024), (2048, 2048), (1024, 1024), (8, 4096), (512, 520), (4096, 2048)], [0] * 6, 4, synth.DIM0,
        torch.float32), 1e-2),
     (W([(2048, 2048), (4096, 512), (16, 1024), (1024, 4096)], [0] * 4, 8, synth.DIM0), 5e-3),
     (W([(1 << 22,), (1 << 21,), (1 << 20,)], [0, 1, 2], 8, synth.FLAT), 1e3),     # clip not active
+    (W([(1 << 22,), (999_999,), (12_345,), (1 << 21,)], [0, 0, 1, 1], 6, synth.FLAT), 1e-2),   # misaligned
 ]
 
 
 @pytest.mark.parametrize("w,max_norm", CLIP_CASES + CLIP_COOP_CASES)
-def test_clip_vs_oracle(oracle_lib, w, max_norm):
+def test_clip_vs_oracle(oracle_lib, w, max_norm, rs_kind):
     st = pu.make_state(w, with_grad_out=True)
     sh = oracle.Shapes(w.shapes, w.unit_ids)
     O = pu.oracle_offsets(w)
@@ -68,8 +71,13 @@ def test_clip_vs_oracle(oracle_lib, w, max_norm):
     norm_out = torch.zeros(2, dtype=torch.float32, device="cuda")
     for t in range(1, 4):
         grads = synth.grad_replicas(w, st.F, t)
-        fs.fsdp_reduce_scatter_clip_adamw(st.layout, 0, st.layout.n_units, grads, st.master, st.exp_avg,
-                                          st.exp_avg_sq, st.param, st.grad_out, max_norm, ws, norm_out, w.hp, t)
+        try:
+            fs.fsdp_reduce_scatter_clip_adamw(st.layout, 0, st.layout.n_units, grads, st.master, st.exp_avg,
+                                              st.exp_avg_sq, st.param, st.grad_out, max_norm, ws, norm_out, w.hp, t)
+        except fs.FsdpError as e:
+            if rs_kind == "staged" and e.status == -1:
+                pytest.skip("two stages of the staged norm pass do not fit this case")
+            raise
         ref_norm = oracle.rs_clip_adamw(sh, w.N, w.mode, pu.grads_np(grads), st.stride, om, m, v, max_norm,
                                         param=op if bf16 else None, grad_out=go, hp=w.hp, step=t)
         torch.cuda.synchronize()
