@@ -1,8 +1,8 @@
 // clip_coop.cu -- the sharded clip_grad_norm_ step ("第18章 FSDP：ZeRO 风格的参数分片"
 // §18.18: every rank's sum of squares of its gradient shard, one all-reduce of the sums,
 // the global norm, every rank scales its own shard) in one cooperative launch, for unit
-// ranges whose pieces all sit in the aligned class (every rank view congruent to its
-// full-layout position mod 8).
+// ranges whose pieces sit in the aligned class (rank view congruent to its full-layout
+// position mod 8) but for a few tiles at most.
 //
 // The two-pass form (rows.cu) writes the whole fp32 gradient shard in pass 1 and reads
 // it back in pass 3.  Here CTA b of G takes tiles b, b + G, b + 2G, ... of the range in
@@ -137,19 +137,23 @@ __device__ __forceinline__ void coop_reduce8_bf16(const GradPtrs& gp, int N, int
 // Phase 1 on one tile, by one 256-thread group (t = thread in the group): the fp32 mean
 // of the N replicas into the gradient shard -- or, for a kept tile, into its shared-memory
 // slot `keep` (2048 floats, indexed by element in the tile) -- and the thread's sum of
-// squares (fp32 over a vector in order, then double, as the two-pass kernels).
+// squares (fp32 over a vector in order, then double, as the two-pass kernels).  A tile
+// whose rank view is not congruent to its full-layout position mod 8 (the launcher lets
+// through ranges where such tiles are rare) takes the per-element path throughout: its
+// replicas cannot be read with aligned 16-byte loads.
 template <typename GT>
 __device__ __forceinline__ double coop_phase1(const Seg& sg, int64_t gt, const GradPtrs& gp, int N, float nf,
                                               float* __restrict__ gout, float* keep, bool hint, uint64_t pol,
                                               int t) {
     const int64_t base = coop_tile_x0(sg, gt);
     const int64_t lo = sg.shard, hi = sg.shard + sg.len, delta = sg.full - sg.shard;
+    const bool al = (delta & (kVec - 1)) == 0;
     double ss = 0.0;
     if constexpr (std::is_same<GT, float>::value) {
         // split lane mapping: lane l owns [4l, 4l+4) and [128+4l, 128+4l+4) of its warp's 256
         const int64_t x0 = base + (t >> 5) * 256 + (t & 31) * 4, x1 = x0 + 128;
         if (x0 >= hi) return 0.0;
-        if (x0 >= lo && x1 + 4 <= hi) {
+        if (al && x0 >= lo && x1 + 4 <= hi) {
             float acc[8], g[8], sq = 0.0f;
             reduce_split_f32(gp, N, x0 + delta, x1 + delta, acc);
 #pragma unroll
@@ -168,7 +172,7 @@ __device__ __forceinline__ double coop_phase1(const Seg& sg, int64_t gt, const G
             return double(sq);
         }
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {                       // a chunk at a segment edge
+        for (int c = 0; c < 2; ++c) {                       // a chunk at a segment edge, or misaligned
             const int64_t xc = c ? x1 : x0;
             const int64_t a = xc > lo ? xc : lo, b = (xc + 4) < hi ? (xc + 4) : hi;
             for (int64_t e = a; e < b; ++e) {
@@ -183,7 +187,7 @@ __device__ __forceinline__ double coop_phase1(const Seg& sg, int64_t gt, const G
         // bf16 replicas: thread t owns the 8 elements [8t, 8t+8) of the tile
         const int64_t e0 = base + int64_t(t) * kVec;
         if (e0 >= hi) return 0.0;
-        if (e0 >= lo && e0 + kVec <= hi) {
+        if (al && e0 >= lo && e0 + kVec <= hi) {
             float acc[8], g[8], sq = 0.0f;
             coop_reduce8_bf16(gp, N, e0 + delta, acc);
 #pragma unroll

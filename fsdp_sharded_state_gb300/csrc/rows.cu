@@ -22,6 +22,7 @@ namespace fsdp {
 namespace {
 
 constexpr int kMaxPartials = 4096;                  // per launch of the norm pass
+constexpr int64_t kCoopMisalignedRatio = 256;       // the cooperative clip: misaligned tiles, at most 1 in this
 constexpr size_t kClipHeader = 64;                  // double norm, float coef
 constexpr size_t kClipWorkspace = kClipHeader + 2 * kMaxPartials * sizeof(double);
 
@@ -714,14 +715,16 @@ int fsdp_reduce_scatter_clip_adamw(const fsdp_layout* L, int32_t ub, int32_t ue,
     double* part = reinterpret_cast<double*>(ws + kClipHeader);
     const bool bf = grad_dtype == FSDP_BF16;
 
-    // The automatic choice runs the whole step in one cooperative launch when every piece
-    // of the range is in the aligned class (clip_coop.cu): each CTA keeps the gradient of
-    // its last tiles in shared memory across the grid-wide barrier, so that part of the
-    // shard is neither written to nor read back from memory between the two phases.
+    // The automatic choice runs the whole step in one cooperative launch when at most one
+    // tile in kCoopMisalignedRatio of the range is in the misaligned class (clip_coop.cu;
+    // such a tile takes the per-element path there, a few times slower than a vector
+    // tile): each CTA keeps the gradient of its last tiles in shared memory across the
+    // grid-wide barrier, so that part of the shard is neither written to nor read back
+    // from memory between the two phases.
     if (rs_kernel_choice() == FSDP_RS_AUTO) {
         const Range Dsh = range_of(L->data_sh, base, ub, ue);
         const Range Dc = range_of(L->data, base, ub, ue);
-        if (Dsh.n_tiles == 0 && Dc.n_tiles > 0) {
+        if (Dsh.n_tiles * kCoopMisalignedRatio <= Dc.n_tiles && Dc.n_tiles > 0) {
             const Range P = range_of(L->pad, base, ub, ue);
             cudaError_t e = fsdp::launch_zero_pad(P.segs, P.tile_base, P.n_tiles, grad_shard, nullptr, st);
             if (e != cudaSuccess) return cuda_fail(e, "k_zero_pad launch");

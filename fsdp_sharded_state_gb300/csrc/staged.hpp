@@ -81,7 +81,8 @@ cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_ti
 cudaError_t launch_wait_selftest(uint64_t wait_ns, cudaStream_t st);
 
 // The sharded clip step in one cooperative launch (clip_coop.cu) over a segment range
-// of the aligned class: the reduce-scatter into gshard (its last tiles per CTA held in
+// (tiles of the misaligned class take a per-element path: meant for ranges where they
+// are rare): the reduce-scatter into gshard (its last tiles per CTA held in
 // shared memory), the sums of squares into part[0 .. grid), a grid-wide barrier on
 // *counter (cleared on the stream first; bounded by wait_ns), the norm and coefficient
 // (CTA 0 stores them in ws_norm, ws_coef and norm_out), AdamW on the clipped shard.

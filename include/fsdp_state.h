@@ -300,8 +300,9 @@ int fsdp_layout_owner(const fsdp_layout* layout, int32_t tensor, int32_t* rank);
  * coef = min(1, max_norm / (norm + 1e-6)), formed in double and rounded to fp32
  * once; each reduced gradient is multiplied by it (one fp32 rounding) and then
  * goes through the AdamW and bf16 steps of fsdp_reduce_scatter_adamw.
- * Under the automatic kernel choice, when every rank view of the unit range sits at
- * a shard index congruent to its full-layout index mod 8, one cooperative launch on
+ * Under the automatic kernel choice, when the rank views of the unit range sit at shard
+ * indices congruent to their full-layout indices mod 8 but for at most one 2048-element
+ * tile in 256 (fsdp_layout_segment tells each piece's class), one cooperative launch on
  * `stream` runs the whole step: each CTA reduce-scatters a fixed set of tiles into
  * the fp32 gradient shard -- holding the last of them in shared memory -- and writes
  * its partial sum of squares; after a grid-wide barrier (bounded: it gives up after
@@ -409,8 +410,8 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
  * fsdp_zero1_adamw_broadcast.
  *   FSDP_RS_AUTO    the staged kernel where at least two of its pipeline stages fit
  *                   in one CTA's shared memory, else the direct kernels; the clip
- *                   runs as one cooperative launch where its unit range has no
- *                   misaligned rank view, else as the direct passes, and ZeRO-1 keeps
+ *                   runs as one cooperative launch where at most one tile in 256 of
+ *                   its unit range is misaligned, else as the direct passes, and ZeRO-1 keeps
  *                   the direct kernel (measured as fast or steadier).  A stage
  *                   holds 2048 elements of each array the call reads: for
  *                   fsdp_reduce_scatter_adamw the three fp32 state arrays and the N

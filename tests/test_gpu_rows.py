@@ -46,14 +46,17 @@ CLIP_CASES = [
 # many segments and tens of tiles per CTA: under the automatic choice the clip runs as one
 # cooperative launch, whose thread groups then meet tiles kept in shared memory, tiles
 # stored with the evict-last policy and plain ones, across segment boundaries, and in the
-# update phase claim the remaining tiles one by one.  The last case has misaligned rank
-# views: the two passes.
+# update phase claim the remaining tiles one by one.  The fourth case has many misaligned
+# rank views (the two passes), the last two a few (the cooperative launch).
 CLIP_COOP_CASES = [
     (W([(4096, 1024), (2048, 2048), (1024, 1024), (8, 4096), (512, 520), (4096, 2048)], [0] * 6, 4, synth.DIM0,
        torch.float32), 1e-2),
     (W([(2048, 2048), (4096, 512), (16, 1024), (1024, 4096)], [0] * 4, 8, synth.DIM0), 5e-3),
     (W([(1 << 22,), (1 << 21,), (1 << 20,)], [0, 1, 2], 8, synth.FLAT), 1e3),     # clip not active
     (W([(1 << 22,), (999_999,), (12_345,), (1 << 21,)], [0, 0, 1, 1], 6, synth.FLAT), 1e-2),   # misaligned
+    # 4 misaligned tiles among 4,641: the cooperative launch, those 4 on the per-element path
+    (W([(4096, 1024), (2048, 2048), (1024, 1024), (8, 4096), (5, 3)], [0] * 5, 6, synth.DIM0), 5e-3),
+    (W([(4096, 1024), (2048, 2048), (1024, 1024), (8, 4096), (5, 3)], [0] * 5, 6, synth.DIM0, torch.float32), 5e-3),
 ]
 
 
