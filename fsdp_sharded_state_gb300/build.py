@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libfsdpstate.so")
 SOURCES = ["api.cu", "kernels.cu", "layout.cpp", "noalloc.cu", "rows.cu", "staged.cu", "allgather.cu", "staged_rows.cu",
-           "clip_coop.cu"]
+           "clip_coop.cu", "claims.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE division and square root, no flush-to-zero, no implicit fma contraction:

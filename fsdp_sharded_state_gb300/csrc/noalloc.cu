@@ -121,9 +121,10 @@ extern "C" int fsdp_reduce_scatter_adamw_noalloc(const fsdp_layout* L, int32_t u
         e = cudaMemcpyAsync(next, L->data.segs.data() + sb, size_t(n) * sizeof(Seg), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "cudaMemcpyAsync(no-allocation table)");
         const int64_t t0 = L->data.segs[sb].tile0, t1 = L->data.segs[se].tile0;
+        // no claim counters: their ring is allocated on first use, and this call allocates nothing
         e = fsdp::launch_rs_adamw_staged(next, t0, t1 - t0, bf16, gp, L->N, master, exp_avg, exp_avg_sq,
                                          static_cast<uint16_t*>(param_shards), grad_shard_out, sc,
-                                         fsdp::detail::kWaitNs, st);
+                                         fsdp::detail::kWaitNs, st, nullptr, false);
         if (e != cudaSuccess) return fsdp::detail::cuda_fail(e, "k_rs_adamw_staged launch");
         next += n;
     }

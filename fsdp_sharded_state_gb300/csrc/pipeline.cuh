@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "device_ops.cuh"
+#include "staged.hpp"
 
 namespace fsdp {
 namespace {
@@ -122,10 +123,11 @@ __device__ __forceinline__ int64_t ceil_to(int64_t x, int64_t a) { return (x + a
 // at t0), the full-layout shift delta, and the 16-byte-aligned sub-ranges the
 // bulk copies bring in: state [as, bs) (shard side), gradients [ag, bg) (full
 // side), staged at shared offset (x - t0) and (f - gbase) respectively.  q is the
-// first replica of a per-replica item.
+// first replica of a per-replica item; end marks the item that tells the consumers
+// a launch with claimed units has no more work for their CTA.
 struct TileGeom {
     int64_t t0, s0, s1, delta, as, bs, ag, bg, gbase;
-    int32_t q;
+    int32_t q, end;
 };
 
 template <typename GT>
@@ -143,6 +145,7 @@ __device__ __forceinline__ TileGeom tile_geom(const Seg& sg, int64_t gt) {
     g.bg = floor_to(g.s1 + g.delta, E);
     g.gbase = floor_to(g.t0 + g.delta, E);
     g.q = 0;
+    g.end = 0;
     return g;
 }
 
@@ -185,8 +188,18 @@ template <typename GT>
 __host__ __device__ constexpr int grank_bytes() { return int(kTileElems * sizeof(GT)) + 16; }
 
 // ----------------------------------------------------------------------------
-// The pipeline.  A launch covers n_units units (tiles); CTA b takes units b, b + G,
-// b + 2G, ... and, when Pol::groups() = NG > 1, every unit as NG consecutive items
+// The pipeline.  A launch covers n_units units (tiles).  Without claim counters CTA b
+// takes units b, b + G, b + 2G, ...; with them (claim = a zeroed pair of device words:
+// units claimed, CTAs done) the producer of each CTA takes the next claim_batch
+// consecutive units from claim[0] whenever it has used up the last ones, so that the
+// SMs that stream faster take more units (measured on GB300: with the static split, the
+// CTAs of the accumulation and HSDP kernels on the same workload ended up to 22 % apart,
+// the same SMs always first).  The producer asks for its next batch while it issues the
+// current one's copies (a batch covers about a microsecond of streaming or more, so the
+// atomic's round trip stays hidden), and after its last unit queues an item marked end,
+// which tells the consumers to stop; the last producer to count itself out in claim[1]
+// clears both words for the slot's next launch.  Either
+// way, when Pol::groups() = NG > 1, every unit is NG consecutive items
 // (group 0 .. NG-1), so that a unit's groups meet the same consumer threads in order
 // and a per-thread Pol::Carry can hold partial results from one group to the next.
 // Pol supplies, for unit u and group k:
@@ -205,7 +218,8 @@ __host__ __device__ constexpr int grank_bytes() { return int(kTileElems * sizeof
 // consumers of item j write its results into output slot j mod kOutSlots (after
 // out.acquire(), then out.publish(header)), and the store warp issues the policy's
 // bulk stores from that slot (store(header, slot, lane)) and frees it once they
-// have read it.  Both sides wait on their own full/empty mbarriers, bounded.
+// have read it.  Both sides wait on their own full/empty mbarriers, bounded.  Such a
+// launch always splits its units statically (its claim is ignored).
 // ----------------------------------------------------------------------------
 struct NoCarry {};
 
@@ -286,13 +300,17 @@ struct OutRing {
 };
 
 template <class Pol>
-__device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, int S, int stage_bytes, uint64_t wait_ns) {
+__device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, int S, int stage_bytes, uint64_t wait_ns,
+                                             unsigned int* claim, int claim_batch) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int kOut = OutSlotBytes<Pol>::value;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t G = gridDim.x;
     const int NG = pol.groups();
-    const int64_t n_mine = blockIdx.x < n_units ? (n_units - blockIdx.x + G - 1) / G * NG : 0;
+    if (kOut > 0) claim = nullptr;
+    // items of this CTA: known with the static split, else until the end item
+    const int64_t n_mine = claim ? INT64_MAX
+                                 : (blockIdx.x < n_units ? (n_units - blockIdx.x + G - 1) / G * NG : 0);
     const uint32_t full0 = smem_addr(smem), empty0 = full0 + 8 * kMaxStages;
     TileGeom* geo = reinterpret_cast<TileGeom*>(smem + kGeoOff);
     const uint32_t ofull0 = full0 + kOutBarOff, oempty0 = ofull0 + 8 * kOutSlots;
@@ -342,21 +360,49 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, in
     if (warp == kConsumerWarps) {
         // ---- producer warp: item j of this CTA into stage j mod S ----
         int cursor = 0;
-        int64_t j = 0;
-        for (; j < n_mine; ++j) {
+        int64_t j = 0, u = -1, u_end = 0;                     // unit; end of the claimed batch
+        unsigned int next = 0;                                // the claim in flight (lane 0)
+        if (claim && lane == 0) next = atomicAdd(claim, unsigned(claim_batch));
+        bool gave_up = false;
+        for (;; ++j) {
+            const int k = int(j % NG);
+            bool end;
+            if (claim) {
+                if (k == 0 && ++u >= u_end) {                 // batch used up: the claim taken before
+                    const int64_t c = int64_t(__shfl_sync(0xffffffffu, next, 0));
+                    u = c;
+                    u_end = c + claim_batch < n_units ? c + claim_batch : n_units;
+                    if (c < n_units && lane == 0) next = atomicAdd(claim, unsigned(claim_batch));
+                }
+                end = u >= n_units;
+            } else {
+                if (j >= n_mine) break;
+                u = blockIdx.x + (j / NG) * G;
+                end = false;
+            }
             const int st = int(j % S);
             const int64_t use = j / S;
             // the item's geometry (segment-table reads) before or after the wait for a
             // free stage: Pol::kGeomFirst, chosen per use by measurement
             TileGeom g;
-            if (Pol::kGeomFirst) g = pol.geom(blockIdx.x + (j / NG) * G, int(j % NG), cursor);
+            if (Pol::kGeomFirst && !end) g = pol.geom(u, k, cursor);
             if (use > 0 &&
                 !__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * st, uint32_t((use - 1) & 1), wait_ns))) {
-                if (lane == 0) atomicOr(&g_wait_error, 1u);
+                gave_up = true;
                 break;
             }
-            if (!Pol::kGeomFirst) g = pol.geom(blockIdx.x + (j / NG) * G, int(j % NG), cursor);
             const uint32_t bar = full0 + 8 * st;
+            if (end) {                                        // no more units: tell the consumers
+                if (lane == 0) {
+                    geo[st].end = 1;                          // released by the arrive
+                    mbar_arrive(bar);
+                }
+                __syncwarp();
+                ++j;
+                break;
+            }
+            if (!Pol::kGeomFirst) g = pol.geom(u, k, cursor);
+            g.end = 0;
             if (lane == 0) {
                 geo[st] = g;                                  // released by the arrive
                 mbar_arrive_tx(bar, pol.bytes(g));
@@ -364,10 +410,19 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, in
             __syncwarp();
             pol.issue(g, smem_addr(stage0 + int64_t(st) * stage_bytes), bar, lane);
         }
-        if (j < n_mine) {
-            // gave up: let the copies already issued land before the shared memory goes away
+        if (gave_up) {
+            // let the copies already issued land before the shared memory goes away
+            if (lane == 0) atomicOr(&g_wait_error, 1u);
             for (int64_t k = j - S > 0 ? j - S : 0; k < j; ++k)
                 mbar_wait_bounded(full0 + 8 * int(k % S), uint32_t((k / S) & 1), wait_ns);
+        }
+        if (claim && lane == 0) {
+            // done claiming (here on every path): the last CTA out leaves the pair at zero
+            __threadfence();
+            if (atomicAdd(claim + 1, 1u) == unsigned(G) - 1u) {
+                atomicExch(claim, 0u);
+                atomicExch(claim + 1, 0u);
+            }
         }
         return;
     }
@@ -386,6 +441,7 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, in
             return;
         }
         const TileGeom g = geo[st];
+        if (g.end) break;                                     // only with claimed units
         const uint32_t empty = empty0 + 8 * st;
         auto release = [&] {
             __syncwarp();
@@ -441,10 +497,19 @@ std::map<std::pair<const void*, int>, std::pair<int, int>> g_st_cache;   // (ker
 template <class Pol>
 constexpr int pipeline_threads() { return kStThreads + 32 + (OutSlotBytes<Pol>::value > 0 ? 32 : 0); }
 
-// One CTA of 544 (576 with a store warp) threads per SM (at most one per item).
+// Launches with at least this many units per CTA claim their units (claims.cu); shorter
+// ones split them statically (a claim costs an atomic, and the host an event).  A claim
+// takes ceil(kClaimBytes / stage_bytes) consecutive units: about 96 KB of stage, which a
+// CTA streams in 2 us or more, well over the atomic's round trip.
+constexpr int64_t kClaimMinUnitsPerCta = 8;
+constexpr int kClaimBytes = 96 * 1024;
+
+// One CTA of 544 (576 with a store warp) threads per SM (at most one per item).  With
+// claims = true (and no output ring) the units are claimed from a counter pair of the
+// device's ring where one is free.
 template <typename K, typename Pol>
 cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage_bytes, uint64_t wait_ns,
-                            cudaStream_t st, int* grid_out = nullptr) {
+                            cudaStream_t st, int* grid_out = nullptr, bool claims = false) {
     if (grid_out) *grid_out = 0;
     if (n_items <= 0) return cudaSuccess;
     int dev = 0;
@@ -470,8 +535,15 @@ cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage
         g_st_cache[key] = std::make_pair(sms, smem);
     }
     const int64_t blocks = n_items < sms ? n_items : (sms > 0 ? sms : 1);
+    unsigned int* claim = nullptr;
+    int slot = -1, cdev = -1;
+    if (claims && OutSlotBytes<Pol>::value == 0 && n_items >= kClaimMinUnitsPerCta * blocks &&
+        n_items < (int64_t(1) << 31))
+        claim = claim_acquire(st, &slot, &cdev);
+    const int batch = (kClaimBytes + stage_bytes - 1) / stage_bytes;
     e = launch(kernel, dim3(unsigned(blocks)), dim3(pipeline_threads<Pol>()), size_t(smem), st, pol, n_items, S,
-               stage_bytes, wait_ns);
+               stage_bytes, wait_ns, claim, batch);
+    claim_release(slot, cdev, st, e == cudaSuccess);
     if (e == cudaSuccess && grid_out) *grid_out = int(blocks);
     return e;
 }

@@ -192,8 +192,9 @@ struct RsAdamw {
 
 template <typename GT, bool PARAM, bool GOUT, bool DC>
 __global__ void __launch_bounds__(kStThreads + 32, 1)
-k_rs_adamw_staged(RsAdamw<GT, PARAM, GOUT, DC> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
-    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+k_rs_adamw_staged(RsAdamw<GT, PARAM, GOUT, DC> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns,
+                  unsigned int* claim, int claim_batch) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns, claim, claim_batch);
 }
 
 // A wait that nothing completes: one mbarrier expects 16 bytes that no copy
@@ -227,7 +228,7 @@ bool staged_fits(int N, bool grad_bf16) {
 cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
                                    const GradPtrs& gp, int N, float* master, float* m, float* v, uint16_t* param,
                                    float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st,
-                                   const AdamScal* dsc) {
+                                   const AdamScal* dsc, bool claims) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -239,10 +240,11 @@ cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n
         constexpr bool P = decltype(tag_p)::value, O = decltype(tag_g)::value;
         if (dsc) {
             RsAdamw<GT, P, O, true> pol{segs, tile_base, gp, N, Q, NG, master, m, v, param, gout, sc, dsc};
-            return launch_pipeline(k_rs_adamw_staged<GT, P, O, true>, pol, n_tiles, sb, wait_ns, st);
+            return launch_pipeline(k_rs_adamw_staged<GT, P, O, true>, pol, n_tiles, sb, wait_ns, st, nullptr,
+                                   claims);
         }
         RsAdamw<GT, P, O, false> pol{segs, tile_base, gp, N, Q, NG, master, m, v, param, gout, sc, nullptr};
-        return launch_pipeline(k_rs_adamw_staged<GT, P, O, false>, pol, n_tiles, sb, wait_ns, st);
+        return launch_pipeline(k_rs_adamw_staged<GT, P, O, false>, pol, n_tiles, sb, wait_ns, st, nullptr, claims);
     };
     using T = std::true_type;
     using F = std::false_type;

@@ -26,12 +26,21 @@ bool zero1_staged_fits(int N, bool grad_bf16);
 // consumer warp of each CTA).
 int norm_staged_partials(int64_t n_tiles);
 
+// A launch's claim counters (claims.cu): a zeroed pair of device words (units claimed,
+// CTAs done) that no launch that may overlap this one uses, or nullptr (stream capture,
+// no free slot, no ring): then the launch splits its units statically.  After queueing
+// the launch (or failing to), claim_release(slot, dev, st, launched) records the slot's
+// event on st.  Thread-safe.
+unsigned int* claim_acquire(cudaStream_t st, int* slot, int* dev);
+void claim_release(int slot, int dev, cudaStream_t st, bool launched);
+
 // Each launcher covers one segment range of either alignment class; wait_ns
 // bounds every mbarrier wait.
 cudaError_t launch_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool grad_bf16,
                                    const GradPtrs& gp, int N, float* master, float* m, float* v, uint16_t* param,
                                    float* gout, const AdamScal& sc, uint64_t wait_ns, cudaStream_t st,
-                                   const AdamScal* dsc = nullptr);   // dsc: constants read on the device
+                                   const AdamScal* dsc = nullptr,    // dsc: constants read on the device
+                                   bool claims = true);              // false: no claim counters (no allocation)
 
 // The last micro-batch of a no_sync accumulation fused with the step: replica q
 // contributes acc.p[q] (fp32 accumulator) + micro.p[q] (micro_bf16 ? bf16 : fp32),

@@ -540,32 +540,37 @@ struct Accumulate {
 
 template <typename GT, bool PARAM>
 __global__ void __launch_bounds__(kStThreads + 32, 1)
-k_hsdp_adamw_staged(HsdpAdamw<GT, PARAM> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
-    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+k_hsdp_adamw_staged(HsdpAdamw<GT, PARAM> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns,
+                  unsigned int* claim, int claim_batch) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns, claim, claim_batch);
 }
 
 template <typename GT, bool MASTER>
 __global__ void __launch_bounds__(kStThreads + 64, 1)
-k_zero1_adamw_staged(Zero1Adamw<GT, MASTER> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
-    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+k_zero1_adamw_staged(Zero1Adamw<GT, MASTER> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns,
+                  unsigned int* claim, int claim_batch) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns, claim, claim_batch);
 }
 
 template <bool PARAM>
 __global__ void __launch_bounds__(kStThreads + 32, 1)
-k_adamw_scaled_staged(ScaledAdamw<PARAM> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
-    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+k_adamw_scaled_staged(ScaledAdamw<PARAM> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns,
+                  unsigned int* claim, int claim_batch) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns, claim, claim_batch);
 }
 
 template <typename GT>
 __global__ void __launch_bounds__(kStThreads + 32, 1)
-k_rs_norm_staged(RsNorm<GT> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
-    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+k_rs_norm_staged(RsNorm<GT> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns,
+                  unsigned int* claim, int claim_batch) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns, claim, claim_batch);
 }
 
 template <typename MT, bool FIRST>
 __global__ void __launch_bounds__(kStThreads + 32, 1)
-k_accumulate_staged(Accumulate<MT, FIRST> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
-    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+k_accumulate_staged(Accumulate<MT, FIRST> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns,
+                  unsigned int* claim, int claim_batch) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns, claim, claim_batch);
 }
 
 // Running sums of a thread's four elements, carried from one replica group to the next.
@@ -717,8 +722,9 @@ struct AccRsAdamw {
 
 template <typename MT, bool PARAM, bool GOUT>
 __global__ void __launch_bounds__(kStThreads + 32, 1)
-k_acc_rs_adamw_staged(AccRsAdamw<MT, PARAM, GOUT> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns) {
-    run_pipeline(pol, n_items, S, stage_bytes, wait_ns);
+k_acc_rs_adamw_staged(AccRsAdamw<MT, PARAM, GOUT> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns,
+                  unsigned int* claim, int claim_batch) {
+    run_pipeline(pol, n_items, S, stage_bytes, wait_ns, claim, claim_batch);
 }
 
 int hsdp_stage_bytes(int N, int R, bool bf16) {
@@ -746,7 +752,7 @@ cudaError_t launch_acc_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64
         using MT = decltype(tag_mt);
         constexpr bool P = decltype(tag_p)::value, O = decltype(tag_g)::value;
         AccRsAdamw<MT, P, O> pol{segs, tile_base, acc, micro, N, Q, NG, master, m, v, param, gout, sc};
-        return launch_pipeline(k_acc_rs_adamw_staged<MT, P, O>, pol, n_tiles, stage(Q), wait_ns, st);
+        return launch_pipeline(k_acc_rs_adamw_staged<MT, P, O>, pol, n_tiles, stage(Q), wait_ns, st, nullptr, true);
     };
     using T = std::true_type;
     using F = std::false_type;
@@ -780,10 +786,10 @@ cudaError_t launch_adamw_scaled_staged(const Seg* segs, int64_t tile_base, int64
     const int sb = 4 * kStateBytes;
     if (param) {
         ScaledAdamw<true> pol{segs, tile_base, gshard, coef, master, m, v, param, sc};
-        return launch_pipeline(k_adamw_scaled_staged<true>, pol, n_tiles, sb, wait_ns, st);
+        return launch_pipeline(k_adamw_scaled_staged<true>, pol, n_tiles, sb, wait_ns, st, nullptr, true);
     }
     ScaledAdamw<false> pol{segs, tile_base, gshard, coef, master, m, v, param, sc};
-    return launch_pipeline(k_adamw_scaled_staged<false>, pol, n_tiles, sb, wait_ns, st);
+    return launch_pipeline(k_adamw_scaled_staged<false>, pol, n_tiles, sb, wait_ns, st, nullptr, true);
 }
 
 int norm_staged_partials(int64_t n_tiles) {
@@ -803,7 +809,7 @@ cudaError_t launch_hsdp_adamw_staged(const Seg* segs, int64_t tile_base, int64_t
         using GT = decltype(tag_gt);
         constexpr bool P = decltype(tag_p)::value;
         HsdpAdamw<GT, P> pol{segs, tile_base, gp, N, R, copy, master, m, v, param, sc, rf};
-        return launch_pipeline(k_hsdp_adamw_staged<GT, P>, pol, n_tiles, sb, wait_ns, st);
+        return launch_pipeline(k_hsdp_adamw_staged<GT, P>, pol, n_tiles, sb, wait_ns, st, nullptr, true);
     };
     if (grad_bf16) return param ? go(uint16_t{}, std::true_type{}) : go(uint16_t{}, std::false_type{});
     return param ? go(float{}, std::true_type{}) : go(float{}, std::false_type{});
@@ -850,7 +856,7 @@ cudaError_t launch_accumulate_staged(const Seg* segs, int64_t tile_base, int64_t
             pol.acc[q] = acc[q];
             pol.micro[q] = micro[q];
         }
-        return launch_pipeline(k_accumulate_staged<MT, FIRST>, pol, n_items, sb, wait_ns, st);
+        return launch_pipeline(k_accumulate_staged<MT, FIRST>, pol, n_items, sb, wait_ns, st, nullptr, true);
     };
     if (micro_bf16) return first ? go(uint16_t{}, std::true_type{}) : go(uint16_t{}, std::false_type{});
     return first ? go(float{}, std::true_type{}) : go(float{}, std::false_type{});

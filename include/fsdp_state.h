@@ -31,14 +31,27 @@
  *   - Memory: every data buffer is owned by the caller and must stay alive until
  *     the work queued on the given stream has finished.  Device buffers are
  *     plain device pointers (cudaMalloc, or any allocator), 16-byte aligned
- *     (else FSDP_EALIGN).  The library owns only the layout object and the
- *     small per-device copy of its segment tables.
+ *     (else FSDP_EALIGN).  The library owns only the layout object, the
+ *     small per-device copy of its segment tables, and per device a ring of 64
+ *     work-claim counter pairs (512 bytes and 64 events, set up by the first
+ *     launch that uses one).
  *   - Streams: fsdp_stream_t is a cudaStream_t (NULL = legacy default stream).
  *     Launch calls are asynchronous and never synchronize; only
  *     fsdp_check_status and fsdp_layout_prepare block.  Kernels are launched as
  *     programmatic dependents of the work before them on the stream: each waits,
  *     before touching memory, for that work to complete, so stream order is kept
  *     exactly; only the launch latency between consecutive kernels is hidden.
+ *   - Work claims: a bulk-copy (staged) launch with at least 8 tiles per CTA --
+ *     the fused step, HSDP, accumulation, the fused last micro-batch, the staged
+ *     clip update -- hands its tiles to its CTAs through a counter pair from the
+ *     device's ring, so that faster SMs take more of them; results do not depend
+ *     on which CTA takes a tile.  A pair is reused only after the event recorded
+ *     behind its last launch has completed (cudaEventQuery), and the kernel leaves
+ *     it at zero.  Under stream capture, with no free pair, or from
+ *     fsdp_reduce_scatter_adamw_noalloc, the tiles are split statically instead.
+ *     The ring is set up (cudaMalloc, cudaMemset, cudaEventCreate) by the first
+ *     such launch on a device: make it before any stream capture, as the layout
+ *     tables (fsdp_layout_prepare).
  *   - Shard arrays are [N][stride] row-major: rank r's shard starts at element
  *     r*stride; stride = fsdp_layout_info.shard_stride >= S.  The layout picks
  *     stride mod 8 so that as many rank views as possible sit at a shard index
