@@ -61,6 +61,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             print(r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+        # a front-end diagnostic (e.g. #549-D, a variable read before it is set) fails the
+        # build; ptxas's register-spill notes do not
+        if "warning #" in r.stdout + r.stderr:
+            os.remove(cmd[cmd.index("-o") + 1])
+            raise RuntimeError(f"nvcc warned: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     if force or _newer(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
         r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-lrt", "-ldl", "-lpthread"],

@@ -10,9 +10,7 @@
 // they do.  No CTA-wide barrier in the loop; the bytes in flight per SM do not
 // depend on registers.  A gradient piece whose full-layout offset is not congruent
 // to its shard offset mod 8 is copied as the 16-byte-aligned window around it and
-// read from shared memory at its offset: no warp shuffle.  A use may also take an
-// output ring: the consumers write an item's results once into a shared-memory slot
-// and a store warp sends them out with cp.async.bulk shared -> global copies.
+// read from shared memory at its offset: no warp shuffle.
 //
 // Every wait on an mbarrier is bounded in time; a warp that gives up records
 // FSDP_ETIMEOUT in this translation unit's device word (g_wait_error, read and
@@ -214,32 +212,8 @@ __host__ __device__ constexpr int grank_bytes() { return int(kTileElems * sizeof
 //                              of each consumer warp call it once) frees the stage;
 //                              returns the thread's contribution to a sum
 //   finish(tid, sum)           after the consumer's last item, with the thread's sum
-// A policy with an output ring (Pol::kOutSlotBytes > 0) also gets a store warp: the
-// consumers of item j write its results into output slot j mod kOutSlots (after
-// out.acquire(), then out.publish(header)), and the store warp issues the policy's
-// bulk stores from that slot (store(header, slot, lane)) and frees it once they
-// have read it.  Both sides wait on their own full/empty mbarriers, bounded.  Such a
-// launch always splits its units statically (its claim is ignored).
 // ----------------------------------------------------------------------------
 struct NoCarry {};
-
-constexpr int kOutSlots = 2;
-
-// What the store warp needs about an item's output slot: the element range [a, b)
-// to store and the element at slot offset 0.
-struct OutHdr {
-    int64_t a, b, base;
-    int64_t pad;
-};
-
-template <class P, class = void>
-struct OutSlotBytes {
-    static constexpr int value = 0;
-};
-template <class P>
-struct OutSlotBytes<P, std::void_t<decltype(P::kOutSlotBytes)>> {
-    static constexpr int value = P::kOutSlotBytes;
-};
 
 // A policy with `static constexpr bool kPrologue = true` gets prologue(tid) called by
 // every consumer thread once, before its first item, followed by a barrier among the
@@ -254,108 +228,40 @@ struct PrologueOf<P, std::void_t<decltype(P::kPrologue)>> {
     static constexpr bool value = P::kPrologue;
 };
 
-// Front region: stage barriers, stage geometry, output barriers, output headers.
+// Front region: stage barriers, stage geometry and, at its end, 64 bytes a policy may
+// use for per-launch data (policy_front()).
 constexpr int kGeoOff = 16 * kMaxStages;
-constexpr int kOutBarOff = kGeoOff + kMaxStages * int(sizeof(TileGeom));
-constexpr int kOutHdrOff = kOutBarOff + 16 * kOutSlots;
-// and, at its end, 64 bytes a policy may use for per-launch data (policy_front())
 constexpr int kPolicyFrontOff = kFrontBytes - 64;
-static_assert(kOutHdrOff + kOutSlots * int(sizeof(OutHdr)) <= kPolicyFrontOff, "front region");
+static_assert(kGeoOff + kMaxStages * int(sizeof(TileGeom)) <= kPolicyFrontOff, "front region");
 
 __device__ __forceinline__ unsigned char* policy_front() {
     extern __shared__ __align__(128) unsigned char smem[];
     return smem + kPolicyFrontOff;
 }
 
-// The consumers' side of the output ring for one item.
-struct OutRing {
-    uint32_t full0, empty0;
-    unsigned char* slot0;
-    OutHdr* hdr;
-    int slot_bytes, lane, warp;
-    int64_t j;
-    uint64_t wait_ns;
-    bool ok;
-    // Waits (all lanes of the warp) until the item's slot is free; nullptr if the wait gave up.
-    __device__ unsigned char* acquire() {
-        const int k = int(j % kOutSlots);
-        const int64_t use = j / kOutSlots;
-        if (use > 0 &&
-            !__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * k, uint32_t((use - 1) & 1), wait_ns))) {
-            ok = false;
-            return nullptr;
-        }
-        return slot0 + k * slot_bytes;
-    }
-    // Hands the slot to the store warp (all lanes of the warp, after their writes).
-    __device__ void publish(const OutHdr& h) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the writes, to the bulk-copy engine
-        __syncwarp();
-        const int k = int(j % kOutSlots);
-        if (lane == 0) {
-            if (warp == 0) hdr[k] = h;                                 // released by the arrive
-            mbar_arrive(full0 + 8 * k);
-        }
-    }
-};
-
 template <class Pol>
 __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, int S, int stage_bytes, uint64_t wait_ns,
                                              unsigned int* claim, int claim_batch) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int kOut = OutSlotBytes<Pol>::value;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t G = gridDim.x;
     const int NG = pol.groups();
-    if (kOut > 0) claim = nullptr;
     // items of this CTA: known with the static split, else until the end item
     const int64_t n_mine = claim ? INT64_MAX
                                  : (blockIdx.x < n_units ? (n_units - blockIdx.x + G - 1) / G * NG : 0);
     const uint32_t full0 = smem_addr(smem), empty0 = full0 + 8 * kMaxStages;
     TileGeom* geo = reinterpret_cast<TileGeom*>(smem + kGeoOff);
-    const uint32_t ofull0 = full0 + kOutBarOff, oempty0 = ofull0 + 8 * kOutSlots;
-    OutHdr* ohdr = reinterpret_cast<OutHdr*>(smem + kOutHdrOff);
     unsigned char* stage0 = smem + kFrontBytes;
-    unsigned char* out0 = stage0 + int64_t(S) * stage_bytes;
 
     if (tid == 0) {
         for (int k = 0; k < S; ++k) {
             mbar_init(full0 + 8 * k, 1);                      // the producer's arrive (+ bytes)
             mbar_init(empty0 + 8 * k, kConsumerWarps);        // one arrive per consumer warp
         }
-        if (kOut > 0)
-            for (int k = 0; k < kOutSlots; ++k) {
-                mbar_init(ofull0 + 8 * k, kConsumerWarps);    // one arrive per consumer warp
-                mbar_init(oempty0 + 8 * k, 1);                // the store warp's arrive
-            }
         mbar_fence_init();
     }
     __syncthreads();
     pdl_wait();
-
-    if constexpr (kOut > 0) {
-        if (warp == kConsumerWarps + 1) {
-            // ---- store warp: the bulk stores of item j from output slot j mod kOutSlots ----
-            for (int64_t j = 0; j < n_mine; ++j) {
-                const int k = int(j % kOutSlots);
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(ofull0 + 8 * k, uint32_t((j / kOutSlots) & 1), wait_ns))) {
-                    if (lane == 0) atomicOr(&g_wait_error, 1u);
-                    break;
-                }
-                const OutHdr h = ohdr[k];
-                if (lane == 0) {
-                    pol.store(h, smem_addr(out0 + k * kOut));
-                    bulk_commit();
-                    bulk_wait_read_all();                     // the slot may be rewritten
-                    mbar_arrive(oempty0 + 8 * k);
-                }
-                __syncwarp();
-            }
-            if (lane == 0) bulk_wait_all();                   // the stores are complete
-            __syncwarp();
-            return;
-        }
-    }
 
     if (warp == kConsumerWarps) {
         // ---- producer warp: item j of this CTA into stage j mod S ----
@@ -447,16 +353,7 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, in
             __syncwarp();
             if (lane == 0) mbar_arrive(empty);
         };
-        if constexpr (kOut > 0) {
-            OutRing out{ofull0, oempty0, out0, ohdr, kOut, lane, warp, j, wait_ns, true};
-            sum += pol.consume(g, stage0 + int64_t(st) * stage_bytes, tid, carry, release, out);
-            if (!out.ok) {
-                if (lane == 0) atomicOr(&g_wait_error, 1u);
-                return;
-            }
-        } else {
-            sum += pol.consume(g, stage0 + int64_t(st) * stage_bytes, tid, carry, release);
-        }
+        sum += pol.consume(g, stage0 + int64_t(st) * stage_bytes, tid, carry, release);
     }
     pol.finish(tid, sum);
 }
@@ -492,10 +389,8 @@ int stage_count(int stage_bytes, int dev, int extra_bytes = 0) {
 std::mutex g_st_mu;
 std::map<std::pair<const void*, int>, std::pair<int, int>> g_st_cache;   // (kernel, dev) -> (SMs, smem set)
 
-// Threads of a pipeline CTA: the consumers, the producer warp, and the store warp
-// of a policy with an output ring.
-template <class Pol>
-constexpr int pipeline_threads() { return kStThreads + 32 + (OutSlotBytes<Pol>::value > 0 ? 32 : 0); }
+// Threads of a pipeline CTA: the consumers and the producer warp.
+constexpr int kPipelineThreads = kStThreads + 32;
 
 // Launches with at least this many units per CTA claim their units (claims.cu); shorter
 // ones split them statically (a claim costs an atomic, and the host an event).  A claim
@@ -504,9 +399,8 @@ constexpr int pipeline_threads() { return kStThreads + 32 + (OutSlotBytes<Pol>::
 constexpr int64_t kClaimMinUnitsPerCta = 8;
 constexpr int kClaimBytes = 96 * 1024;
 
-// One CTA of 544 (576 with a store warp) threads per SM (at most one per item).  With
-// claims = true (and no output ring) the units are claimed from a counter pair of the
-// device's ring where one is free.
+// One CTA of 544 threads per SM (at most one per item).  With claims = true the units
+// are claimed from a counter pair of the device's ring where one is free.
 template <typename K, typename Pol>
 cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage_bytes, uint64_t wait_ns,
                             cudaStream_t st, int* grid_out = nullptr, bool claims = false) {
@@ -515,10 +409,9 @@ cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    constexpr int kOutBytes = kOutSlots * OutSlotBytes<Pol>::value;
-    const int S = stage_count(stage_bytes, dev, kOutBytes);
+    const int S = stage_count(stage_bytes, dev);
     if (S < 2) return cudaErrorInvalidValue;
-    const int smem = kFrontBytes + S * stage_bytes + kOutBytes;
+    const int smem = kFrontBytes + S * stage_bytes;
     const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
     int sms = 0, set = 0;
     {
@@ -537,11 +430,11 @@ cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage
     const int64_t blocks = n_items < sms ? n_items : (sms > 0 ? sms : 1);
     unsigned int* claim = nullptr;
     int slot = -1, cdev = -1;
-    if (claims && OutSlotBytes<Pol>::value == 0 && n_items >= kClaimMinUnitsPerCta * blocks &&
+    if (claims && n_items >= kClaimMinUnitsPerCta * blocks &&
         n_items < (int64_t(1) << 31))
         claim = claim_acquire(st, &slot, &cdev);
     const int batch = (kClaimBytes + stage_bytes - 1) / stage_bytes;
-    e = launch(kernel, dim3(unsigned(blocks)), dim3(pipeline_threads<Pol>()), size_t(smem), st, pol, n_items, S,
+    e = launch(kernel, dim3(unsigned(blocks)), dim3(kPipelineThreads), size_t(smem), st, pol, n_items, S,
                stage_bytes, wait_ns, claim, batch);
     claim_release(slot, cdev, st, e == cudaSuccess);
     if (e == cudaSuccess && grid_out) *grid_out = int(blocks);

@@ -962,11 +962,11 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* L, int32_t ub, int32_t ue, con
     const Range D = range_of(L->data, base, ub, ue);
     const bool bf = grad_dtype == FSDP_BF16;
     bool staged = false;
-    // the automatic choice keeps the direct kernel: measured on GB300, the staged one
-    // (bulk-store broadcast) ran the 4-block Llama at 0.93-0.96 of the copy peak from
-    // one box to the next against a steady 0.95 direct, and 128 MiB of fp32 replicas
-    // at 0.90 against 0.94
-    if ((rc = choose_staged(fsdp::zero1_staged_fits(L->N, bf), false, &staged))) return rc;
+    // the automatic choice takes the staged kernel where two of its stages fit: measured
+    // on GB300 (tiles claimed from a counter, the broadcast stored from registers), the
+    // 128 MiB fp32 layout at 1.00 of the copy peak against 0.94 for the direct kernel,
+    // the 4-block Llama at 1.04 against 0.96
+    if ((rc = choose_staged(fsdp::zero1_staged_fits(L->N, bf), true, &staged))) return rc;
     if (D.n_tiles <= 0) return FSDP_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (staged) {

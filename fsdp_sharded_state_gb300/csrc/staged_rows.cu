@@ -150,13 +150,14 @@ struct HsdpAdamw {
 // Parameters are whole and replicated; each tensor's optimizer state lives in its
 // owner's row.  g = mean over the N replicas; the owner's AdamW on its state (p from
 // the fp32 master in the row when the replicas are bf16, else from the owner's own
-// fp32 replica); the updated parameter goes to all N replicas.  The broadcast is
-// the bulk-copy engine's: the consumers write the tile's updated parameters once
-// into an output slot and the store warp issues one cp.async.bulk shared -> global
-// per replica from it.  Owner rows keep every tensor congruent to its full offset
-// mod 8 (delta = 0 mod 8), so the tile's window starts at slot offset 0; anything
-// else, and the at most 7 elements at each end that 16-byte copies leave out, is
-// stored element by element.
+// fp32 replica); the updated parameter goes to all N replicas, stored straight from
+// the consumers' registers (16-byte fp32 or 8-byte bf16 stores, a warp covering 512
+// contiguous bytes of each replica).  Owner rows keep every tensor congruent to its
+// full offset mod 8 (delta = 0 mod 8); anything else, and the at most 7 elements at
+// each end that 16-byte copies leave out, is stored element by element.  (A form that
+// wrote each tile's result once into a shared-memory output slot and broadcast it with
+// one cp.async.bulk per replica from a store warp measured slower on GB300: 0.89 of the
+// copy peak on the 128 MiB fp32 layout, 0.93-0.96 on the 4-block Llama.)
 struct ParamReplicas {
     void* p[kMaxRanks];
 };
@@ -164,8 +165,6 @@ struct ParamReplicas {
 template <typename GT, bool MASTER>
 struct Zero1Adamw {
     static constexpr bool kGeomFirst = true;
-    static constexpr int kPB = MASTER ? 2 : 4;                     // replica element bytes
-    static constexpr int kOutSlotBytes = int(kTileElems) * kPB;
     const Seg* segs;
     int64_t tile_base;
     GradPtrs gp;
@@ -213,25 +212,16 @@ struct Zero1Adamw {
             }
         }
     }
-    // The broadcast of one slot (lane 0 of the store warp): [h.a, h.b) to every replica.
-    __device__ void store(const OutHdr& h, uint32_t slot) const {
-        if (h.b <= h.a) return;
-        const uint32_t src = slot + uint32_t(h.a - h.base) * kPB, bytes = uint32_t(h.b - h.a) * kPB;
-        for (int q = 0; q < N; ++q) bulk_s2g(static_cast<unsigned char*>(pr.p[q]) + h.a * kPB, src, bytes);
-    }
     template <class Release>
-    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, Carry&, Release release,
-                              OutRing& out) const {
+    __device__ double consume(const TileGeom& g, const unsigned char* sb, int tid, NoCarry&, Release release) const {
         const int c = tid * 4;
         const int64_t x = g.t0 + c, f = x + g.delta;
         const bool live = x + 4 > g.s0 && x < g.s1;
-        // owner rows keep delta = 0 mod 8; anything else goes element by element
-        const bool al = (g.delta & 7) == 0;
+        const bool al = (g.delta & 7) == 0;              // owner rows keep delta = 0 mod 8
         const bool fast = x >= g.s0 && x + 4 <= g.s1 && f >= g.ag && f + 4 <= g.bg && al;
         float4 pv, mv, vv;
         float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
         if (fast) {
-            // p at the shard offset (master) or at the full offset (the owner's replica; gbase = t0 + delta)
             pv = lds4(sb + c * 4);
             mv = lds4(sb + 1 * kStateBytes + c * 4);
             vv = lds4(sb + 2 * kStateBytes + c * 4);
@@ -245,12 +235,6 @@ struct Zero1Adamw {
             }
         }
         release();
-        // the range the bulk stores cover: 16-byte aligned in every replica and inside the
-        // gradient window (every chunk in it takes the fast path)
-        constexpr int64_t PE = (16 / kPB) > int64_t(16 / sizeof(GT)) ? (16 / kPB) : int64_t(16 / sizeof(GT));
-        const int64_t pa = al ? ceil_to(g.s0 + g.delta, PE) : 0, pb = al ? floor_to(g.s1 + g.delta, PE) : 0;
-        unsigned char* slot = out.acquire();
-        if (slot == nullptr) return 0.0;
         if (fast) {
             float p[4] = {pv.x, pv.y, pv.z, pv.w};
             float m[4] = {mv.x, mv.y, mv.z, mv.w};
@@ -261,16 +245,13 @@ struct Zero1Adamw {
             if (MASTER) st4(master + x, make_float4(p[0], p[1], p[2], p[3]));
             st4(exp_avg + x, make_float4(m[0], m[1], m[2], m[3]));
             st4(exp_avg_sq + x, make_float4(v[0], v[1], v[2], v[3]));
-            if (f >= pa && f + 4 <= pb) {                 // into the slot, for the bulk stores
-                if (MASTER)
-                    *reinterpret_cast<uint2*>(slot + c * kPB) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
-                else
-                    *reinterpret_cast<float4*>(slot + c * kPB) = make_float4(p[0], p[1], p[2], p[3]);
-            } else if (MASTER) {                          // next to a segment end: every replica directly
+            if (MASTER) {
                 const uint2 w = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
+#pragma unroll 1
                 for (int q = 0; q < N; ++q) *reinterpret_cast<uint2*>(static_cast<uint16_t*>(pr.p[q]) + f) = w;
             } else {
                 const float4 w = make_float4(p[0], p[1], p[2], p[3]);
+#pragma unroll 1
                 for (int q = 0; q < N; ++q) st4(static_cast<float*>(pr.p[q]) + f, w);
             }
         } else if (live) {
@@ -289,7 +270,6 @@ struct Zero1Adamw {
                 }
             }
         }
-        out.publish(OutHdr{pa, pb, g.t0 + g.delta, 0});
         return 0.0;
     }
     __device__ void finish(int, double) const {}
@@ -546,9 +526,9 @@ k_hsdp_adamw_staged(HsdpAdamw<GT, PARAM> pol, int64_t n_items, int S, int stage_
 }
 
 template <typename GT, bool MASTER>
-__global__ void __launch_bounds__(kStThreads + 64, 1)
+__global__ void __launch_bounds__(kStThreads + 32, 1)
 k_zero1_adamw_staged(Zero1Adamw<GT, MASTER> pol, int64_t n_items, int S, int stage_bytes, uint64_t wait_ns,
-                  unsigned int* claim, int claim_batch) {
+                 unsigned int* claim, int claim_batch) {
     run_pipeline(pol, n_items, S, stage_bytes, wait_ns, claim, claim_batch);
 }
 
@@ -775,10 +755,7 @@ bool hsdp_staged_fits(int N, int R, bool grad_bf16, int64_t copy) {
 
 bool norm_staged_fits(int N, bool grad_bf16) { return fits(norm_stage_bytes(N, grad_bf16)); }
 
-bool zero1_staged_fits(int N, bool grad_bf16) {
-    // the stage plus two output slots (fp32 replicas: 8 KB each)
-    return fits(rs_stage_bytes(N, grad_bf16), kOutSlots * int(kTileElems) * 4);
-}
+bool zero1_staged_fits(int N, bool grad_bf16) { return fits(rs_stage_bytes(N, grad_bf16)); }
 
 cudaError_t launch_adamw_scaled_staged(const Seg* segs, int64_t tile_base, int64_t n_tiles, float* gshard,
                                        const float* coef, float* master, float* m, float* v, uint16_t* param,
@@ -881,7 +858,7 @@ cudaError_t launch_zero1_adamw_staged(const Seg* segs, int64_t tile_base, int64_
         pol.exp_avg = m;
         pol.exp_avg_sq = v;
         pol.sc = sc;
-        return launch_pipeline(k_zero1_adamw_staged<GT, M>, pol, n_tiles, sb, wait_ns, st);
+        return launch_pipeline(k_zero1_adamw_staged<GT, M>, pol, n_tiles, sb, wait_ns, st, nullptr, true);
     };
     if (grad_bf16) return master ? go(uint16_t{}, std::true_type{}) : go(uint16_t{}, std::false_type{});
     return master ? go(float{}, std::true_type{}) : go(float{}, std::false_type{});

@@ -424,8 +424,7 @@ int fsdp_zero1_adamw_broadcast(const fsdp_layout* layout, int32_t unit_begin, in
  *   FSDP_RS_AUTO    the staged kernel where at least two of its pipeline stages fit
  *                   in one CTA's shared memory, else the direct kernels; the clip
  *                   runs as one cooperative launch where at most one tile in 256 of
- *                   its unit range is misaligned, else as the direct passes, and ZeRO-1 keeps
- *                   the direct kernel (measured as fast or steadier).  A stage
+ *                   its unit range is misaligned, else as the direct passes.  A stage
  *                   holds 2048 elements of each array the call reads: for
  *                   fsdp_reduce_scatter_adamw the three fp32 state arrays and the N
  *                   gradient replicas, the replicas in groups where all of them do
