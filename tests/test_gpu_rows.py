@@ -156,6 +156,8 @@ ACC_RS_CASES = [
     (W([(1 << 22,)], [0], 4, synth.FLAT, torch.float32), torch.float32),
     (W([(300, 40), (9,)], [0, 0], 8, synth.FLAT, torch.float32), torch.float32),    # replica groups
     (W([(5000,), (33,)], [0, 0], 16, synth.FLAT), torch.bfloat16),                  # replica groups
+    # replica groups in a launch that claims its tiles (2,048 tiles: 8 per CTA and more)
+    (W([(1 << 22,)], [0], 16, synth.FLAT), torch.bfloat16),
 ]
 
 
