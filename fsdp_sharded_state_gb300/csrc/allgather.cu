@@ -25,7 +25,18 @@ namespace {
 // with 8 loads ahead ran at 40 %.  Lane 0 issues the copies; the at most 7
 // elements at each end of a segment that the copies leave out are copied by the
 // warp's lanes with plain loads and stores.
+//
+// A bf16 launch with enough tiles claims them from a counter pair (claims.cu), as the
+// pipeline kernels do: lane 0 starts on the CTA's own first kUClaimTiles tiles, then
+// takes kUClaimTiles consecutive tiles per claim when it needs the next tile to load,
+// and records each loaded tile in a small ring that the store side reads.  Measured on
+// GB300, FULL_SHARD steps with two all-gathers: bf16 layouts from 2^24 to 2^29
+// parameters 0.3-2 % faster with the claims; fp32 (8 KB tiles, one load ahead) 0.7-1 %
+// faster at 2^26 and 2^28 parameters but 0.9 % slower on the 128 MiB, 8-unit layout,
+// so fp32 keeps the static split.
 constexpr int kUCtasPerSm = 4;
+constexpr int kUClaimTiles = 2;                 // tiles per claim
+constexpr int64_t kUClaimMinTilesPerCta = 8;    // shorter launches split their tiles statically
 // Loads ahead and ring buffers per CTA: about 32 KB in flight per SM for both element
 // sizes (bf16 tiles are 4 KB: 2 ahead; fp32 tiles 8 KB: 1 ahead).  Measured on GB300:
 // fp32 128 MiB all-gather 44.2 us with 1 ahead against 46.5 us with 2.
@@ -38,14 +49,22 @@ struct Ring {
 template <int ES>
 __global__ void __launch_bounds__(32)
 k_unshard_bulk(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles, const unsigned char* src,
-               unsigned char* dst, uint64_t wait_ns) {
+               unsigned char* dst, uint64_t wait_ns, unsigned int* claim) {
     constexpr int64_t E = 16 / ES;              // elements per 16 bytes
     using W = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
     __shared__ __align__(128) unsigned char buf[Ring<ES>::size][kTileElems * ES];
     __shared__ __align__(8) uint64_t bars[Ring<ES>::size];
+    __shared__ int64_t seq[Ring<ES>::size];     // the tile of item j, at j mod size
     const int lane = threadIdx.x;
     const int64_t G = gridDim.x;
-    const int64_t n_mine = blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + G - 1) / G : 0;
+    // items of this CTA: known with the static split, else found when the claims run out
+    int64_t n_mine = claim ? INT64_MAX : (blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + G - 1) / G : 0);
+    unsigned int next = 0;                      // lane 0: the claim in flight
+    // lane 0: what is left of the current batch; the first is the CTA's own, [b B, b B + B),
+    // so no claim is waited for at the start, and the claims hand out the tiles from G B on
+    int64_t bat = int64_t(blockIdx.x) * kUClaimTiles;
+    int64_t bat_end = bat + kUClaimTiles < n_tiles ? bat + kUClaimTiles : n_tiles;
+    if (claim && lane == 0) next = atomicAdd(claim, unsigned(kUClaimTiles));
     const uint32_t bar0 = smem_addr(&bars[0]);
     if (lane == 0) {
         for (int k = 0; k < Ring<ES>::size; ++k) mbar_init(bar0 + 8 * k, 1);
@@ -55,8 +74,8 @@ k_unshard_bulk(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
     pdl_wait();
 
     struct Piece { int64_t t0, s0, s1, delta, a, b; };     // tile range, aligned interior [a, b)
-    auto piece = [&](int& cur, int64_t j) {
-        const int64_t gt = tile_base + blockIdx.x + j * G;
+    auto piece = [&](int& cur, int64_t t) {
+        const int64_t gt = tile_base + t;
         cur = advance_seg(segs, cur, gt);
         const Seg sg = segs[cur];
         Piece p;
@@ -70,14 +89,35 @@ k_unshard_bulk(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
         return p;
     };
     int load_cur = 0, store_cur = 0;             // segment cursors of the two sides
+    // Loads item j (lane 0; j one more each call): its tile -- the static split's, or the
+    // next of the claimed batch, claiming again when it is used up -- into seq, or, when
+    // there is none, n_mine = j.  Every lane then takes n_mine from lane 0.
     auto load = [&](int64_t j) {
-        const Piece p = piece(load_cur, j);
         if (lane == 0) {
-            const int k = int(j % Ring<ES>::size);
-            const uint32_t bytes = p.b > p.a ? uint32_t(p.b - p.a) * ES : 0u;
-            mbar_arrive_tx(bar0 + 8 * k, bytes);
-            if (bytes) bulk_g2s(smem_addr(&buf[k][(p.a - p.t0) * ES]), src + p.a * ES, bytes, bar0 + 8 * k);
+            int64_t t;
+            if (claim) {
+                if (bat >= bat_end) {
+                    const int64_t c = G * kUClaimTiles + int64_t(next);
+                    bat = c;
+                    bat_end = c + kUClaimTiles < n_tiles ? c + kUClaimTiles : n_tiles;
+                    if (c < n_tiles) next = atomicAdd(claim, unsigned(kUClaimTiles));
+                }
+                t = bat < bat_end ? bat++ : n_tiles;
+            } else {
+                t = blockIdx.x + j * G;
+            }
+            if (t >= n_tiles) {
+                n_mine = j;
+            } else {
+                const int k = int(j % Ring<ES>::size);
+                seq[k] = t;
+                const Piece p = piece(load_cur, t);
+                const uint32_t bytes = p.b > p.a ? uint32_t(p.b - p.a) * ES : 0u;
+                mbar_arrive_tx(bar0 + 8 * k, bytes);
+                if (bytes) bulk_g2s(smem_addr(&buf[k][(p.a - p.t0) * ES]), src + p.a * ES, bytes, bar0 + 8 * k);
+            }
         }
+        n_mine = __shfl_sync(0xffffffffu, n_mine, 0);
     };
     for (int64_t j = 0; j < n_mine && j < Ring<ES>::ahead; ++j) load(j);
     int64_t j = 0;
@@ -92,7 +132,8 @@ k_unshard_bulk(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
         const int k = int(j % Ring<ES>::size);
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * k, uint32_t((j / Ring<ES>::size) & 1), wait_ns));
         if (!ok) break;
-        const Piece p = piece(store_cur, j);
+        __syncwarp();
+        const Piece p = piece(store_cur, seq[k]);
         if (lane == 0) {
             if (p.b > p.a) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -117,13 +158,21 @@ k_unshard_bulk(const Seg* __restrict__ segs, int64_t tile_base, int64_t n_tiles,
             mbar_wait_bounded(bar0 + 8 * int(q % Ring<ES>::size), uint32_t((q / Ring<ES>::size) & 1), wait_ns);
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    if (claim && lane == 0) {
+        // done claiming (here on every path): the last CTA out leaves the pair at zero
+        __threadfence();
+        if (atomicAdd(claim + 1, 1u) == unsigned(G) - 1u) {
+            atomicExch(claim, 0u);
+            atomicExch(claim + 1, 0u);
+        }
+    }
     __syncwarp();
 }
 
 }  // namespace
 
 cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16, const void* src,
-                                void* dst, uint64_t wait_ns, cudaStream_t st) {
+                                void* dst, uint64_t wait_ns, cudaStream_t st, bool claims) {
     if (n_tiles <= 0) return cudaSuccess;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -134,9 +183,16 @@ cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_ti
     if (blocks > n_tiles) blocks = n_tiles;
     const auto* s8 = static_cast<const unsigned char*>(src);
     auto* d8 = static_cast<unsigned char*>(dst);
-    if (bf16) return launch(k_unshard_bulk<2>, dim3(unsigned(blocks)), dim3(32), 0, st, segs, tile_base, n_tiles, s8, d8,
-                            wait_ns);
-    return launch(k_unshard_bulk<4>, dim3(unsigned(blocks)), dim3(32), 0, st, segs, tile_base, n_tiles, s8, d8, wait_ns);
+    unsigned int* claim = nullptr;
+    int slot = -1, cdev = -1;
+    if (claims && bf16 && n_tiles >= kUClaimMinTilesPerCta * blocks && n_tiles < (int64_t(1) << 31))
+        claim = claim_acquire(st, &slot, &cdev);
+    e = bf16 ? launch(k_unshard_bulk<2>, dim3(unsigned(blocks)), dim3(32), 0, st, segs, tile_base, n_tiles, s8, d8,
+                      wait_ns, claim)
+             : launch(k_unshard_bulk<4>, dim3(unsigned(blocks)), dim3(32), 0, st, segs, tile_base, n_tiles, s8, d8,
+                      wait_ns, claim);
+    claim_release(slot, cdev, st, e == cudaSuccess);
+    return e;
 }
 
 cudaError_t take_wait_error_allgather(unsigned int* flag) { return take_local_wait_error(flag); }

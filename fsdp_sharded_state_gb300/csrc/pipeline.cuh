@@ -188,8 +188,9 @@ __host__ __device__ constexpr int grank_bytes() { return int(kTileElems * sizeof
 // ----------------------------------------------------------------------------
 // The pipeline.  A launch covers n_units units (tiles).  Without claim counters CTA b
 // takes units b, b + G, b + 2G, ...; with them (claim = a zeroed pair of device words:
-// units claimed, CTAs done) the producer of each CTA takes the next claim_batch
-// consecutive units from claim[0] whenever it has used up the last ones, so that the
+// units claimed, CTAs done) the producer of CTA b starts on the units [b B, b B + B)
+// (B = claim_batch) and then takes the next B consecutive units from G B + claim[0]
+// whenever it has used up the last ones, so that the
 // SMs that stream faster take more units (measured on GB300: with the static split, the
 // CTAs of the accumulation and HSDP kernels on the same workload ended up to 22 % apart,
 // the same SMs always first).  The producer asks for its next batch while it issues the
@@ -266,7 +267,10 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, in
     if (warp == kConsumerWarps) {
         // ---- producer warp: item j of this CTA into stage j mod S ----
         int cursor = 0;
-        int64_t j = 0, u = -1, u_end = 0;                     // unit; end of the claimed batch
+        int64_t j = 0, u = -1, u_end = 0;                     // unit; end of the current batch
+        // the first batch is the CTA's own, [b B, b B + B): no claim to wait for at the start;
+        // the claims hand out the units from G B on
+        int64_t first = int64_t(blockIdx.x) * claim_batch;
         unsigned int next = 0;                                // the claim in flight (lane 0)
         if (claim && lane == 0) next = atomicAdd(claim, unsigned(claim_batch));
         bool gave_up = false;
@@ -275,10 +279,14 @@ __device__ __forceinline__ void run_pipeline(const Pol& pol, int64_t n_units, in
             bool end;
             if (claim) {
                 if (k == 0 && ++u >= u_end) {                 // batch used up: the claim taken before
-                    const int64_t c = int64_t(__shfl_sync(0xffffffffu, next, 0));
+                    int64_t c = first;
+                    if (first < 0) {
+                        c = G * claim_batch + int64_t(__shfl_sync(0xffffffffu, next, 0));
+                        if (c < n_units && lane == 0) next = atomicAdd(claim, unsigned(claim_batch));
+                    }
+                    first = -1;
                     u = c;
                     u_end = c + claim_batch < n_units ? c + claim_batch : n_units;
-                    if (c < n_units && lane == 0) next = atomicAdd(claim, unsigned(claim_batch));
                 }
                 end = u >= n_units;
             } else {

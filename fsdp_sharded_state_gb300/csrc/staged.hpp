@@ -82,9 +82,10 @@ cudaError_t launch_zero1_adamw_staged(const Seg* segs, int64_t tile_base, int64_
                                       float* master, float* m, float* v, const AdamScal& sc, uint64_t wait_ns,
                                       cudaStream_t st);
 
-// All-gather (shard -> full, bitwise) of a segment range of the aligned class.
+// All-gather (shard -> full, bitwise) of a segment range of the aligned class; with
+// claims, a bf16 launch with at least 8 tiles per CTA claims them from a counter pair.
 cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16, const void* src,
-                                void* dst, uint64_t wait_ns, cudaStream_t st);
+                                void* dst, uint64_t wait_ns, cudaStream_t st, bool claims = true);
 
 // One kernel whose only wait cannot complete: exercises the bounded-wait exit.
 cudaError_t launch_wait_selftest(uint64_t wait_ns, cudaStream_t st);

@@ -42,10 +42,10 @@
  *     before touching memory, for that work to complete, so stream order is kept
  *     exactly; only the launch latency between consecutive kernels is hidden.
  *   - Work claims: a bulk-copy (staged) launch with at least 8 tiles per CTA --
- *     the fused step, HSDP, accumulation, the fused last micro-batch, the staged
- *     clip update -- hands its tiles to its CTAs through a counter pair from the
- *     device's ring, so that faster SMs take more of them; results do not depend
- *     on which CTA takes a tile.  A pair is reused only after the event recorded
+ *     the fused step, HSDP, accumulation, the fused last micro-batch, ZeRO-1, the
+ *     staged clip update, the bf16 all-gather -- hands its tiles to its CTAs through a
+ *     counter pair from the device's ring, so that faster SMs take more of them;
+ *     results do not depend on which CTA takes a tile.  A pair is reused only after the event recorded
  *     behind its last launch has completed (cudaEventQuery), and the kernel leaves
  *     it at zero.  Under stream capture, with no free pair, or from
  *     fsdp_reduce_scatter_adamw_noalloc, the tiles are split statically instead.
