@@ -41,7 +41,7 @@ __device__ unsigned int g_wait_error = 0;
 constexpr int kStThreads = 512;                 // consumer threads: 4 elements each per item
 constexpr int kConsumerWarps = kStThreads / 32;
 constexpr int kMaxStages = 8;
-constexpr int kInFlightBytes = 96 * 1024;       // stage bytes in flight per SM to aim for
+constexpr int kInFlightBytes = 116 * 1024;      // stage bytes in flight per SM to aim for
 constexpr int kFrontBytes = 1024;               // mbarriers + per-stage item geometry
 constexpr int kStateBytes = int(kTileElems) * 4;
 
@@ -379,16 +379,21 @@ int optin_smem(int dev) {
     return v;
 }
 
-// Stages for a stage of `stage_bytes`: as many as keep about 96 KB in flight (the
-// stages beyond the one being consumed), 4 for stages under 36 KB, between 2 and
-// kMaxStages, within the opt-in shared memory; 0 if two do not fit.  Measured on
-// GB300 (fused step): about 50-100 KB in flight per SM streams best; 3-4 stages of
-// 57 KB lost up to 10 % of the bandwidth, fewer than 40 KB in flight lost 8 %, and
-// stages of 33 KB (bf16, N = 2) ran best with 4.
-int stage_count(int stage_bytes, int dev, int extra_bytes = 0) {
+// Stages for a stage of `stage_bytes`: as many as keep about `in_flight` bytes in flight
+// (the stages beyond the one being consumed), 4 for stages under 36 KB, between 2 and
+// kMaxStages, within the opt-in shared memory; 0 if two do not fit.  Measured on GB300,
+// with the tiles claimed from a counter: the fused step ran 1-3 % faster with 3 stages of
+// 49-57 KB than with 2 (mlp128m 195.8 against 199.0 us, llama4 4.671 against 4.725 ms,
+// dim0_n6 1.310 against 1.351 ms) and 0.9 % slower with 4 stages of 40 KB than with 3
+// (fp32, N = 2); 41 KB stages (bf16, N = 4) ran the same with 3 or 4, stages of 33 KB
+// (bf16, N = 2) best with 4.  The default target (116 KB) gives 3 stages from 40 to
+// 57 KB; the accumulation passes 128 KB (3 stages of 64 KB: 0.4 % faster than 2), ZeRO-1
+// 96 KB (2 stages of 57 KB: 0.5 % faster than 3).  (With the tiles split statically,
+// 3-4 stages of 57 KB had lost up to 10 %.)
+int stage_count(int stage_bytes, int dev, int extra_bytes = 0, int in_flight = kInFlightBytes) {
     const int avail = optin_smem(dev) - kFrontBytes - extra_bytes;
     const int fit = avail > 0 ? avail / stage_bytes : 0;
-    int want = stage_bytes < 36 * 1024 ? 4 : kInFlightBytes / stage_bytes + 1;
+    int want = stage_bytes < 36 * 1024 ? 4 : in_flight / stage_bytes + 1;
     want = want < 2 ? 2 : (want > kMaxStages ? kMaxStages : want);
     const int s = fit < want ? fit : want;
     return s >= 2 ? s : 0;
@@ -411,13 +416,14 @@ constexpr int kClaimBytes = 96 * 1024;
 // are claimed from a counter pair of the device's ring where one is free.
 template <typename K, typename Pol>
 cudaError_t launch_pipeline(K kernel, const Pol& pol, int64_t n_items, int stage_bytes, uint64_t wait_ns,
-                            cudaStream_t st, int* grid_out = nullptr, bool claims = false) {
+                            cudaStream_t st, int* grid_out = nullptr, bool claims = false,
+                            int in_flight = kInFlightBytes) {
     if (grid_out) *grid_out = 0;
     if (n_items <= 0) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int S = stage_count(stage_bytes, dev);
+    const int S = stage_count(stage_bytes, dev, 0, in_flight);
     if (S < 2) return cudaErrorInvalidValue;
     const int smem = kFrontBytes + S * stage_bytes;
     const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
