@@ -713,6 +713,9 @@ constexpr int kAccItemBytes = 96 * 1024;
 // accumulation at 128 KB (3 stages of 64 KB): 0.4 % faster than 2.
 constexpr int kZero1InFlightBytes = 96 * 1024;
 constexpr int kAccInFlightBytes = 128 * 1024;
+// The last micro-batch fused with the step aims at 160 KB: 3 stages where they fit (the
+// 4-block Llama's two replica groups, 74 KB stages: 8.71 against 8.87 ms with 2).
+constexpr int kAccStepInFlightBytes = 160 * 1024;
 
 int hsdp_stage_bytes(int N, int R, bool bf16) {
     return 3 * R * kStateBytes + R * N * (bf16 ? grank_bytes<uint16_t>() : grank_bytes<float>());
@@ -739,7 +742,8 @@ cudaError_t launch_acc_rs_adamw_staged(const Seg* segs, int64_t tile_base, int64
         using MT = decltype(tag_mt);
         constexpr bool P = decltype(tag_p)::value, O = decltype(tag_g)::value;
         AccRsAdamw<MT, P, O> pol{segs, tile_base, acc, micro, N, Q, NG, master, m, v, param, gout, sc};
-        return launch_pipeline(k_acc_rs_adamw_staged<MT, P, O>, pol, n_tiles, stage(Q), wait_ns, st, nullptr, true);
+        return launch_pipeline(k_acc_rs_adamw_staged<MT, P, O>, pol, n_tiles, stage(Q), wait_ns, st, nullptr, true,
+                               kAccStepInFlightBytes);
     };
     using T = std::true_type;
     using F = std::false_type;
