@@ -32,9 +32,9 @@
  *     the work queued on the given stream has finished.  Device buffers are
  *     plain device pointers (cudaMalloc, or any allocator), 16-byte aligned
  *     (else FSDP_EALIGN).  The library owns only the layout object, the
- *     small per-device copy of its segment tables, and per device a ring of 64
- *     work-claim counter pairs (512 bytes and 64 events, set up by the first
- *     launch that uses one).
+ *     small per-device copy of its segment tables, and per device a ring of 1024
+ *     work-claim counter pairs (8 KB and 1024 events, set up by the first launch
+ *     that uses one).
  *   - Streams: fsdp_stream_t is a cudaStream_t (NULL = legacy default stream).
  *     Launch calls are asynchronous and never synchronize; only
  *     fsdp_check_status and fsdp_layout_prepare block.  Kernels are launched as

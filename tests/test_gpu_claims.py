@@ -4,8 +4,9 @@ A launch with enough units per CTA takes a counter pair from the device's ring a
 CTAs claim units from it; a slot is reused only after the launch that used it has
 completed, and the kernel leaves the pair at zero.  The checks count: the accumulation
 adds an exact integer per call, so a unit skipped or done twice changes the count.
-  - 100 calls queued without a synchronisation (more than the ring's 64 slots: the
-    later calls find no free slot and split their units statically);
+  - 1,200 calls queued without a synchronisation (more than the ring's 1,024 slots, so
+    that calls find no free slot and split their units statically while the GPU catches
+    up);
   - calls on two streams at once, each with its own accumulators;
   - the fused step with claims against its static form (CUDA graph capture) bit for bit
     lives in tests/test_gpu_graph.py, and against the no-allocation entry point in
@@ -34,12 +35,12 @@ def test_queued_calls_count_exactly():
     F = L.info["full_numel"]
     acc = [torch.zeros(F, dtype=torch.float32, device="cuda") for _ in range(N)]
     ones = [torch.ones(F, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
-    for k in range(100):
+    for k in range(1200):
         fs.fsdp_accumulate_grads(L, 0, L.n_units, acc, ones, first=(k == 0))
     torch.cuda.synchronize()
     fs.fsdp_check_status()
     for q in range(N):
-        assert torch.equal(acc[q], torch.full_like(acc[q], 100.0))
+        assert torch.equal(acc[q], torch.full_like(acc[q], 1200.0))
 
 
 def test_two_streams_count_exactly():
