@@ -26,17 +26,19 @@ namespace {
 // elements at each end of a segment that the copies leave out are copied by the
 // warp's lanes with plain loads and stores.
 //
-// A bf16 launch with enough tiles claims them from a counter pair (claims.cu), as the
+// A launch with enough tiles claims them from a counter pair (claims.cu), as the
 // pipeline kernels do: lane 0 starts on the CTA's own first kUClaimTiles tiles, then
 // takes kUClaimTiles consecutive tiles per claim when it needs the next tile to load,
 // and records each loaded tile in a small ring that the store side reads.  Measured on
 // GB300, FULL_SHARD steps with two all-gathers: bf16 layouts from 2^24 to 2^29
-// parameters 0.3-2 % faster with the claims; fp32 (8 KB tiles, one load ahead) 0.7-1 %
-// faster at 2^26 and 2^28 parameters but 0.9 % slower on the 128 MiB, 8-unit layout,
-// so fp32 keeps the static split.
+// parameters (13 tiles per CTA and more) 0.3-2 % faster with the claims; fp32 (8 KB
+// tiles, one load ahead) 1.2 % faster at 2^26 parameters (54 tiles per CTA) and 1 % at
+// 2^28, but 0.2-1 % slower at 2^25 (27 tiles per CTA: the 128 MiB layouts), so fp32
+// claims from kUClaimMinTilesPerCtaF32 tiles per CTA.
 constexpr int kUCtasPerSm = 4;
 constexpr int kUClaimTiles = 2;                 // tiles per claim
 constexpr int64_t kUClaimMinTilesPerCta = 8;    // shorter launches split their tiles statically
+constexpr int64_t kUClaimMinTilesPerCtaF32 = 48;
 // Loads ahead and ring buffers per CTA: about 32 KB in flight per SM for both element
 // sizes (bf16 tiles are 4 KB: 2 ahead; fp32 tiles 8 KB: 1 ahead).  Measured on GB300:
 // fp32 128 MiB all-gather 44.2 us with 1 ahead against 46.5 us with 2.
@@ -185,7 +187,8 @@ cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_ti
     auto* d8 = static_cast<unsigned char*>(dst);
     unsigned int* claim = nullptr;
     int slot = -1, cdev = -1;
-    if (claims && bf16 && n_tiles >= kUClaimMinTilesPerCta * blocks && n_tiles < (int64_t(1) << 31))
+    if (claims && n_tiles >= (bf16 ? kUClaimMinTilesPerCta : kUClaimMinTilesPerCtaF32) * blocks &&
+        n_tiles < (int64_t(1) << 31))
         claim = claim_acquire(st, &slot, &cdev);
     e = bf16 ? launch(k_unshard_bulk<2>, dim3(unsigned(blocks)), dim3(32), 0, st, segs, tile_base, n_tiles, s8, d8,
                       wait_ns, claim)

@@ -83,7 +83,8 @@ cudaError_t launch_zero1_adamw_staged(const Seg* segs, int64_t tile_base, int64_
                                       cudaStream_t st);
 
 // All-gather (shard -> full, bitwise) of a segment range of the aligned class; with
-// claims, a bf16 launch with at least 8 tiles per CTA claims them from a counter pair.
+// claims, a launch with at least 8 (bf16) or 48 (fp32) tiles per CTA claims them from a
+// counter pair.
 cudaError_t launch_unshard_bulk(const Seg* segs, int64_t tile_base, int64_t n_tiles, bool bf16, const void* src,
                                 void* dst, uint64_t wait_ns, cudaStream_t st, bool claims = true);
 

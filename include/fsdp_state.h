@@ -43,15 +43,15 @@
  *     exactly; only the launch latency between consecutive kernels is hidden.
  *   - Work claims: a bulk-copy (staged) launch with at least 8 tiles per CTA --
  *     the fused step, HSDP, accumulation, the fused last micro-batch, ZeRO-1, the
- *     staged clip update, the bf16 all-gather -- hands its tiles to its CTAs through a
- *     counter pair from the device's ring, so that faster SMs take more of them;
- *     results do not depend on which CTA takes a tile.  A pair is reused only after the event recorded
- *     behind its last launch has completed (cudaEventQuery), and the kernel leaves
- *     it at zero.  Under stream capture, with no free pair, or from
- *     fsdp_reduce_scatter_adamw_noalloc, the tiles are split statically instead.
- *     The ring is set up (cudaMalloc, cudaMemset, cudaEventCreate) by the first
- *     such launch on a device: make it before any stream capture, as the layout
- *     tables (fsdp_layout_prepare).
+ *     staged clip update, the all-gather (fp32 from 48 tiles per CTA) -- hands its
+ *     tiles to its CTAs through a counter pair from the device's ring, so that
+ *     faster SMs take more of them; results do not depend on which CTA takes a
+ *     tile.  A pair is reused only after the event recorded behind its last launch
+ *     has completed (cudaEventQuery), and the kernel leaves it at zero.  Under
+ *     stream capture, with no free pair, or from fsdp_reduce_scatter_adamw_noalloc,
+ *     the tiles are split statically instead.  The ring is set up (cudaMalloc,
+ *     cudaMemset, cudaEventCreate) by the first such launch on a device: make it
+ *     before any stream capture, as the layout tables (fsdp_layout_prepare).
  *   - Shard arrays are [N][stride] row-major: rank r's shard starts at element
  *     r*stride; stride = fsdp_layout_info.shard_stride >= S.  The layout picks
  *     stride mod 8 so that as many rank views as possible sit at a shard index
