@@ -84,6 +84,13 @@ def test_sweep_fp32_params_full_compare(oracle_lib, P, N, grad_dtype):
     pu.run_full_parity(w, strategy="full_shard" if N % 4 else "shard_grad_op")
 
 
+@pytest.mark.parametrize("P,N", [((1 << 22) + 1, 64), ((1 << 22) + 1, 1)])
+def test_rank_count_extremes_full_compare(oracle_lib, P, N):
+    # the largest N the layout takes (64: three replica groups of 22 per tile) and a single
+    # rank, each large enough for the CTAs to claim their tiles, over the whole state
+    pu.run_full_parity(synth.sweep(P, N), strategy="full_shard")
+
+
 @pytest.mark.parametrize("P,N", [((1 << 26) + 1, 8), ((1 << 29) + 1, 32), (1 << 29, 2)])
 def test_sweep_large_sampled(oracle_lib, P, N):
     pu.run_sampled_parity(synth.sweep(P, N), n_random=100_000)

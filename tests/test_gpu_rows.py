@@ -39,6 +39,7 @@ CLIP_CASES = [
     (W([(130, 64), (7,), (9, 3)], [0, 0, 0], 4, synth.DIM0), 5e-3),
     (W([(1 << 24,)], [0], 8, synth.FLAT), 1e-2),                           # 16M params
     (W([(64, 32), (64,)], [0, 0], 4, synth.FLAT, torch.float32), 2e-3),    # fp32
+    (W([(300, 7), (5,)], [0, 0], 1, synth.FLAT), 1e-3),                     # a single rank
 ]
 
 
@@ -158,6 +159,7 @@ ACC_RS_CASES = [
     (W([(5000,), (33,)], [0, 0], 16, synth.FLAT), torch.bfloat16),                  # replica groups
     # replica groups in a launch that claims its tiles (2,048 tiles: 8 per CTA and more)
     (W([(1 << 22,)], [0], 16, synth.FLAT), torch.bfloat16),
+    (W([(300, 40), (9,)], [0, 0], 1, synth.FLAT), torch.float32),                     # a single rank
 ]
 
 
