@@ -117,7 +117,8 @@ def test_clip_inactive_equals_plain_step(oracle_lib):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("w", [W([(37, 5), (3,), (11, 13)], [0, 1, 1], 6, synth.FLAT),
                                W([(130, 64), (7,), (9, 3)], [0, 0, 1], 4, synth.DIM0),
-                               W([(1 << 22,)], [0], 4, synth.FLAT)])
+                               W([(1 << 22,)], [0], 4, synth.FLAT),
+                               W([(1 << 22,)], [0], 1, synth.FLAT)])                # a single rank
 @pytest.mark.parametrize("micro_dtype", [torch.bfloat16, torch.float32])
 def test_accumulate_then_step_vs_oracle(oracle_lib, w, micro_dtype):
     M = 3
@@ -214,7 +215,8 @@ def test_accumulate_reduce_scatter_vs_oracle(oracle_lib, w, micro_dtype):
                                  (W([(64, 32), (64,)], [0, 0], 2, synth.FLAT, torch.float32), 3),
                                  (W([((1 << 20) + 1,)], [0], 8, synth.FLAT), 2),
                                  (W([(333, 17), (5,), (64, 64)], [0, 0, 1], 2, synth.FLAT), 3),
-                                 (W([(300, 40), (9,)], [0, 0], 4, synth.FLAT, torch.float32), 2)])
+                                 (W([(300, 40), (9,)], [0, 0], 4, synth.FLAT, torch.float32), 2),
+                                 (W([(1 << 21,), (77,)], [0, 0], 1, synth.FLAT), 2)])   # one rank per group
 def test_hsdp_vs_oracle(oracle_lib, rs_kind, w, R):
     L = fs.Layout(w.shapes, w.unit_ids, w.N, w.mode)
     sh = oracle.Shapes(w.shapes, w.unit_ids)
@@ -259,7 +261,7 @@ oracle_zero1_rows = pu.oracle_zero1_rows
 
 
 @pytest.mark.parametrize("shapes,N", [(ZSHAPES, 3), (ZSHAPES, 4), ([(1 << 20,), (1000, 17), (333,)], 2),
-                                     (ZSHAPES + [(4096, 300), (77, 5)], 8)])
+                                     (ZSHAPES + [(4096, 300), (77, 5)], 8), (ZSHAPES, 1)])
 @pytest.mark.parametrize("bf16,grad_bf16", [(False, False), (True, True), (False, True), (True, False)])
 def test_zero1_vs_oracle(oracle_lib, shapes, N, bf16, grad_bf16):
     L = fs.Layout(shapes, None, N, fs.FSDP_ZERO1)
