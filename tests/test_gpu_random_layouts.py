@@ -243,3 +243,58 @@ def _zero1_vs_oracle(w, out, N, bf16):
         b = o * ostride + ooff[k]
         pu.assert_f32_close(gm[a:a + sizes[k]], rm[b:b + sizes[k]], f"zero1 exp_avg t{k}")
         pu.assert_f32_close(gv[a:a + sizes[k]], rv[b:b + sizes[k]], f"zero1 exp_avg_sq t{k}")
+
+
+# ---------------------------------------------------------------------------
+# Large random layouts: hundreds of tensors (many small, some large), 3-8M parameters,
+# so that a launch has thousands of tiles and its CTAs claim them from a counter, each
+# claim jumping the CTA's segment cursor across many segments.  The staged kernels
+# (claimed tiles) against the direct ones (a static split) bit for bit, and every other
+# layout against the oracle.
+def big_random_workload(seed: int) -> synth.Workload:
+    rng = np.random.default_rng(7000 + seed)
+    mode = synth.FLAT if seed % 2 == 0 else synth.DIM0
+    N = int(rng.choice([2, 3, 4, 6, 8, 16]))
+    shapes = [(int(rng.integers(1, 5000)),) if rng.random() < 0.5 else (int(rng.integers(1, 40)), int(rng.integers(1, 200)))
+              for _ in range(int(rng.integers(100, 300)))]
+    shapes += [(int(rng.integers(200, 2000)), int(rng.integers(64, 1024))) for _ in range(int(rng.integers(10, 30)))]
+    order = rng.permutation(len(shapes))
+    shapes = [shapes[i] for i in order]
+    units, u = [], 0
+    for t in range(len(shapes)):
+        if t > 0 and rng.random() < 0.05:
+            u += 1
+        units.append(u)
+    dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float32
+    return synth.Workload(f"bigrandom{seed}", 20, shapes, units, N, mode, dtype, dtype, 2, 1e-3)
+
+
+@pytest.mark.parametrize("seed", list(range(6)))
+def test_staged_equals_direct_on_large_random_layouts(oracle_lib, seed):
+    w = big_random_workload(seed)
+    L = fs.Layout(w.shapes, w.unit_ids, w.N, w.mode)
+    assert L.stride * w.N >= 8 * 152 * 2048          # enough tiles for the claims
+    strategy = "full_shard"
+    a = run(w, "direct", strategy)
+    b = run(w, "staged", strategy)
+    for name in ("master", "exp_avg", "exp_avg_sq", "grad_out"):
+        assert torch.equal(getattr(a, name).view(torch.int32), getattr(b, name).view(torch.int32)), (name, w.N)
+    if a.param is not None:
+        assert torch.equal(a.param.view(torch.int16), b.param.view(torch.int16)), ("param", w.N)
+    if seed % 2 == 0:
+        pu.run_full_parity(w, strategy=strategy)
+
+
+@pytest.mark.parametrize("seed", list(range(4)))
+def test_staged_rows_equal_direct_on_large_random_layouts(oracle_lib, seed):
+    w = big_random_workload(seed)
+    R = 2
+    a, b = run_rows(w, "direct", R), run_rows(w, "staged", R)
+    for row in ("hsdp", "acc", "zero1"):
+        if seed % 2 == 0:
+            rows_vs_oracle(w, R, a, row)
+        if row not in b:
+            continue                  # the staged kernel does not hold this layout
+        for x, y in zip(a[row], b[row]):
+            if x is not None:
+                assert torch.equal(_bits(x), _bits(y)), (row, w.N)
