@@ -38,6 +38,37 @@ def test_byte_model_per_element():
     assert tot1 == 46 * P
 
 
+def test_row_byte_model_per_parameter():
+    # the rows' bytes per logical parameter (each array read or written once):
+    #   clip:  N gradient replicas, the fp32 shard written, re-read, rewritten clipped,
+    #          master/m/v read and written (+ the bf16 parameter written);
+    #   accum: per replica the micro-batch read, the fp32 accumulator read and written;
+    #   accum_step: per replica the accumulator and the micro-batch read; the state as
+    #          in the step;
+    #   hsdp:  R x N replicas; R copies of the state (+ R bf16 parameters);
+    #   zero1: N replicas; the owner's m, v (and master, or its own fp32 replica); the
+    #          updated parameter written into all N replicas.
+    # The DRAM reads ncu measured equal the reads counted here: the accumulation on the
+    # 128 MiB layout 1.074 GB (32 B per parameter), the fused last micro-batch 1.476 GB
+    # (44 B), ZeRO-1 0.940 GB (28 B).
+    m = synth.mlp128m()                     # fp32, N = 4
+    P = 33554432
+    assert bench.row_bytes("clip", m, P, 4) == 52 * P
+    assert bench.row_bytes("accum", m, P, 4) == 48 * P
+    assert bench.row_bytes("accum_step", m, P, 4) == 56 * P
+    assert bench.row_bytes("hsdp", m, P, 4, R=2) == 80 * P
+    assert bench.row_bytes("zero1", m, P, 4) == 52 * P
+    l4 = synth.llama4()                     # bf16 parameters and gradients, N = 8
+    P = 809533440
+    assert bench.row_bytes("clip", l4, P, 8) == 54 * P
+    assert bench.row_bytes("accum", l4, P, 8) == 80 * P
+    assert bench.row_bytes("accum_step", l4, P, 8) == 74 * P
+    assert bench.row_bytes("hsdp", l4, P, 8, R=2) == 84 * P
+    assert bench.row_bytes("zero1", l4, P, 8) == 56 * P
+    with pytest.raises(KeyError):
+        bench.row_bytes("nope", m, P, 4)
+
+
 def test_parse_clocks():
     csv = "\n".join([
         "0, 1965 MHz, 2070 MHz, 900.1 W, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
