@@ -187,20 +187,20 @@ __host__ __device__ constexpr int grank_bytes() { return int(kTileElems * sizeof
 
 // ----------------------------------------------------------------------------
 // The pipeline.  A launch covers n_units units (tiles).  Without claim counters CTA b
-// takes units b, b + G, b + 2G, ...; with them (claim = a zeroed pair of device words:
+// takes units b, b + G, b + 2G, ...  With them (claim = a zeroed pair of device words:
 // units claimed, CTAs done) the producer of CTA b starts on the units [b B, b B + B)
-// (B = claim_batch) and then takes the next B consecutive units from G B + claim[0]
-// whenever it has used up the last ones, so that the
-// SMs that stream faster take more units (measured on GB300: with the static split, the
-// CTAs of the accumulation and HSDP kernels on the same workload ended up to 22 % apart,
-// the same SMs always first).  The producer asks for its next batch while it issues the
-// current one's copies (a batch covers about a microsecond of streaming or more, so the
-// atomic's round trip stays hidden), and after its last unit queues an item marked end,
-// which tells the consumers to stop; the last producer to count itself out in claim[1]
-// clears both words for the slot's next launch.  Either
-// way, when Pol::groups() = NG > 1, every unit is NG consecutive items
-// (group 0 .. NG-1), so that a unit's groups meet the same consumer threads in order
-// and a per-thread Pol::Carry can hold partial results from one group to the next.
+// (B = claim_batch), then takes the next B consecutive units from G B + claim[0] whenever
+// it has used up the last ones, so that the SMs that stream faster take more units
+// (measured on GB300: with the static split, the CTAs of the accumulation and HSDP
+// kernels on the same workload ended up to 22 % apart, the same SMs always first).  The
+// producer asks for its next batch while it issues the current one's copies (a batch
+// covers a microsecond of streaming or more, so the atomic's round trip stays hidden);
+// after its last unit it queues an item marked end, which tells the consumers to stop,
+// and the last producer to count itself out in claim[1] clears both words for the
+// slot's next launch.  Either way, when Pol::groups() = NG > 1, every unit is NG
+// consecutive items (group 0 .. NG-1), so that a unit's groups meet the same consumer
+// threads in order and a per-thread Pol::Carry can hold partial results from one group
+// to the next.
 // Pol supplies, for unit u and group k:
 //   geom(u, k, cursor)         the item's geometry (producer side, once per item), resolved
 //                              before the producer waits for a free stage when
